@@ -1,0 +1,178 @@
+/*
+ * moe.h -- C ABI of the single-GPU mixture-of-experts layer for GB300 (sm_103a).
+ *
+ * One MoE layer: top-k routing, a schedule table (per-expert counts, prefix-sum
+ * offsets, stable expert-contiguous permutation), a gather of token rows into
+ * expert order, a grouped SwiGLU expert FFN on tcgen05 tensor cores, and a
+ * fixed-order weighted merge back to token order; forward and backward.
+ *
+ * Sources (web pages on Cursor's "Mixture-of-Kittens" MoE megakernel):
+ *   [LP] leiphone, "MoK：把 token 调度、跨 GPU 通信和专家计算塞进同一个 GPU 内核",
+ *        sections 01 (communication tax), 02 (transfer while computing),
+ *        03 (specialised execution)
+ *   [MT] Marktechpost, "Cursor开源MoK：GB300 NVL72机架上的确定性MoE训练大内核",
+ *        sections "three design decisions", "benchmarks", "key points"
+ *
+ * Conventions for every call:
+ *  - Ownership: the caller owns every buffer.  The library never allocates
+ *    device memory and never synchronises the stream (moe_read_status is the
+ *    one exception).  Device pointers must be 128-byte aligned.
+ *  - Layouts are row-major.  bf16 tensors are passed as moe_bf16 (raw bits).
+ *    W1 is [E, d, 2f] with the gate in columns [0, f) and the up projection
+ *    in [f, 2f); W2 is [E, f, d].
+ *  - Errors: argument errors return at once without touching the GPU
+ *    (MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE_TOO_SMALL).
+ *    Launch failures return MOE_ERR_CUDA.  Conditions found on the device
+ *    (a bounded wait that ran out) are written to a status word inside the
+ *    workspace and read back with moe_read_status; nothing traps.
+ *  - Determinism: for the same inputs, configuration and device every output
+ *    is bitwise identical from run to run (the pages' megakernel is fully
+ *    deterministic: [MT] three design decisions, last paragraph).  No
+ *    floating-point atomics are used; every reduction has a fixed order.
+ *  - Workspace: moe_schedule, moe_forward and moe_backward of one layer call
+ *    must share the same workspace (it carries the padded expert layout from
+ *    the schedule to the FFN) and the same moe_sched arrays.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+typedef uint16_t moe_bf16;                /* bfloat16 bit pattern */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,         /* null pointer, bad size, misalignment, k > E ... */
+  MOE_ERR_UNSUPPORTED = 2,         /* valid request this build does not implement */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 3, /* ws_bytes < moe_workspace_bytes(cfg) */
+  MOE_ERR_CUDA = 4,                /* a CUDA runtime call or launch failed */
+  MOE_ERR_TIMEOUT = 5,             /* a bounded device wait ran out (status word) */
+  MOE_ERR_DEVICE_CHECK = 6         /* a device-side bounds check failed (status word) */
+} moe_status;
+
+typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_precision;
+
+/* Layer configuration.
+ *   T tokens, d hidden size, f expert intermediate size, E experts, k top-k.
+ *   Limits: 1 <= k <= min(E, 32); 1 <= E <= 1024; T >= 1; d and f multiples
+ *   of 64 (d also of 128 in MXFP8 mode).
+ *   minibatch_rows: 0 runs the layer as a chain of kernels over the whole
+ *     expert-ordered buffer.  > 0 runs the forward as one persistent kernel
+ *     that hands windows of this many expert-ordered rows (a multiple of 128)
+ *     from gather CTAs to GEMM CTAs through a ring of ring_slots slots
+ *     ([LP] 02: SM partition, local counters, minibatch, ring token buffer).
+ *   ring_slots: ring depth (>= 2) when minibatch_rows > 0.
+ *   gather_ctas: CTAs on the gather/combine side of the SM split (0 = auto). */
+typedef struct {
+  int32_t T, d, f, E, k;
+  int32_t prec; /* moe_precision */
+  int32_t minibatch_rows;
+  int32_t ring_slots;
+  int32_t gather_ctas;
+} moe_config;
+
+/* Schedule table, all device arrays written by moe_schedule ([LP] 01: count
+ * tokens per expert, decide where each goes, keep an expert's tokens
+ * contiguous; [MT] three design decisions: one table serves all four
+ * transfer modes).  Flat routed row r = t*k + j, j = slot = rank.
+ *   topk_ids [T*k] int32   expert of row r (ranked by logit, ties -> lower id)
+ *   topk_w   [T*k] fp32    renormalised softmax weight of row r
+ *   counts   [E]   int32   rows routed to each expert
+ *   offsets  [E+1] int32   exclusive prefix sum of counts, offsets[E] = T*k
+ *   perm     [T*k] int32   perm[p] = r: expert-major, ascending r within an expert
+ *   inv      [T*k] int32   inverse of perm */
+typedef struct {
+  int32_t* topk_ids;
+  float* topk_w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm;
+  int32_t* inv;
+} moe_sched;
+
+/* Activations the forward saves for the backward, in the library's padded
+ * expert order (each expert's rows start on a multiple of 128; padding rows
+ * are zero).  H: [moe_saved_rows(cfg), 2f] bf16 (X W1 before SwiGLU);
+ * A: [moe_saved_rows(cfg), f] bf16 (SwiGLU output).  Opaque to the caller. */
+typedef struct {
+  moe_bf16* H;
+  moe_bf16* A;
+} moe_saved;
+
+/* Bytes of device workspace moe_schedule / moe_forward / moe_backward need
+ * for cfg (pure host arithmetic; 0 if cfg is invalid). */
+size_t moe_workspace_bytes(const moe_config* cfg);
+
+/* Rows of the saved H / A buffers (pure host arithmetic; 0 if invalid). */
+int64_t moe_saved_rows(const moe_config* cfg);
+
+/* Smallest minibatch (rows) that gives the grouped GEMM at least two full
+ * waves of tiles on compute_sms SMs: ceil(2 * compute_sms * bm * bn / n_cols)
+ * with n_cols the GEMM's output width ([LP] 02 and [MT] three design
+ * decisions: "at least two full SM waves"; for hidden 7168 / intermediate
+ * 2048 the pages quote ~2,368 tokens).  Returns 0 on non-positive input. */
+int32_t moe_min_minibatch(int32_t compute_sms, int32_t bm, int32_t bn, int32_t n_cols);
+
+/* Routing + schedule table ([LP] 01; [MT] three design decisions).
+ *   logits: device fp32 [T, E] (finite; non-finite logits give unspecified
+ *   routing).  Writes every array of `sched` and the padded expert layout in
+ *   `ws`; clears the workspace status word. */
+moe_status moe_schedule(const moe_config* cfg, const float* logits, moe_sched sched,
+                        void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* MXFP8 quantisation of weights for the MXFP8 forward ([LP] 02 MXFP8
+ * paragraph; [MT] "BF16 and MXFP8 modes").  w: device bf16 [batch, K, N]
+ * (a W1 or W2 stack).  Writes q: e4m3 [batch, N, K] (K contiguous) and
+ * scales: UE8M0 [batch, N, K/32], one scale per 32 consecutive K elements
+ * (scale 2^s with s the smallest exponent such that the block's max |v| <=
+ * 448 * 2^s, clamped to [-127, 127]; elements rounded to nearest even with
+ * saturation).  K must be a multiple of 128 and N of 64. */
+moe_status moe_quantize_mxfp8(const moe_bf16* w, int64_t batch, int32_t K, int32_t N,
+                              uint8_t* q, uint8_t* scales, moe_stream_t stream);
+
+/* Forward: Dispatch -> Expert FFN -> Combine -> weighted merge ([LP] 03;
+ * dispatch by pull, combine by push, [LP] 02).
+ *   x [T, d] bf16.  BF16 mode: w1 = W1 bf16 [E, d, 2f], w2 = W2 bf16 [E, f, d],
+ *   w1_scales = w2_scales = NULL.  MXFP8 mode: w1/w2 and their scales as
+ *   written by moe_quantize_mxfp8 from W1 / W2.
+ *   out [T, d] bf16: out[t] = sum_j topk_w[t,j] * FFN_{topk_ids[t,j]}(x[t]),
+ *   summed in slot order in fp32, rounded once to bf16.
+ *   saved: NULL for inference; else H and A are written for moe_backward. */
+moe_status moe_forward(const moe_config* cfg, const moe_bf16* x, const void* w1,
+                       const uint8_t* w1_scales, const void* w2, const uint8_t* w2_scales,
+                       moe_sched sched, moe_bf16* out, const moe_saved* saved, void* ws,
+                       size_t ws_bytes, moe_stream_t stream);
+
+/* Backward (BF16): reverse combine, expert FFN dgrad / wgrad, SwiGLU backward
+ * fused with the routing-weight gradient, reverse dispatch ([LP] 02: pull
+ * reverse-combine, push reverse-dispatch; [MT] three design decisions: the
+ * routing-weight gradient is fused into the SwiGLU backward).
+ *   dout [T, d] bf16 upstream gradient; x, w1, w2 as in the forward; saved
+ *   as written by moe_forward with the same sched and ws.
+ *   dx [T, d] bf16; dw1 [E, d, 2f] bf16; dw2 [E, f, d] bf16 (experts with no
+ *   rows get exact zeros); dtopk_w [T*k] fp32 = d loss / d topk_w;
+ *   dlogits [T, E] fp32 or NULL: gradient through the renormalised softmax
+ *   (zero for unselected experts). */
+moe_status moe_backward(const moe_config* cfg, const moe_bf16* dout, const moe_bf16* x,
+                        const moe_bf16* w1, const moe_bf16* w2, moe_sched sched,
+                        const moe_saved* saved, moe_bf16* dx, moe_bf16* dw1, moe_bf16* dw2,
+                        float* dtopk_w, float* dlogits, void* ws, size_t ws_bytes,
+                        moe_stream_t stream);
+
+/* Synchronises `stream` and returns the device status word of `ws` (MOE_OK,
+ * MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK).  Test / debug use. */
+moe_status moe_read_status(const void* ws, moe_stream_t stream);
+
+/* Static English name of a status code. */
+const char* moe_status_string(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,223 @@
+// api.cu -- the C ABI declared in include/moe.h: argument validation,
+// workspace layout and the launch sequence of each call.  No call allocates
+// device memory or synchronises the stream (moe_read_status excepted).
+#include <cuda_bf16.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool config_valid(const moe_config* c) {
+  if (c == nullptr) return false;
+  if (c->T < 1 || c->d < 64 || c->f < 64 || c->E < 1 || c->k < 1) return false;
+  if (c->E > kMaxE || c->k > kMaxK || c->k > c->E) return false;
+  if (c->d % 64 || c->f % 64) return false;
+  if (c->prec != MOE_BF16 && c->prec != MOE_MXFP8) return false;
+  if (c->prec == MOE_MXFP8 && (c->d % 128 || c->f % 128)) return false;
+  if ((int64_t)c->T * c->k > (int64_t)1 << 28) return false;
+  if (c->minibatch_rows < 0 || (c->minibatch_rows > 0 && c->minibatch_rows % kBM)) return false;
+  if (c->minibatch_rows > 0 && c->ring_slots < 2) return false;
+  return true;
+}
+
+WsLayout ws_layout(const moe_config* c) {
+  WsLayout L;
+  L.R = (int64_t)c->T * c->k;
+  const int64_t nonempty = c->E < L.R ? c->E : L.R;
+  L.Rp_max = (int64_t)align_up((size_t)(L.R + nonempty * (kBM - 1)), kBM);
+  L.MT_max = L.Rp_max / kBM;
+  L.nblk = (c->T + kSchedTokPerBlock - 1) / kSchedTokPerBlock;
+  L.nt_dg = (c->f + 255) / 256;
+  const size_t A = 1024;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, A);
+    return o;
+  };
+  const size_t rp = (size_t)L.Rp_max;
+  L.hdr = take(kHdrWords * sizeof(int));
+  L.hist = take((size_t)L.nblk * c->E * sizeof(int));
+  L.poff = take((size_t)(c->E + 1) * sizeof(int));
+  L.mt_off = take((size_t)(c->E + 1) * sizeof(int));
+  L.pos_pad = take((size_t)L.R * sizeof(int));
+  L.row_of_pad = take(rp * sizeof(int));
+  L.g_pad = take(rp * sizeof(float));
+  L.Xp = take(rp * c->d * 2);     // bf16 rows; MXFP8: e4m3 rows + scales
+  L.Abuf = take(rp * c->f * 2);   // SwiGLU output when nothing is saved
+  L.Yp = take(rp * c->d * 2);     // expert outputs; backward: dX in expert order
+  L.dYp = take(rp * c->d * 2);
+  L.dH = take(rp * 2 * c->f * 2);
+  L.gA = take(rp * c->f * 2);
+  L.dgp = take(rp * L.nt_dg * sizeof(float));
+  L.Aq = take(c->prec == MOE_MXFP8 ? rp * c->f + rp * (c->f / 32) : 0);
+  L.ring = 0;
+  L.total = off;
+  return L;
+}
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+static bool aligned(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 127) == 0; }
+
+static bool sched_ok(const moe_sched& s) {
+  return aligned(s.topk_ids) && aligned(s.topk_w) && aligned(s.counts) && aligned(s.offsets) &&
+         aligned(s.perm) && aligned(s.inv);
+}
+
+static moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_workspace_bytes(const moe_config* cfg) {
+  if (!config_valid(cfg)) return 0;
+  return ws_layout(cfg).total;
+}
+
+int64_t moe_saved_rows(const moe_config* cfg) {
+  if (!config_valid(cfg)) return 0;
+  return ws_layout(cfg).Rp_max;
+}
+
+int32_t moe_min_minibatch(int32_t compute_sms, int32_t bm, int32_t bn, int32_t n_cols) {
+  if (compute_sms <= 0 || bm <= 0 || bn <= 0 || n_cols <= 0) return 0;
+  const int64_t num = 2ll * compute_sms * bm * bn;
+  const int64_t v = (num + n_cols - 1) / n_cols;
+  return v > INT32_MAX ? INT32_MAX : (int32_t)v;
+}
+
+moe_status moe_schedule(const moe_config* cfg, const float* logits, moe_sched sched, void* ws,
+                        size_t ws_bytes, moe_stream_t stream) {
+  if (!config_valid(cfg) || !aligned(logits) || !sched_ok(sched) || !aligned(ws))
+    return MOE_ERR_INVALID_ARG;
+  Ws w;
+  w.L = ws_layout(cfg);
+  w.base = static_cast<uint8_t*>(ws);
+  if (ws_bytes < w.L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return cuda_status(launch_schedule(*cfg, logits, sched, w, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_quantize_mxfp8(const moe_bf16* w, int64_t batch, int32_t K, int32_t N, uint8_t* q,
+                              uint8_t* scales, moe_stream_t stream) {
+  if (!aligned(w) || !aligned(q) || !aligned(scales) || batch < 1 || K < 128 || N < 64 ||
+      K % 128 || N % 64)
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_quantize_mxfp8(reinterpret_cast<const __nv_bfloat16*>(w), batch, K, N,
+                                           q, scales, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_forward(const moe_config* cfg, const moe_bf16* x, const void* w1,
+                       const uint8_t* w1_scales, const void* w2, const uint8_t* w2_scales,
+                       moe_sched sched, moe_bf16* out, const moe_saved* saved, void* ws,
+                       size_t ws_bytes, moe_stream_t stream) {
+  if (!config_valid(cfg) || !aligned(x) || !aligned(w1) || !aligned(w2) || !aligned(out) ||
+      !sched_ok(sched) || !aligned(ws))
+    return MOE_ERR_INVALID_ARG;
+  if (saved != nullptr && (!aligned(saved->H) || !aligned(saved->A))) return MOE_ERR_INVALID_ARG;
+  Ws W;
+  W.L = ws_layout(cfg);
+  W.base = static_cast<uint8_t*>(ws);
+  if (ws_bytes < W.L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const moe_config& c = *cfg;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (c.prec == MOE_MXFP8) return MOE_ERR_UNSUPPORTED;
+  if (w1_scales != nullptr || w2_scales != nullptr) return MOE_ERR_INVALID_ARG;
+  if (c.minibatch_rows > 0) return MOE_ERR_UNSUPPORTED;
+
+  auto* Xp = static_cast<__nv_bfloat16*>(W.at(W.L.Xp));
+  auto* A = saved ? reinterpret_cast<__nv_bfloat16*>(saved->A)
+                  : static_cast<__nv_bfloat16*>(W.at(W.L.Abuf));
+  auto* H = saved ? reinterpret_cast<__nv_bfloat16*>(saved->H) : nullptr;
+  auto* Yp = static_cast<__nv_bfloat16*>(W.at(W.L.Yp));
+  cudaError_t e = launch_gather(c, W, reinterpret_cast<const __nv_bfloat16*>(x), Xp, nullptr,
+                                nullptr, st);
+  if (e == cudaSuccess)
+    e = gemm_fwd1(c, W, Xp, static_cast<const __nv_bfloat16*>(w1), A, H, st);
+  if (e == cudaSuccess) e = gemm_fwd2(c, W, A, static_cast<const __nv_bfloat16*>(w2), Yp, st);
+  if (e == cudaSuccess)
+    e = launch_merge(c, W, Yp, sched.topk_w, reinterpret_cast<__nv_bfloat16*>(out), st);
+  return cuda_status(e);
+}
+
+moe_status moe_backward(const moe_config* cfg, const moe_bf16* dout, const moe_bf16* x,
+                        const moe_bf16* w1, const moe_bf16* w2, moe_sched sched,
+                        const moe_saved* saved, moe_bf16* dx, moe_bf16* dw1, moe_bf16* dw2,
+                        float* dtopk_w, float* dlogits, void* ws, size_t ws_bytes,
+                        moe_stream_t stream) {
+  if (!config_valid(cfg) || !aligned(dout) || !aligned(x) || !aligned(w1) || !aligned(w2) ||
+      !sched_ok(sched) || !aligned(dx) || !aligned(dw1) || !aligned(dw2) || !aligned(dtopk_w) ||
+      !aligned(ws))
+    return MOE_ERR_INVALID_ARG;
+  if (dlogits != nullptr && !aligned(dlogits)) return MOE_ERR_INVALID_ARG;
+  if (saved == nullptr || !aligned(saved->H) || !aligned(saved->A)) return MOE_ERR_INVALID_ARG;
+  if (cfg->prec != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  Ws W;
+  W.L = ws_layout(cfg);
+  W.base = static_cast<uint8_t*>(ws);
+  if (ws_bytes < W.L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const moe_config& c = *cfg;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  auto bf = [](const moe_bf16* p) { return reinterpret_cast<const __nv_bfloat16*>(p); };
+  auto* Xp = static_cast<__nv_bfloat16*>(W.at(W.L.Xp));
+  auto* dYp = static_cast<__nv_bfloat16*>(W.at(W.L.dYp));
+  auto* dH = static_cast<__nv_bfloat16*>(W.at(W.L.dH));
+  auto* gA = static_cast<__nv_bfloat16*>(W.at(W.L.gA));
+  auto* dXp = static_cast<__nv_bfloat16*>(W.at(W.L.Yp));
+  auto* dgp = static_cast<float*>(W.at(W.L.dgp));
+  const auto* Hs = reinterpret_cast<const __nv_bfloat16*>(saved->H);
+  const auto* As = reinterpret_cast<const __nv_bfloat16*>(saved->A);
+
+  cudaError_t e = launch_gather(c, W, bf(x), Xp, bf(dout), dYp, st);
+  if (e == cudaSuccess) e = gemm_dgrad2(c, W, dYp, bf(w2), Hs, As, dH, gA, dgp, st);
+  if (e == cudaSuccess) e = launch_dg_reduce(c, W, sched, dtopk_w, dlogits, st);
+  if (e == cudaSuccess)
+    e = gemm_wgrad(c, W, sched, gA, c.f, dYp, c.d, reinterpret_cast<__nv_bfloat16*>(dw2), st);
+  if (e == cudaSuccess)
+    e = gemm_wgrad(c, W, sched, Xp, c.d, dH, 2 * c.f, reinterpret_cast<__nv_bfloat16*>(dw1), st);
+  if (e == cudaSuccess) e = gemm_dgrad1(c, W, dH, bf(w1), dXp, st);
+  if (e == cudaSuccess) e = launch_merge(c, W, dXp, nullptr, reinterpret_cast<__nv_bfloat16*>(dx), st);
+  return cuda_status(e);
+}
+
+moe_status moe_read_status(const void* ws, moe_stream_t stream) {
+  if (!aligned(ws)) return MOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  int h[2] = {0, 0};
+  if (cudaMemcpy(h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  return static_cast<moe_status>(h[0]);
+}
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_DEVICE_CHECK: return "device bounds check failed";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,306 @@
+// gather_merge.cu -- the memory-bound steps of the layer.
+//
+//  * gather (dispatch by pull, leiphone "MoK..." section 02): the expert side
+//    reads each routed token row from its source position and lays rows out
+//    in expert order.  On one GPU this is an HBM row gather into the padded
+//    expert-ordered buffer (padding rows are written as zeros).
+//  * merge (combine + final weighted merge, leiphone section 03): each token
+//    sums its k expert outputs in slot order in fp32 and rounds once to bf16.
+//    The same kernel without weights is the backward's reverse dispatch.
+//  * dg reduce: the routing-weight gradient, summed from the per-tile partials
+//    of the fused SwiGLU backward (Marktechpost "Cursor开源MoK..." three design
+//    decisions, last paragraph), and its softmax backward to the logits.
+//  * MXFP8 quantisation (leiphone section 02, MXFP8 paragraph): fused into the
+//    gather for activations; a separate pass for weights.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void stg_v4(void* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// One warp per padded row; 16-byte vectors; up to 4 loads in flight per lane.
+__global__ void __launch_bounds__(256) gather_kernel(const __nv_bfloat16* __restrict__ src,
+                                                     __nv_bfloat16* __restrict__ dst,
+                                                     const __nv_bfloat16* __restrict__ src2,
+                                                     __nv_bfloat16* __restrict__ dst2,
+                                                     const int* __restrict__ row_of_pad,
+                                                     const int* __restrict__ hdr, int k, int d) {
+  const int rows = hdr[kHdrRpTotal];
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  const int nvec = d >> 3;
+  for (int pp = gw; pp < rows; pp += nw) {
+    const int r = row_of_pad[pp];
+    for (int pass = 0; pass < 2; ++pass) {
+      const __nv_bfloat16* s = pass ? src2 : src;
+      __nv_bfloat16* o = pass ? dst2 : dst;
+      if (o == nullptr) break;
+      const uint4* sv = reinterpret_cast<const uint4*>(s + (size_t)(r < 0 ? 0 : r / k) * d);
+      uint4* ov = reinterpret_cast<uint4*>(o + (size_t)pp * d);
+      for (int v0 = lane; v0 < nvec; v0 += 32 * 4) {
+        uint4 buf[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int v = v0 + u * 32;
+          buf[u] = (r >= 0 && v < nvec) ? ldg_nc_v4(sv + v) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int v = v0 + u * 32;
+          if (v < nvec) stg_v4(ov + v, buf[u]);
+        }
+      }
+    }
+  }
+}
+
+// UE8M0 scale of a block with max |v| = amax (fp32 bits): the smallest s with
+// amax <= 448 * 2^s, clamped to [-127, 127]; amax = 0 (or fp32-subnormal) -> -127.
+__device__ __forceinline__ int mx_scale_exp(float amax) {
+  const uint32_t b = __float_as_uint(amax);
+  const int eb = (int)((b >> 23) & 0xFF);
+  if (eb == 0) return -127;
+  const uint32_t mant = b & 0x7FFFFFu;
+  // amax = m * 2^q with m in [0.5, 1): q = eb - 126, m <= 0.875 <=> mant <= 0x600000
+  int s = (eb - 126) - ((mant <= 0x600000u) ? 9 : 8);
+  return max(-127, min(127, s));
+}
+
+__device__ __forceinline__ float exp2i(int s) {  // 2^s for s in [-127, 127], exact
+  return (s >= -126) ? __uint_as_float((uint32_t)(s + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+// Quantise 32 bf16 values (4 x uint4) to e4m3 with one UE8M0 scale.
+__device__ __forceinline__ void quant32(const uint4 (&in)[4], uint4 (&out)[2], uint8_t& scale) {
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&in[i]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __bfloat1622float2(h[j]);
+      v[i * 8 + j * 2] = f.x;
+      v[i * 8 + j * 2 + 1] = f.y;
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const int s = mx_scale_exp(amax);
+  scale = (uint8_t)(s + 127);
+  // 2^-s may not be representable as one fp32 for s = -127: scale in two steps
+  const int s1 = -s / 2, s2 = -s - s1;
+  const float f1 = exp2i(s1), f2 = exp2i(s2);
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    w[i] = pack_e4m3x4(v[4 * i] * f1 * f2, v[4 * i + 1] * f1 * f2, v[4 * i + 2] * f1 * f2,
+                       v[4 * i + 3] * f1 * f2);
+  out[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  out[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// Gather + quantise: one warp per padded row, each lane one block of 32.
+__global__ void __launch_bounds__(256) gather_mxfp8_kernel(const __nv_bfloat16* __restrict__ src,
+                                                           uint8_t* __restrict__ q,
+                                                           uint8_t* __restrict__ sc,
+                                                           const int* __restrict__ row_of_pad,
+                                                           const int* __restrict__ hdr, int k,
+                                                           int d) {
+  const int rows = hdr[kHdrRpTotal];
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  const int nblk = d >> 5;
+  for (int pp = gw; pp < rows; pp += nw) {
+    const int r = row_of_pad[pp];
+    const uint4* sv = reinterpret_cast<const uint4*>(src + (size_t)(r < 0 ? 0 : r / k) * d);
+    for (int b = lane; b < nblk; b += 32) {
+      uint4 in[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) in[i] = (r >= 0) ? ldg_nc_v4(sv + b * 4 + i) : make_uint4(0, 0, 0, 0);
+      uint4 out[2];
+      uint8_t s;
+      quant32(in, out, s);
+      uint4* qv = reinterpret_cast<uint4*>(q + (size_t)pp * d + b * 32);
+      stg_v4(qv, out[0]);
+      stg_v4(qv + 1, out[1]);
+      sc[(size_t)pp * nblk + b] = s;
+    }
+  }
+}
+
+// Weights [batch, K, N] bf16 -> codes [batch, N, K] and scales [batch, N, K/32].
+// One thread per (batch, n, 32-block of K): reads a strided column block.
+__global__ void __launch_bounds__(256) quant_weights_kernel(const __nv_bfloat16* __restrict__ w,
+                                                            int64_t batch, int K, int N,
+                                                            uint8_t* __restrict__ q,
+                                                            uint8_t* __restrict__ sc) {
+  const int nkb = K >> 5;
+  const int64_t total = batch * (int64_t)N * nkb;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    // consecutive threads take consecutive n so the strided reads coalesce
+    const int n = (int)(i % N);
+    const int64_t rest = i / N;
+    const int kb = (int)(rest % nkb);
+    const int64_t b = rest / nkb;
+    const __nv_bfloat16* col = w + (b * K + (int64_t)kb * 32) * N + n;
+    uint4 in[4];
+    uint16_t* hv = reinterpret_cast<uint16_t*>(in);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) hv[j] = __bfloat16_as_ushort(col[(int64_t)j * N]);
+    uint4 out[2];
+    uint8_t s;
+    quant32(in, out, s);
+    uint4* qv = reinterpret_cast<uint4*>(q + (b * N + n) * (int64_t)K + kb * 32);
+    stg_v4(qv, out[0]);
+    stg_v4(qv + 1, out[1]);
+    sc[(b * N + n) * (int64_t)nkb + kb] = s;
+  }
+}
+
+// One CTA per token (grid-stride); each thread owns 8-column vectors.
+__global__ void __launch_bounds__(128) merge_kernel(const __nv_bfloat16* __restrict__ rows,
+                                                    const int* __restrict__ pos_pad,
+                                                    const float* __restrict__ w, int T, int k,
+                                                    int d, __nv_bfloat16* __restrict__ out) {
+  __shared__ int sp[kMaxK];
+  __shared__ float sw[kMaxK];
+  const int nvec = d >> 3;
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    __syncthreads();
+    if (threadIdx.x < k) {
+      sp[threadIdx.x] = pos_pad[(size_t)t * k + threadIdx.x];
+      sw[threadIdx.x] = w ? w[(size_t)t * k + threadIdx.x] : 1.f;
+    }
+    __syncthreads();
+    for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+      for (int j = 0; j < k; ++j) {
+        const uint4 y = ldg_nc_v4(rows + (size_t)sp[j] * d + (size_t)v * 8);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&y);
+        const float g = sw[j];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __bfloat1622float2(h[i]);
+          if (w) {
+            acc[2 * i] = fmaf(g, f.x, acc[2 * i]);
+            acc[2 * i + 1] = fmaf(g, f.y, acc[2 * i + 1]);
+          } else {
+            acc[2 * i] += f.x;
+            acc[2 * i + 1] += f.y;
+          }
+        }
+      }
+      uint4 o;
+      __nv_bfloat162 p0 = __floats2bfloat162_rn(acc[0], acc[1]);
+      __nv_bfloat162 p1 = __floats2bfloat162_rn(acc[2], acc[3]);
+      __nv_bfloat162 p2 = __floats2bfloat162_rn(acc[4], acc[5]);
+      __nv_bfloat162 p3 = __floats2bfloat162_rn(acc[6], acc[7]);
+      o.x = *reinterpret_cast<uint32_t*>(&p0);
+      o.y = *reinterpret_cast<uint32_t*>(&p1);
+      o.z = *reinterpret_cast<uint32_t*>(&p2);
+      o.w = *reinterpret_cast<uint32_t*>(&p3);
+      stg_v4(out + (size_t)t * d + (size_t)v * 8, o);
+    }
+  }
+}
+
+// One warp per token: dg[t,j] = sum of the fused-epilogue partials (tile
+// order), dlogits = g_l (dg_l - sum_j g_j dg_j) at the selected experts.
+__global__ void __launch_bounds__(256) dg_reduce_kernel(
+    const float* __restrict__ dgp, int nt, const int* __restrict__ pos_pad,
+    const float* __restrict__ w, const int* __restrict__ ids, int T, int k, int E,
+    float* __restrict__ dtopk_w, float* __restrict__ dlogits) {
+  const int lane = threadIdx.x & 31;
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (t >= T) return;
+  float dg = 0.f, g = 0.f;
+  int id = 0;
+  if (lane < k) {
+    const int pp = pos_pad[(size_t)t * k + lane];
+    for (int n = 0; n < nt; ++n) dg += dgp[(size_t)pp * nt + n];
+    g = w[(size_t)t * k + lane];
+    id = ids[(size_t)t * k + lane];
+    dtopk_w[(size_t)t * k + lane] = dg;
+  }
+  if (dlogits == nullptr) return;
+  float s = 0.f;
+  for (int j = 0; j < k; ++j) s += __shfl_sync(0xffffffffu, g * dg, j);
+  float* row = dlogits + (size_t)t * E;
+  for (int e = lane; e < E; e += 32) row[e] = 0.f;
+  __syncwarp();
+  if (lane < k) row[id] = g * (dg - s);
+}
+
+}  // namespace
+
+cudaError_t launch_gather(const moe_config& c, const Ws& ws, const __nv_bfloat16* src,
+                          __nv_bfloat16* dst, const __nv_bfloat16* src2, __nv_bfloat16* dst2,
+                          cudaStream_t st) {
+  const int grid = num_sms() * 8;
+  gather_kernel<<<grid, 256, 0, st>>>(src, dst, src2, dst2, ws.row_of_pad(), ws.hdr(), c.k, c.d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_mxfp8(const moe_config& c, const Ws& ws, const __nv_bfloat16* src,
+                                uint8_t* q, uint8_t* sc, cudaStream_t st) {
+  const int grid = num_sms() * 8;
+  gather_mxfp8_kernel<<<grid, 256, 0, st>>>(src, q, sc, ws.row_of_pad(), ws.hdr(), c.k, c.d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge(const moe_config& c, const Ws& ws, const __nv_bfloat16* rows,
+                         const float* w, __nv_bfloat16* out, cudaStream_t st) {
+  const int grid = c.T < num_sms() * 16 ? c.T : num_sms() * 16;
+  merge_kernel<<<grid, 128, 0, st>>>(rows, ws.pos_pad(), w, c.T, c.k, c.d, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dg_reduce(const moe_config& c, const Ws& ws, const moe_sched& s,
+                             float* dtopk_w, float* dlogits, cudaStream_t st) {
+  const int grid = (c.T * 32 + 255) / 256;
+  dg_reduce_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const float*>(ws.at(ws.L.dgp)),
+                                          (int)ws.L.nt_dg, ws.pos_pad(), s.topk_w, s.topk_ids,
+                                          c.T, c.k, c.E, dtopk_w, dlogits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_mxfp8(const __nv_bfloat16* w, int64_t batch, int K, int N, uint8_t* q,
+                                  uint8_t* sc, cudaStream_t st) {
+  const int64_t total = batch * (int64_t)N * (K / 32);
+  int64_t blocks = (total + 255) / 256;
+  const int64_t cap = (int64_t)num_sms() * 16;
+  if (blocks > cap) blocks = cap;
+  quant_weights_kernel<<<(int)blocks, 256, 0, st>>>(w, batch, K, N, q, sc);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

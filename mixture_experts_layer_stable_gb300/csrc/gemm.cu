@@ -1,0 +1,568 @@
+// gemm.cu -- grouped expert GEMMs on the 5th-generation tensor cores (tcgen05).
+//
+// The expert FFN is a grouped GEMM over each expert's contiguous rows, fed to
+// the tensor cores (leiphone "MoK..." sections 01 and 02); its SwiGLU and the
+// SwiGLU backward with the routing-weight gradient are fused into the GEMM
+// epilogues (Marktechpost "Cursor开源MoK..." three design decisions).
+//
+// One persistent kernel template, one CTA per SM (192 threads):
+//   warp 0      TMA producer: 64-wide K slices of A and B into a 4-stage ring
+//               of 128-byte-swizzled shared-memory tiles (mbarrier full/empty)
+//   warp 1      TMEM allocator and MMA issuer: one thread issues
+//               tcgen05.mma.cta_group::1.kind::f16 (128 x N x 16, bf16 -> fp32)
+//               into one of two TMEM accumulators (2 x 256 columns), commits
+//               to the stage's "empty" barrier and, per tile, to "tmem full"
+//   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter, fused math,
+//               stores (TMA tensor stores through swizzled staging tiles, or
+//               direct vector stores), then "tmem empty"
+// Tiles (all modes 128 rows x up to 256 columns):
+//   ROWS   forward / dgrad: M tiles are 128-row blocks of the padded
+//          expert-ordered buffer (one expert each), N tiles across the output,
+//          K = d, f or 2f.  Tile order: expert, then N tile, then M tile, so
+//          tiles sharing an expert's weight slice run side by side.
+//   WGRAD  weight gradients: per expert e, an (M x N) grid of tiles of
+//          dW[e] = A_e^T B_e with K = the expert's rows (zero-padded to 64);
+//          experts without rows produce zero tiles.
+// Every wait is bounded (%globaltimer); on expiry the CTA records
+// MOE_ERR_TIMEOUT in the workspace status word, stops, drains its in-flight
+// copies and MMAs, frees TMEM and returns.
+#include <cuda_bf16.h>
+
+#include "moe_internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int BK = 64;
+constexpr int kStages = 4;
+constexpr int kABytes = kBM * BK * 2;     // 16 KB
+constexpr int kBBytes = 256 * BK * 2;     // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kThreads = 192;
+constexpr int kEpiWarps = 4;
+constexpr int kOutTile = 32 * 128;        // 32 rows x 64 bf16, swizzled staging tile
+constexpr int kTmemCols = 512;
+
+enum Epi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2 };
+
+struct Params {
+  int E;
+  int num_kb;      // ROWS: K / 64
+  int n_tiles;     // tiles along N
+  int m_tiles_w;   // WGRAD: tiles along M
+  int umma_n;      // MMA N (64..256)
+  int hn;          // SWIGLU: gate (and up) columns per tile
+  int f;
+  int out_cols;    // output width (stores starting at or past it are skipped)
+  int out_rows;    // WGRAD: output height
+  const int* mt_off;  // ROWS: [E+1] prefix of 128-row tiles per expert
+  const int* counts;  // WGRAD: [E] rows per expert
+  const int* poff;    // WGRAD: [E+1] padded row prefix
+  __nv_bfloat16* out0;  // SWIGLU: A [rows, f]      DSWIGLU: dH [rows, 2f]
+  __nv_bfloat16* out1;  // SWIGLU: H [rows, 2f] / 0 DSWIGLU: gA [rows, f]
+  const __nv_bfloat16* Hs;  // DSWIGLU: saved H
+  const __nv_bfloat16* As;  // DSWIGLU: saved A
+  const float* g_pad;       // DSWIGLU: routing weight per padded row
+  float* dgp;               // DSWIGLU: [rows, n_tiles] partial <dA', A>
+  int* status;
+};
+
+template <int EPI>
+constexpr size_t smem_bytes() {
+  return 1024 + (size_t)kStages * kStageBytes + (EPI == EPI_STORE ? kEpiWarps * 2 * kOutTile : 0) +
+         256;
+}
+
+struct Tile {
+  int e, m, n, kb_count, row0, krow0;
+};
+
+__device__ __forceinline__ int find_expert(const int* off, int E, int key) {
+  // largest e in [0, E) with off[e] <= key
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(off + mid) <= key) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <bool WGRAD>
+__device__ __forceinline__ int total_tiles(const Params& p) {
+  if (WGRAD) return p.E * p.m_tiles_w * p.n_tiles;
+  return __ldg(p.mt_off + p.E) * p.n_tiles;
+}
+
+template <bool WGRAD>
+__device__ __forceinline__ Tile decode(const Params& p, int L) {
+  Tile t;
+  if (!WGRAD) {
+    const int e = find_expert(p.mt_off, p.E, L / p.n_tiles);
+    const int m0 = __ldg(p.mt_off + e);
+    const int me = __ldg(p.mt_off + e + 1) - m0;
+    const int loc = L - m0 * p.n_tiles;
+    t.e = e;
+    t.n = loc / me;
+    t.m = m0 + loc % me;
+    t.row0 = t.m * kBM;
+    t.kb_count = p.num_kb;
+    t.krow0 = 0;
+  } else {
+    const int per = p.m_tiles_w * p.n_tiles;
+    t.e = L / per;
+    const int loc = L - t.e * per;
+    t.m = loc % p.m_tiles_w;
+    t.n = loc / p.m_tiles_w;
+    t.kb_count = (__ldg(p.counts + t.e) + BK - 1) / BK;
+    t.krow0 = __ldg(p.poff + t.e);
+    t.row0 = 0;
+  }
+  return t;
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+__device__ __forceinline__ void unpack8(const uint4& v, float* o) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    o[2 * i] = f.x;
+    o[2 * i + 1] = f.y;
+  }
+}
+
+// Store 32 fp32 as bf16 (64 bytes) to a 64-byte-aligned global address.
+__device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const float* v) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 w;
+    w.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
+    w.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
+    w.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
+    w.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
+    d[i] = w;
+  }
+}
+
+__device__ __forceinline__ void load32_bf16(const __nv_bfloat16* src, float* v) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) unpack8(__ldg(s + i), v + 8 * i);
+}
+
+template <bool WGRAD, bool A_MN, bool B_MN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmO, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* stages = smem;
+  uint8_t* staging = smem + (size_t)kStages * kStageBytes;
+  uint8_t* ctrl = staging + (EPI == EPI_STORE ? kEpiWarps * 2 * kOutTile : 0);
+  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], kEpiWarps * 32);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    if (EPI == EPI_STORE) tma_prefetch_desc(&tmO);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = total_tiles<WGRAD>(p);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      const uint32_t b_bytes = B_MN ? (uint32_t)(p.umma_n / 64) * 8192u : (uint32_t)kBBytes;
+      const int nbox = p.umma_n / 64;
+      int s = 0;
+      uint32_t ph = 0, used = 0, last_par = 0;
+      for (int L = blockIdx.x; L < total; L += gridDim.x) {
+        const Tile t = decode<WGRAD>(p, L);
+        for (int kb = 0; kb < t.kb_count; ++kb) {
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status, 100 + s)) goto producer_done;
+          const uint32_t sa = smem_u32(stages + (size_t)s * kStageBytes);
+          const uint32_t sb = sa + kABytes;
+          const uint32_t fb = smem_u32(&full[s]);
+          mbar_arrive_expect_tx(&full[s], (uint32_t)kABytes + b_bytes);
+          if (!A_MN) {
+            tma_load_2d(sa, &tmA, fb, kb * BK, t.row0);
+          } else {
+            const int kr = t.krow0 + kb * BK;
+            tma_load_2d(sa, &tmA, fb, t.m * kBM, kr);
+            tma_load_2d(sa + 8192, &tmA, fb, t.m * kBM + 64, kr);
+          }
+          if (WGRAD) {
+            const int kr = t.krow0 + kb * BK;
+            for (int i = 0; i < nbox; ++i) tma_load_2d(sb + i * 8192, &tmB, fb, t.n * 256 + 64 * i, kr);
+          } else if (B_MN) {
+            for (int i = 0; i < nbox; ++i) {
+              int col;
+              if (EPI == EPI_SWIGLU) {
+                const int half = nbox / 2;
+                col = (i < half) ? t.n * p.hn + 64 * i : p.f + t.n * p.hn + 64 * (i - half);
+              } else {
+                col = t.n * 256 + 64 * i;
+              }
+              tma_load_3d(sb + i * 8192, &tmB, fb, col, kb * BK, t.e);
+            }
+          } else {
+            tma_load_3d(sb, &tmB, fb, kb * BK, t.n * 256, t.e);
+          }
+          used |= 1u << s;
+          last_par = (last_par & ~(1u << s)) | (ph << s);
+          if (++s == kStages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+    producer_done:
+      // every issued copy has landed before the CTA can exit
+      for (int i = 0; i < kStages; ++i)
+        if ((used >> i) & 1u) mbar_wait_drain(&full[i], (last_par >> i) & 1u);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      const uint32_t idesc = idesc_bf16(kBM, p.umma_n, A_MN, B_MN);
+      int s = 0, acc = 0;
+      uint32_t ph = 0, aph = 0;
+      for (int L = blockIdx.x; L < total; L += gridDim.x) {
+        const Tile t = decode<WGRAD>(p, L);
+        if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, p.status, 200 + acc)) goto mma_done;
+        tc_fence_after();
+        const uint32_t dt = tmem_base + (uint32_t)acc * 256u;
+        for (int kb = 0; kb < t.kb_count; ++kb) {
+          if (!mbar_wait(&full[s], ph, abort_flag, p.status, 300 + s)) goto mma_done;
+          tc_fence_after();
+          const uint32_t sa = smem_u32(stages + (size_t)s * kStageBytes);
+          const uint32_t sb = sa + kABytes;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = A_MN ? sdesc_sw128(sa + kk * 2048, 8192, 1024)
+                                     : sdesc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, 8192, 1024)
+                                     : sdesc_sw128(sb + kk * 32, 16, 1024);
+            tc_mma_f16(dt, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&empty[s]));
+          if (++s == kStages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        tc_commit(smem_u32(&tfull[acc]));
+        if (++acc == 2) {
+          acc = 0;
+          aph ^= 1u;
+        }
+      }
+    mma_done:
+      // all issued MMAs complete before TMEM is released
+      tc_commit(smem_u32(drain));
+      mbar_wait_drain(drain, 0);
+    }
+  } else {
+    // -------------------------------------------------- epilogue warps
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int acc = 0, buf = 0;
+    uint32_t aph = 0;
+    const uint32_t stg = smem_u32(staging) + (uint32_t)(warp - 2) * 2u * kOutTile;
+    for (int L = blockIdx.x; L < total; L += gridDim.x) {
+      const Tile t = decode<WGRAD>(p, L);
+      if (!mbar_wait(&tfull[acc], aph, abort_flag, p.status, 400 + acc)) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + (uint32_t)acc * 256u + ((uint32_t)(q * 32) << 16);
+      const bool zero = (t.kb_count == 0);
+
+      if constexpr (EPI == EPI_STORE) {
+        const int row = (WGRAD ? t.m * kBM : t.row0) + q * 32;
+        for (int c = 0; c < p.umma_n / 64; ++c) {
+          float v[64];
+          if (!zero) {
+            tmem_ld32(tb + c * 64, v);
+            tmem_ld32(tb + c * 64 + 32, v + 32);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) v[i] = 0.f;
+          }
+          const int col = t.n * 256 + c * 64;
+          if (col >= p.out_cols || (WGRAD && row >= p.out_rows)) continue;
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+          const uint32_t sbuf = stg + (uint32_t)buf * kOutTile;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            st_shared_v4(sbuf + lane * 128 + ((j ^ (lane & 7)) << 4),
+                         pack_bf16x2(v[8 * j + 0], v[8 * j + 1]),
+                         pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                         pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
+                         pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (WGRAD) tma_store_3d(&tmO, sbuf, col, row, t.e);
+            else tma_store_2d(&tmO, sbuf, col, row);
+            bulk_commit();
+          }
+          buf ^= 1;
+        }
+      } else if constexpr (EPI == EPI_SWIGLU) {
+        const size_t row = (size_t)t.row0 + q * 32 + lane;
+        for (int c = 0; c < p.hn; c += 32) {
+          float g[32], u[32], a[32];
+          tmem_ld32(tb + c, g);
+          tmem_ld32(tb + p.hn + c, u);
+          const int col = t.n * p.hn + c;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) a[i] = silu_f(g[i]) * u[i];
+          store32_bf16(p.out0 + row * p.f + col, a);
+          if (p.out1 != nullptr) {
+            store32_bf16(p.out1 + row * (2 * p.f) + col, g);
+            store32_bf16(p.out1 + row * (2 * p.f) + p.f + col, u);
+          }
+        }
+      } else {
+        // EPI_DSWIGLU: acc = dA' = dOut_p W2^T for f columns [n*256, n*256+256)
+        const size_t row = (size_t)t.row0 + q * 32 + lane;
+        const float gw = p.g_pad[row];
+        float dg = 0.f;
+        for (int c = 0; c < 256; c += 32) {
+          const int col = t.n * 256 + c;
+          if (col >= p.f) break;
+          float da[32], av[32], hg[32], hu[32], o1[32], o2[32], o3[32];
+          tmem_ld32(tb + c, da);
+          load32_bf16(p.As + row * p.f + col, av);
+          load32_bf16(p.Hs + row * (2 * p.f) + col, hg);
+          load32_bf16(p.Hs + row * (2 * p.f) + p.f + col, hu);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            dg = fmaf(da[i], av[i], dg);
+            const float dA = gw * da[i];
+            const float sg = 1.0f / (1.0f + __expf(-hg[i]));
+            o1[i] = dA * hu[i] * sg * (1.0f + hg[i] * (1.0f - sg));  // d gate
+            o2[i] = dA * hg[i] * sg;                                // d up
+            o3[i] = gw * av[i];                                     // g * A (for dW2)
+          }
+          store32_bf16(p.out0 + row * (2 * p.f) + col, o1);
+          store32_bf16(p.out0 + row * (2 * p.f) + p.f + col, o2);
+          store32_bf16(p.out1 + row * p.f + col, o3);
+        }
+        p.dgp[row * p.n_tiles + t.n] = dg;
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        aph ^= 1u;
+      }
+    }
+    if (EPI == EPI_STORE && lane == 0) bulk_wait<0>();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// bf16 2-D map: `cols` contiguous elements per row, `rows` rows.
+bool map2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+           uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// bf16 3-D map over a stack [d2][d1][d0] (d0 contiguous).
+bool map3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0,
+           uint32_t b1) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  cuuint32_t box[3] = {b0, b1, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool WGRAD, bool A_MN, bool B_MN, int EPI>
+cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
+                   const Params& p, long long max_tiles, cudaStream_t st) {
+  auto kern = grouped_gemm_kernel<WGRAD, A_MN, B_MN, EPI>;
+  const size_t smem = smem_bytes<EPI>();
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  long long grid = num_sms();
+  if (max_tiles < grid) grid = max_tiles;
+  if (grid < 1) grid = 1;
+  kern<<<(int)grid, kThreads, smem, st>>>(a, b, o, p);
+  return cudaGetLastError();
+}
+
+Params base_params(const moe_config& c, const Ws& ws) {
+  Params p{};
+  p.E = c.E;
+  p.f = c.f;
+  p.mt_off = ws.mt_off();
+  p.poff = ws.poff();
+  p.status = ws.hdr() + kHdrStatus;
+  return p;
+}
+
+}  // namespace
+
+cudaError_t gemm_fwd1(const moe_config& c, const Ws& ws, const __nv_bfloat16* Xp,
+                      const __nv_bfloat16* W1, __nv_bfloat16* A, __nv_bfloat16* H, cudaStream_t st) {
+  CUtensorMap ta, tb, to;
+  const uint64_t rows = (uint64_t)ws.L.Rp_max;
+  Params p = base_params(c, ws);
+  p.hn = (c.f % 128 == 0) ? 128 : 64;
+  p.umma_n = 2 * p.hn;
+  p.n_tiles = c.f / p.hn;
+  p.num_kb = c.d / BK;
+  p.out_cols = c.f;
+  p.out0 = A;
+  p.out1 = H;
+  if (!map2d(&ta, Xp, c.d, rows, 64, kBM) || !map3d(&tb, W1, 2ull * c.f, c.d, c.E, 64, 64))
+    return cudaErrorInvalidValue;
+  to = tb;
+  return launch<false, false, true, EPI_SWIGLU>(ta, tb, to, p, ws.L.MT_max * p.n_tiles, st);
+}
+
+cudaError_t gemm_fwd2(const moe_config& c, const Ws& ws, const __nv_bfloat16* A,
+                      const __nv_bfloat16* W2, __nv_bfloat16* Yp, cudaStream_t st) {
+  CUtensorMap ta, tb, to;
+  const uint64_t rows = (uint64_t)ws.L.Rp_max;
+  Params p = base_params(c, ws);
+  p.umma_n = 256;
+  p.n_tiles = (c.d + 255) / 256;
+  p.num_kb = c.f / BK;
+  p.out_cols = c.d;
+  if (!map2d(&ta, A, c.f, rows, 64, kBM) || !map3d(&tb, W2, c.d, c.f, c.E, 64, 64) ||
+      !map2d(&to, Yp, c.d, rows, 64, 32))
+    return cudaErrorInvalidValue;
+  return launch<false, false, true, EPI_STORE>(ta, tb, to, p, ws.L.MT_max * p.n_tiles, st);
+}
+
+cudaError_t gemm_dgrad2(const moe_config& c, const Ws& ws, const __nv_bfloat16* dYp,
+                        const __nv_bfloat16* W2, const __nv_bfloat16* Hs, const __nv_bfloat16* As,
+                        __nv_bfloat16* dH, __nv_bfloat16* gA, float* dgp, cudaStream_t st) {
+  CUtensorMap ta, tb, to;
+  const uint64_t rows = (uint64_t)ws.L.Rp_max;
+  Params p = base_params(c, ws);
+  p.umma_n = 256;
+  p.n_tiles = (int)ws.L.nt_dg;
+  p.num_kb = c.d / BK;
+  p.out_cols = c.f;
+  p.out0 = dH;
+  p.out1 = gA;
+  p.Hs = Hs;
+  p.As = As;
+  p.g_pad = ws.g_pad();
+  p.dgp = dgp;
+  // B = W2[e]^T: K = d contiguous, N = f rows -> K-major box of 256 rows
+  if (!map2d(&ta, dYp, c.d, rows, 64, kBM) || !map3d(&tb, W2, c.d, c.f, c.E, 64, 256))
+    return cudaErrorInvalidValue;
+  to = tb;
+  return launch<false, false, false, EPI_DSWIGLU>(ta, tb, to, p, ws.L.MT_max * p.n_tiles, st);
+}
+
+cudaError_t gemm_dgrad1(const moe_config& c, const Ws& ws, const __nv_bfloat16* dH,
+                        const __nv_bfloat16* W1, __nv_bfloat16* dXp, cudaStream_t st) {
+  CUtensorMap ta, tb, to;
+  const uint64_t rows = (uint64_t)ws.L.Rp_max;
+  Params p = base_params(c, ws);
+  p.umma_n = 256;
+  p.n_tiles = (c.d + 255) / 256;
+  p.num_kb = 2 * c.f / BK;
+  p.out_cols = c.d;
+  // B = W1[e]^T: K = 2f contiguous, N = d rows
+  if (!map2d(&ta, dH, 2ull * c.f, rows, 64, kBM) ||
+      !map3d(&tb, W1, 2ull * c.f, c.d, c.E, 64, 256) || !map2d(&to, dXp, c.d, rows, 64, 32))
+    return cudaErrorInvalidValue;
+  return launch<false, false, false, EPI_STORE>(ta, tb, to, p, ws.L.MT_max * p.n_tiles, st);
+}
+
+cudaError_t gemm_wgrad(const moe_config& c, const Ws& ws, const moe_sched& s,
+                       const __nv_bfloat16* Amn, int M, const __nv_bfloat16* Bmn, int N,
+                       __nv_bfloat16* dW, cudaStream_t st) {
+  CUtensorMap ta, tb, to;
+  const uint64_t rows = (uint64_t)ws.L.Rp_max;
+  Params p = base_params(c, ws);
+  p.umma_n = 256;
+  p.m_tiles_w = (M + kBM - 1) / kBM;
+  p.n_tiles = (N + 255) / 256;
+  p.out_cols = N;
+  p.out_rows = M;
+  p.counts = s.counts;
+  if (!map2d(&ta, Amn, M, rows, 64, 64) || !map2d(&tb, Bmn, N, rows, 64, 64) ||
+      !map3d(&to, dW, N, M, c.E, 64, 32))
+    return cudaErrorInvalidValue;
+  return launch<true, true, true, EPI_STORE>(ta, tb, to, p,
+                                             (long long)c.E * p.m_tiles_w * p.n_tiles, st);
+}
+
+}  // namespace moe

@@ -1,0 +1,89 @@
+// moe_internal.h -- workspace layout and kernel launchers shared by the
+// translation units of libmoe.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kBM = 128;           // rows of an expert tile; expert segments are padded to it
+constexpr int kSchedTokPerBlock = 64;
+constexpr int kSchedThreads = 256;
+constexpr int kMaxE = 1024;
+constexpr int kMaxK = 32;
+
+// Header words at the start of the workspace.
+enum HdrWord {
+  kHdrStatus = 0,     // device status (moe_status code), first error wins
+  kHdrWhere = 1,      // which wait / check reported it
+  kHdrDone = 2,       // schedule: blocks finished (last-block ticket)
+  kHdrRpTotal = 4,    // padded rows of all experts (multiple of kBM)
+  kHdrMtTotal = 5,    // kRpTotal / kBM
+  kHdrInject = 8,     // fault-injection word for tests of the bounded waits
+  kHdrWords = 64
+};
+
+struct WsLayout {
+  int64_t R = 0, Rp_max = 0, MT_max = 0, nblk = 0, nt_dg = 0;
+  size_t hdr = 0, hist = 0, poff = 0, mt_off = 0, pos_pad = 0, row_of_pad = 0, g_pad = 0;
+  size_t Xp = 0, Abuf = 0, Yp = 0, dYp = 0, dH = 0, gA = 0, dgp = 0, Aq = 0, ring = 0;
+  size_t total = 0;
+};
+
+bool config_valid(const moe_config* c);
+WsLayout ws_layout(const moe_config* c);
+
+// Pointers into a workspace, typed.
+struct Ws {
+  WsLayout L;
+  uint8_t* base = nullptr;
+  int* hdr() const { return reinterpret_cast<int*>(base + L.hdr); }
+  int* hist() const { return reinterpret_cast<int*>(base + L.hist); }
+  int* poff() const { return reinterpret_cast<int*>(base + L.poff); }
+  int* mt_off() const { return reinterpret_cast<int*>(base + L.mt_off); }
+  int* pos_pad() const { return reinterpret_cast<int*>(base + L.pos_pad); }
+  int* row_of_pad() const { return reinterpret_cast<int*>(base + L.row_of_pad); }
+  float* g_pad() const { return reinterpret_cast<float*>(base + L.g_pad); }
+  void* at(size_t off) const { return base + off; }
+};
+
+int num_sms();
+
+// ---- launchers (return a cudaError_t from the launch) ----
+cudaError_t launch_schedule(const moe_config& c, const float* logits, const moe_sched& s,
+                            const Ws& ws, cudaStream_t st);
+// dst[pp] = src[row_of_pad[pp] / k] (zero rows for padding), pp < Rp_total.
+cudaError_t launch_gather(const moe_config& c, const Ws& ws, const __nv_bfloat16* src,
+                          __nv_bfloat16* dst, const __nv_bfloat16* src2, __nv_bfloat16* dst2,
+                          cudaStream_t st);
+// MXFP8 gather: e4m3 codes [Rp, d] and UE8M0 scales [Rp, d/32].
+cudaError_t launch_gather_mxfp8(const moe_config& c, const Ws& ws, const __nv_bfloat16* src,
+                                uint8_t* q, uint8_t* sc, cudaStream_t st);
+// out[t] = sum_j w[t,j] * rows[pos_pad[t*k+j]] (w == nullptr: plain sum).
+cudaError_t launch_merge(const moe_config& c, const Ws& ws, const __nv_bfloat16* rows,
+                         const float* w, __nv_bfloat16* out, cudaStream_t st);
+cudaError_t launch_dg_reduce(const moe_config& c, const Ws& ws, const moe_sched& s,
+                             float* dtopk_w, float* dlogits, cudaStream_t st);
+cudaError_t launch_quantize_mxfp8(const __nv_bfloat16* w, int64_t batch, int K, int N, uint8_t* q,
+                                  uint8_t* sc, cudaStream_t st);
+
+// Grouped GEMMs on tcgen05 (gemm.cu).
+cudaError_t gemm_fwd1(const moe_config& c, const Ws& ws, const __nv_bfloat16* Xp,
+                      const __nv_bfloat16* W1, __nv_bfloat16* A, __nv_bfloat16* H, cudaStream_t st);
+cudaError_t gemm_fwd2(const moe_config& c, const Ws& ws, const __nv_bfloat16* A,
+                      const __nv_bfloat16* W2, __nv_bfloat16* Yp, cudaStream_t st);
+cudaError_t gemm_dgrad2(const moe_config& c, const Ws& ws, const __nv_bfloat16* dYp,
+                        const __nv_bfloat16* W2, const __nv_bfloat16* Hs, const __nv_bfloat16* As,
+                        __nv_bfloat16* dH, __nv_bfloat16* gA, float* dgp, cudaStream_t st);
+cudaError_t gemm_dgrad1(const moe_config& c, const Ws& ws, const __nv_bfloat16* dH,
+                        const __nv_bfloat16* W1, __nv_bfloat16* dXp, cudaStream_t st);
+cudaError_t gemm_wgrad(const moe_config& c, const Ws& ws, const moe_sched& s,
+                       const __nv_bfloat16* Amn, int M, const __nv_bfloat16* Bmn, int N,
+                       __nv_bfloat16* dW, cudaStream_t st);
+
+}  // namespace moe

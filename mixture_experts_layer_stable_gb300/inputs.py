@@ -32,7 +32,7 @@ def zipf_bias(E: int, s: float) -> torch.Tensor:
 
 
 def make_inputs(cfg, device="cpu", seed: int = 0, with_grad: bool = True,
-                x_std=None):
+                x_std=None, parts=("logits", "x", "W1", "W2", "dOut")):
     if isinstance(cfg, str):
         cfg = CONFIGS[cfg]
     assert isinstance(cfg, LayerConfig)
@@ -42,20 +42,27 @@ def make_inputs(cfg, device="cpu", seed: int = 0, with_grad: bool = True,
     def gen(i):
         return torch.Generator(device=dev).manual_seed(seed + i)
 
-    logits = torch.randn(T, E, generator=gen(0), device=dev) * cfg.logit_std
-    if cfg.zipf > 0:
-        logits = logits + zipf_bias(E, cfg.zipf).to(dev)
-    xs = (1.0 / math.sqrt(d)) if x_std is None else x_std
-    x = (torch.randn(T, d, generator=gen(1), device=dev) * xs).to(torch.bfloat16)
-    g2 = gen(2)
-    W1 = torch.empty(E, d, 2 * f, dtype=torch.bfloat16, device=dev)
-    for e in range(E):
-        W1[e] = (torch.randn(d, 2 * f, generator=g2, device=dev) / math.sqrt(d)).to(torch.bfloat16)
-    g3 = gen(3)
-    W2 = torch.empty(E, f, d, dtype=torch.bfloat16, device=dev)
-    for e in range(E):
-        W2[e] = (torch.randn(f, d, generator=g3, device=dev) / math.sqrt(f)).to(torch.bfloat16)
-    out = {"logits": logits.contiguous(), "x": x, "W1": W1, "W2": W2}
-    if with_grad:
+    out = {}
+    if "logits" in parts:
+        logits = torch.randn(T, E, generator=gen(0), device=dev) * cfg.logit_std
+        if cfg.zipf > 0:
+            logits = logits + zipf_bias(E, cfg.zipf).to(dev)
+        out["logits"] = logits.contiguous()
+    if "x" in parts:
+        xs = (1.0 / math.sqrt(d)) if x_std is None else x_std
+        out["x"] = (torch.randn(T, d, generator=gen(1), device=dev) * xs).to(torch.bfloat16)
+    if "W1" in parts:
+        g2 = gen(2)
+        W1 = torch.empty(E, d, 2 * f, dtype=torch.bfloat16, device=dev)
+        for e in range(E):
+            W1[e] = (torch.randn(d, 2 * f, generator=g2, device=dev) / math.sqrt(d)).to(torch.bfloat16)
+        out["W1"] = W1
+    if "W2" in parts:
+        g3 = gen(3)
+        W2 = torch.empty(E, f, d, dtype=torch.bfloat16, device=dev)
+        for e in range(E):
+            W2[e] = (torch.randn(f, d, generator=g3, device=dev) / math.sqrt(f)).to(torch.bfloat16)
+        out["W2"] = W2
+    if with_grad and "dOut" in parts:
         out["dOut"] = torch.randn(T, d, generator=gen(4), device=dev).to(torch.bfloat16)
     return out
