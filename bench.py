@@ -1,0 +1,454 @@
+#!/usr/bin/env python
+"""Benchmark of the single-GPU MoE layer (routing -> schedule -> gather ->
+grouped SwiGLU FFN -> weighted merge, forward and backward) on GB300.
+
+One step = moe_schedule + moe_forward (saving activations) + moe_backward on
+one batch of seeded synthetic input already resident in HBM.  Prints ONE JSON
+line (rank 0).  `--impl reference` times the fp64 CPU oracle instead, on a
+bounded sample of the same workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload balanced]
+  python -m torch.distributed.run --nproc-per-node N bench.py --gpus N ...
+
+With N > 1 every rank runs an independent replica of the layer (the layer has
+no exchange step on one GPU); value = routed tokens of all ranks / max time.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer fwd/bwd ms, TFLOP/s and routed tokens/s; % of tensor peak and HBM BW"
+UNIT = "routed tokens/s"
+
+# kernel -> (unit kind, per-step algorithmic amount as a function of the workload)
+#   flop: 2*M*N*K of the real (unpadded) rows; bytes: one read of each input
+#   row and one write of each output row.
+def kernel_units(c):
+    R, T, d, f, k = c["T"] * c["k"], c["T"], c["d"], c["f"], c["k"]
+    return {
+        "gemm1_swiglu": ("flop", 2.0 * R * d * 2 * f),
+        "gemm2": ("flop", 2.0 * R * f * d),
+        "dgrad2_dswiglu": ("flop", 2.0 * R * d * f),
+        "wgrad2": ("flop", 2.0 * R * f * d),
+        "wgrad1": ("flop", 2.0 * R * d * 2 * f),
+        "dgrad1": ("flop", 2.0 * R * 2 * f * d),
+        "gather": ("bytes", 2.0 * R * d * 2),
+        "gather_x_dy": ("bytes", 4.0 * R * d * 2),
+        "merge": ("bytes", T * (k + 1) * d * 2.0 + R * 4.0 * 2),
+        "reverse_dispatch": ("bytes", T * (k + 1) * d * 2.0 + R * 4.0),
+    }
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            m = json.load(fh)
+        return {"hbm_gbs": m["hbm_gbs"], "bf16": m["bf16_tflops"],
+                "bf16_sustained": m.get("bf16_tflops_sustained", m["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+def src_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mixture_experts_layer_stable_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(name.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload, kernel):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken on
+    the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        tab = json.load(fh)
+    ent = tab.get(f"{workload}/{kernel}")
+    if not ent or ent.get("src_digest") != src_digest():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu):
+        self.gpu = gpu
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)], stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        rows = [l.strip().split(", ") for l in self.out.read().splitlines() if l.strip()]
+        os.unlink(self.out.name)
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = max(mx, float(r[2]))
+                for nm, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(nm)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def workload_dict(cfg):
+    return {"T": cfg.T, "d": cfg.d, "f": cfg.f, "E": cfg.E, "k": cfg.k}
+
+
+# --------------------------------------------------------------- the oracle
+def oracle_sample(cfg, n_experts, seed=0):
+    """CPU inputs of the workload for the first n_experts experts (the same
+    seeded draws as the full workload) -- used only by the CPU baseline."""
+    import torch
+    from mixture_experts_layer_stable_gb300.inputs import make_inputs
+    inp = make_inputs(cfg, device="cpu", seed=seed, parts=("logits", "x", "dOut"))
+    w = make_inputs(cfg, device="cpu", seed=seed, parts=("W1", "W2"), experts=n_experts)
+    inp.update(w)
+    return inp
+
+
+def oracle_step(cfg, inp, experts):
+    """One oracle pass over a sample: routing + schedule for every token,
+    then forward + backward of every row routed to `experts`.  Returns the
+    number of routed rows processed."""
+    import numpy as np
+    import torch
+    from oracle import moe_oracle as O
+
+    class View:
+        def __init__(self, t):
+            self.t = t
+
+        def __len__(self):
+            return cfg.E
+
+        def __getitem__(self, e):
+            return self.t[e].to(torch.float64).numpy()
+
+    ids, g = O.route(inp["logits"].numpy(), cfg.k)
+    counts, offsets, perm, inv = O.schedule(ids, cfg.E)
+    x = inp["x"].to(torch.float64).numpy()
+    dO = inp["dOut"].to(torch.float64).numpy()
+    O.backward_experts(x, View(inp["W1"]), View(inp["W2"]), ids, g, dO, list(experts))
+    return int(sum(int(counts[e]) for e in experts))
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def time_oracle(cfg, budget_s, steps=1, warmup=0):
+    """Pick the sample (first n experts) so that one oracle pass takes about
+    budget_s, run warmup + steps passes, return (rows/s, sample description)."""
+    inp = oracle_sample(cfg, 2)
+    oracle_step(cfg, inp, range(1))           # first call: BLAS start-up
+    t0 = time.perf_counter()
+    rows1 = oracle_step(cfg, inp, range(2))
+    t1 = max(time.perf_counter() - t0, 1e-3)
+    per_row = t1 / max(rows1, 1)
+    avg_rows = cfg.T * cfg.k / cfg.E
+    n = int(max(1, min(cfg.E, budget_s / (per_row * avg_rows))))
+    inp = oracle_sample(cfg, n)
+    experts = range(n)
+    for _ in range(warmup):
+        oracle_step(cfg, inp, experts)
+    rows = 0
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        rows += oracle_step(cfg, inp, experts)
+    dt = time.perf_counter() - t0
+    desc = (f"routing + schedule of all {cfg.T} tokens, then forward+backward (fp64 numpy) of the "
+            f"rows routed to experts 0..{n - 1} of {cfg.E}; {rows // max(steps, 1)} routed rows per pass")
+    return rows / dt, desc, dt
+
+
+# --------------------------------------------------------------- main
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="balanced")
+    ap.add_argument("--passes", default=None, help="fwd or fwd+bwd (default: fwd+bwd)")
+    ap.add_argument("--minibatch-rows", type=int, default=0)
+    ap.add_argument("--ring-slots", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    return ap.parse_args()
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args, cfg, rank):
+    if rank != 0:
+        return
+    budget = 0.5 if args.steps + args.warmup <= 200 else max(0.05, 100.0 / (args.steps + args.warmup))
+    v, desc, dt = time_oracle(cfg, budget, steps=args.steps, warmup=args.warmup)
+    cores = blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * dt / max(args.steps, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded torch generators; no dataset)",
+        "config": {"workload": cfg.name, **workload_dict(cfg), "passes": "fwd+bwd"},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup()
+    from mixture_experts_layer_stable_gb300.configs import CONFIGS
+    cfg = CONFIGS[args.workload]
+    passes = args.passes or "fwd+bwd"
+    if args.impl == "reference":
+        run_reference(args, cfg, rank)
+        return
+
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from mixture_experts_layer_stable_gb300 import binding as B
+    from mixture_experts_layer_stable_gb300.inputs import make_inputs
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    prec = B.MOE_MXFP8 if cfg.prec == "mxfp8" else B.MOE_BF16
+    c = B.make_config(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, prec, args.minibatch_rows,
+                      args.ring_slots, 0)
+    inp = make_inputs(cfg, device="cuda", seed=0, with_grad=(passes != "fwd"))
+    sched = B.alloc_sched(c)
+    ws = B.alloc_workspace(c)
+    saved = B.alloc_saved(c) if passes != "fwd" else None
+    out = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device="cuda")
+    bwd = passes != "fwd"
+    if bwd:
+        dx = torch.empty_like(out)
+        dW1 = torch.empty_like(inp["W1"])
+        dW2 = torch.empty_like(inp["W2"])
+        dtw = torch.empty(cfg.T * cfg.k, dtype=torch.float32, device="cuda")
+        dlog = torch.empty(cfg.T, cfg.E, dtype=torch.float32, device="cuda")
+
+    def step(logits=inp["logits"], x=inp["x"], dOut=inp.get("dOut")):
+        B.moe_schedule(c, logits, sched, ws)
+        B.moe_forward(c, x, inp["W1"], None, inp["W2"], None, sched, out, saved, ws)
+        if bwd:
+            B.moe_backward(c, dOut, x, inp["W1"], inp["W2"], sched, saved, dx, dW1, dW2, dtw, dlog, ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = B.moe_read_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {B.moe_status_string(st)}")
+
+    # ---------------- timed region (device-resident inputs)
+    B.moe_trace_enable(0)
+    B.moe_trace_enable(64 * args.steps + 64)
+    gpu_idx = local
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        try:
+            gpu_idx = int(vis.split(",")[local])
+        except ValueError:
+            pass
+    clocks = ClockSampler(gpu_idx)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for _ in range(args.steps):
+        step()
+    ev1.record()
+    barrier()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    n_launch = B.moe_trace_count()
+    per = {}
+    for i in range(n_launch):
+        name, kms = B.moe_trace_read(i)
+        a = per.setdefault(name, [0, 0.0])
+        a[0] += 1
+        a[1] += kms
+    B.moe_trace_enable(0)
+    st = B.moe_read_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status after timed region: {B.moe_status_string(st)}")
+    ms_max = ms
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    R = cfg.T * cfg.k
+    value = R * args.steps * world / (ms_max / 1000.0)
+    ms_step = ms_max / args.steps
+
+    # ---------------- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host = {k: inp[k].cpu().pin_memory() for k in (("logits", "x", "dOut") if bwd else ("logits", "x"))}
+        dev_in = {k: torch.empty_like(inp[k]) for k in host}
+        h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        h_dx = torch.empty(out.shape, dtype=out.dtype, pin_memory=True) if bwd else None
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = h_out.numel() * 2 + (h_dx.numel() * 2 if bwd else 0)
+        k_e2e = args.e2e_steps or max(10, args.steps // 4)
+
+        def e2e_step():
+            for k_, t in host.items():
+                dev_in[k_].copy_(t, non_blocking=True)
+            step(dev_in["logits"], dev_in["x"], dev_in.get("dOut"))
+            h_out.copy_(out, non_blocking=True)
+            if bwd:
+                h_dx.copy_(dx, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(k_e2e):
+            e2e_step()
+        e1.record()
+        barrier()
+        ems = e0.elapsed_time(e1)
+        if dist is not None:
+            t = torch.tensor([ems], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": R * k_e2e * world / (ems / 1000.0), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": k_e2e}
+
+    # ---------------- per-kernel roofline
+    peaks = load_peaks()
+    units = kernel_units(workload_dict(cfg))
+    kernels = {}
+    for name, (cnt, tot) in per.items():
+        avg = tot / cnt
+        ent = {"launches": cnt, "ms_per_launch": avg, "share": tot / max(sum(v[1] for v in per.values()), 1e-9)}
+        if name in units:
+            kind, amount = units[name]
+            if kind == "flop":
+                ent["TFLOP/s"] = amount / (avg / 1e3) / 1e12
+            else:
+                ent["GB/s"] = amount / (avg / 1e3) / 1e9
+        kernels[name] = ent
+    dom = max(per.items(), key=lambda kv: kv[1][1])[0]
+    kind, amount = units.get(dom, ("flop", 0.0))
+    avg = per[dom][1] / per[dom][0]
+    if kind == "flop":
+        achieved = amount / (avg / 1e3) / 1e12
+        peak = peaks["bf16_sustained"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": ncu_traffic(cfg.name, dom), "kernel": dom,
+                "algorithmic_per_launch": amount,
+                "peak_source": f"{peaks['source']} bf16 sustained (MEASURED_PEAKS.json)"}
+    else:
+        achieved = amount / (avg / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": ncu_traffic(cfg.name, dom), "kernel": dom,
+                "algorithmic_per_launch": amount, "peak_source": f"{peaks['source']} hbm"}
+    fwd_names = ("gather", "gather_mxfp8", "gemm1_swiglu", "gemm2", "merge")
+    sched_names = ("sched_topk", "sched_scatter")
+    fwd_ms = sum(per[n][1] for n in per if n in fwd_names) / args.steps
+    sch_ms = sum(per[n][1] for n in per if n in sched_names) / args.steps
+    bwd_ms = sum(per[n][1] for n in per if n not in fwd_names + sched_names) / args.steps
+    flops = (6.0 if not bwd else 18.0) * R * cfg.d * cfg.f
+
+    # ---------------- CPU baseline: the oracle on a bounded sample
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, desc, dt = time_oracle(cfg, 12.0, steps=1)
+        cpu = {"value": v, "unit": UNIT, "cores": blas_threads(), "kind": "oracle", "sample": desc,
+               "seconds": dt}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded torch generators on device; no dataset, random-init weights)",
+        "config": {"workload": cfg.name, **workload_dict(cfg), "passes": passes,
+                   "minibatch_rows": args.minibatch_rows,
+                   "l2": "inputs larger than L2 (weights %.2f GB per step)" % (
+                       (inp["W1"].numel() + inp["W2"].numel()) * 2 / 1e9),
+                   "parallelism": f"replicas x{world}"},
+        "tflops": flops / (ms_step / 1e3) / 1e12,
+        "sched_ms": sch_ms, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+        "roofline": roof, "kernels": kernels,
+        "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": int(n_launch), "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -172,6 +172,18 @@ moe_status moe_read_status(const void* ws, moe_stream_t stream);
 /* Static English name of a status code. */
 const char* moe_status_string(moe_status s);
 
+/* Tracing (profiling aid; the pages describe none).  moe_trace_enable(n)
+ * creates 2n CUDA events on the current device; from then on every kernel the
+ * library launches records one event before and one after its launch, on the
+ * call's stream, until n launches have been recorded.  moe_trace_enable(0)
+ * turns tracing off and frees the events.  moe_trace_count returns the number
+ * of launches recorded; moe_trace_read(i, ...) waits for launch i's second
+ * event and returns the kernel's static name and its duration in ms.  Tracing
+ * state is process-wide and not thread-safe. */
+moe_status moe_trace_enable(int32_t capacity);
+int32_t moe_trace_count(void);
+moe_status moe_trace_read(int32_t i, const char** name, float* ms);
+
 #ifdef __cplusplus
 }
 #endif

@@ -30,6 +30,7 @@ MOE_MXFP8 = 1
 EXPORTED = [
     "moe_workspace_bytes", "moe_saved_rows", "moe_min_minibatch", "moe_schedule",
     "moe_quantize_mxfp8", "moe_forward", "moe_backward", "moe_read_status", "moe_status_string",
+    "moe_trace_enable", "moe_trace_count", "moe_trace_read",
 ]
 
 
@@ -86,6 +87,12 @@ def lib():
         L.moe_read_status.restype = ctypes.c_int
         L.moe_status_string.argtypes = [ctypes.c_int]
         L.moe_status_string.restype = ctypes.c_char_p
+        L.moe_trace_enable.argtypes = [i32]
+        L.moe_trace_enable.restype = ctypes.c_int
+        L.moe_trace_count.argtypes = []
+        L.moe_trace_count.restype = i32
+        L.moe_trace_read.argtypes = [i32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float)]
+        L.moe_trace_read.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -162,6 +169,21 @@ def moe_backward(cfg, dout, x, w1, w2, sched, saved, dx, dw1, dw2, dtopk_w, dlog
 
 def moe_read_status(ws, stream=None):
     return int(lib().moe_read_status(_ptr(ws), _stream(stream)))
+
+
+def moe_trace_enable(capacity):
+    _check(lib().moe_trace_enable(int(capacity)), "moe_trace_enable")
+
+
+def moe_trace_count():
+    return int(lib().moe_trace_count())
+
+
+def moe_trace_read(i):
+    name = ctypes.c_char_p()
+    ms = ctypes.c_float()
+    _check(lib().moe_trace_read(int(i), ctypes.byref(name), ctypes.byref(ms)), "moe_trace_read")
+    return name.value.decode(), float(ms.value)
 
 
 # ---------------------------------------------------------------- buffers

@@ -82,6 +82,34 @@ static bool sched_ok(const moe_sched& s) {
 
 static moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+namespace {
+struct Trace {
+  int cap = 0, n = 0;
+  cudaEvent_t* ev = nullptr;
+  const char** names = nullptr;
+};
+Trace g_trace;
+
+void trace_free() {
+  for (int i = 0; i < 2 * g_trace.cap; ++i) cudaEventDestroy(g_trace.ev[i]);
+  delete[] g_trace.ev;
+  delete[] g_trace.names;
+  g_trace = Trace();
+}
+}  // namespace
+
+void trace_before(const char* name, cudaStream_t st) {
+  if (g_trace.n >= g_trace.cap) return;
+  g_trace.names[g_trace.n] = name;
+  cudaEventRecord(g_trace.ev[2 * g_trace.n], st);
+}
+
+void trace_after(cudaStream_t st) {
+  if (g_trace.n >= g_trace.cap) return;
+  cudaEventRecord(g_trace.ev[2 * g_trace.n + 1], st);
+  ++g_trace.n;
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -205,6 +233,36 @@ moe_status moe_read_status(const void* ws, moe_stream_t stream) {
   int h[2] = {0, 0};
   if (cudaMemcpy(h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
   return static_cast<moe_status>(h[0]);
+}
+
+moe_status moe_trace_enable(int32_t capacity) {
+  if (capacity < 0 || capacity > (1 << 22)) return MOE_ERR_INVALID_ARG;
+  trace_free();
+  if (capacity == 0) return MOE_OK;
+  g_trace.ev = new cudaEvent_t[2 * (size_t)capacity];
+  g_trace.names = new const char*[capacity];
+  for (int i = 0; i < 2 * capacity; ++i) {
+    if (cudaEventCreate(&g_trace.ev[i]) != cudaSuccess) {
+      g_trace.cap = i / 2;
+      trace_free();
+      return MOE_ERR_CUDA;
+    }
+    g_trace.cap = (i + 1) / 2;
+  }
+  g_trace.cap = capacity;
+  g_trace.n = 0;
+  return MOE_OK;
+}
+
+int32_t moe_trace_count(void) { return g_trace.n; }
+
+moe_status moe_trace_read(int32_t i, const char** name, float* ms) {
+  if (i < 0 || i >= g_trace.n || name == nullptr || ms == nullptr) return MOE_ERR_INVALID_ARG;
+  if (cudaEventSynchronize(g_trace.ev[2 * i + 1]) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaEventElapsedTime(ms, g_trace.ev[2 * i], g_trace.ev[2 * i + 1]) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  *name = g_trace.names[i];
+  return MOE_OK;
 }
 
 const char* moe_status_string(moe_status s) {

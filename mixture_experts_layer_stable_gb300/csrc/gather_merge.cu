@@ -266,6 +266,7 @@ cudaError_t launch_gather(const moe_config& c, const Ws& ws, const __nv_bfloat16
                           __nv_bfloat16* dst, const __nv_bfloat16* src2, __nv_bfloat16* dst2,
                           cudaStream_t st) {
   const int grid = num_sms() * 8;
+  TraceScope ts(dst2 ? "gather_x_dy" : "gather", st);
   gather_kernel<<<grid, 256, 0, st>>>(src, dst, src2, dst2, ws.row_of_pad(), ws.hdr(), c.k, c.d);
   return cudaGetLastError();
 }
@@ -273,6 +274,7 @@ cudaError_t launch_gather(const moe_config& c, const Ws& ws, const __nv_bfloat16
 cudaError_t launch_gather_mxfp8(const moe_config& c, const Ws& ws, const __nv_bfloat16* src,
                                 uint8_t* q, uint8_t* sc, cudaStream_t st) {
   const int grid = num_sms() * 8;
+  TraceScope ts("gather_mxfp8", st);
   gather_mxfp8_kernel<<<grid, 256, 0, st>>>(src, q, sc, ws.row_of_pad(), ws.hdr(), c.k, c.d);
   return cudaGetLastError();
 }
@@ -280,6 +282,7 @@ cudaError_t launch_gather_mxfp8(const moe_config& c, const Ws& ws, const __nv_bf
 cudaError_t launch_merge(const moe_config& c, const Ws& ws, const __nv_bfloat16* rows,
                          const float* w, __nv_bfloat16* out, cudaStream_t st) {
   const int grid = c.T < num_sms() * 16 ? c.T : num_sms() * 16;
+  TraceScope ts(w ? "merge" : "reverse_dispatch", st);
   merge_kernel<<<grid, 128, 0, st>>>(rows, ws.pos_pad(), w, c.T, c.k, c.d, out);
   return cudaGetLastError();
 }
@@ -287,6 +290,7 @@ cudaError_t launch_merge(const moe_config& c, const Ws& ws, const __nv_bfloat16*
 cudaError_t launch_dg_reduce(const moe_config& c, const Ws& ws, const moe_sched& s,
                              float* dtopk_w, float* dlogits, cudaStream_t st) {
   const int grid = (c.T * 32 + 255) / 256;
+  TraceScope ts("dg_reduce", st);
   dg_reduce_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const float*>(ws.at(ws.L.dgp)),
                                           (int)ws.L.nt_dg, ws.pos_pad(), s.topk_w, s.topk_ids,
                                           c.T, c.k, c.E, dtopk_w, dlogits);
@@ -299,6 +303,7 @@ cudaError_t launch_quantize_mxfp8(const __nv_bfloat16* w, int64_t batch, int K, 
   int64_t blocks = (total + 255) / 256;
   const int64_t cap = (int64_t)num_sms() * 16;
   if (blocks > cap) blocks = cap;
+  TraceScope ts("quantize_weights", st);
   quant_weights_kernel<<<(int)blocks, 256, 0, st>>>(w, batch, K, N, q, sc);
   return cudaGetLastError();
 }

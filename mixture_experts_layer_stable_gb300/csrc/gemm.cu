@@ -449,8 +449,8 @@ bool map3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t 
 }
 
 template <bool WGRAD, bool A_MN, bool B_MN, int EPI>
-cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
-                   const Params& p, long long max_tiles, cudaStream_t st) {
+cudaError_t launch(const char* name, const CUtensorMap& a, const CUtensorMap& b,
+                   const CUtensorMap& o, const Params& p, long long max_tiles, cudaStream_t st) {
   auto kern = grouped_gemm_kernel<WGRAD, A_MN, B_MN, EPI>;
   const size_t smem = smem_bytes<EPI>();
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -458,6 +458,7 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap
   long long grid = num_sms();
   if (max_tiles < grid) grid = max_tiles;
   if (grid < 1) grid = 1;
+  TraceScope ts(name, st);
   kern<<<(int)grid, kThreads, smem, st>>>(a, b, o, p);
   return cudaGetLastError();
 }
@@ -489,7 +490,7 @@ cudaError_t gemm_fwd1(const moe_config& c, const Ws& ws, const __nv_bfloat16* Xp
   if (!map2d(&ta, Xp, c.d, rows, 64, kBM) || !map3d(&tb, W1, 2ull * c.f, c.d, c.E, 64, 64))
     return cudaErrorInvalidValue;
   to = tb;
-  return launch<false, false, true, EPI_SWIGLU>(ta, tb, to, p, ws.L.MT_max * p.n_tiles, st);
+  return launch<false, false, true, EPI_SWIGLU>("gemm1_swiglu", ta, tb, to, p, ws.L.MT_max * p.n_tiles, st);
 }
 
 cudaError_t gemm_fwd2(const moe_config& c, const Ws& ws, const __nv_bfloat16* A,
@@ -504,7 +505,7 @@ cudaError_t gemm_fwd2(const moe_config& c, const Ws& ws, const __nv_bfloat16* A,
   if (!map2d(&ta, A, c.f, rows, 64, kBM) || !map3d(&tb, W2, c.d, c.f, c.E, 64, 64) ||
       !map2d(&to, Yp, c.d, rows, 64, 32))
     return cudaErrorInvalidValue;
-  return launch<false, false, true, EPI_STORE>(ta, tb, to, p, ws.L.MT_max * p.n_tiles, st);
+  return launch<false, false, true, EPI_STORE>("gemm2", ta, tb, to, p, ws.L.MT_max * p.n_tiles, st);
 }
 
 cudaError_t gemm_dgrad2(const moe_config& c, const Ws& ws, const __nv_bfloat16* dYp,
@@ -527,7 +528,7 @@ cudaError_t gemm_dgrad2(const moe_config& c, const Ws& ws, const __nv_bfloat16* 
   if (!map2d(&ta, dYp, c.d, rows, 64, kBM) || !map3d(&tb, W2, c.d, c.f, c.E, 64, 256))
     return cudaErrorInvalidValue;
   to = tb;
-  return launch<false, false, false, EPI_DSWIGLU>(ta, tb, to, p, ws.L.MT_max * p.n_tiles, st);
+  return launch<false, false, false, EPI_DSWIGLU>("dgrad2_dswiglu", ta, tb, to, p, ws.L.MT_max * p.n_tiles, st);
 }
 
 cudaError_t gemm_dgrad1(const moe_config& c, const Ws& ws, const __nv_bfloat16* dH,
@@ -543,7 +544,7 @@ cudaError_t gemm_dgrad1(const moe_config& c, const Ws& ws, const __nv_bfloat16* 
   if (!map2d(&ta, dH, 2ull * c.f, rows, 64, kBM) ||
       !map3d(&tb, W1, 2ull * c.f, c.d, c.E, 64, 256) || !map2d(&to, dXp, c.d, rows, 64, 32))
     return cudaErrorInvalidValue;
-  return launch<false, false, false, EPI_STORE>(ta, tb, to, p, ws.L.MT_max * p.n_tiles, st);
+  return launch<false, false, false, EPI_STORE>("dgrad1", ta, tb, to, p, ws.L.MT_max * p.n_tiles, st);
 }
 
 cudaError_t gemm_wgrad(const moe_config& c, const Ws& ws, const moe_sched& s,
@@ -561,7 +562,7 @@ cudaError_t gemm_wgrad(const moe_config& c, const Ws& ws, const moe_sched& s,
   if (!map2d(&ta, Amn, M, rows, 64, 64) || !map2d(&tb, Bmn, N, rows, 64, 64) ||
       !map3d(&to, dW, N, M, c.E, 64, 32))
     return cudaErrorInvalidValue;
-  return launch<true, true, true, EPI_STORE>(ta, tb, to, p,
+  return launch<true, true, true, EPI_STORE>(M == c.f ? "wgrad2" : "wgrad1", ta, tb, to, p,
                                              (long long)c.E * p.m_tiles_w * p.n_tiles, st);
 }
 

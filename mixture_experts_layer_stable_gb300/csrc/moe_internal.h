@@ -54,6 +54,15 @@ struct Ws {
 
 int num_sms();
 
+// Tracing hooks around every kernel launch (no-ops unless moe_trace_enable).
+void trace_before(const char* name, cudaStream_t st);
+void trace_after(cudaStream_t st);
+struct TraceScope {
+  cudaStream_t st;
+  TraceScope(const char* name, cudaStream_t s) : st(s) { trace_before(name, s); }
+  ~TraceScope() { trace_after(st); }
+};
+
 // ---- launchers (return a cudaError_t from the launch) ----
 cudaError_t launch_schedule(const moe_config& c, const float* logits, const moe_sched& s,
                             const Ws& ws, cudaStream_t st);

@@ -208,11 +208,15 @@ cudaError_t launch_schedule(const moe_config& c, const float* logits, const moe_
   const int nblk = (int)ws.L.nblk;
   cudaError_t err = cudaMemsetAsync(ws.hdr(), 0, kHdrWords * sizeof(int), st);
   if (err != cudaSuccess) return err;
-  sched_topk_kernel<<<nblk, kSchedThreads, 0, st>>>(logits, c.T, c.E, c.k, s.topk_ids, s.topk_w,
-                                                     ws.hist(), ws.hdr(), s.counts, s.offsets,
-                                                     ws.poff(), ws.mt_off());
-  err = cudaGetLastError();
+  {
+    TraceScope ts("sched_topk", st);
+    sched_topk_kernel<<<nblk, kSchedThreads, 0, st>>>(logits, c.T, c.E, c.k, s.topk_ids, s.topk_w,
+                                                       ws.hist(), ws.hdr(), s.counts, s.offsets,
+                                                       ws.poff(), ws.mt_off());
+    err = cudaGetLastError();
+  }
   if (err != cudaSuccess) return err;
+  TraceScope ts("sched_scatter", st);
   sched_scatter_kernel<<<nblk, kSchedThreads, 0, st>>>(
       s.topk_ids, s.topk_w, c.T, c.E, c.k, ws.hist(), s.counts, s.offsets, ws.poff(), s.perm,
       s.inv, ws.pos_pad(), ws.row_of_pad(), ws.g_pad());

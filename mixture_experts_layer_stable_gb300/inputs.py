@@ -32,7 +32,7 @@ def zipf_bias(E: int, s: float) -> torch.Tensor:
 
 
 def make_inputs(cfg, device="cpu", seed: int = 0, with_grad: bool = True,
-                x_std=None, parts=("logits", "x", "W1", "W2", "dOut")):
+                x_std=None, parts=("logits", "x", "W1", "W2", "dOut"), experts=None):
     if isinstance(cfg, str):
         cfg = CONFIGS[cfg]
     assert isinstance(cfg, LayerConfig)
@@ -42,6 +42,7 @@ def make_inputs(cfg, device="cpu", seed: int = 0, with_grad: bool = True,
     def gen(i):
         return torch.Generator(device=dev).manual_seed(seed + i)
 
+    nE = E if experts is None else min(E, int(experts))  # first nE experts' weights only
     out = {}
     if "logits" in parts:
         logits = torch.randn(T, E, generator=gen(0), device=dev) * cfg.logit_std
@@ -53,14 +54,14 @@ def make_inputs(cfg, device="cpu", seed: int = 0, with_grad: bool = True,
         out["x"] = (torch.randn(T, d, generator=gen(1), device=dev) * xs).to(torch.bfloat16)
     if "W1" in parts:
         g2 = gen(2)
-        W1 = torch.empty(E, d, 2 * f, dtype=torch.bfloat16, device=dev)
-        for e in range(E):
+        W1 = torch.empty(nE, d, 2 * f, dtype=torch.bfloat16, device=dev)
+        for e in range(nE):
             W1[e] = (torch.randn(d, 2 * f, generator=g2, device=dev) / math.sqrt(d)).to(torch.bfloat16)
         out["W1"] = W1
     if "W2" in parts:
         g3 = gen(3)
-        W2 = torch.empty(E, f, d, dtype=torch.bfloat16, device=dev)
-        for e in range(E):
+        W2 = torch.empty(nE, f, d, dtype=torch.bfloat16, device=dev)
+        for e in range(nE):
             W2[e] = (torch.randn(f, d, generator=g3, device=dev) / math.sqrt(f)).to(torch.bfloat16)
         out["W2"] = W2
     if with_grad and "dOut" in parts:
