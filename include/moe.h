@@ -126,6 +126,28 @@ int32_t moe_min_minibatch(int32_t compute_sms, int32_t bm, int32_t bn, int32_t n
 moe_status moe_schedule(const moe_config* cfg, const float* logits, moe_sched sched,
                         void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* moe_schedule without a workspace.  The pages have no counterpart: this is a
+ * convenience for callers that cannot allocate device memory -- for example a
+ * plugin running inside a host framework that hands it only its input and
+ * output tensors and forbids cudaMalloc after start-up (cudaMalloc may
+ * synchronise the device and bypasses the framework's own allocator).
+ * Computes the same `sched` arrays as moe_schedule, bit for bit, from the same
+ * kernels, whose scratch (status and ticket words, per-block histograms,
+ * padded offsets, row positions) is a 1.5 MiB array in the library's own
+ * device data; every GPU that loads the library holds it until the process
+ * exits.  No device memory is allocated and no allocating routine is called.
+ * Limit: configurations whose schedule scratch exceeds 1.5 MiB return
+ * MOE_ERR_INVALID_ARG; T <= 16384, E <= 256 and T*k <= 65536 always fit.
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * All calls share the one array and leave their contents in it: calls that
+ * overlap on the GPU (different streams, or different host threads, without
+ * ordering between them) race and give undefined results.  The result does
+ * not carry over to moe_forward / moe_backward, which need the workspace
+ * written by moe_schedule. */
+moe_status moe_schedule_noalloc(const moe_config* cfg, const float* logits, moe_sched sched,
+                                moe_stream_t stream);
+
 /* MXFP8 quantisation of weights for the MXFP8 forward ([LP] 02 MXFP8
  * paragraph; [MT] "BF16 and MXFP8 modes").  w: device bf16 [batch, K, N]
  * (a W1 or W2 stack).  Writes q: e4m3 [batch, N, K] (K contiguous) and

@@ -30,7 +30,7 @@ MOE_MXFP8 = 1
 EXPORTED = [
     "moe_workspace_bytes", "moe_saved_rows", "moe_min_minibatch", "moe_schedule",
     "moe_quantize_mxfp8", "moe_forward", "moe_backward", "moe_read_status", "moe_status_string",
-    "moe_trace_enable", "moe_trace_count", "moe_trace_read",
+    "moe_trace_enable", "moe_trace_count", "moe_trace_read", "moe_schedule_noalloc",
 ]
 
 
@@ -93,6 +93,8 @@ def lib():
         L.moe_trace_count.restype = i32
         L.moe_trace_read.argtypes = [i32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float)]
         L.moe_trace_read.restype = ctypes.c_int
+        L.moe_schedule_noalloc.argtypes = [cfgp, vp, moe_sched, vp]
+        L.moe_schedule_noalloc.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -145,6 +147,13 @@ def sched_struct(s):
 def moe_schedule(cfg, logits, sched, ws, stream=None):
     _check(lib().moe_schedule(ctypes.byref(cfg), _ptr(logits), sched_struct(sched), _ptr(ws),
                               ws.numel() * ws.element_size(), _stream(stream)), "moe_schedule")
+
+
+def moe_schedule_noalloc(cfg, logits, sched, stream=None):
+    """moe_schedule for callers that cannot allocate: no workspace argument;
+    the library's built-in 1.5 MiB device scratch is used (calls share it)."""
+    _check(lib().moe_schedule_noalloc(ctypes.byref(cfg), _ptr(logits), sched_struct(sched),
+                                      _stream(stream)), "moe_schedule_noalloc")
 
 
 def moe_quantize_mxfp8(w, batch, K, N, q, scales, stream=None):

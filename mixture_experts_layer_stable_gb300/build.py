@@ -15,7 +15,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe.so")
-SOURCES = ["api.cu", "sched.cu", "gather_merge.cu", "gemm.cu", "ring.cu", "mxfp8_gemm.cu"]
+SOURCES = ["api.cu", "sched.cu", "gather_merge.cu", "gemm.cu", "ring.cu", "mxfp8_gemm.cu",
+           "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xcompiler", "-Wall", "-DNDEBUG"]
