@@ -151,10 +151,14 @@ moe_status moe_schedule_noalloc(const moe_config* cfg, const float* logits, moe_
 /* MXFP8 quantisation of weights for the MXFP8 forward ([LP] 02 MXFP8
  * paragraph; [MT] "BF16 and MXFP8 modes").  w: device bf16 [batch, K, N]
  * (a W1 or W2 stack).  Writes q: e4m3 [batch, N, K] (K contiguous) and
- * scales: UE8M0 [batch, N, K/32], one scale per 32 consecutive K elements
- * (scale 2^s with s the smallest exponent such that the block's max |v| <=
+ * scales: one UE8M0 byte per 32 consecutive K elements (batch*N*K/32 bytes;
+ * scale 2^s with s the smallest exponent such that the block's max |v| <=
  * 448 * 2^s, clamped to [-127, 127]; elements rounded to nearest even with
- * saturation).  K must be a multiple of 128 and N of 64. */
+ * saturation).  Scales are stored in 512-byte tiles, one per 128 rows
+ * (rows = batch*N) x 128 K elements, tiles ordered row-block-major; within a
+ * tile the scale of row r, 32-element block kb is at byte
+ * 16*(r%32) + 4*((r%128)/32) + kb%4 (the order the tensor cores read them).
+ * K and N must be multiples of 128. */
 moe_status moe_quantize_mxfp8(const moe_bf16* w, int64_t batch, int32_t K, int32_t N,
                               uint8_t* q, uint8_t* scales, moe_stream_t stream);
 

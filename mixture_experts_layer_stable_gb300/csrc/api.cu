@@ -146,8 +146,8 @@ moe_status moe_schedule(const moe_config* cfg, const float* logits, moe_sched sc
 
 moe_status moe_quantize_mxfp8(const moe_bf16* w, int64_t batch, int32_t K, int32_t N, uint8_t* q,
                               uint8_t* scales, moe_stream_t stream) {
-  if (!aligned(w) || !aligned(q) || !aligned(scales) || batch < 1 || K < 128 || N < 64 ||
-      K % 128 || N % 64)
+  if (!aligned(w) || !aligned(q) || !aligned(scales) || batch < 1 || K < 128 || N < 128 ||
+      K % 128 || N % 128)
     return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_quantize_mxfp8(reinterpret_cast<const __nv_bfloat16*>(w), batch, K, N,
                                            q, scales, reinterpret_cast<cudaStream_t>(stream)));
@@ -167,9 +167,27 @@ moe_status moe_forward(const moe_config* cfg, const moe_bf16* x, const void* w1,
   if (ws_bytes < W.L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   const moe_config& c = *cfg;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (c.prec == MOE_MXFP8) return MOE_ERR_UNSUPPORTED;
-  if (w1_scales != nullptr || w2_scales != nullptr) return MOE_ERR_INVALID_ARG;
   if (c.minibatch_rows > 0) return MOE_ERR_UNSUPPORTED;
+  if (c.prec == MOE_MXFP8) {
+    if (!aligned(w1_scales) || !aligned(w2_scales)) return MOE_ERR_INVALID_ARG;
+    const size_t rp = (size_t)W.L.Rp_max;
+    auto* Xq = static_cast<uint8_t*>(W.at(W.L.Xp));
+    uint8_t* Xs = Xq + rp * c.d;
+    auto* Aq = static_cast<uint8_t*>(W.at(W.L.Aq));
+    uint8_t* As = Aq + rp * c.f;
+    auto* Yp = static_cast<__nv_bfloat16*>(W.at(W.L.Yp));
+    cudaError_t e = launch_gather_mxfp8(c, W, reinterpret_cast<const __nv_bfloat16*>(x), Xq, Xs, st);
+    if (e == cudaSuccess)
+      e = gemm_fwd1_mx(c, W, Xq, Xs, static_cast<const uint8_t*>(w1), w1_scales, Aq, As,
+                       saved ? reinterpret_cast<__nv_bfloat16*>(saved->A) : nullptr,
+                       saved ? reinterpret_cast<__nv_bfloat16*>(saved->H) : nullptr, st);
+    if (e == cudaSuccess)
+      e = gemm_fwd2_mx(c, W, Aq, As, static_cast<const uint8_t*>(w2), w2_scales, Yp, st);
+    if (e == cudaSuccess)
+      e = launch_merge(c, W, Yp, sched.topk_w, reinterpret_cast<__nv_bfloat16*>(out), st);
+    return cuda_status(e);
+  }
+  if (w1_scales != nullptr || w2_scales != nullptr) return MOE_ERR_INVALID_ARG;
 
   auto* Xp = static_cast<__nv_bfloat16*>(W.at(W.L.Xp));
   auto* A = saved ? reinterpret_cast<__nv_bfloat16*>(saved->A)

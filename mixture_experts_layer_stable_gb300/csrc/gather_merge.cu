@@ -16,6 +16,7 @@
 #include <cuda_fp8.h>
 
 #include "moe_internal.h"
+#include "mx.cuh"
 
 namespace moe {
 
@@ -72,29 +73,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const __nv_bfloat16* __rest
   }
 }
 
-// UE8M0 scale of a block with max |v| = amax (fp32 bits): the smallest s with
-// amax <= 448 * 2^s, clamped to [-127, 127]; amax = 0 (or fp32-subnormal) -> -127.
-__device__ __forceinline__ int mx_scale_exp(float amax) {
-  const uint32_t b = __float_as_uint(amax);
-  const int eb = (int)((b >> 23) & 0xFF);
-  if (eb == 0) return -127;
-  const uint32_t mant = b & 0x7FFFFFu;
-  // amax = m * 2^q with m in [0.5, 1): q = eb - 126, m <= 0.875 <=> mant <= 0x600000
-  int s = (eb - 126) - ((mant <= 0x600000u) ? 9 : 8);
-  return max(-127, min(127, s));
-}
-
-__device__ __forceinline__ float exp2i(int s) {  // 2^s for s in [-127, 127], exact
-  return (s >= -126) ? __uint_as_float((uint32_t)(s + 127) << 23) : __uint_as_float(0x00400000u);
-}
-
-__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
-  const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-  const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
-  return (uint32_t)lo | ((uint32_t)hi << 16);
-}
-
-// Quantise 32 bf16 values (4 x uint4) to e4m3 with one UE8M0 scale.
+// Quantise 32 bf16 values (4 x uint4) to E4M3 codes with one UE8M0 scale.
 __device__ __forceinline__ void quant32(const uint4 (&in)[4], uint4 (&out)[2], uint8_t& scale) {
   float v[32];
 #pragma unroll
@@ -107,21 +86,7 @@ __device__ __forceinline__ void quant32(const uint4 (&in)[4], uint4 (&out)[2], u
       v[i * 8 + j * 2 + 1] = f.y;
     }
   }
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  const int s = mx_scale_exp(amax);
-  scale = (uint8_t)(s + 127);
-  // 2^-s may not be representable as one fp32 for s = -127: scale in two steps
-  const int s1 = -s / 2, s2 = -s - s1;
-  const float f1 = exp2i(s1), f2 = exp2i(s2);
-  uint32_t w[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-    w[i] = pack_e4m3x4(v[4 * i] * f1 * f2, v[4 * i + 1] * f1 * f2, v[4 * i + 2] * f1 * f2,
-                       v[4 * i + 3] * f1 * f2);
-  out[0] = make_uint4(w[0], w[1], w[2], w[3]);
-  out[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  scale = mx_quant32(v, out[0], out[1]);
 }
 
 // Gather + quantise: one warp per padded row, each lane one block of 32.
@@ -149,12 +114,12 @@ __global__ void __launch_bounds__(256) gather_mxfp8_kernel(const __nv_bfloat16* 
       uint4* qv = reinterpret_cast<uint4*>(q + (size_t)pp * d + b * 32);
       stg_v4(qv, out[0]);
       stg_v4(qv + 1, out[1]);
-      sc[(size_t)pp * nblk + b] = s;
+      sc[mx_sf_offset((size_t)pp, b, d >> 7)] = s;
     }
   }
 }
 
-// Weights [batch, K, N] bf16 -> codes [batch, N, K] and scales [batch, N, K/32].
+// Weights [batch, K, N] bf16 -> codes [batch, N, K] and scale tiles over [batch*N, K].
 // One thread per (batch, n, 32-block of K): reads a strided column block.
 __global__ void __launch_bounds__(256) quant_weights_kernel(const __nv_bfloat16* __restrict__ w,
                                                             int64_t batch, int K, int N,
@@ -180,7 +145,7 @@ __global__ void __launch_bounds__(256) quant_weights_kernel(const __nv_bfloat16*
     uint4* qv = reinterpret_cast<uint4*>(q + (b * N + n) * (int64_t)K + kb * 32);
     stg_v4(qv, out[0]);
     stg_v4(qv + 1, out[1]);
-    sc[(b * N + n) * (int64_t)nkb + kb] = s;
+    sc[mx_sf_offset((size_t)(b * N + n), kb, K >> 7)] = s;
   }
 }
 

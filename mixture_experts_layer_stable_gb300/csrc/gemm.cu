@@ -29,23 +29,43 @@
 #include <cuda_bf16.h>
 
 #include "moe_internal.h"
+#include "mx.cuh"
 #include "ptx.cuh"
 
 namespace moe {
 
 namespace {
 
-constexpr int BK = 64;
-constexpr int kStages = 4;
+constexpr int BK = 64;                    // bf16 K elements per stage (128 bytes)
+constexpr int BK8 = 128;                  // fp8 K elements per stage (128 bytes)
 constexpr int kABytes = kBM * BK * 2;     // 16 KB
 constexpr int kBBytes = 256 * BK * 2;     // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kSfBytes = 1536;            // fp8 stage: one A scale tile + two B scale tiles
 constexpr int kThreads = 192;
 constexpr int kEpiWarps = 4;
 constexpr int kOutTile = 32 * 128;        // 32 rows x 64 bf16, swizzled staging tile
 constexpr int kTmemCols = 512;
+constexpr int kTmemSf = 256;              // fp8: per-stage scale columns start here
+constexpr int kTmemSfStride = 16;         // fp8: TMEM columns per stage (A: 4, B: 8; 8-aligned)
 
 enum Epi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2 };
+
+// Pipeline shape per variant.  The fp8 kernels keep one TMEM accumulator
+// (256 columns) and put the per-stage scale factors (16 columns a stage) in
+// the other half; the fp8 store variant has 3 stages to leave room for the
+// store staging tiles.
+template <int EPI, bool FP8>
+struct KCfg {
+  static constexpr int kStages = (FP8 && EPI == EPI_STORE) ? 3 : 4;
+  static constexpr int kAcc = FP8 ? 1 : 2;
+  // scale-tile region rounded to 1024 bytes: the swizzled staging tiles after
+  // it must start on a 1024-byte boundary for the 128-byte swizzle pattern
+  static constexpr size_t kSfRegion = FP8 ? ((size_t)kStages * kSfBytes + 1023) / 1024 * 1024 : 0;
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kSfRegion +
+                                  (EPI == EPI_STORE ? (size_t)kEpiWarps * 2 * kOutTile : 0) + 256;
+  static_assert(kSmem <= 232448, "shared memory budget");
+};
 
 struct Params {
   int E;
@@ -66,14 +86,14 @@ struct Params {
   const __nv_bfloat16* As;  // DSWIGLU: saved A
   const float* g_pad;       // DSWIGLU: routing weight per padded row
   float* dgp;               // DSWIGLU: [rows, n_tiles] partial <dA', A>
+  const uint8_t* sfa;       // FP8: scale tiles of A [rows, K]
+  const uint8_t* sfb;       // FP8: scale tiles of the weight stack [E * b_rows, K]
+  int k_groups;             // FP8: K / 128
+  int b_rows;               // FP8: rows (N) of one expert's weight
+  uint8_t* q_out;           // FP8 SWIGLU: E4M3 codes of A [rows, f]
+  uint8_t* q_sf;            // FP8 SWIGLU: scale tiles of A
   int* status;
 };
-
-template <int EPI>
-constexpr size_t smem_bytes() {
-  return 1024 + (size_t)kStages * kStageBytes + (EPI == EPI_STORE ? kEpiWarps * 2 * kOutTile : 0) +
-         256;
-}
 
 struct Tile {
   int e, m, n, kb_count, row0, krow0;
@@ -155,16 +175,20 @@ __device__ __forceinline__ void load32_bf16(const __nv_bfloat16* src, float* v) 
   for (int i = 0; i < 4; ++i) unpack8(__ldg(s + i), v + 8 * i);
 }
 
-template <bool WGRAD, bool A_MN, bool B_MN, int EPI>
+template <bool WGRAD, bool A_MN, bool B_MN, int EPI, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmO, const Params p) {
+  using Cfg = KCfg<EPI, FP8>;
+  constexpr int kStages = Cfg::kStages;
+  constexpr int kAcc = Cfg::kAcc;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* stages = smem;
-  uint8_t* staging = smem + (size_t)kStages * kStageBytes;
+  uint8_t* sfbuf = smem + (size_t)kStages * kStageBytes;  // fp8 scale tiles, kSfBytes a stage
+  uint8_t* staging = sfbuf + Cfg::kSfRegion;
   uint8_t* ctrl = staging + (EPI == EPI_STORE ? kEpiWarps * 2 * kOutTile : 0);
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
   uint64_t* empty = full + kStages;
@@ -204,7 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------ TMA producer
-      const uint32_t b_bytes = B_MN ? (uint32_t)(p.umma_n / 64) * 8192u : (uint32_t)kBBytes;
+      const uint32_t b_bytes = (B_MN && !FP8) ? (uint32_t)(p.umma_n / 64) * 8192u : (uint32_t)kBBytes;
+      const uint32_t tx = (uint32_t)kABytes + b_bytes + (FP8 ? (uint32_t)kSfBytes : 0u);
       const int nbox = p.umma_n / 64;
       int s = 0;
       uint32_t ph = 0, used = 0, last_par = 0;
@@ -215,30 +240,51 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = smem_u32(stages + (size_t)s * kStageBytes);
           const uint32_t sb = sa + kABytes;
           const uint32_t fb = smem_u32(&full[s]);
-          mbar_arrive_expect_tx(&full[s], (uint32_t)kABytes + b_bytes);
-          if (!A_MN) {
-            tma_load_2d(sa, &tmA, fb, kb * BK, t.row0);
-          } else {
-            const int kr = t.krow0 + kb * BK;
-            tma_load_2d(sa, &tmA, fb, t.m * kBM, kr);
-            tma_load_2d(sa + 8192, &tmA, fb, t.m * kBM + 64, kr);
-          }
-          if (WGRAD) {
-            const int kr = t.krow0 + kb * BK;
-            for (int i = 0; i < nbox; ++i) tma_load_2d(sb + i * 8192, &tmB, fb, t.n * 256 + 64 * i, kr);
-          } else if (B_MN) {
-            for (int i = 0; i < nbox; ++i) {
-              int col;
-              if (EPI == EPI_SWIGLU) {
-                const int half = nbox / 2;
-                col = (i < half) ? t.n * p.hn + 64 * i : p.f + t.n * p.hn + 64 * (i - half);
-              } else {
-                col = t.n * 256 + 64 * i;
-              }
-              tma_load_3d(sb + i * 8192, &tmB, fb, col, kb * BK, t.e);
+          mbar_arrive_expect_tx(&full[s], tx);
+          if constexpr (FP8) {
+            // K-major E4M3 tiles (128 bytes of K per row) plus their scale tiles
+            const int nbt = p.b_rows >> 7;  // 128-row scale tiles per expert
+            int nb0, nb1;
+            tma_load_2d(sa, &tmA, fb, kb * BK8, t.row0);
+            if (EPI == EPI_SWIGLU) {
+              tma_load_3d(sb, &tmB, fb, kb * BK8, t.n * 128, t.e);
+              tma_load_3d(sb + 16384, &tmB, fb, kb * BK8, p.f + t.n * 128, t.e);
+              nb0 = t.n;
+              nb1 = (p.f >> 7) + t.n;
+            } else {
+              tma_load_3d(sb, &tmB, fb, kb * BK8, t.n * 256, t.e);
+              nb0 = 2 * t.n;
+              nb1 = min(2 * t.n + 1, nbt - 1);  // rows past N are zero-filled; any finite scale
             }
+            const uint32_t sf = smem_u32(sfbuf + (size_t)s * kSfBytes);
+            bulk_load(sf, p.sfa + ((size_t)(t.row0 >> 7) * p.k_groups + kb) * 512u, 512u, fb);
+            bulk_load(sf + 512, p.sfb + (((size_t)t.e * nbt + nb0) * p.k_groups + kb) * 512u, 512u, fb);
+            bulk_load(sf + 1024, p.sfb + (((size_t)t.e * nbt + nb1) * p.k_groups + kb) * 512u, 512u, fb);
           } else {
-            tma_load_3d(sb, &tmB, fb, kb * BK, t.n * 256, t.e);
+            if (!A_MN) {
+              tma_load_2d(sa, &tmA, fb, kb * BK, t.row0);
+            } else {
+              const int kr = t.krow0 + kb * BK;
+              tma_load_2d(sa, &tmA, fb, t.m * kBM, kr);
+              tma_load_2d(sa + 8192, &tmA, fb, t.m * kBM + 64, kr);
+            }
+            if (WGRAD) {
+              const int kr = t.krow0 + kb * BK;
+              for (int i = 0; i < nbox; ++i) tma_load_2d(sb + i * 8192, &tmB, fb, t.n * 256 + 64 * i, kr);
+            } else if (B_MN) {
+              for (int i = 0; i < nbox; ++i) {
+                int col;
+                if (EPI == EPI_SWIGLU) {
+                  const int half = nbox / 2;
+                  col = (i < half) ? t.n * p.hn + 64 * i : p.f + t.n * p.hn + 64 * (i - half);
+                } else {
+                  col = t.n * 256 + 64 * i;
+                }
+                tma_load_3d(sb + i * 8192, &tmB, fb, col, kb * BK, t.e);
+              }
+            } else {
+              tma_load_3d(sb, &tmB, fb, kb * BK, t.n * 256, t.e);
+            }
           }
           used |= 1u << s;
           last_par = (last_par & ~(1u << s)) | (ph << s);
@@ -269,13 +315,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t sa = smem_u32(stages + (size_t)s * kStageBytes);
           const uint32_t sb = sa + kABytes;
+          if constexpr (FP8) {
+            // stage the scale tiles into this stage's TMEM columns, then 4 MMAs
+            // of K = 32, each reading its 32-element block's scale byte
+            const uint32_t sf = smem_u32(sfbuf + (size_t)s * kSfBytes);
+            const uint32_t tsa = tmem_base + kTmemSf + (uint32_t)s * kTmemSfStride;
+            const uint32_t tsb = tsa + 8u;
+            tc_cp_32x128b_warpx4(tsa, sdesc_plain(sf, 16, 128));
+            tc_cp_32x128b_warpx4(tsb, sdesc_plain(sf + 512, 16, 128));
+            tc_cp_32x128b_warpx4(tsb + 4u, sdesc_plain(sf + 1024, 16, 128));
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = A_MN ? sdesc_sw128(sa + kk * 2048, 8192, 1024)
-                                     : sdesc_sw128(sa + kk * 32, 16, 1024);
-            const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, 8192, 1024)
-                                     : sdesc_sw128(sb + kk * 32, 16, 1024);
-            tc_mma_f16(dt, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {
+              tc_mma_mxf8(dt, sdesc_sw128(sa + kk * 32, 16, 1024), sdesc_sw128(sb + kk * 32, 16, 1024),
+                          idesc_mxf8(kBM, 256, kk), tsa, tsb, (kb > 0 || kk > 0) ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t ad = A_MN ? sdesc_sw128(sa + kk * 2048, 8192, 1024)
+                                       : sdesc_sw128(sa + kk * 32, 16, 1024);
+              const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, 8192, 1024)
+                                       : sdesc_sw128(sb + kk * 32, 16, 1024);
+              tc_mma_f16(dt, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            }
           }
           tc_commit(smem_u32(&empty[s]));
           if (++s == kStages) {
@@ -284,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tc_commit(smem_u32(&tfull[acc]));
-        if (++acc == 2) {
+        if (++acc == kAcc) {
           acc = 0;
           aph ^= 1u;
         }
@@ -349,7 +411,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int col = t.n * p.hn + c;
 #pragma unroll
           for (int i = 0; i < 32; ++i) a[i] = silu_f(g[i]) * u[i];
-          store32_bf16(p.out0 + row * p.f + col, a);
+          if constexpr (FP8) {
+            // quantise A for the fp8 GEMM2: this thread's 32 columns are one block
+            uint4 lo, hi;
+            const uint8_t sc = mx_quant32(a, lo, hi);
+            uint4* qd = reinterpret_cast<uint4*>(p.q_out + row * p.f + col);
+            qd[0] = lo;
+            qd[1] = hi;
+            p.q_sf[mx_sf_offset(row, col >> 5, p.f >> 7)] = sc;
+          }
+          if (p.out0 != nullptr) store32_bf16(p.out0 + row * p.f + col, a);
           if (p.out1 != nullptr) {
             store32_bf16(p.out1 + row * (2 * p.f) + col, g);
             store32_bf16(p.out1 + row * (2 * p.f) + p.f + col, u);
@@ -385,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
-      if (++acc == 2) {
+      if (++acc == kAcc) {
         acc = 0;
         aph ^= 1u;
       }
@@ -420,39 +491,40 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// bf16 2-D map: `cols` contiguous elements per row, `rows` rows.
+// 2-D map (bf16, or bytes for fp8): `cols` contiguous elements per row, `rows` rows.
 bool map2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-           uint32_t box_rows) {
+           uint32_t box_rows, bool bytes = false) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
+  cuuint64_t strides[1] = {cols * (bytes ? 1 : 2)};
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+  return fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// bf16 3-D map over a stack [d2][d1][d0] (d0 contiguous).
+// 3-D map over a stack [d2][d1][d0] (d0 contiguous; bf16, or bytes for fp8).
 bool map3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0,
-           uint32_t b1) {
+           uint32_t b1, bool bytes = false) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
+  const uint64_t es_b = bytes ? 1 : 2;
   cuuint64_t dims[3] = {d0, d1, d2};
-  cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  cuuint64_t strides[2] = {d0 * es_b, d0 * d1 * es_b};
   cuuint32_t box[3] = {b0, b1, 1};
   cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+  return fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool WGRAD, bool A_MN, bool B_MN, int EPI>
+template <bool WGRAD, bool A_MN, bool B_MN, int EPI, bool FP8 = false>
 cudaError_t launch(const char* name, const CUtensorMap& a, const CUtensorMap& b,
                    const CUtensorMap& o, const Params& p, long long max_tiles, cudaStream_t st) {
-  auto kern = grouped_gemm_kernel<WGRAD, A_MN, B_MN, EPI>;
-  const size_t smem = smem_bytes<EPI>();
+  auto kern = grouped_gemm_kernel<WGRAD, A_MN, B_MN, EPI, FP8>;
+  const size_t smem = KCfg<EPI, FP8>::kSmem;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   long long grid = num_sms();
@@ -564,6 +636,57 @@ cudaError_t gemm_wgrad(const moe_config& c, const Ws& ws, const moe_sched& s,
     return cudaErrorInvalidValue;
   return launch<true, true, true, EPI_STORE>(M == c.f ? "wgrad2" : "wgrad1", ta, tb, to, p,
                                              (long long)c.E * p.m_tiles_w * p.n_tiles, st);
+}
+
+// MXFP8 GEMM1: Xq [rows, d] E4M3 (+ scale tiles) x W1q [E, 2f, d] E4M3 (+ scale
+// tiles) -> SwiGLU -> Aq [rows, f] E4M3 + scale tiles; optionally A and H in bf16.
+cudaError_t gemm_fwd1_mx(const moe_config& c, const Ws& ws, const uint8_t* Xq, const uint8_t* Xs,
+                         const uint8_t* W1q, const uint8_t* W1s, uint8_t* Aq, uint8_t* As,
+                         __nv_bfloat16* A, __nv_bfloat16* H, cudaStream_t st) {
+  CUtensorMap ta, tb, to;
+  const uint64_t rows = (uint64_t)ws.L.Rp_max;
+  Params p = base_params(c, ws);
+  p.hn = 128;
+  p.umma_n = 256;
+  p.n_tiles = c.f / 128;
+  p.num_kb = c.d / BK8;
+  p.out_cols = c.f;
+  p.out0 = A;
+  p.out1 = H;
+  p.sfa = Xs;
+  p.sfb = W1s;
+  p.k_groups = c.d / 128;
+  p.b_rows = 2 * c.f;
+  p.q_out = Aq;
+  p.q_sf = As;
+  if (!map2d(&ta, Xq, c.d, rows, 128, kBM, true) ||
+      !map3d(&tb, W1q, c.d, 2ull * c.f, c.E, 128, 128, true))
+    return cudaErrorInvalidValue;
+  to = tb;
+  return launch<false, false, false, EPI_SWIGLU, true>("gemm1_swiglu_mxfp8", ta, tb, to, p,
+                                                       ws.L.MT_max * p.n_tiles, st);
+}
+
+// MXFP8 GEMM2: Aq [rows, f] x W2q [E, d, f] -> Y [rows, d] bf16.
+cudaError_t gemm_fwd2_mx(const moe_config& c, const Ws& ws, const uint8_t* Aq, const uint8_t* As,
+                         const uint8_t* W2q, const uint8_t* W2s, __nv_bfloat16* Yp,
+                         cudaStream_t st) {
+  CUtensorMap ta, tb, to;
+  const uint64_t rows = (uint64_t)ws.L.Rp_max;
+  Params p = base_params(c, ws);
+  p.umma_n = 256;
+  p.n_tiles = (c.d + 255) / 256;
+  p.num_kb = c.f / BK8;
+  p.out_cols = c.d;
+  p.sfa = As;
+  p.sfb = W2s;
+  p.k_groups = c.f / 128;
+  p.b_rows = c.d;
+  if (!map2d(&ta, Aq, c.f, rows, 128, kBM, true) ||
+      !map3d(&tb, W2q, c.f, c.d, c.E, 128, 256, true) || !map2d(&to, Yp, c.d, rows, 64, 32))
+    return cudaErrorInvalidValue;
+  return launch<false, false, false, EPI_STORE, true>("gemm2_mxfp8", ta, tb, to, p,
+                                                      ws.L.MT_max * p.n_tiles, st);
 }
 
 }  // namespace moe

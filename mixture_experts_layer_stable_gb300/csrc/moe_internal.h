@@ -71,7 +71,7 @@ cudaError_t launch_schedule(const moe_config& c, const float* logits, const moe_
 cudaError_t launch_gather(const moe_config& c, const Ws& ws, const __nv_bfloat16* src,
                           __nv_bfloat16* dst, const __nv_bfloat16* src2, __nv_bfloat16* dst2,
                           cudaStream_t st);
-// MXFP8 gather: e4m3 codes [Rp, d] and UE8M0 scales [Rp, d/32].
+// MXFP8 gather: E4M3 codes [Rp, d] and UE8M0 scale tiles (mx.cuh layout).
 cudaError_t launch_gather_mxfp8(const moe_config& c, const Ws& ws, const __nv_bfloat16* src,
                                 uint8_t* q, uint8_t* sc, cudaStream_t st);
 // out[t] = sum_j w[t,j] * rows[pos_pad[t*k+j]] (w == nullptr: plain sum).
@@ -95,5 +95,11 @@ cudaError_t gemm_dgrad1(const moe_config& c, const Ws& ws, const __nv_bfloat16* 
 cudaError_t gemm_wgrad(const moe_config& c, const Ws& ws, const moe_sched& s,
                        const __nv_bfloat16* Amn, int M, const __nv_bfloat16* Bmn, int N,
                        __nv_bfloat16* dW, cudaStream_t st);
+cudaError_t gemm_fwd1_mx(const moe_config& c, const Ws& ws, const uint8_t* Xq, const uint8_t* Xs,
+                         const uint8_t* W1q, const uint8_t* W1s, uint8_t* Aq, uint8_t* As,
+                         __nv_bfloat16* A, __nv_bfloat16* H, cudaStream_t st);
+cudaError_t gemm_fwd2_mx(const moe_config& c, const Ws& ws, const uint8_t* Aq, const uint8_t* As,
+                         const uint8_t* W2q, const uint8_t* W2s, __nv_bfloat16* Yp,
+                         cudaStream_t st);
 
 }  // namespace moe

@@ -220,6 +220,58 @@ MOE_DEV uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return d;
 }
 
+// Block-scaled FP8 MMA: D[tmem] (+)= (A * sfA) (B * sfB), E4M3 inputs, one
+// UE8M0 scale per 32 K elements, scales read from TMEM at sfa / sfb with the
+// byte (32-element block) chosen by the scale-factor ids in idesc.
+MOE_DEV void tc_mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::
+          "r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of kind::mxf8f6f4 block_scale: E4M3 A and B (K-major),
+// UE8M0 scales, M x N, scale-factor ids (byte within the 32-bit TMEM column).
+MOE_DEV constexpr uint32_t idesc_mxf8(int M, int N, int sf_id) {
+  return ((uint32_t)(sf_id & 3) << 4)      // B scale-factor id
+         | (0u << 7) | (0u << 10)          // A, B format: E4M3
+         | ((uint32_t)(N >> 3) << 17)      // N / 8
+         | (1u << 23)                      // scale format: UE8M0
+         | ((uint32_t)(M >> 4) << 24)      // M / 16
+         | ((uint32_t)(sf_id & 3) << 29);  // A scale-factor id
+}
+
+// Copy a 32-row x 16-byte shared-memory block into TMEM columns
+// [taddr, taddr+4) of all four 32-lane quarters (scale-factor staging).
+MOE_DEV void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// Shared-memory descriptor without swizzle (8-row x 16-byte core matrices).
+MOE_DEV uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+// Plain bulk copy global -> shared (16-byte aligned, size a multiple of 16),
+// completing as transaction bytes on `bar`.
+MOE_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- misc
 MOE_DEV uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
