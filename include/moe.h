@@ -63,12 +63,17 @@ typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_precision;
  *   Limits: 1 <= k <= min(E, 32); 1 <= E <= 1024; T >= 1; d and f multiples
  *   of 64 (d also of 128 in MXFP8 mode).
  *   minibatch_rows: 0 runs the layer as a chain of kernels over the whole
- *     expert-ordered buffer.  > 0 runs the forward as one persistent kernel
- *     that hands windows of this many expert-ordered rows (a multiple of 128)
- *     from gather CTAs to GEMM CTAs through a ring of ring_slots slots
- *     ([LP] 02: SM partition, local counters, minibatch, ring token buffer).
- *   ring_slots: ring depth (>= 2) when minibatch_rows > 0.
- *   gather_ctas: CTAs on the gather/combine side of the SM split (0 = auto). */
+ *     expert-ordered buffer.  > 0 runs the BF16 forward as one persistent
+ *     cooperative kernel that hands windows of this many expert-ordered rows
+ *     (rounded up to a multiple of 128) from gather CTAs to GEMM CTAs through
+ *     a ring of ring_slots slots, with GPU-side counters and the weighted
+ *     merge at the end ([LP] 02: SM partition, local counters, minibatch,
+ *     ring token buffer).  Results are bitwise identical to the chain path
+ *     for every window size.  MXFP8 with minibatch_rows > 0 returns
+ *     MOE_ERR_UNSUPPORTED; the backward always runs as a chain of kernels.
+ *   ring_slots: ring depth, 2..64, when minibatch_rows > 0.
+ *   gather_ctas: CTAs on the gather side of the SM split (0 = SMs / 8); must
+ *     be below the SM count. */
 typedef struct {
   int32_t T, d, f, E, k;
   int32_t prec; /* moe_precision */

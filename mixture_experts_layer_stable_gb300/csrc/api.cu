@@ -19,8 +19,9 @@ bool config_valid(const moe_config* c) {
   if (c->prec != MOE_BF16 && c->prec != MOE_MXFP8) return false;
   if (c->prec == MOE_MXFP8 && (c->d % 128 || c->f % 128)) return false;
   if ((int64_t)c->T * c->k > (int64_t)1 << 28) return false;
-  if (c->minibatch_rows < 0 || (c->minibatch_rows > 0 && c->minibatch_rows % kBM)) return false;
-  if (c->minibatch_rows > 0 && c->ring_slots < 2) return false;
+  if (c->minibatch_rows < 0 || c->minibatch_rows > (1 << 24)) return false;
+  if (c->minibatch_rows > 0 && (c->ring_slots < 2 || c->ring_slots > 64)) return false;
+  if (c->gather_ctas < 0) return false;
   return true;
 }
 
@@ -55,7 +56,11 @@ WsLayout ws_layout(const moe_config* c) {
   L.gA = take(rp * c->f * 2);
   L.dgp = take(rp * L.nt_dg * sizeof(float));
   L.Aq = take(c->prec == MOE_MXFP8 ? rp * c->f + rp * (c->f / 32) : 0);
-  L.ring = 0;
+  if (c->minibatch_rows > 0) {
+    L.ring = take((size_t)c->ring_slots * ring_window_rows(*c) * c->d * 2);
+    L.ctr_bytes = (size_t)(2 * c->ring_slots + 2 + L.MT_max) * sizeof(int);
+    L.ctr = take(L.ctr_bytes);
+  }
   L.total = off;
   return L;
 }
@@ -167,7 +172,20 @@ moe_status moe_forward(const moe_config* cfg, const moe_bf16* x, const void* w1,
   if (ws_bytes < W.L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   const moe_config& c = *cfg;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (c.minibatch_rows > 0) return MOE_ERR_UNSUPPORTED;
+  if (c.minibatch_rows > 0) {
+    // persistent kernel: SM split, ring of windows, device counters
+    if (c.prec != MOE_BF16 || w1_scales != nullptr || w2_scales != nullptr) return MOE_ERR_UNSUPPORTED;
+    if (c.gather_ctas >= num_sms()) return MOE_ERR_INVALID_ARG;
+    auto* A = saved ? reinterpret_cast<__nv_bfloat16*>(saved->A)
+                    : static_cast<__nv_bfloat16*>(W.at(W.L.Abuf));
+    auto* H = saved ? reinterpret_cast<__nv_bfloat16*>(saved->H) : nullptr;
+    const cudaError_t e = ring_forward(c, W, reinterpret_cast<const __nv_bfloat16*>(x),
+                                       static_cast<const __nv_bfloat16*>(w1),
+                                       static_cast<const __nv_bfloat16*>(w2), sched.topk_w, A, H,
+                                       reinterpret_cast<__nv_bfloat16*>(out), st);
+    if (e == cudaErrorCooperativeLaunchTooLarge) return MOE_ERR_UNSUPPORTED;
+    return cuda_status(e);
+  }
   if (c.prec == MOE_MXFP8) {
     if (!aligned(w1_scales) || !aligned(w2_scales)) return MOE_ERR_INVALID_ARG;
     const size_t rp = (size_t)W.L.Rp_max;

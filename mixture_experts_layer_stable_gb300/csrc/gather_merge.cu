@@ -17,24 +17,11 @@
 
 #include "moe_internal.h"
 #include "mx.cuh"
+#include "rowops.cuh"
 
 namespace moe {
 
 namespace {
-
-__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ void stg_v4(void* p, uint4 v) {
-  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
-}
 
 // One warp per padded row; 16-byte vectors; up to 4 loads in flight per lane.
 __global__ void __launch_bounds__(256) gather_kernel(const __nv_bfloat16* __restrict__ src,
@@ -156,7 +143,6 @@ __global__ void __launch_bounds__(128) merge_kernel(const __nv_bfloat16* __restr
                                                     int d, __nv_bfloat16* __restrict__ out) {
   __shared__ int sp[kMaxK];
   __shared__ float sw[kMaxK];
-  const int nvec = d >> 3;
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
     __syncthreads();
     if (threadIdx.x < k) {
@@ -164,37 +150,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const __nv_bfloat16* __restr
       sw[threadIdx.x] = w ? w[(size_t)t * k + threadIdx.x] : 1.f;
     }
     __syncthreads();
-    for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
-      float acc[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-      for (int j = 0; j < k; ++j) {
-        const uint4 y = ldg_nc_v4(rows + (size_t)sp[j] * d + (size_t)v * 8);
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&y);
-        const float g = sw[j];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = __bfloat1622float2(h[i]);
-          if (w) {
-            acc[2 * i] = fmaf(g, f.x, acc[2 * i]);
-            acc[2 * i + 1] = fmaf(g, f.y, acc[2 * i + 1]);
-          } else {
-            acc[2 * i] += f.x;
-            acc[2 * i + 1] += f.y;
-          }
-        }
-      }
-      uint4 o;
-      __nv_bfloat162 p0 = __floats2bfloat162_rn(acc[0], acc[1]);
-      __nv_bfloat162 p1 = __floats2bfloat162_rn(acc[2], acc[3]);
-      __nv_bfloat162 p2 = __floats2bfloat162_rn(acc[4], acc[5]);
-      __nv_bfloat162 p3 = __floats2bfloat162_rn(acc[6], acc[7]);
-      o.x = *reinterpret_cast<uint32_t*>(&p0);
-      o.y = *reinterpret_cast<uint32_t*>(&p1);
-      o.z = *reinterpret_cast<uint32_t*>(&p2);
-      o.w = *reinterpret_cast<uint32_t*>(&p3);
-      stg_v4(out + (size_t)t * d + (size_t)v * 8, o);
-    }
+    merge_token<false>(rows, sp, sw, w != nullptr, t, k, d, out, threadIdx.x, blockDim.x);
   }
 }
 

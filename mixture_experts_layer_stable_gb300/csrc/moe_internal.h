@@ -33,6 +33,7 @@ struct WsLayout {
   int64_t R = 0, Rp_max = 0, MT_max = 0, nblk = 0, nt_dg = 0;
   size_t hdr = 0, hist = 0, poff = 0, mt_off = 0, pos_pad = 0, row_of_pad = 0, g_pad = 0;
   size_t Xp = 0, Abuf = 0, Yp = 0, dYp = 0, dH = 0, gA = 0, dgp = 0, Aq = 0, ring = 0;
+  size_t ctr = 0, ctr_bytes = 0;  // ring path: window counters
   size_t total = 0;
 };
 
@@ -54,6 +55,11 @@ struct Ws {
 };
 
 int num_sms();
+
+// Ring path: rows per window (minibatch_rows rounded up to 128-row tiles) and
+// the default number of gather CTAs of the SM split.
+inline int ring_window_rows(const moe_config& c) { return (c.minibatch_rows + kBM - 1) / kBM * kBM; }
+inline int ring_default_gather_ctas(int sms) { return sms >= 64 ? sms / 8 : 2; }
 
 // Tracing hooks around every kernel launch (no-ops unless moe_trace_enable).
 void trace_before(const char* name, cudaStream_t st);
@@ -95,6 +101,10 @@ cudaError_t gemm_dgrad1(const moe_config& c, const Ws& ws, const __nv_bfloat16* 
 cudaError_t gemm_wgrad(const moe_config& c, const Ws& ws, const moe_sched& s,
                        const __nv_bfloat16* Amn, int M, const __nv_bfloat16* Bmn, int N,
                        __nv_bfloat16* dW, cudaStream_t st);
+// Persistent forward with an SM split and a ring of windows (ring.cu).
+cudaError_t ring_forward(const moe_config& c, const Ws& ws, const __nv_bfloat16* x,
+                         const __nv_bfloat16* W1, const __nv_bfloat16* W2, const float* topk_w,
+                         __nv_bfloat16* A, __nv_bfloat16* H, __nv_bfloat16* out, cudaStream_t st);
 cudaError_t gemm_fwd1_mx(const moe_config& c, const Ws& ws, const uint8_t* Xq, const uint8_t* Xs,
                          const uint8_t* W1q, const uint8_t* W1s, uint8_t* Aq, uint8_t* As,
                          __nv_bfloat16* A, __nv_bfloat16* H, cudaStream_t st);

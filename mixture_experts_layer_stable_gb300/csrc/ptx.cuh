@@ -34,6 +34,36 @@ MOE_DEV void report_status(int* status, int code, int where) {
   if (atomicCAS(status, 0, code) == 0) atomicExch(status + 1, where);
 }
 
+// ---------------------------------------------------------------- counters
+// GPU-scope acquire load / release add on global counters shared by CTAs.
+MOE_DEV int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+MOE_DEV void red_release_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Wait until *ctr >= target.  Gives up (false) when *gabort is set by another
+// CTA or after limit_ns, in which case it sets *gabort and reports
+// MOE_ERR_TIMEOUT with `where`.
+MOE_DEV bool wait_counter(const int* ctr, int target, int* gabort, int* status, int where,
+                          uint64_t limit_ns) {
+  if (ld_acquire(ctr) >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    __nanosleep(128);
+    if (ld_acquire(ctr) >= target) return true;
+    if (ld_acquire(gabort) != 0) return false;
+    if (global_timer_ns() - t0 > limit_ns) {
+      atomicExch(gabort, 1);
+      report_status(status, kStatusTimeout, where);
+      return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- mbarrier
 MOE_DEV void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)

@@ -55,10 +55,15 @@ def test_workspace_and_saved_sizes(B):
     for bad in (B.make_config(64, 100, 64, 8, 2), B.make_config(64, 128, 64, 8, 9),
                 B.make_config(0, 128, 64, 8, 2), B.make_config(64, 128, 64, 2000, 2),
                 B.make_config(64, 128, 64, 64, 33), B.make_config(64, 128, 64, 8, 2, prec=7),
-                B.make_config(64, 128, 64, 8, 2, minibatch_rows=100, ring_slots=2),
+                B.make_config(64, 128, 64, 8, 2, minibatch_rows=-1, ring_slots=2),
+                B.make_config(64, 128, 64, 8, 2, minibatch_rows=128, ring_slots=65),
+                B.make_config(64, 128, 64, 8, 2, gather_ctas=-1),
                 B.make_config(64, 128, 64, 8, 2, minibatch_rows=128, ring_slots=1)):
         assert B.moe_workspace_bytes(bad) == 0
         assert B.moe_saved_rows(bad) == 0
+    # a ring window of 100 rows rounds up to one 128-row tile: valid, with ring space
+    ring = B.make_config(64, 128, 64, 8, 2, minibatch_rows=100, ring_slots=2)
+    assert B.moe_workspace_bytes(ring) >= ws + 2 * 128 * 128 * 2
 
 
 def test_host_validation_returns_before_any_gpu_work(B):

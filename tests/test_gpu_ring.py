@@ -1,0 +1,134 @@
+"""The persistent ring forward (SM split into gather and GEMM CTAs, minibatch
+windows handed over through device counters, leiphone "MoK..." section 02).
+
+It computes the same tiles in the same K order as the kernel-chain forward, so
+its outputs and saved activations must be bitwise identical to that path, for
+every minibatch size and ring depth (the results do not depend on the
+minibatch), and within 1e-2 of the oracle.  A withheld window must end in
+MOE_ERR_TIMEOUT through the bounded waits, leaving the context usable.
+"""
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_layer_stable_gb300 import binding as B
+from mixture_experts_layer_stable_gb300.configs import CONFIGS
+from mixture_experts_layer_stable_gb300.inputs import make_inputs
+from oracle import moe_oracle as O
+
+from gpu_util import Layer, cfg_struct, with_config
+from helpers import ExpertView, rel_err, to_np
+
+pytestmark = pytest.mark.gpu
+
+HDR_INJECT = 8  # workspace header word of the wait test hook (int32 index)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cuda_lib):
+    yield
+
+
+def _run(cfg, dev, mb=0, slots=0, gather=0, save=True, backward=False):
+    L = Layer(cfg, cfg_struct(cfg, minibatch_rows=mb, ring_slots=slots, gather_ctas=gather))
+    L.schedule(dev["logits"])
+    L.forward(dev["x"], dev["W1"], dev["W2"], save=save)
+    if backward:
+        L.backward(dev["dOut"], dev["x"], dev["W1"], dev["W2"])
+    torch.cuda.synchronize()
+    assert L.status() == 0
+    return L
+
+
+def _same(a, b):
+    return torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def _rows_written(L):
+    """Rows of the saved activations the forward writes: the padded total."""
+    c = L.sched["counts"].cpu().numpy().astype(np.int64)
+    return int(((c + 127) // 128 * 128).sum())
+
+
+@pytest.mark.parametrize("name,kw,mbs", [
+    ("tiny", {}, [(128, 2), (256, 3)]),
+    ("tiny", dict(f=192, d=256, T=300), [(128, 2), (384, 2)]),
+    ("tiny", dict(T=1, k=8), [(128, 2)]),
+    ("balanced", {}, [(1024, 2), (512, 4), (2368, 2), (8192, 2)]),
+])
+def test_ring_equals_chain_bitwise(name, kw, mbs):
+    cfg = with_config(name, **kw)
+    inp = make_inputs(cfg, x_std=1.0 if name == "tiny" else None)
+    dev = {k: v.cuda() for k, v in inp.items()}
+    ref = _run(cfg, dev)
+    for mb, slots in mbs:
+        for gather in (0, 3):
+            L = _run(cfg, dev, mb, slots, gather)
+            assert _same(L.out, ref.out), (mb, slots, gather)
+            rp = _rows_written(ref)
+            assert _same(L.saved["H"][:rp], ref.saved["H"][:rp])
+            assert _same(L.saved["A"][:rp], ref.saved["A"][:rp])
+    ids, g = O.route(inp["logits"].numpy(), cfg.k)
+    want, _ = O.forward(to_np(inp["x"]), ExpertView(inp["W1"]), ExpertView(inp["W2"]), ids, g)
+    assert rel_err(ref.out.float().cpu().numpy(), want) <= 1e-2
+
+
+def test_ring_forward_then_backward():
+    cfg = with_config("tiny", T=256)
+    inp = make_inputs(cfg, x_std=1.0)
+    dev = {k: v.cuda() for k, v in inp.items()}
+    ref = _run(cfg, dev, backward=True)
+    L = _run(cfg, dev, 128, 2, backward=True)
+    for a, b in ((L.dx, ref.dx), (L.dW1, ref.dW1), (L.dW2, ref.dW2)):
+        assert _same(a, b)
+    assert torch.equal(L.dtopk_w, ref.dtopk_w)
+
+
+def test_ring_inference_without_saved():
+    cfg = with_config("balanced")
+    dev = {k: v.cuda() for k, v in make_inputs(cfg, with_grad=False).items()}
+    ref = _run(cfg, dev, save=False)
+    L = _run(cfg, dev, 1024, 2, save=False)
+    assert _same(L.out, ref.out)
+
+
+def test_ring_withheld_window_times_out_cleanly():
+    cfg = with_config("balanced")
+    dev = {k: v.cuda() for k, v in make_inputs(cfg, with_grad=False).items()}
+    c = cfg_struct(cfg, minibatch_rows=1024, ring_slots=2)
+    L = Layer(cfg, c)
+    L.schedule(dev["logits"])
+    hdr = L.ws[:64 * 4].view(torch.int32)
+    hdr[HDR_INJECT] = 3       # window 2's arrival is never released
+    hdr[HDR_INJECT + 1] = 50  # bounded waits give up after 50 ms
+    L.forward(dev["x"], dev["W1"], dev["W2"])
+    assert L.status() == B.MOE_ERR_TIMEOUT
+    # the context is still usable and a normal call succeeds afterwards
+    L.schedule(dev["logits"])
+    L.forward(dev["x"], dev["W1"], dev["W2"])
+    torch.cuda.synchronize()
+    assert L.status() == 0
+    ref = _run(cfg, dev)
+    assert _same(L.out, ref.out)
+
+
+def test_ring_rejects_unsupported_combinations():
+    cfg = with_config("tiny", f=128, prec="mxfp8")
+    c = cfg_struct(cfg, minibatch_rows=128, ring_slots=2)
+    L = Layer(cfg, c)
+    dev = {k: v.cuda() for k, v in make_inputs(cfg, with_grad=False).items()}
+    L.schedule(dev["logits"])
+    w = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(B.MoeError) as ei:
+        B.moe_forward(c, dev["x"], w, w, w, w, L.sched, L.out, None, L.ws)
+    assert ei.value.code == B.MOE_ERR_UNSUPPORTED
+
+
+@pytest.mark.slow
+def test_kimi_zipf_ring_equals_chain():
+    cfg = CONFIGS["kimi_zipf"]
+    dev = make_inputs(cfg, device="cuda", with_grad=False)
+    ref = _run(cfg, dev, save=False)
+    for mb in (512, 2368, 4096):
+        L = _run(cfg, dev, mb, 4, save=False)
+        assert _same(L.out, ref.out), mb
