@@ -429,8 +429,8 @@ def main():
                 "frac": achieved / peak, "traffic": ncu_traffic(cfg.name, dom), "kernel": dom,
                 "algorithmic_per_launch": amount, "peak_source": f"{peaks['source']} hbm"}
     fwd_names = ("gather", "gather_mxfp8", "gemm1_swiglu", "gemm2", "gemm1_swiglu_mxfp8",
-                 "gemm2_mxfp8", "merge")
-    sched_names = ("sched_topk", "sched_scatter")
+                 "gemm2_mxfp8", "merge", "ring_forward")
+    sched_names = ("sched_topk", "sched_hist", "sched_scatter")
     fwd_ms = sum(per[n][1] for n in per if n in fwd_names) / args.steps
     sch_ms = sum(per[n][1] for n in per if n in sched_names) / args.steps
     bwd_ms = sum(per[n][1] for n in per if n not in fwd_names + sched_names) / args.steps

@@ -31,7 +31,7 @@ WsLayout ws_layout(const moe_config* c) {
   const int64_t nonempty = c->E < L.R ? c->E : L.R;
   L.Rp_max = (int64_t)align_up((size_t)(L.R + nonempty * (kBM - 1)), kBM);
   L.MT_max = L.Rp_max / kBM;
-  L.nblk = (c->T + kSchedTokPerBlock - 1) / kSchedTokPerBlock;
+  L.nblk = (L.R + kSchedChunk - 1) / kSchedChunk;
   L.nt_dg = (c->f + 255) / 256;
   const size_t A = 1024;
   size_t off = 0;

@@ -56,15 +56,16 @@ enum Epi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2 };
 // (256 columns) and put the per-stage scale factors (16 columns a stage) in
 // the other half; the fp8 store variant has 3 stages to leave room for the
 // store staging tiles.
-template <int EPI, bool FP8>
+template <int EPI, bool FP8, bool WGRAD>
 struct KCfg {
   static constexpr int kStages = (FP8 && EPI == EPI_STORE) ? 3 : 4;
+  static constexpr int kOutBufs = (EPI == EPI_STORE) ? 2 : 0;  // staging tiles per epilogue warp
   static constexpr int kAcc = FP8 ? 1 : 2;
   // scale-tile region rounded to 1024 bytes: the swizzled staging tiles after
   // it must start on a 1024-byte boundary for the 128-byte swizzle pattern
   static constexpr size_t kSfRegion = FP8 ? ((size_t)kStages * kSfBytes + 1023) / 1024 * 1024 : 0;
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kSfRegion +
-                                  (EPI == EPI_STORE ? (size_t)kEpiWarps * 2 * kOutTile : 0) + 256;
+                                  (size_t)kEpiWarps * kOutBufs * kOutTile + 256;
   static_assert(kSmem <= 232448, "shared memory budget");
 };
 
@@ -138,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmO, const Params p) {
-  using Cfg = KCfg<EPI, FP8>;
+  using Cfg = KCfg<EPI, FP8, WGRAD>;
   constexpr int kStages = Cfg::kStages;
   constexpr int kAcc = Cfg::kAcc;
   extern __shared__ uint8_t smem_raw[];
@@ -147,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* stages = smem;
   uint8_t* sfbuf = smem + (size_t)kStages * kStageBytes;  // fp8 scale tiles, kSfBytes a stage
   uint8_t* staging = sfbuf + Cfg::kSfRegion;
-  uint8_t* ctrl = staging + (EPI == EPI_STORE ? kEpiWarps * 2 * kOutTile : 0);
+  uint8_t* ctrl = staging + (size_t)kEpiWarps * Cfg::kOutBufs * kOutTile;
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
@@ -319,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int acc = 0, buf = 0;
     uint32_t aph = 0;
-    const uint32_t stg = smem_u32(staging) + (uint32_t)(warp - 2) * 2u * kOutTile;
+    const uint32_t stg = smem_u32(staging) + (uint32_t)(warp - 2) * (uint32_t)Cfg::kOutBufs * kOutTile;
     for (int L = blockIdx.x; L < total; L += gridDim.x) {
       const Tile t = decode<WGRAD>(p, L);
       if (!mbar_wait(&tfull[acc], aph, abort_flag, p.status, 400 + acc)) break;
@@ -340,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int col = t.n * 256 + c * 64;
           if (col >= p.out_cols || (WGRAD && row >= p.out_rows)) continue;
-          if (lane == 0) bulk_wait_read<1>();
+          if (lane == 0) bulk_wait_read<Cfg::kOutBufs - 1>();
           __syncwarp();
           const uint32_t sbuf = stg + (uint32_t)buf * kOutTile;
 #pragma unroll
@@ -358,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             else tma_store_2d(&tmO, sbuf, col, row);
             bulk_commit();
           }
-          buf ^= 1;
+          if (++buf == Cfg::kOutBufs) buf = 0;
         }
       } else if constexpr (EPI == EPI_SWIGLU) {
         const size_t row = (size_t)t.row0 + q * 32 + lane;
@@ -389,14 +390,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         const size_t row = (size_t)t.row0 + q * 32 + lane;
         const float gw = p.g_pad[row];
         float dg = 0.f;
+        // fragments of A, H_gate, H_up for the next 32 columns are loaded while
+        // the current ones are processed
+        uint4 nxt[12];
+        auto fetch = [&](int col) {
+          const uint4* a = reinterpret_cast<const uint4*>(p.As + row * p.f + col);
+          const uint4* g = reinterpret_cast<const uint4*>(p.Hs + row * (2 * p.f) + col);
+          const uint4* u = reinterpret_cast<const uint4*>(p.Hs + row * (2 * p.f) + p.f + col);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            nxt[i] = __ldg(a + i);
+            nxt[4 + i] = __ldg(g + i);
+            nxt[8 + i] = __ldg(u + i);
+          }
+        };
+        if (t.n * 256 < p.f) fetch(t.n * 256);
         for (int c = 0; c < 256; c += 32) {
           const int col = t.n * 256 + c;
           if (col >= p.f) break;
           float da[32], av[32], hg[32], hu[32], o1[32], o2[32], o3[32];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            unpack8(nxt[i], av + 8 * i);
+            unpack8(nxt[4 + i], hg + 8 * i);
+            unpack8(nxt[8 + i], hu + 8 * i);
+          }
+          if (c + 32 < 256 && col + 32 < p.f) fetch(col + 32);
           tmem_ld32(tb + c, da);
-          load32_bf16(p.As + row * p.f + col, av);
-          load32_bf16(p.Hs + row * (2 * p.f) + col, hg);
-          load32_bf16(p.Hs + row * (2 * p.f) + p.f + col, hu);
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             dg = fmaf(da[i], av[i], dg);
@@ -435,7 +455,7 @@ template <bool WGRAD, bool A_MN, bool B_MN, int EPI, bool FP8 = false>
 cudaError_t launch(const char* name, const CUtensorMap& a, const CUtensorMap& b,
                    const CUtensorMap& o, const Params& p, long long max_tiles, cudaStream_t st) {
   auto kern = grouped_gemm_kernel<WGRAD, A_MN, B_MN, EPI, FP8>;
-  const size_t smem = KCfg<EPI, FP8>::kSmem;
+  const size_t smem = KCfg<EPI, FP8, WGRAD>::kSmem;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   long long grid = num_sms();

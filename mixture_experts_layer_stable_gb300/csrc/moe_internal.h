@@ -13,7 +13,7 @@
 namespace moe {
 
 constexpr int kBM = 128;           // rows of an expert tile; expert segments are padded to it
-constexpr int kSchedTokPerBlock = 64;
+constexpr int kSchedChunk = 1024;  // flat routed rows per histogram / scatter block
 constexpr int kSchedThreads = 256;
 constexpr int kMaxE = 1024;
 constexpr int kMaxK = 32;

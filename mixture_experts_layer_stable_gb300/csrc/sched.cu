@@ -4,17 +4,19 @@
 // "MoK..." section 01).  The schedule table counts rows per expert, places
 // every row and keeps an expert's rows contiguous for the grouped GEMM
 // (same section; Marktechpost "Cursor开源MoK..." three design decisions:
-// one table serves all four transfer modes).
+// one table serves all four transfer modes, at < 3 % of the MoE runtime).
 //
-// Two kernels, no host synchronisation:
+// Three kernels, no host synchronisation:
 //  1. sched_topk: one warp per token, k rounds of a warp arg-max over the E
-//     fp32 logits (value descending, id ascending), weights = softmax over the
-//     k selected logits in fp32; block-local integer histogram; the last block
-//     to finish (atomic ticket) turns the per-block histograms into per-block
-//     exclusive prefixes, per-expert counts, offsets and the padded layout
-//     (each expert's segment rounded up to 128 rows).  Integer sums are order
-//     independent, so the table is deterministic.
-//  2. sched_scatter: every block re-walks its rows in index order and ranks
+//     fp32 logits (value descending, id ascending); weights = softmax over the
+//     k selected logits in fp32, summed in slot order.
+//  2. sched_hist: per chunk of kSchedChunk flat rows, an integer histogram
+//     over experts; the last block to finish (atomic ticket) turns the chunk
+//     histograms into per-chunk exclusive prefixes and computes counts,
+//     offsets and the padded layout (each expert's segment rounded up to 128
+//     rows).  Integer sums do not depend on order, so the table is
+//     deterministic.
+//  3. sched_scatter: every chunk re-walks its rows in index order and ranks
 //     each row among the earlier rows of the same expert (warp match + prefix
 //     over warps), which makes the permutation stable without atomics.
 #include <cuda_bf16.h>
@@ -34,68 +36,72 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
 
 __global__ void __launch_bounds__(kSchedThreads) sched_topk_kernel(
     const float* __restrict__ logits, int T, int E, int k, int* __restrict__ ids,
-    float* __restrict__ wts, int* __restrict__ hist, int* __restrict__ hdr,
-    int* __restrict__ counts, int* __restrict__ offsets, int* __restrict__ poff,
-    int* __restrict__ mt_off) {
-  __shared__ int sh_cnt[kMaxE];
-  __shared__ int sh_last;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int e = tid; e < E; e += blockDim.x) sh_cnt[e] = 0;
-  __syncthreads();
-
+    float* __restrict__ wts) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (t >= T) return;
   const int nchunk = (E + 31) >> 5;
-  const int t_begin = blockIdx.x * kSchedTokPerBlock;
-  const int t_end = min(T, t_begin + kSchedTokPerBlock);
-  for (int t = t_begin + warp; t < t_end; t += kWarps) {
-    float v[kMaxE / 32];
-    uint32_t taken = 0;
-    const float* zrow = logits + (size_t)t * E;
+  float v[kMaxE / 32];
+  uint32_t taken = 0;
+  const float* zrow = logits + (size_t)t * E;
+#pragma unroll
+  for (int c = 0; c < kMaxE / 32; ++c) {
+    const int e = c * 32 + lane;
+    const bool in = c < nchunk && e < E;
+    v[c] = in ? __ldg(zrow + e) : 0.f;
+    if (!in) taken |= 1u << c;
+  }
+  int my_id = 0;
+  float my_v = 0.f;
+  for (int r = 0; r < k; ++r) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
 #pragma unroll
     for (int c = 0; c < kMaxE / 32; ++c) {
-      const int e = c * 32 + lane;
-      v[c] = (c < nchunk && e < E) ? __ldg(zrow + e) : 0.f;
-      if (!(c < nchunk && e < E)) taken |= 1u << c;
-    }
-    int my_id = 0;
-    float my_v = 0.f;
-    for (int r = 0; r < k; ++r) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-#pragma unroll
-      for (int c = 0; c < kMaxE / 32; ++c) {
-        if (!((taken >> c) & 1u) && better(v[c], c * 32 + lane, bv, bi)) {
-          bv = v[c];
-          bi = c * 32 + lane;
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (better(ov, oi, bv, bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (lane == r) {
-        my_id = bi;
-        my_v = bv;
+      if (c < nchunk && !((taken >> c) & 1u) && better(v[c], c * 32 + lane, bv, bi)) {
+        bv = v[c];
+        bi = c * 32 + lane;
       }
     }
-    // weights: exp(z_j - z_0) / sum_l exp(z_l - z_0), summed in slot order
-    const float z0 = __shfl_sync(0xffffffffu, my_v, 0);
-    const float ex = (lane < k) ? expf(my_v - z0) : 0.f;
-    float s = 0.f;
-    for (int j = 0; j < k; ++j) s += __shfl_sync(0xffffffffu, ex, j);
-    if (lane < k) {
-      ids[(size_t)t * k + lane] = my_id;
-      wts[(size_t)t * k + lane] = ex / s;
-      atomicAdd(&sh_cnt[my_id], 1);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (better(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == r) {
+      my_id = bi;
+      my_v = bv;
     }
   }
+  // weights: exp(z_j - z_0) / sum_l exp(z_l - z_0), summed in slot order
+  const float z0 = __shfl_sync(0xffffffffu, my_v, 0);
+  const float ex = (lane < k) ? expf(my_v - z0) : 0.f;
+  float s = 0.f;
+  for (int j = 0; j < k; ++j) s += __shfl_sync(0xffffffffu, ex, j);
+  if (lane < k) {
+    ids[(size_t)t * k + lane] = my_id;
+    wts[(size_t)t * k + lane] = ex / s;
+  }
+}
+
+__global__ void __launch_bounds__(kSchedThreads) sched_hist_kernel(
+    const int* __restrict__ ids, int R, int E, int* __restrict__ hist, int* __restrict__ hdr,
+    int* __restrict__ counts, int* __restrict__ offsets, int* __restrict__ poff,
+    int* __restrict__ mt_off) {
+  __shared__ int sh[kMaxE];
+  __shared__ int sh_last;
+  const int tid = threadIdx.x;
+  for (int e = tid; e < E; e += blockDim.x) sh[e] = 0;
   __syncthreads();
-  for (int e = tid; e < E; e += blockDim.x) hist[(size_t)blockIdx.x * E + e] = sh_cnt[e];
+  const int r0 = blockIdx.x * kSchedChunk, r1 = min(R, r0 + kSchedChunk);
+  for (int r = r0 + tid; r < r1; r += blockDim.x) atomicAdd(&sh[ids[r]], 1);
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) hist[(size_t)blockIdx.x * E + e] = sh[e];
   __threadfence();
   __syncthreads();
   if (tid == 0) sh_last = (atomicAdd(hdr + kHdrDone, 1) == (int)gridDim.x - 1);
@@ -103,17 +109,24 @@ __global__ void __launch_bounds__(kSchedThreads) sched_topk_kernel(
   if (!sh_last) return;
   __threadfence();
 
-  // Last block: per-expert column prefix over blocks, then scans over experts.
+  // Last block: per-expert exclusive prefix over chunks (loads issued in
+  // batches so they overlap), then the scans over experts.
   const int nb = gridDim.x;
   for (int e = tid; e < E; e += blockDim.x) {
     int run = 0;
-    for (int b = 0; b < nb; ++b) {
-      volatile int* h = hist + (size_t)b * E + e;
-      const int c = *h;
-      *h = run;
-      run += c;
+    for (int b0 = 0; b0 < nb; b0 += 8) {
+      int c[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) c[u] = (b0 + u < nb) ? __ldcg(hist + (size_t)(b0 + u) * E + e) : 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (b0 + u < nb) {
+          hist[(size_t)(b0 + u) * E + e] = run;
+          run += c[u];
+        }
+      }
     }
-    sh_cnt[e] = run;
+    sh[e] = run;
     counts[e] = run;
   }
   __syncthreads();
@@ -123,8 +136,8 @@ __global__ void __launch_bounds__(kSchedThreads) sched_topk_kernel(
       offsets[e] = o;
       poff[e] = po;
       mt_off[e] = po / kBM;
-      o += sh_cnt[e];
-      po += (sh_cnt[e] + kBM - 1) / kBM * kBM;
+      o += sh[e];
+      po += (sh[e] + kBM - 1) / kBM * kBM;
     }
     offsets[E] = o;
     poff[E] = po;
@@ -132,20 +145,19 @@ __global__ void __launch_bounds__(kSchedThreads) sched_topk_kernel(
     hdr[kHdrRpTotal] = po;
     hdr[kHdrMtTotal] = po / kBM;
     hdr[kHdrDone] = 0;
-    __threadfence();
   }
 }
 
 __global__ void __launch_bounds__(kSchedThreads) sched_scatter_kernel(
-    const int* __restrict__ ids, const float* __restrict__ wts, int T, int E, int k,
+    const int* __restrict__ ids, const float* __restrict__ wts, int R, int E,
     const int* __restrict__ hist_prefix, const int* __restrict__ counts,
     const int* __restrict__ offsets, const int* __restrict__ poff, int* __restrict__ perm,
     int* __restrict__ inv, int* __restrict__ pos_pad, int* __restrict__ row_of_pad,
     float* __restrict__ g_pad) {
   __shared__ int wcnt[kWarps][kMaxE];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int r_begin = blockIdx.x * kSchedTokPerBlock * k;
-  const int r_end = min(T, (blockIdx.x + 1) * kSchedTokPerBlock) * k;
+  const int r_begin = blockIdx.x * kSchedChunk;
+  const int r_end = min(R, r_begin + kSchedChunk);
   const int per_warp = (r_end - r_begin + kWarps - 1) / kWarps;
   const int w_begin = r_begin + warp * per_warp;
   const int w_end = min(r_end, w_begin + per_warp);
@@ -205,21 +217,28 @@ __global__ void __launch_bounds__(kSchedThreads) sched_scatter_kernel(
 
 cudaError_t launch_schedule(const moe_config& c, const float* logits, const moe_sched& s,
                             const Ws& ws, cudaStream_t st) {
-  const int nblk = (int)ws.L.nblk;
+  const int R = c.T * c.k;
+  const int nchunk = (int)ws.L.nblk;
   cudaError_t err = cudaMemsetAsync(ws.hdr(), 0, kHdrWords * sizeof(int), st);
   if (err != cudaSuccess) return err;
   {
     TraceScope ts("sched_topk", st);
-    sched_topk_kernel<<<nblk, kSchedThreads, 0, st>>>(logits, c.T, c.E, c.k, s.topk_ids, s.topk_w,
-                                                       ws.hist(), ws.hdr(), s.counts, s.offsets,
-                                                       ws.poff(), ws.mt_off());
+    sched_topk_kernel<<<(c.T + kWarps - 1) / kWarps, kSchedThreads, 0, st>>>(logits, c.T, c.E, c.k,
+                                                                            s.topk_ids, s.topk_w);
+    err = cudaGetLastError();
+  }
+  if (err != cudaSuccess) return err;
+  {
+    TraceScope ts("sched_hist", st);
+    sched_hist_kernel<<<nchunk, kSchedThreads, 0, st>>>(s.topk_ids, R, c.E, ws.hist(), ws.hdr(),
+                                                        s.counts, s.offsets, ws.poff(), ws.mt_off());
     err = cudaGetLastError();
   }
   if (err != cudaSuccess) return err;
   TraceScope ts("sched_scatter", st);
-  sched_scatter_kernel<<<nblk, kSchedThreads, 0, st>>>(
-      s.topk_ids, s.topk_w, c.T, c.E, c.k, ws.hist(), s.counts, s.offsets, ws.poff(), s.perm,
-      s.inv, ws.pos_pad(), ws.row_of_pad(), ws.g_pad());
+  sched_scatter_kernel<<<nchunk, kSchedThreads, 0, st>>>(
+      s.topk_ids, s.topk_w, R, c.E, ws.hist(), s.counts, s.offsets, ws.poff(), s.perm, s.inv,
+      ws.pos_pad(), ws.row_of_pad(), ws.g_pad());
   return cudaGetLastError();
 }
 
