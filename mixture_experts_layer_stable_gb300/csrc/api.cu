@@ -179,7 +179,7 @@ moe_status moe_forward(const moe_config* cfg, const moe_bf16* x, const void* w1,
     auto* A = saved ? reinterpret_cast<__nv_bfloat16*>(saved->A)
                     : static_cast<__nv_bfloat16*>(W.at(W.L.Abuf));
     auto* H = saved ? reinterpret_cast<__nv_bfloat16*>(saved->H) : nullptr;
-    const cudaError_t e = ring_forward(c, W, reinterpret_cast<const __nv_bfloat16*>(x),
+    const cudaError_t e = ring_forward(c, W, sched.counts, reinterpret_cast<const __nv_bfloat16*>(x),
                                        static_cast<const __nv_bfloat16*>(w1),
                                        static_cast<const __nv_bfloat16*>(w2), sched.topk_w, A, H,
                                        reinterpret_cast<__nv_bfloat16*>(out), st);
@@ -215,7 +215,7 @@ moe_status moe_forward(const moe_config* cfg, const moe_bf16* x, const void* w1,
   cudaError_t e = launch_gather(c, W, reinterpret_cast<const __nv_bfloat16*>(x), Xp, nullptr,
                                 nullptr, st);
   if (e == cudaSuccess)
-    e = gemm_fwd1(c, W, Xp, static_cast<const __nv_bfloat16*>(w1), A, H, st);
+    e = gemm_fwd1(c, W, sched.counts, Xp, static_cast<const __nv_bfloat16*>(w1), A, H, st);
   if (e == cudaSuccess) e = gemm_fwd2(c, W, A, static_cast<const __nv_bfloat16*>(w2), Yp, st);
   if (e == cudaSuccess)
     e = launch_merge(c, W, Yp, sched.topk_w, reinterpret_cast<__nv_bfloat16*>(out), st);

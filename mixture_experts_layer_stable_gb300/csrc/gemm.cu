@@ -49,6 +49,7 @@ constexpr int kOutTile = 32 * 128;        // 32 rows x 64 bf16, swizzled staging
 constexpr int kTmemCols = 512;
 constexpr int kTmemSf = 256;              // fp8: per-stage scale columns start here
 constexpr int kTmemSfStride = 16;         // fp8: TMEM columns per stage (A: 4, B: 8; 8-aligned)
+constexpr int kTrTile = 32 * 80;          // 32 rows x (64 + 16 pad) bytes: per-warp transpose tile
 
 enum Epi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2 };
 
@@ -64,8 +65,10 @@ struct KCfg {
   // scale-tile region rounded to 1024 bytes: the swizzled staging tiles after
   // it must start on a 1024-byte boundary for the 128-byte swizzle pattern
   static constexpr size_t kSfRegion = FP8 ? ((size_t)kStages * kSfBytes + 1023) / 1024 * 1024 : 0;
+  // bf16 SwiGLU: per-warp transpose tiles for the thin (swapped) tiles
+  static constexpr size_t kTrBytes = (EPI == EPI_SWIGLU && !FP8) ? (size_t)kEpiWarps * kTrTile : 0;
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kSfRegion +
-                                  (size_t)kEpiWarps * kOutBufs * kOutTile + 256;
+                                  (size_t)kEpiWarps * kOutBufs * kOutTile + kTrBytes + 256;
   static_assert(kSmem <= 232448, "shared memory budget");
 };
 
@@ -94,11 +97,14 @@ struct Params {
   int b_rows;               // FP8: rows (N) of one expert's weight
   uint8_t* q_out;           // FP8 SWIGLU: E4M3 codes of A [rows, f]
   uint8_t* q_sf;            // FP8 SWIGLU: scale tiles of A
+  int thin;                 // bf16 GEMM1: compute an expert's partial last tile swapped
   int* status;
 };
 
 struct Tile {
   int e, m, n, kb_count, row0, krow0;
+  int rows;   // valid rows of a ROWS tile
+  bool thin;  // partial tile computed as (weights)^T x (rows)^T, tokens on N
 };
 
 template <bool WGRAD>
@@ -121,6 +127,16 @@ __device__ __forceinline__ Tile decode(const Params& p, int L) {
     t.row0 = t.m * kBM;
     t.kb_count = p.num_kb;
     t.krow0 = 0;
+    t.rows = kBM;
+    t.thin = false;
+    if (p.thin) {
+      const int cnt = __ldg(p.counts + e);
+      const int rows = cnt - (t.m - m0) * kBM;
+      if (thin_tile(rows, cnt)) {
+        t.rows = rows;
+        t.thin = true;
+      }
+    }
   } else {
     const int per = p.m_tiles_w * p.n_tiles;
     t.e = L / per;
@@ -130,8 +146,31 @@ __device__ __forceinline__ Tile decode(const Params& p, int L) {
     t.kb_count = (__ldg(p.counts + t.e) + BK - 1) / BK;
     t.krow0 = __ldg(p.poff + t.e);
     t.row0 = 0;
+    t.rows = kBM;
+    t.thin = false;
   }
   return t;
+}
+
+// A 32-token x 32-column block held one column per lane (v[i] = token i) is
+// written to rows [0, nrows) at dst (row-major, leading dimension ld) through
+// a per-warp shared transpose tile, so that each lane stores a contiguous
+// 64-byte row fragment.
+__device__ __forceinline__ void store_cols_t(uint8_t* tr, const float* v, __nv_bfloat16* dst,
+                                             size_t ld, int nrows, int lane) {
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    *reinterpret_cast<__nv_bfloat16*>(tr + i * 80 + lane * 2) = __float2bfloat16_rn(v[i]);
+  __syncwarp();
+  if (lane < nrows) {
+    const uint4* s = reinterpret_cast<const uint4*>(tr + lane * 80);
+    uint4* d = reinterpret_cast<uint4*>(dst + (size_t)lane * ld);
+    d[0] = s[0];
+    d[1] = s[1];
+    d[2] = s[2];
+    d[3] = s[3];
+  }
 }
 
 template <bool WGRAD, bool A_MN, bool B_MN, int EPI, bool FP8>
@@ -148,7 +187,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* stages = smem;
   uint8_t* sfbuf = smem + (size_t)kStages * kStageBytes;  // fp8 scale tiles, kSfBytes a stage
   uint8_t* staging = sfbuf + Cfg::kSfRegion;
-  uint8_t* ctrl = staging + (size_t)kEpiWarps * Cfg::kOutBufs * kOutTile;
+  uint8_t* trbuf = staging + (size_t)kEpiWarps * Cfg::kOutBufs * kOutTile;
+  uint8_t* ctrl = trbuf + Cfg::kTrBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
@@ -288,6 +328,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_mma_mxf8(dt, sdesc_sw128(sa + kk * 32, 16, 1024), sdesc_sw128(sb + kk * 32, 16, 1024),
                           idesc_mxf8(kBM, 256, kk), tsa, tsb, (kb > 0 || kk > 0) ? 1u : 0u);
             }
+          } else if (!WGRAD && !A_MN && B_MN && t.thin) {
+            // thin tile: the gate and up weight slices (MN-major, the MMA's A,
+            // M = 128 columns each) times the tile's rows (K-major, the MMA's B,
+            // N = rows rounded up to 16); D columns are tokens: gate at [0, N),
+            // up at [128, 128 + N)
+            const uint32_t idt = idesc_bf16(kBM, (t.rows + 15) & ~15, true, false);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t bd = sdesc_sw128(sa + kk * 32, 16, 1024);
+              const uint32_t accf = (kb > 0 || kk > 0) ? 1u : 0u;
+              tc_mma_f16(dt, sdesc_sw128(sb + kk * 2048, 8192, 1024), bd, idt, accf);
+              tc_mma_f16(dt + 128u, sdesc_sw128(sb + 16384 + kk * 2048, 8192, 1024), bd, idt, accf);
+            }
           } else {
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
@@ -360,6 +413,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             bulk_commit();
           }
           if (++buf == Cfg::kOutBufs) buf = 0;
+        }
+      } else if (EPI == EPI_SWIGLU && !FP8 && t.thin) {
+        // thin tile: lane = gate / up column, TMEM columns = tokens.  All 128
+        // rows are written (zeros past the expert's rows) so that the saved
+        // activations of the padding rows stay zero.
+        uint8_t* tr = trbuf + (size_t)(warp - 2) * kTrTile;
+        const int nthin = (t.rows + 15) & ~15;
+        const int c0 = t.n * 128 + q * 32;
+        for (int t0 = 0; t0 < kBM; t0 += 32) {
+          float g[32], u[32], a[32];
+          if (t0 < nthin) {
+            tmem_ld32(tb + t0, g);
+            tmem_ld32(tb + 128 + t0, u);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) g[i] = u[i] = 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const bool ok = t0 + i < t.rows;
+            g[i] = ok ? g[i] : 0.f;
+            u[i] = ok ? u[i] : 0.f;
+            a[i] = ok ? silu_f(g[i]) * u[i] : 0.f;
+          }
+          const size_t r0 = (size_t)t.row0 + t0;
+          store_cols_t(tr, a, p.out0 + r0 * p.f + c0, p.f, 32, lane);
+          if (p.out1 != nullptr) {
+            store_cols_t(tr, g, p.out1 + r0 * (2 * p.f) + c0, 2 * p.f, 32, lane);
+            store_cols_t(tr, u, p.out1 + r0 * (2 * p.f) + p.f + c0, 2 * p.f, 32, lane);
+          }
         }
       } else if constexpr (EPI == EPI_SWIGLU) {
         const size_t row = (size_t)t.row0 + q * 32 + lane;
@@ -478,7 +561,7 @@ Params base_params(const moe_config& c, const Ws& ws) {
 
 }  // namespace
 
-cudaError_t gemm_fwd1(const moe_config& c, const Ws& ws, const __nv_bfloat16* Xp,
+cudaError_t gemm_fwd1(const moe_config& c, const Ws& ws, const int* counts, const __nv_bfloat16* Xp,
                       const __nv_bfloat16* W1, __nv_bfloat16* A, __nv_bfloat16* H, cudaStream_t st) {
   CUtensorMap ta, tb, to;
   const uint64_t rows = (uint64_t)ws.L.Rp_max;
@@ -490,6 +573,8 @@ cudaError_t gemm_fwd1(const moe_config& c, const Ws& ws, const __nv_bfloat16* Xp
   p.out_cols = c.f;
   p.out0 = A;
   p.out1 = H;
+  p.counts = counts;
+  p.thin = gemm1_thin_enabled(c) ? 1 : 0;
   if (!map2d(&ta, Xp, c.d, rows, 64, kBM) || !map3d(&tb, W1, 2ull * c.f, c.d, c.E, 64, 64))
     return cudaErrorInvalidValue;
   to = tb;

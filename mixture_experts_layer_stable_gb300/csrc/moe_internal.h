@@ -13,6 +13,17 @@
 namespace moe {
 
 constexpr int kBM = 128;           // rows of an expert tile; expert segments are padded to it
+
+// "Thin" GEMM1 tiles: an expert's last, partial 128-row tile is computed
+// swapped -- its gate / up weight slices on the MMA's M side and its rows on N
+// (rounded up to 16) -- so no padding rows are multiplied.  Measured on GB300
+// it pays off when the contraction is short (d = 2048: GEMM1 -20 %) and costs
+// a few percent at d = 7168, so it is enabled for d <= 4096 only (and needs
+// 128-column gate / up slices).  The chain and ring paths use the same rule,
+// so their results stay bitwise identical.
+__host__ __device__ inline bool thin_tile(int rows, int /*cnt*/) { return rows >= 1 && rows < kBM; }
+inline bool gemm1_thin_enabled(const moe_config& c) { return c.f % 128 == 0 && c.d <= 4096; }
+
 constexpr int kSchedChunk = 1024;  // flat routed rows per histogram / scatter block
 constexpr int kSchedThreads = 256;
 constexpr int kMaxE = 1024;
@@ -89,7 +100,7 @@ cudaError_t launch_quantize_mxfp8(const __nv_bfloat16* w, int64_t batch, int K, 
                                   uint8_t* sc, cudaStream_t st);
 
 // Grouped GEMMs on tcgen05 (gemm.cu).
-cudaError_t gemm_fwd1(const moe_config& c, const Ws& ws, const __nv_bfloat16* Xp,
+cudaError_t gemm_fwd1(const moe_config& c, const Ws& ws, const int* counts, const __nv_bfloat16* Xp,
                       const __nv_bfloat16* W1, __nv_bfloat16* A, __nv_bfloat16* H, cudaStream_t st);
 cudaError_t gemm_fwd2(const moe_config& c, const Ws& ws, const __nv_bfloat16* A,
                       const __nv_bfloat16* W2, __nv_bfloat16* Yp, cudaStream_t st);
@@ -102,7 +113,7 @@ cudaError_t gemm_wgrad(const moe_config& c, const Ws& ws, const moe_sched& s,
                        const __nv_bfloat16* Amn, int M, const __nv_bfloat16* Bmn, int N,
                        __nv_bfloat16* dW, cudaStream_t st);
 // Persistent forward with an SM split and a ring of windows (ring.cu).
-cudaError_t ring_forward(const moe_config& c, const Ws& ws, const __nv_bfloat16* x,
+cudaError_t ring_forward(const moe_config& c, const Ws& ws, const int* counts, const __nv_bfloat16* x,
                          const __nv_bfloat16* W1, const __nv_bfloat16* W2, const float* topk_w,
                          __nv_bfloat16* A, __nv_bfloat16* H, __nv_bfloat16* out, cudaStream_t st);
 cudaError_t gemm_fwd1_mx(const moe_config& c, const Ws& ws, const uint8_t* Xq, const uint8_t* Xs,

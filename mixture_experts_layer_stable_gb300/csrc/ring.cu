@@ -55,6 +55,8 @@ struct RingParams {
   int G, S, mb, mtw;          // gather CTAs, ring slots, rows per window, 128-row tiles per window
   int hn, nt1, nt2, kb1, kb2;  // GEMM1 half width, N tiles of GEMM1 / GEMM2, K blocks
   const int* mt_off;
+  const int* counts;   // rows per expert: a partial last tile runs thin (swapped)
+  int thin;
   const int* hdr;
   const int* row_of_pad;
   const int* pos_pad;
@@ -92,7 +94,28 @@ __device__ __forceinline__ Geo make_geo(const RingParams& p) {
 
 struct RTile {
   int phase, w, mloc, mt, n, e;
+  int rows;   // valid rows of the 128-row tile
+  bool thin;  // computed as (weights)^T x (rows)^T with the tokens on N
 };
+
+// A 32-token x 32-column block held one column per lane is written to rows
+// [0, nrows) at dst through a shared transpose tile (see gemm.cu).
+__device__ __forceinline__ void ring_store_cols_t(uint8_t* tr, const float* v, __nv_bfloat16* dst,
+                                                  size_t ld, int nrows, int lane) {
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    *reinterpret_cast<__nv_bfloat16*>(tr + i * 80 + lane * 2) = __float2bfloat16_rn(v[i]);
+  __syncwarp();
+  if (lane < nrows) {
+    const uint4* s = reinterpret_cast<const uint4*>(tr + lane * 80);
+    uint4* d = reinterpret_cast<uint4*>(dst + (size_t)lane * ld);
+    d[0] = s[0];
+    d[1] = s[1];
+    d[2] = s[2];
+    d[3] = s[3];
+  }
+}
 
 // Tile L of the stream G1(0), [G1(1) G2(0)], ..., [G1(nW-1) G2(nW-2)], G2(nW-1).
 // Inside a phase block, tiles run N-tile-major so that the tiles sharing an
@@ -128,6 +151,16 @@ __device__ __forceinline__ RTile ring_decode(const RingParams& p, const Geo& g, 
   t.n = loc / mtw;
   t.mt = w * p.mtw + t.mloc;
   t.e = find_expert(p.mt_off, p.E, t.mt);
+  t.rows = kBM;
+  t.thin = false;
+  if (p.thin && t.phase == 1) {
+    const int cnt = __ldg(p.counts + t.e);
+    const int rows = cnt - (t.mt - __ldg(p.mt_off + t.e)) * kBM;
+    if (thin_tile(rows, cnt)) {
+      t.rows = rows;
+      t.thin = true;
+    }
+  }
   return t;
 }
 
@@ -293,10 +326,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (g1 && kb == nkb - 1) red_release_add(&p.freed[t.w % p.S], 1);  // ring rows landed
             const uint32_t sa = smem_u32(stages + (size_t)s * kStageBytes);
             const uint32_t sb = sa + kABytes;
+            if (t.thin) {
+              // weight slices (MN-major) x tile rows (K-major, N = rows rounded to 16)
+              const uint32_t idt = idesc_bf16(kBM, (t.rows + 15) & ~15, true, false);
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)
-              tc_mma_f16(dt, sdesc_sw128(sa + kk * 32, 16, 1024), sdesc_sw128(sb + kk * 2048, 8192, 1024),
-                         g1 ? idesc1 : idesc2, (kb > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < BK / 16; ++kk) {
+                const uint64_t bd = sdesc_sw128(sa + kk * 32, 16, 1024);
+                const uint32_t accf = (kb > 0 || kk > 0) ? 1u : 0u;
+                tc_mma_f16(dt, sdesc_sw128(sb + kk * 2048, 8192, 1024), bd, idt, accf);
+                tc_mma_f16(dt + 128u, sdesc_sw128(sb + 16384 + kk * 2048, 8192, 1024), bd, idt, accf);
+              }
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < BK / 16; ++kk)
+                tc_mma_f16(dt, sdesc_sw128(sa + kk * 32, 16, 1024), sdesc_sw128(sb + kk * 2048, 8192, 1024),
+                           g1 ? idesc1 : idesc2, (kb > 0 || kk > 0) ? 1u : 0u);
+            }
             tc_commit(smem_u32(&empty[s]));
             if (++s == kStages) {
               s = 0;
@@ -324,7 +369,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&tfull[acc], aph, abort_flag, p.status, 400 + acc)) break;
         tc_fence_after();
         const uint32_t tb = tmem_base + (uint32_t)acc * 256u + ((uint32_t)(q * 32) << 16);
-        if (t.phase == 1) {
+        if (t.thin) {
+          // thin GEMM1 tile: lanes hold gate / up columns, TMEM columns hold
+          // tokens; rows go out through the warp's drained staging area used as
+          // a transpose tile (all 128 rows: zeros past the expert's rows)
+          if (lane == 0) bulk_wait_read<0>();
+          uint8_t* tr = staging + (size_t)(warp - 2) * 2 * kOutTile;
+          const int nthin = (t.rows + 15) & ~15;
+          const int c0 = t.n * 128 + q * 32;
+          for (int t0 = 0; t0 < kBM; t0 += 32) {
+            float g[32], u[32], a[32];
+            if (t0 < nthin) {
+              tmem_ld32(tb + t0, g);
+              tmem_ld32(tb + 128 + t0, u);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) g[i] = u[i] = 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const bool ok = t0 + i < t.rows;
+              g[i] = ok ? g[i] : 0.f;
+              u[i] = ok ? u[i] : 0.f;
+              a[i] = ok ? silu_f(g[i]) * u[i] : 0.f;
+            }
+            const size_t r0 = (size_t)t.mt * kBM + t0;
+            ring_store_cols_t(tr, a, p.A + r0 * p.f + c0, p.f, 32, lane);
+            if (p.H != nullptr) {
+              ring_store_cols_t(tr, g, p.H + r0 * (2 * p.f) + c0, 2 * p.f, 32, lane);
+              ring_store_cols_t(tr, u, p.H + r0 * (2 * p.f) + p.f + c0, 2 * p.f, 32, lane);
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(&tempty[acc]);
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) red_release_add(&p.a_ready[t.mt], 1);
+        } else if (t.phase == 1) {
           // SwiGLU: A (and H when saving) with direct row stores
           const size_t row = (size_t)t.mt * kBM + q * 32 + lane;
           for (int c = 0; c < p.hn; c += 32) {
@@ -376,6 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) {
             bulk_wait<0>();              // this warp's Y rows are in global memory
             fence_proxy_async_global();
+            __threadfence();
             red_release_add(p.done2, 1);
           }
           __syncwarp();
@@ -413,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t ring_forward(const moe_config& c, const Ws& ws, const __nv_bfloat16* x,
+cudaError_t ring_forward(const moe_config& c, const Ws& ws, const int* counts, const __nv_bfloat16* x,
                          const __nv_bfloat16* W1, const __nv_bfloat16* W2, const float* topk_w,
                          __nv_bfloat16* A, __nv_bfloat16* H, __nv_bfloat16* out, cudaStream_t st) {
   const int sms = num_sms();
@@ -434,6 +516,8 @@ cudaError_t ring_forward(const moe_config& c, const Ws& ws, const __nv_bfloat16*
   p.kb1 = c.d / BK;
   p.kb2 = c.f / BK;
   p.mt_off = ws.mt_off();
+  p.counts = counts;
+  p.thin = gemm1_thin_enabled(c) ? 1 : 0;
   p.hdr = ws.hdr();
   p.row_of_pad = ws.row_of_pad();
   p.pos_pad = ws.pos_pad();
