@@ -41,7 +41,7 @@ constexpr int BK = 64;                    // bf16 K elements per stage (128 byte
 constexpr int BK8 = 128;                  // fp8 K elements per stage (128 bytes)
 constexpr int kABytes = kBM * BK * 2;     // 16 KB
 constexpr int kBBytes = 256 * BK * 2;     // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kBHalfBytes = 128 * BK * 2; // 16 KB: a CTA's half of B in pair mode
 constexpr int kSfBytes = 1536;            // fp8 stage: one A scale tile + two B scale tiles
 constexpr int kThreads = 192;
 constexpr int kEpiWarps = 4;
@@ -56,19 +56,23 @@ enum Epi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2 };
 // Pipeline shape per variant.  The fp8 kernels keep one TMEM accumulator
 // (256 columns) and put the per-stage scale factors (16 columns a stage) in
 // the other half; the fp8 store variant has 3 stages to leave room for the
-// store staging tiles.
-template <int EPI, bool FP8, bool WGRAD>
+// store staging tiles.  In pair mode a stage holds the CTA's 128 rows of A
+// and its half (128 columns) of B: 32 KB, so six stages fit.
+template <int EPI, bool FP8, bool WGRAD, bool PAIR>
 struct KCfg {
-  static constexpr int kStages = (FP8 && EPI == EPI_STORE) ? 3 : 4;
-  static constexpr int kOutBufs = (EPI == EPI_STORE) ? 2 : 0;  // staging tiles per epilogue warp
+  static_assert(!(PAIR && FP8), "pair mode is bf16 only");
+  static constexpr int kStageBytes = kABytes + (PAIR ? kBHalfBytes : kBBytes);
+  static constexpr int kStages = PAIR ? 6 : (FP8 && EPI == EPI_STORE) ? 3 : 4;
+  // swizzled staging tiles per epilogue warp for the TMA-store epilogues
+  static constexpr int kOutBufs = (EPI == EPI_STORE || (EPI == EPI_SWIGLU && !FP8)) ? 2 : 0;
   static constexpr int kAcc = FP8 ? 1 : 2;
   // scale-tile region rounded to 1024 bytes: the swizzled staging tiles after
   // it must start on a 1024-byte boundary for the 128-byte swizzle pattern
   static constexpr size_t kSfRegion = FP8 ? ((size_t)kStages * kSfBytes + 1023) / 1024 * 1024 : 0;
-  // bf16 SwiGLU: per-warp transpose tiles for the thin (swapped) tiles
-  static constexpr size_t kTrBytes = (EPI == EPI_SWIGLU && !FP8) ? (size_t)kEpiWarps * kTrTile : 0;
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kSfRegion +
-                                  (size_t)kEpiWarps * kOutBufs * kOutTile + kTrBytes + 256;
+                                  (size_t)kEpiWarps * kOutBufs * kOutTile + 256;
+  // the thin tiles' transpose tile lives in the warp's staging tiles
+  static_assert(EPI != EPI_SWIGLU || FP8 || kOutBufs * kOutTile >= kTrTile, "transpose tile");
   static_assert(kSmem <= 232448, "shared memory budget");
 };
 
@@ -83,6 +87,7 @@ struct Params {
   int out_cols;    // output width (stores starting at or past it are skipped)
   int out_rows;    // WGRAD: output height
   const int* mt_off;  // ROWS: [E+1] prefix of 128-row tiles per expert
+  const int* pt_off;  // ROWS, pair mode: [E+1] prefix of tile pairs per expert
   const int* counts;  // WGRAD: [E] rows per expert
   const int* poff;    // WGRAD: [E+1] padded row prefix
   __nv_bfloat16* out0;  // SWIGLU: A [rows, f]      DSWIGLU: dH [rows, 2f]
@@ -103,33 +108,44 @@ struct Params {
 
 struct Tile {
   int e, m, n, kb_count, row0, krow0;
-  int rows;   // valid rows of a ROWS tile
-  bool thin;  // partial tile computed as (weights)^T x (rows)^T, tokens on N
+  int rows;    // valid rows of a ROWS tile
+  bool thin;   // partial tile computed as (weights)^T x (rows)^T, tokens on N
+  bool valid;  // pair mode: the odd CTA's tile past the expert's last tile is not
 };
 
-template <bool WGRAD>
-__device__ __forceinline__ int total_tiles(const Params& p) {
-  if (WGRAD) return p.E * p.m_tiles_w * p.n_tiles;
-  return __ldg(p.mt_off + p.E) * p.n_tiles;
+// Work units: tiles, or in pair mode pairs of M-adjacent tiles of one expert
+// (the even CTA of the pair takes M tile 2j, the odd one 2j + 1).
+template <bool WGRAD, bool PAIR>
+__device__ __forceinline__ int total_units(const Params& p) {
+  if (WGRAD) return p.E * (PAIR ? (p.m_tiles_w + 1) >> 1 : p.m_tiles_w) * p.n_tiles;
+  return __ldg((PAIR ? p.pt_off : p.mt_off) + p.E) * p.n_tiles;
 }
 
-template <bool WGRAD>
-__device__ __forceinline__ Tile decode(const Params& p, int L) {
+template <bool WGRAD, bool PAIR>
+__device__ __forceinline__ Tile decode(const Params& p, int L, int rank) {
   Tile t;
+  t.valid = true;
   if (!WGRAD) {
-    const int e = find_expert(p.mt_off, p.E, L / p.n_tiles);
-    const int m0 = __ldg(p.mt_off + e);
-    const int me = __ldg(p.mt_off + e + 1) - m0;
-    const int loc = L - m0 * p.n_tiles;
+    const int* uoff = PAIR ? p.pt_off : p.mt_off;
+    const int e = find_expert(uoff, p.E, L / p.n_tiles);
+    const int u0 = __ldg(uoff + e);
+    const int ue = __ldg(uoff + e + 1) - u0;
+    const int m0 = PAIR ? __ldg(p.mt_off + e) : u0;
+    const int loc = L - u0 * p.n_tiles;
+    int mrel = loc % ue;
+    if (PAIR) {
+      mrel = 2 * mrel + rank;
+      t.valid = mrel < __ldg(p.mt_off + e + 1) - m0;
+    }
     t.e = e;
-    t.n = loc / me;
-    t.m = m0 + loc % me;
+    t.n = loc / ue;
+    t.m = m0 + mrel;
     t.row0 = t.m * kBM;
     t.kb_count = p.num_kb;
     t.krow0 = 0;
     t.rows = kBM;
     t.thin = false;
-    if (p.thin) {
+    if (!PAIR && p.thin) {
       const int cnt = __ldg(p.counts + e);
       const int rows = cnt - (t.m - m0) * kBM;
       if (thin_tile(rows, cnt)) {
@@ -138,11 +154,13 @@ __device__ __forceinline__ Tile decode(const Params& p, int L) {
       }
     }
   } else {
-    const int per = p.m_tiles_w * p.n_tiles;
+    const int mu = PAIR ? (p.m_tiles_w + 1) >> 1 : p.m_tiles_w;
+    const int per = mu * p.n_tiles;
     t.e = L / per;
     const int loc = L - t.e * per;
-    t.m = loc % p.m_tiles_w;
-    t.n = loc / p.m_tiles_w;
+    t.m = PAIR ? 2 * (loc % mu) + rank : loc % mu;
+    t.n = loc / mu;
+    t.valid = t.m < p.m_tiles_w;
     t.kb_count = (__ldg(p.counts + t.e) + BK - 1) / BK;
     t.krow0 = __ldg(p.poff + t.e);
     t.row0 = 0;
@@ -173,22 +191,66 @@ __device__ __forceinline__ void store_cols_t(uint8_t* tr, const float* v, __nv_b
   }
 }
 
-template <bool WGRAD, bool A_MN, bool B_MN, int EPI, bool FP8>
+// The bf16 boxes this CTA copies for k-block kb of tile t: op2 / op3 get the
+// box's byte offset in the stage (A at 0, B at kABytes), its tensor map and
+// coordinates.
+template <bool WGRAD, bool A_MN, bool B_MN, int EPI, bool PAIR, typename Op2, typename Op3>
+__device__ __forceinline__ void for_each_box(const Params& p, const Tile& t, int kb, int rank,
+                                             const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                             Op2&& op2, Op3&& op3) {
+  // MN-major B arrives in 64-column boxes; in pair mode each CTA loads half
+  const int nbox = PAIR ? p.umma_n / 128 : p.umma_n / 64;
+  const int kr = t.krow0 + kb * BK;
+  if (t.valid) {
+    if (!A_MN) {
+      op2(0u, tmA, kb * BK, t.row0);
+    } else {
+      op2(0u, tmA, t.m * kBM, kr);
+      op2(8192u, tmA, t.m * kBM + 64, kr);
+    }
+  }
+  // first column (MN-major) or row (K-major) of this CTA's part of B
+  const int bpart = t.n * 256 + (PAIR ? rank * 128 : 0);
+  if (WGRAD) {
+    for (int i = 0; i < nbox; ++i) op2((uint32_t)(kABytes + i * 8192), tmB, bpart + 64 * i, kr);
+  } else if (B_MN) {
+    for (int i = 0; i < nbox; ++i) {
+      int col;
+      if (EPI == EPI_SWIGLU) {
+        // gate columns first, then up (pair: the even CTA holds gate)
+        if (PAIR) {
+          col = (rank == 0 ? t.n * p.hn : p.f + t.n * p.hn) + 64 * i;
+        } else {
+          const int half = nbox / 2;
+          col = (i < half) ? t.n * p.hn + 64 * i : p.f + t.n * p.hn + 64 * (i - half);
+        }
+      } else {
+        col = bpart + 64 * i;
+      }
+      op3((uint32_t)(kABytes + i * 8192), tmB, col, kb * BK, t.e);
+    }
+  } else {
+    op3((uint32_t)kABytes, tmB, kb * BK, bpart, t.e);
+  }
+}
+
+template <bool WGRAD, bool A_MN, bool B_MN, int EPI, bool FP8, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmO, const Params p) {
-  using Cfg = KCfg<EPI, FP8, WGRAD>;
+                        const __grid_constant__ CUtensorMap tmO,
+                        const __grid_constant__ CUtensorMap tmO2, const Params p) {
+  using Cfg = KCfg<EPI, FP8, WGRAD, PAIR>;
   constexpr int kStages = Cfg::kStages;
   constexpr int kAcc = Cfg::kAcc;
+  constexpr int kStageB = Cfg::kStageBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* stages = smem;
-  uint8_t* sfbuf = smem + (size_t)kStages * kStageBytes;  // fp8 scale tiles, kSfBytes a stage
+  uint8_t* sfbuf = smem + (size_t)kStages * kStageB;  // fp8 scale tiles, kSfBytes a stage
   uint8_t* staging = sfbuf + Cfg::kSfRegion;
-  uint8_t* trbuf = staging + (size_t)kEpiWarps * Cfg::kOutBufs * kOutTile;
-  uint8_t* ctrl = trbuf + Cfg::kTrBytes;
+  uint8_t* ctrl = staging + (size_t)kEpiWarps * Cfg::kOutBufs * kOutTile;
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
@@ -198,6 +260,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Pair mode: the two CTAs of a cluster walk the same work units; the even
+  // CTA issues the MMAs, and its "full" and "tmem empty" barriers count both
+  // CTAs' copies and epilogues.
+  const int rank = PAIR ? (int)cluster_ctarank() : 0;
+  const int unit0 = PAIR ? (int)cluster_idx() : (int)blockIdx.x;
+  const int ustride = PAIR ? (int)cluster_count() : (int)gridDim.x;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -205,41 +273,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], kEpiWarps * 32);
+      mbar_init(&tempty[a], PAIR ? 2 * kEpiWarps : kEpiWarps * 32);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (EPI == EPI_STORE) tma_prefetch_desc(&tmO);
+    if (Cfg::kOutBufs > 0) tma_prefetch_desc(&tmO);
+    if (EPI == EPI_SWIGLU && !FP8) tma_prefetch_desc(&tmO2);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);  // both CTAs, collectively
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // the peer's barriers exist before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int total = total_tiles<WGRAD>(p);
+  const int total = total_units<WGRAD, PAIR>(p);
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------ TMA producer
-      const uint32_t b_bytes = (B_MN && !FP8) ? (uint32_t)(p.umma_n / 64) * 8192u : (uint32_t)kBBytes;
-      const uint32_t tx = (uint32_t)kABytes + b_bytes + (FP8 ? (uint32_t)kSfBytes : 0u);
-      const int nbox = p.umma_n / 64;
+      const int nbox = PAIR ? p.umma_n / 128 : p.umma_n / 64;
+      const uint32_t b_bytes = FP8 ? (uint32_t)kBBytes
+                               : (B_MN ? (uint32_t)nbox * 8192u
+                                       : (uint32_t)(PAIR ? kBHalfBytes : kBBytes));
       int s = 0;
       uint32_t ph = 0, used = 0, last_par = 0;
-      for (int L = blockIdx.x; L < total; L += gridDim.x) {
-        const Tile t = decode<WGRAD>(p, L);
+      for (int L = unit0; L < total; L += ustride) {
+        const Tile t = decode<WGRAD, PAIR>(p, L, rank);
+        // bytes landing on this stage's "full" barrier (pair: both CTAs' copies)
+        uint32_t tx = (t.valid ? (uint32_t)kABytes : 0u) + b_bytes + (FP8 ? (uint32_t)kSfBytes : 0u);
+        if (PAIR && rank == 0)
+          tx += (decode<WGRAD, PAIR>(p, L, 1).valid ? (uint32_t)kABytes : 0u) + b_bytes;
         for (int kb = 0; kb < t.kb_count; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status, 100 + s)) goto producer_done;
-          const uint32_t sa = smem_u32(stages + (size_t)s * kStageBytes);
+          const uint32_t sa = smem_u32(stages + (size_t)s * kStageB);
           const uint32_t sb = sa + kABytes;
-          const uint32_t fb = smem_u32(&full[s]);
-          mbar_arrive_expect_tx(&full[s], tx);
+          const uint32_t fb = PAIR ? mapa_shared(smem_u32(&full[s]), 0) : smem_u32(&full[s]);
+          if (!PAIR || rank == 0) mbar_arrive_expect_tx(&full[s], tx);
           if constexpr (FP8) {
             // K-major E4M3 tiles (128 bytes of K per row) plus their scale tiles
             const int nbt = p.b_rows >> 7;  // 128-row scale tiles per expert
@@ -260,30 +340,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             bulk_load(sf + 512, p.sfb + (((size_t)t.e * nbt + nb0) * p.k_groups + kb) * 512u, 512u, fb);
             bulk_load(sf + 1024, p.sfb + (((size_t)t.e * nbt + nb1) * p.k_groups + kb) * 512u, 512u, fb);
           } else {
-            if (!A_MN) {
-              tma_load_2d(sa, &tmA, fb, kb * BK, t.row0);
-            } else {
-              const int kr = t.krow0 + kb * BK;
-              tma_load_2d(sa, &tmA, fb, t.m * kBM, kr);
-              tma_load_2d(sa + 8192, &tmA, fb, t.m * kBM + 64, kr);
-            }
-            if (WGRAD) {
-              const int kr = t.krow0 + kb * BK;
-              for (int i = 0; i < nbox; ++i) tma_load_2d(sb + i * 8192, &tmB, fb, t.n * 256 + 64 * i, kr);
-            } else if (B_MN) {
-              for (int i = 0; i < nbox; ++i) {
-                int col;
-                if (EPI == EPI_SWIGLU) {
-                  const int half = nbox / 2;
-                  col = (i < half) ? t.n * p.hn + 64 * i : p.f + t.n * p.hn + 64 * (i - half);
-                } else {
-                  col = t.n * 256 + 64 * i;
-                }
-                tma_load_3d(sb + i * 8192, &tmB, fb, col, kb * BK, t.e);
-              }
-            } else {
-              tma_load_3d(sb, &tmB, fb, kb * BK, t.n * 256, t.e);
-            }
+            auto load2 = [&](uint32_t off, const CUtensorMap* m, int c0, int c1) {
+              if constexpr (PAIR) tma_load_2d_pair(sa + off, m, fb, c0, c1);
+              else tma_load_2d(sa + off, m, fb, c0, c1);
+            };
+            auto load3 = [&](uint32_t off, const CUtensorMap* m, int c0, int c1, int c2) {
+              if constexpr (PAIR) tma_load_3d_pair(sa + off, m, fb, c0, c1, c2);
+              else tma_load_3d(sa + off, m, fb, c0, c1, c2);
+            };
+            for_each_box<WGRAD, A_MN, B_MN, EPI, PAIR>(p, t, kb, rank, &tmA, &tmB, load2, load3);
           }
           used |= 1u << s;
           last_par = (last_par & ~(1u << s)) | (ph << s);
@@ -294,25 +359,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     producer_done:
-      // every issued copy has landed before the CTA can exit
-      for (int i = 0; i < kStages; ++i)
-        if ((used >> i) & 1u) mbar_wait_drain(&full[i], (last_par >> i) & 1u);
+      // every issued copy has landed before the CTA can exit (in pair mode the
+      // even CTA's "full" barriers also count the odd CTA's copies)
+      if (!PAIR || rank == 0)
+        for (int i = 0; i < kStages; ++i)
+          if ((used >> i) & 1u) mbar_wait_drain(&full[i], (last_par >> i) & 1u);
+      if constexpr (PAIR) {
+        // and every stage this CTA filled has been released by the pair's MMAs,
+        // so no multicast arrival is still on its way to this CTA's barriers
+        for (int i = 0; i < kStages; ++i)
+          if ((used >> i) & 1u)
+            if (!mbar_wait_drain(&empty[i], (last_par >> i) & 1u)) break;
+      }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && (!PAIR || rank == 0)) {
       // ------------------------------------------------ MMA issuer
-      const uint32_t idesc = idesc_bf16(kBM, p.umma_n, A_MN, B_MN);
+      const uint32_t idesc = idesc_bf16(PAIR ? 2 * kBM : kBM, p.umma_n, A_MN, B_MN);
       int s = 0, acc = 0;
       uint32_t ph = 0, aph = 0;
-      for (int L = blockIdx.x; L < total; L += gridDim.x) {
-        const Tile t = decode<WGRAD>(p, L);
+      for (int L = unit0; L < total; L += ustride) {
+        const Tile t = decode<WGRAD, PAIR>(p, L, 0);
         if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, p.status, 200 + acc)) goto mma_done;
         tc_fence_after();
         const uint32_t dt = tmem_base + (uint32_t)acc * 256u;
         for (int kb = 0; kb < t.kb_count; ++kb) {
           if (!mbar_wait(&full[s], ph, abort_flag, p.status, 300 + s)) goto mma_done;
           tc_fence_after();
-          const uint32_t sa = smem_u32(stages + (size_t)s * kStageBytes);
+          const uint32_t sa = smem_u32(stages + (size_t)s * kStageB);
           const uint32_t sb = sa + kABytes;
           if constexpr (FP8) {
             // stage the scale tiles into this stage's TMEM columns, then 4 MMAs
@@ -328,36 +402,47 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_mma_mxf8(dt, sdesc_sw128(sa + kk * 32, 16, 1024), sdesc_sw128(sb + kk * 32, 16, 1024),
                           idesc_mxf8(kBM, 256, kk), tsa, tsb, (kb > 0 || kk > 0) ? 1u : 0u);
             }
-          } else if (!WGRAD && !A_MN && B_MN && t.thin) {
-            // thin tile: the gate and up weight slices (MN-major, the MMA's A,
-            // M = 128 columns each) times the tile's rows (K-major, the MMA's B,
-            // N = rows rounded up to 16); D columns are tokens: gate at [0, N),
-            // up at [128, 128 + N)
-            const uint32_t idt = idesc_bf16(kBM, (t.rows + 15) & ~15, true, false);
-#pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
-              const uint64_t bd = sdesc_sw128(sa + kk * 32, 16, 1024);
-              const uint32_t accf = (kb > 0 || kk > 0) ? 1u : 0u;
-              tc_mma_f16(dt, sdesc_sw128(sb + kk * 2048, 8192, 1024), bd, idt, accf);
-              tc_mma_f16(dt + 128u, sdesc_sw128(sb + 16384 + kk * 2048, 8192, 1024), bd, idt, accf);
-            }
           } else {
+            bool issued = false;
+            if constexpr (!PAIR && !WGRAD && !A_MN && B_MN) {
+              if (t.thin) {
+                // thin tile: the gate and up weight slices (MN-major, the MMA's
+                // A, M = 128 columns each) times the tile's rows (K-major, the
+                // MMA's B, N = rows rounded up to 16); D columns are tokens:
+                // gate at [0, N), up at [128, 128 + N)
+                const uint32_t idt = idesc_bf16(kBM, (t.rows + 15) & ~15, true, false);
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
-              const uint64_t ad = A_MN ? sdesc_sw128(sa + kk * 2048, 8192, 1024)
-                                       : sdesc_sw128(sa + kk * 32, 16, 1024);
-              const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, 8192, 1024)
-                                       : sdesc_sw128(sb + kk * 32, 16, 1024);
-              tc_mma_f16(dt, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                  const uint64_t bd = sdesc_sw128(sa + kk * 32, 16, 1024);
+                  const uint32_t accf = (kb > 0 || kk > 0) ? 1u : 0u;
+                  tc_mma_f16(dt, sdesc_sw128(sb + kk * 2048, 8192, 1024), bd, idt, accf);
+                  tc_mma_f16(dt + 128u, sdesc_sw128(sb + 16384 + kk * 2048, 8192, 1024), bd, idt, accf);
+                }
+                issued = true;
+              }
+            }
+            if (!issued) {
+#pragma unroll
+              for (int kk = 0; kk < BK / 16; ++kk) {
+                const uint64_t ad = A_MN ? sdesc_sw128(sa + kk * 2048, 8192, 1024)
+                                         : sdesc_sw128(sa + kk * 32, 16, 1024);
+                const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, 8192, 1024)
+                                         : sdesc_sw128(sb + kk * 32, 16, 1024);
+                const uint32_t accf = (kb > 0 || kk > 0) ? 1u : 0u;
+                if constexpr (PAIR) tc_mma_f16_pair(dt, ad, bd, idesc, accf);
+                else tc_mma_f16(dt, ad, bd, idesc, accf);
+              }
             }
           }
-          tc_commit(smem_u32(&empty[s]));
+          if constexpr (PAIR) tc_commit_pair(smem_u32(&empty[s]), 3);
+          else tc_commit(smem_u32(&empty[s]));
           if (++s == kStages) {
             s = 0;
             ph ^= 1u;
           }
         }
-        tc_commit(smem_u32(&tfull[acc]));
+        if constexpr (PAIR) tc_commit_pair(smem_u32(&tfull[acc]), 3);
+        else tc_commit(smem_u32(&tfull[acc]));
         if (++acc == kAcc) {
           acc = 0;
           aph ^= 1u;
@@ -365,7 +450,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     mma_done:
       // all issued MMAs complete before TMEM is released
-      tc_commit(smem_u32(drain));
+      if constexpr (PAIR) tc_commit_pair(smem_u32(drain), 1);
+      else tc_commit(smem_u32(drain));
       mbar_wait_drain(drain, 0);
     }
   } else {
@@ -374,14 +460,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0, buf = 0;
     uint32_t aph = 0;
     const uint32_t stg = smem_u32(staging) + (uint32_t)(warp - 2) * (uint32_t)Cfg::kOutBufs * kOutTile;
-    for (int L = blockIdx.x; L < total; L += gridDim.x) {
-      const Tile t = decode<WGRAD>(p, L);
+    // This warp's 32 rows x 64 columns (v = this lane's row) as bf16 through
+    // the next swizzled staging tile to a TMA store at (col, row) of m.  A
+    // tile is rewritten only after the store issued from it two tiles ago has
+    // finished reading it.
+    auto put_tile = [&](const CUtensorMap* m, const float* v, int col, int row) {
+      if (lane == 0) bulk_wait_read<(Cfg::kOutBufs > 0 ? Cfg::kOutBufs - 1 : 0)>();
+      __syncwarp();
+      const uint32_t sbuf = stg + (uint32_t)buf * kOutTile;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        st_shared_v4(sbuf + lane * 128 + ((j ^ (lane & 7)) << 4), pack_bf16x2(v[8 * j + 0], v[8 * j + 1]),
+                     pack_bf16x2(v[8 * j + 2], v[8 * j + 3]), pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
+                     pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(m, sbuf, col, row);
+        bulk_commit();
+      }
+      if (++buf == Cfg::kOutBufs) buf = 0;
+    };
+    for (int L = unit0; L < total; L += ustride) {
+      const Tile t = decode<WGRAD, PAIR>(p, L, rank);
       if (!mbar_wait(&tfull[acc], aph, abort_flag, p.status, 400 + acc)) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + (uint32_t)acc * 256u + ((uint32_t)(q * 32) << 16);
       const bool zero = (t.kb_count == 0);
 
-      if constexpr (EPI == EPI_STORE) {
+      if (!t.valid) {
+        // pair mode: the odd CTA's rows past the expert's last tile
+      } else if constexpr (EPI == EPI_STORE) {
         const int row = (WGRAD ? t.m * kBM : t.row0) + q * 32;
         for (int c = 0; c < p.umma_n / 64; ++c) {
           float v[64];
@@ -394,6 +504,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int col = t.n * 256 + c * 64;
           if (col >= p.out_cols || (WGRAD && row >= p.out_rows)) continue;
+          if (!WGRAD) {
+            put_tile(&tmO, v, col, row);
+            continue;
+          }
           if (lane == 0) bulk_wait_read<Cfg::kOutBufs - 1>();
           __syncwarp();
           const uint32_t sbuf = stg + (uint32_t)buf * kOutTile;
@@ -408,17 +522,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            if (WGRAD) tma_store_3d(&tmO, sbuf, col, row, t.e);
-            else tma_store_2d(&tmO, sbuf, col, row);
+            tma_store_3d(&tmO, sbuf, col, row, t.e);
             bulk_commit();
           }
           if (++buf == Cfg::kOutBufs) buf = 0;
         }
-      } else if (EPI == EPI_SWIGLU && !FP8 && t.thin) {
+      } else if (EPI == EPI_SWIGLU && !FP8 && !PAIR && t.thin) {
         // thin tile: lane = gate / up column, TMEM columns = tokens.  All 128
         // rows are written (zeros past the expert's rows) so that the saved
         // activations of the padding rows stay zero.
-        uint8_t* tr = trbuf + (size_t)(warp - 2) * kTrTile;
+        // the transpose tile reuses this warp's staging tiles once the TMA
+        // stores reading them are done
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+        uint8_t* tr = staging + (size_t)(warp - 2) * Cfg::kOutBufs * kOutTile;
         const int nthin = (t.rows + 15) & ~15;
         const int c0 = t.n * 128 + q * 32;
         for (int t0 = 0; t0 < kBM; t0 += 32) {
@@ -443,6 +560,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             store_cols_t(tr, g, p.out1 + r0 * (2 * p.f) + c0, 2 * p.f, 32, lane);
             store_cols_t(tr, u, p.out1 + r0 * (2 * p.f) + p.f + c0, 2 * p.f, 32, lane);
           }
+        }
+      } else if constexpr (EPI == EPI_SWIGLU && !FP8) {
+        // 64 gate and 64 up columns at a time: H (gate, up) and A = SiLU(gate) * up
+        // leave through TMA stores of 32-row x 64-column tiles
+        const int row = t.row0 + q * 32;
+        for (int c = 0; c < p.hn; c += 64) {
+          float g[64], u[64];
+          tmem_ld32(tb + c, g);
+          tmem_ld32(tb + c + 32, g + 32);
+          tmem_ld32(tb + p.hn + c, u);
+          tmem_ld32(tb + p.hn + c + 32, u + 32);
+          const int col = t.n * p.hn + c;
+          if (p.out1 != nullptr) {
+            put_tile(&tmO2, g, col, row);
+            put_tile(&tmO2, u, p.f + col, row);
+          }
+#pragma unroll
+          for (int i = 0; i < 64; ++i) g[i] = silu_f(g[i]) * u[i];
+          put_tile(&tmO, g, col, row);
         }
       } else if constexpr (EPI == EPI_SWIGLU) {
         const size_t row = (size_t)t.row0 + q * 32 + lane;
@@ -504,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) {
             dg = fmaf(da[i], av[i], dg);
             const float dA = gw * da[i];
-            const float sg = 1.0f / (1.0f + __expf(-hg[i]));
+            const float sg = sigmoid_f(hg[i]);
             o1[i] = dA * hu[i] * sg * (1.0f + hg[i] * (1.0f - sg));  // d gate
             o2[i] = dA * hg[i] * sg;                                // d up
             o3[i] = gw * av[i];                                     // g * A (for dW2)
@@ -516,37 +652,78 @@ __global__ void __launch_bounds__(kThreads, 1)
         p.dgp[row * p.n_tiles + t.n] = dg;
       }
       tc_fence_before();
-      mbar_arrive(&tempty[acc]);
+      if constexpr (PAIR) {
+        // one arrival per warp on the even CTA's barrier
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+      } else {
+        mbar_arrive(&tempty[acc]);
+      }
       if (++acc == kAcc) {
         acc = 0;
         aph ^= 1u;
       }
     }
-    if (EPI == EPI_STORE && lane == 0) bulk_wait<0>();
+    if (Cfg::kOutBufs > 0 && lane == 0) bulk_wait<0>();
   }
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // the pair's MMAs and remote arrivals are done
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, kTmemCols);
+    else tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
 // ------------------------------------------------------------------ host side
-template <bool WGRAD, bool A_MN, bool B_MN, int EPI, bool FP8 = false>
+template <bool WGRAD, bool A_MN, bool B_MN, int EPI, bool FP8 = false, bool PAIR = false>
 cudaError_t launch(const char* name, const CUtensorMap& a, const CUtensorMap& b,
-                   const CUtensorMap& o, const Params& p, long long max_tiles, cudaStream_t st) {
-  auto kern = grouped_gemm_kernel<WGRAD, A_MN, B_MN, EPI, FP8>;
-  const size_t smem = KCfg<EPI, FP8, WGRAD>::kSmem;
+                   const CUtensorMap& o, const CUtensorMap& o2, const Params& p, long long max_units,
+                   cudaStream_t st) {
+  auto kern = grouped_gemm_kernel<WGRAD, A_MN, B_MN, EPI, FP8, PAIR>;
+  const size_t smem = KCfg<EPI, FP8, WGRAD, PAIR>::kSmem;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  long long grid = num_sms();
-  if (max_tiles < grid) grid = max_tiles;
-  if (grid < 1) grid = 1;
-  TraceScope ts(name, st);
-  kern<<<(int)grid, kThreads, smem, st>>>(a, b, o, p);
-  return cudaGetLastError();
+  if constexpr (!PAIR) {
+    long long grid = num_sms();
+    if (max_units < grid) grid = max_units;
+    if (grid < 1) grid = 1;
+    TraceScope ts(name, st);
+    kern<<<(int)grid, kThreads, smem, st>>>(a, b, o, o2, p);
+    return cudaGetLastError();
+  } else {
+    // persistent clusters of two CTAs: as many as can be resident at once
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(num_sms() & ~1));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    static int resident[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    if (resident[dev] == 0) {
+      int n = 0;
+      err = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+      if (err != cudaSuccess) return err;
+      if (n < 1) return cudaErrorInvalidConfiguration;
+      resident[dev] = n;
+    }
+    long long clusters = resident[dev];
+    if (max_units < clusters) clusters = max_units;
+    if (clusters < 1) clusters = 1;
+    cfg.gridDim = dim3((unsigned)(2 * clusters));
+    TraceScope ts(name, st);
+    return cudaLaunchKernelEx(&cfg, kern, a, b, o, o2, p);
+  }
 }
 
 Params base_params(const moe_config& c, const Ws& ws) {
@@ -554,6 +731,7 @@ Params base_params(const moe_config& c, const Ws& ws) {
   p.E = c.E;
   p.f = c.f;
   p.mt_off = ws.mt_off();
+  p.pt_off = ws.pt_off();
   p.poff = ws.poff();
   p.status = ws.hdr() + kHdrStatus;
   return p;
@@ -574,11 +752,19 @@ cudaError_t gemm_fwd1(const moe_config& c, const Ws& ws, const int* counts, cons
   p.out0 = A;
   p.out1 = H;
   p.counts = counts;
-  p.thin = gemm1_thin_enabled(c) ? 1 : 0;
-  if (!map2d(&ta, Xp, c.d, rows, 64, kBM) || !map3d(&tb, W1, 2ull * c.f, c.d, c.E, 64, 64))
+  const bool pair = gemm_pair_enabled(c, kGemmFwd1);
+  p.thin = (!pair && gemm1_thin_enabled(c)) ? 1 : 0;
+  // outputs: A [rows, f] and (when saved) H [rows, 2f], stored as 32 x 64 tiles
+  CUtensorMap th;
+  if (!map2d(&ta, Xp, c.d, rows, 64, kBM) || !map3d(&tb, W1, 2ull * c.f, c.d, c.E, 64, 64) ||
+      !map2d(&to, A, c.f, rows, 64, 32) || (H != nullptr && !map2d(&th, H, 2ull * c.f, rows, 64, 32)))
     return cudaErrorInvalidValue;
-  to = tb;
-  return launch<false, false, true, EPI_SWIGLU>("gemm1_swiglu", ta, tb, to, p, ws.L.MT_max * p.n_tiles, st);
+  if (H == nullptr) th = to;
+  if (pair)
+    return launch<false, false, true, EPI_SWIGLU, false, true>("gemm1_swiglu", ta, tb, to, th, p,
+                                                               ws.L.MT_max * p.n_tiles, st);
+  return launch<false, false, true, EPI_SWIGLU>("gemm1_swiglu", ta, tb, to, th, p,
+                                                ws.L.MT_max * p.n_tiles, st);
 }
 
 cudaError_t gemm_fwd2(const moe_config& c, const Ws& ws, const __nv_bfloat16* A,
@@ -593,7 +779,10 @@ cudaError_t gemm_fwd2(const moe_config& c, const Ws& ws, const __nv_bfloat16* A,
   if (!map2d(&ta, A, c.f, rows, 64, kBM) || !map3d(&tb, W2, c.d, c.f, c.E, 64, 64) ||
       !map2d(&to, Yp, c.d, rows, 64, 32))
     return cudaErrorInvalidValue;
-  return launch<false, false, true, EPI_STORE>("gemm2", ta, tb, to, p, ws.L.MT_max * p.n_tiles, st);
+  if (gemm_pair_enabled(c, kGemmFwd2))
+    return launch<false, false, true, EPI_STORE, false, true>("gemm2", ta, tb, to, to, p,
+                                                              ws.L.MT_max * p.n_tiles, st);
+  return launch<false, false, true, EPI_STORE>("gemm2", ta, tb, to, to, p, ws.L.MT_max * p.n_tiles, st);
 }
 
 cudaError_t gemm_dgrad2(const moe_config& c, const Ws& ws, const __nv_bfloat16* dYp,
@@ -612,11 +801,15 @@ cudaError_t gemm_dgrad2(const moe_config& c, const Ws& ws, const __nv_bfloat16* 
   p.As = As;
   p.g_pad = ws.g_pad();
   p.dgp = dgp;
-  // B = W2[e]^T: K = d contiguous, N = f rows -> K-major box of 256 rows
-  if (!map2d(&ta, dYp, c.d, rows, 64, kBM) || !map3d(&tb, W2, c.d, c.f, c.E, 64, 256))
+  // B = W2[e]^T: K = d contiguous, N = f rows -> K-major box of 256 rows (pair: 128 a CTA)
+  const bool pair = gemm_pair_enabled(c, kGemmDgrad2);
+  if (!map2d(&ta, dYp, c.d, rows, 64, kBM) || !map3d(&tb, W2, c.d, c.f, c.E, 64, pair ? 128 : 256))
     return cudaErrorInvalidValue;
   to = tb;
-  return launch<false, false, false, EPI_DSWIGLU>("dgrad2_dswiglu", ta, tb, to, p, ws.L.MT_max * p.n_tiles, st);
+  if (pair)
+    return launch<false, false, false, EPI_DSWIGLU, false, true>("dgrad2_dswiglu", ta, tb, to, to, p,
+                                                                 ws.L.MT_max * p.n_tiles, st);
+  return launch<false, false, false, EPI_DSWIGLU>("dgrad2_dswiglu", ta, tb, to, to, p, ws.L.MT_max * p.n_tiles, st);
 }
 
 cudaError_t gemm_dgrad1(const moe_config& c, const Ws& ws, const __nv_bfloat16* dH,
@@ -628,11 +821,15 @@ cudaError_t gemm_dgrad1(const moe_config& c, const Ws& ws, const __nv_bfloat16* 
   p.n_tiles = (c.d + 255) / 256;
   p.num_kb = 2 * c.f / BK;
   p.out_cols = c.d;
-  // B = W1[e]^T: K = 2f contiguous, N = d rows
+  // B = W1[e]^T: K = 2f contiguous, N = d rows (box of 256 rows; pair: 128 a CTA)
+  const bool pair = gemm_pair_enabled(c, kGemmDgrad1);
   if (!map2d(&ta, dH, 2ull * c.f, rows, 64, kBM) ||
-      !map3d(&tb, W1, 2ull * c.f, c.d, c.E, 64, 256) || !map2d(&to, dXp, c.d, rows, 64, 32))
+      !map3d(&tb, W1, 2ull * c.f, c.d, c.E, 64, pair ? 128 : 256) || !map2d(&to, dXp, c.d, rows, 64, 32))
     return cudaErrorInvalidValue;
-  return launch<false, false, false, EPI_STORE>("dgrad1", ta, tb, to, p, ws.L.MT_max * p.n_tiles, st);
+  if (pair)
+    return launch<false, false, false, EPI_STORE, false, true>("dgrad1", ta, tb, to, to, p,
+                                                               ws.L.MT_max * p.n_tiles, st);
+  return launch<false, false, false, EPI_STORE>("dgrad1", ta, tb, to, to, p, ws.L.MT_max * p.n_tiles, st);
 }
 
 cudaError_t gemm_wgrad(const moe_config& c, const Ws& ws, const moe_sched& s,
@@ -650,7 +847,11 @@ cudaError_t gemm_wgrad(const moe_config& c, const Ws& ws, const moe_sched& s,
   if (!map2d(&ta, Amn, M, rows, 64, 64) || !map2d(&tb, Bmn, N, rows, 64, 64) ||
       !map3d(&to, dW, N, M, c.E, 64, 32))
     return cudaErrorInvalidValue;
-  return launch<true, true, true, EPI_STORE>(M == c.f ? "wgrad2" : "wgrad1", ta, tb, to, p,
+  const char* name = M == c.f ? "wgrad2" : "wgrad1";
+  if (gemm_pair_enabled(c, kGemmWgrad))
+    return launch<true, true, true, EPI_STORE, false, true>(
+        name, ta, tb, to, to, p, (long long)c.E * ((p.m_tiles_w + 1) / 2) * p.n_tiles, st);
+  return launch<true, true, true, EPI_STORE>(name, ta, tb, to, to, p,
                                              (long long)c.E * p.m_tiles_w * p.n_tiles, st);
 }
 
@@ -679,7 +880,7 @@ cudaError_t gemm_fwd1_mx(const moe_config& c, const Ws& ws, const uint8_t* Xq, c
       !map3d(&tb, W1q, c.d, 2ull * c.f, c.E, 128, 128, true))
     return cudaErrorInvalidValue;
   to = tb;
-  return launch<false, false, false, EPI_SWIGLU, true>("gemm1_swiglu_mxfp8", ta, tb, to, p,
+  return launch<false, false, false, EPI_SWIGLU, true>("gemm1_swiglu_mxfp8", ta, tb, to, to, p,
                                                        ws.L.MT_max * p.n_tiles, st);
 }
 
@@ -701,7 +902,7 @@ cudaError_t gemm_fwd2_mx(const moe_config& c, const Ws& ws, const uint8_t* Aq, c
   if (!map2d(&ta, Aq, c.f, rows, 128, kBM, true) ||
       !map3d(&tb, W2q, c.f, c.d, c.E, 128, 256, true) || !map2d(&to, Yp, c.d, rows, 64, 32))
     return cudaErrorInvalidValue;
-  return launch<false, false, false, EPI_STORE, true>("gemm2_mxfp8", ta, tb, to, p,
+  return launch<false, false, false, EPI_STORE, true>("gemm2_mxfp8", ta, tb, to, to, p,
                                                       ws.L.MT_max * p.n_tiles, st);
 }
 

@@ -23,7 +23,12 @@ __device__ __forceinline__ int find_expert(const int* off, int E, int key) {
   return lo;
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+// Logistic sigmoid and SiLU in fp32 with the hardware reciprocal (a few ulp;
+// the IEEE-rounded division costs about ten times as much in the epilogues).
+// For g below about -87 the denominator exceeds 2^126 and both return 0,
+// where the exact values are below 1e-36.
+__device__ __forceinline__ float sigmoid_f(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 __device__ __forceinline__ void unpack8(const uint4& v, float* o) {
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);

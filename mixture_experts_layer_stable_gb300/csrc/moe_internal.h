@@ -24,6 +24,23 @@ constexpr int kBM = 128;           // rows of an expert tile; expert segments ar
 __host__ __device__ inline bool thin_tile(int rows, int /*cnt*/) { return rows >= 1 && rows < kBM; }
 inline bool gemm1_thin_enabled(const moe_config& c) { return c.f % 128 == 0 && c.d <= 4096; }
 
+// The bf16 grouped GEMMs of the chain path can run on CTA pairs: a cluster of
+// two CTAs shares one tcgen05 MMA of 256 rows (128 per CTA) whose B operand
+// is split between them, so each SM loads a third less per FLOP than with a
+// one-CTA 128-row tile.  That pays where the contraction is long (the row
+// GEMMs, K = d, f or 2f); the weight-gradient GEMMs contract over one
+// expert's rows, often a handful of 64-row steps, and run one CTA per tile.
+// MOE_GEMM_PAIR=0 / 2 at build time forces one mode for every GEMM.
+enum GemmKind { kGemmFwd1, kGemmFwd2, kGemmDgrad2, kGemmDgrad1, kGemmWgrad };
+#ifndef MOE_GEMM_PAIR
+#define MOE_GEMM_PAIR 1
+#endif
+inline bool gemm_pair_enabled(const moe_config&, GemmKind k) {
+  if (MOE_GEMM_PAIR == 0) return false;
+  if (MOE_GEMM_PAIR == 2) return true;
+  return k != kGemmWgrad;
+}
+
 constexpr int kSchedChunk = 1024;  // flat routed rows per histogram / scatter block
 constexpr int kSchedThreads = 256;
 constexpr int kMaxE = 1024;
@@ -42,7 +59,7 @@ enum HdrWord {
 
 struct WsLayout {
   int64_t R = 0, Rp_max = 0, MT_max = 0, nblk = 0, nt_dg = 0;
-  size_t hdr = 0, hist = 0, poff = 0, mt_off = 0, pos_pad = 0, row_of_pad = 0, g_pad = 0;
+  size_t hdr = 0, hist = 0, poff = 0, mt_off = 0, pt_off = 0, pos_pad = 0, row_of_pad = 0, g_pad = 0;
   size_t Xp = 0, Abuf = 0, Yp = 0, dYp = 0, dH = 0, gA = 0, dgp = 0, Aq = 0, ring = 0;
   size_t ctr = 0, ctr_bytes = 0;  // ring path: window counters
   size_t total = 0;
@@ -59,6 +76,7 @@ struct Ws {
   int* hist() const { return reinterpret_cast<int*>(base + L.hist); }
   int* poff() const { return reinterpret_cast<int*>(base + L.poff); }
   int* mt_off() const { return reinterpret_cast<int*>(base + L.mt_off); }
+  int* pt_off() const { return reinterpret_cast<int*>(base + L.pt_off); }
   int* pos_pad() const { return reinterpret_cast<int*>(base + L.pos_pad); }
   int* row_of_pad() const { return reinterpret_cast<int*>(base + L.row_of_pad); }
   float* g_pad() const { return reinterpret_cast<float*>(base + L.g_pad); }

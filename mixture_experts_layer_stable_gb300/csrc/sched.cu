@@ -14,7 +14,8 @@
 //     over experts; the last block to finish (atomic ticket) turns the chunk
 //     histograms into per-chunk exclusive prefixes and computes counts,
 //     offsets and the padded layout (each expert's segment rounded up to 128
-//     rows).  Integer sums do not depend on order, so the table is
+//     rows; prefixes over experts of their 128-row tiles and of their pairs
+//     of tiles).  Integer sums do not depend on order, so the table is
 //     deterministic.
 //  3. sched_scatter: every chunk re-walks its rows in index order and ranks
 //     each row among the earlier rows of the same expert (warp match + prefix
@@ -92,7 +93,7 @@ __global__ void __launch_bounds__(kSchedThreads) sched_topk_kernel(
 __global__ void __launch_bounds__(kSchedThreads) sched_hist_kernel(
     const int* __restrict__ ids, int R, int E, int* __restrict__ hist, int* __restrict__ hdr,
     int* __restrict__ counts, int* __restrict__ offsets, int* __restrict__ poff,
-    int* __restrict__ mt_off) {
+    int* __restrict__ mt_off, int* __restrict__ pt_off) {
   __shared__ int sh[kMaxE];
   __shared__ int sh_last;
   const int tid = threadIdx.x;
@@ -131,17 +132,21 @@ __global__ void __launch_bounds__(kSchedThreads) sched_hist_kernel(
   }
   __syncthreads();
   if (tid == 0) {
-    int o = 0, po = 0;
+    int o = 0, po = 0, pt = 0;
     for (int e = 0; e < E; ++e) {
       offsets[e] = o;
       poff[e] = po;
       mt_off[e] = po / kBM;
+      pt_off[e] = pt;
+      const int mt = (sh[e] + kBM - 1) / kBM;
       o += sh[e];
-      po += (sh[e] + kBM - 1) / kBM * kBM;
+      po += mt * kBM;
+      pt += (mt + 1) >> 1;
     }
     offsets[E] = o;
     poff[E] = po;
     mt_off[E] = po / kBM;
+    pt_off[E] = pt;
     hdr[kHdrRpTotal] = po;
     hdr[kHdrMtTotal] = po / kBM;
     hdr[kHdrDone] = 0;
@@ -231,7 +236,8 @@ cudaError_t launch_schedule(const moe_config& c, const float* logits, const moe_
   {
     TraceScope ts("sched_hist", st);
     sched_hist_kernel<<<nchunk, kSchedThreads, 0, st>>>(s.topk_ids, R, c.E, ws.hist(), ws.hdr(),
-                                                        s.counts, s.offsets, ws.poff(), ws.mt_off());
+                                                        s.counts, s.offsets, ws.poff(), ws.mt_off(),
+                                                        ws.pt_off());
     err = cudaGetLastError();
   }
   if (err != cudaSuccess) return err;
