@@ -109,7 +109,8 @@ struct Params {
 struct Tile {
   int e, m, n, kb_count, row0, krow0;
   int rows;    // valid rows of a ROWS tile
-  bool thin;   // partial tile computed as (weights)^T x (rows)^T, tokens on N
+  int nt;      // thin pair unit: MMA N (rows rounded up to 32), half in each CTA
+  bool thin;   // tile computed as (weights)^T x (rows)^T, tokens on N
   bool valid;  // pair mode: the odd CTA's tile past the expert's last tile is not
 };
 
@@ -119,6 +120,21 @@ template <bool WGRAD, bool PAIR>
 __device__ __forceinline__ int total_units(const Params& p) {
   if (WGRAD) return p.E * (PAIR ? (p.m_tiles_w + 1) >> 1 : p.m_tiles_w) * p.n_tiles;
   return __ldg((PAIR ? p.pt_off : p.mt_off) + p.E) * p.n_tiles;
+}
+
+// Position L of a CTA's (cluster's) walk -> work unit.  Units are numbered
+// expert by expert; positions 2h and 2h + 1 take unit h from the front and
+// unit total-1-h from the back (which one goes first flips every `stride`
+// positions), so every wave mixes the first experts' units with the last
+// experts' and each CTA alternates between the two.  When the expert loads
+// are skewed, tiles of busy experts (limited by the tensor cores and L2) then
+// run beside tiles of experts with a few rows (limited by streaming their
+// weights from HBM).  A bijection on [0, total).
+__device__ __forceinline__ int unit_at(int L, int total, int stride) {
+  const int h = L >> 1;
+  const bool swap = (((L - (L & 1)) / stride) & 1) != 0;
+  const bool back = ((L & 1) != 0) != swap;
+  return back ? total - 1 - h : h;
 }
 
 template <bool WGRAD, bool PAIR>
@@ -133,9 +149,22 @@ __device__ __forceinline__ Tile decode(const Params& p, int L, int rank) {
     const int m0 = PAIR ? __ldg(p.mt_off + e) : u0;
     const int loc = L - u0 * p.n_tiles;
     int mrel = loc % ue;
+    t.rows = kBM;
+    t.nt = 0;
+    t.thin = false;
     if (PAIR) {
-      mrel = 2 * mrel + rank;
-      t.valid = mrel < __ldg(p.mt_off + e + 1) - m0;
+      const int me = __ldg(p.mt_off + e + 1) - m0;
+      mrel *= 2;
+      if (p.thin && mrel + 1 == me) {
+        // thin pair unit: the expert's last tile has no partner; both CTAs
+        // compute it, each with half of the weight columns on M
+        t.thin = true;
+        t.rows = min(kBM, __ldg(p.counts + e) - mrel * kBM);
+        t.nt = (t.rows + 31) & ~31;
+      } else {
+        mrel += rank;
+        t.valid = mrel < me;
+      }
     }
     t.e = e;
     t.n = loc / ue;
@@ -143,8 +172,6 @@ __device__ __forceinline__ Tile decode(const Params& p, int L, int rank) {
     t.row0 = t.m * kBM;
     t.kb_count = p.num_kb;
     t.krow0 = 0;
-    t.rows = kBM;
-    t.thin = false;
     if (!PAIR && p.thin) {
       const int cnt = __ldg(p.counts + e);
       const int rows = cnt - (t.m - m0) * kBM;
@@ -154,6 +181,7 @@ __device__ __forceinline__ Tile decode(const Params& p, int L, int rank) {
       }
     }
   } else {
+    t.nt = 0;
     const int mu = PAIR ? (p.m_tiles_w + 1) >> 1 : p.m_tiles_w;
     const int per = mu * p.n_tiles;
     t.e = L / per;
@@ -237,6 +265,7 @@ __device__ __forceinline__ void for_each_box(const Params& p, const Tile& t, int
 template <bool WGRAD, bool A_MN, bool B_MN, int EPI, bool FP8, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmA2,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmO,
                         const __grid_constant__ CUtensorMap tmO2, const Params p) {
@@ -279,6 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
+    if (PAIR && EPI == EPI_SWIGLU) tma_prefetch_desc(&tmA2);
     tma_prefetch_desc(&tmB);
     if (Cfg::kOutBufs > 0) tma_prefetch_desc(&tmO);
     if (EPI == EPI_SWIGLU && !FP8) tma_prefetch_desc(&tmO2);
@@ -309,11 +339,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       int s = 0;
       uint32_t ph = 0, used = 0, last_par = 0;
       for (int L = unit0; L < total; L += ustride) {
-        const Tile t = decode<WGRAD, PAIR>(p, L, rank);
+        const int U = unit_at(L, total, ustride);
+        const Tile t = decode<WGRAD, PAIR>(p, U, rank);
         // bytes landing on this stage's "full" barrier (pair: both CTAs' copies)
         uint32_t tx = (t.valid ? (uint32_t)kABytes : 0u) + b_bytes + (FP8 ? (uint32_t)kSfBytes : 0u);
+        if (PAIR && t.thin) tx = 16384u + (uint32_t)(t.nt / 2) * 128u;  // weights + half the rows
         if (PAIR && rank == 0)
-          tx += (decode<WGRAD, PAIR>(p, L, 1).valid ? (uint32_t)kABytes : 0u) + b_bytes;
+          tx += t.thin ? tx : (decode<WGRAD, PAIR>(p, U, 1).valid ? (uint32_t)kABytes : 0u) + b_bytes;
         for (int kb = 0; kb < t.kb_count; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status, 100 + s)) goto producer_done;
           const uint32_t sa = smem_u32(stages + (size_t)s * kStageB);
@@ -348,7 +380,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               if constexpr (PAIR) tma_load_3d_pair(sa + off, m, fb, c0, c1, c2);
               else tma_load_3d(sa + off, m, fb, c0, c1, c2);
             };
-            for_each_box<WGRAD, A_MN, B_MN, EPI, PAIR>(p, t, kb, rank, &tmA, &tmB, load2, load3);
+            if (PAIR && EPI == EPI_SWIGLU && t.thin) {
+              // thin pair unit: this CTA's 64 gate and 64 up weight columns
+              // (the MMA's A, MN-major), then its half of the rows in 16-row
+              // boxes (the MMA's B, K-major)
+              const int c0 = t.n * p.hn + rank * 64;
+              load3(0u, &tmB, c0, kb * BK, t.e);
+              load3(8192u, &tmB, p.f + c0, kb * BK, t.e);
+              const int nt2 = t.nt / 2;
+              for (int i = 0; i < nt2; i += 16)
+                load2((uint32_t)(kABytes + i * 128), &tmA2, kb * BK, t.row0 + rank * nt2 + i);
+            } else {
+              for_each_box<WGRAD, A_MN, B_MN, EPI, PAIR>(p, t, kb, rank, &tmA, &tmB, load2, load3);
+            }
           }
           used |= 1u << s;
           last_par = (last_par & ~(1u << s)) | (ph << s);
@@ -379,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int s = 0, acc = 0;
       uint32_t ph = 0, aph = 0;
       for (int L = unit0; L < total; L += ustride) {
-        const Tile t = decode<WGRAD, PAIR>(p, L, 0);
+        const Tile t = decode<WGRAD, PAIR>(p, unit_at(L, total, ustride), 0);
         if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, p.status, 200 + acc)) goto mma_done;
         tc_fence_after();
         const uint32_t dt = tmem_base + (uint32_t)acc * 256u;
@@ -418,6 +462,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                   tc_mma_f16(dt, sdesc_sw128(sb + kk * 2048, 8192, 1024), bd, idt, accf);
                   tc_mma_f16(dt + 128u, sdesc_sw128(sb + 16384 + kk * 2048, 8192, 1024), bd, idt, accf);
                 }
+                issued = true;
+              }
+            }
+            if constexpr (PAIR && EPI == EPI_SWIGLU) {
+              if (t.thin) {
+                // thin pair unit: D^T (weight columns on TMEM lanes: gate 0..63,
+                // up 64..127 in each CTA; tokens on TMEM columns) = W^T x rows^T
+                const uint32_t idt = idesc_bf16(2 * kBM, t.nt, true, false);
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)
+                  tc_mma_f16_pair(dt, sdesc_sw128(sa + kk * 2048, 8192, 1024),
+                                  sdesc_sw128(sb + kk * 32, 16, 1024), idt,
+                                  (kb > 0 || kk > 0) ? 1u : 0u);
                 issued = true;
               }
             }
@@ -483,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (++buf == Cfg::kOutBufs) buf = 0;
     };
     for (int L = unit0; L < total; L += ustride) {
-      const Tile t = decode<WGRAD, PAIR>(p, L, rank);
+      const Tile t = decode<WGRAD, PAIR>(p, unit_at(L, total, ustride), rank);
       if (!mbar_wait(&tfull[acc], aph, abort_flag, p.status, 400 + acc)) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + (uint32_t)acc * 256u + ((uint32_t)(q * 32) << 16);
@@ -560,6 +617,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             store_cols_t(tr, g, p.out1 + r0 * (2 * p.f) + c0, 2 * p.f, 32, lane);
             store_cols_t(tr, u, p.out1 + r0 * (2 * p.f) + p.f + c0, 2 * p.f, 32, lane);
           }
+        }
+      } else if (EPI == EPI_SWIGLU && !FP8 && PAIR && t.thin) {
+        // thin pair unit: TMEM lane = weight column (gate in lane quarters 0-1,
+        // up in 2-3, the same 64 columns), TMEM column = token.  Each up warp
+        // hands its values to the gate warp of the same columns through
+        // shared memory.  All 128 rows are written (zeros past the expert's
+        // rows) so that the saved activations of the padding rows stay zero.
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+        const bool is_gate = q < 2;
+        uint8_t* tr = staging + (size_t)(warp - 2) * Cfg::kOutBufs * kOutTile + 4096;
+        float* xb = reinterpret_cast<float*>(staging + (size_t)(is_gate ? q : q - 2) * Cfg::kOutBufs * kOutTile);
+        const int c0 = t.n * p.hn + rank * 64 + (q & 1) * 32;
+        for (int t0 = 0; t0 < kBM; t0 += 32) {
+          float v[32];
+          if (t0 < t.nt) {
+            tmem_ld32(tb + t0, v);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = (t0 + i < t.rows) ? v[i] : 0.f;
+          const size_t r0 = (size_t)t.row0 + t0;
+          if (!is_gate) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) xb[i * 32 + lane] = v[i];
+            if (p.out1 != nullptr) store_cols_t(tr, v, p.out1 + r0 * (2 * p.f) + p.f + c0, 2 * p.f, 32, lane);
+          }
+          named_bar_sync(1, kEpiWarps * 32);
+          if (is_gate) {
+            float a[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) a[i] = silu_f(v[i]) * xb[i * 32 + lane];
+            store_cols_t(tr, a, p.out0 + r0 * p.f + c0, p.f, 32, lane);
+            if (p.out1 != nullptr) store_cols_t(tr, v, p.out1 + r0 * (2 * p.f) + c0, 2 * p.f, 32, lane);
+          }
+          named_bar_sync(1, kEpiWarps * 32);
         }
       } else if constexpr (EPI == EPI_SWIGLU && !FP8) {
         // 64 gate and 64 up columns at a time: H (gate, up) and A = SiLU(gate) * up
@@ -679,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ host side
 template <bool WGRAD, bool A_MN, bool B_MN, int EPI, bool FP8 = false, bool PAIR = false>
-cudaError_t launch(const char* name, const CUtensorMap& a, const CUtensorMap& b,
+cudaError_t launch(const char* name, const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b,
                    const CUtensorMap& o, const CUtensorMap& o2, const Params& p, long long max_units,
                    cudaStream_t st) {
   auto kern = grouped_gemm_kernel<WGRAD, A_MN, B_MN, EPI, FP8, PAIR>;
@@ -691,7 +786,7 @@ cudaError_t launch(const char* name, const CUtensorMap& a, const CUtensorMap& b,
     if (max_units < grid) grid = max_units;
     if (grid < 1) grid = 1;
     TraceScope ts(name, st);
-    kern<<<(int)grid, kThreads, smem, st>>>(a, b, o, o2, p);
+    kern<<<(int)grid, kThreads, smem, st>>>(a, a2, b, o, o2, p);
     return cudaGetLastError();
   } else {
     // persistent clusters of two CTAs: as many as can be resident at once
@@ -722,7 +817,7 @@ cudaError_t launch(const char* name, const CUtensorMap& a, const CUtensorMap& b,
     if (clusters < 1) clusters = 1;
     cfg.gridDim = dim3((unsigned)(2 * clusters));
     TraceScope ts(name, st);
-    return cudaLaunchKernelEx(&cfg, kern, a, b, o, o2, p);
+    return cudaLaunchKernelEx(&cfg, kern, a, a2, b, o, o2, p);
   }
 }
 
@@ -753,17 +848,20 @@ cudaError_t gemm_fwd1(const moe_config& c, const Ws& ws, const int* counts, cons
   p.out1 = H;
   p.counts = counts;
   const bool pair = gemm_pair_enabled(c, kGemmFwd1);
-  p.thin = (!pair && gemm1_thin_enabled(c)) ? 1 : 0;
+  // one CTA: partial last tiles swapped when gemm1_thin_enabled; pairs: an
+  // expert's unpartnered last tile as a thin pair unit (128-column slices)
+  p.thin = (pair ? p.hn == 128 : gemm1_thin_enabled(c)) ? 1 : 0;
   // outputs: A [rows, f] and (when saved) H [rows, 2f], stored as 32 x 64 tiles
-  CUtensorMap th;
-  if (!map2d(&ta, Xp, c.d, rows, 64, kBM) || !map3d(&tb, W1, 2ull * c.f, c.d, c.E, 64, 64) ||
+  CUtensorMap th, ta16;
+  if (!map2d(&ta, Xp, c.d, rows, 64, kBM) || !map2d(&ta16, Xp, c.d, rows, 64, 16) ||
+      !map3d(&tb, W1, 2ull * c.f, c.d, c.E, 64, 64) ||
       !map2d(&to, A, c.f, rows, 64, 32) || (H != nullptr && !map2d(&th, H, 2ull * c.f, rows, 64, 32)))
     return cudaErrorInvalidValue;
   if (H == nullptr) th = to;
   if (pair)
-    return launch<false, false, true, EPI_SWIGLU, false, true>("gemm1_swiglu", ta, tb, to, th, p,
+    return launch<false, false, true, EPI_SWIGLU, false, true>("gemm1_swiglu", ta, ta16, tb, to, th, p,
                                                                ws.L.MT_max * p.n_tiles, st);
-  return launch<false, false, true, EPI_SWIGLU>("gemm1_swiglu", ta, tb, to, th, p,
+  return launch<false, false, true, EPI_SWIGLU>("gemm1_swiglu", ta, ta, tb, to, th, p,
                                                 ws.L.MT_max * p.n_tiles, st);
 }
 
@@ -780,9 +878,9 @@ cudaError_t gemm_fwd2(const moe_config& c, const Ws& ws, const __nv_bfloat16* A,
       !map2d(&to, Yp, c.d, rows, 64, 32))
     return cudaErrorInvalidValue;
   if (gemm_pair_enabled(c, kGemmFwd2))
-    return launch<false, false, true, EPI_STORE, false, true>("gemm2", ta, tb, to, to, p,
+    return launch<false, false, true, EPI_STORE, false, true>("gemm2", ta, ta, tb, to, to, p,
                                                               ws.L.MT_max * p.n_tiles, st);
-  return launch<false, false, true, EPI_STORE>("gemm2", ta, tb, to, to, p, ws.L.MT_max * p.n_tiles, st);
+  return launch<false, false, true, EPI_STORE>("gemm2", ta, ta, tb, to, to, p, ws.L.MT_max * p.n_tiles, st);
 }
 
 cudaError_t gemm_dgrad2(const moe_config& c, const Ws& ws, const __nv_bfloat16* dYp,
@@ -807,9 +905,9 @@ cudaError_t gemm_dgrad2(const moe_config& c, const Ws& ws, const __nv_bfloat16* 
     return cudaErrorInvalidValue;
   to = tb;
   if (pair)
-    return launch<false, false, false, EPI_DSWIGLU, false, true>("dgrad2_dswiglu", ta, tb, to, to, p,
+    return launch<false, false, false, EPI_DSWIGLU, false, true>("dgrad2_dswiglu", ta, ta, tb, to, to, p,
                                                                  ws.L.MT_max * p.n_tiles, st);
-  return launch<false, false, false, EPI_DSWIGLU>("dgrad2_dswiglu", ta, tb, to, to, p, ws.L.MT_max * p.n_tiles, st);
+  return launch<false, false, false, EPI_DSWIGLU>("dgrad2_dswiglu", ta, ta, tb, to, to, p, ws.L.MT_max * p.n_tiles, st);
 }
 
 cudaError_t gemm_dgrad1(const moe_config& c, const Ws& ws, const __nv_bfloat16* dH,
@@ -827,9 +925,9 @@ cudaError_t gemm_dgrad1(const moe_config& c, const Ws& ws, const __nv_bfloat16* 
       !map3d(&tb, W1, 2ull * c.f, c.d, c.E, 64, pair ? 128 : 256) || !map2d(&to, dXp, c.d, rows, 64, 32))
     return cudaErrorInvalidValue;
   if (pair)
-    return launch<false, false, false, EPI_STORE, false, true>("dgrad1", ta, tb, to, to, p,
+    return launch<false, false, false, EPI_STORE, false, true>("dgrad1", ta, ta, tb, to, to, p,
                                                                ws.L.MT_max * p.n_tiles, st);
-  return launch<false, false, false, EPI_STORE>("dgrad1", ta, tb, to, to, p, ws.L.MT_max * p.n_tiles, st);
+  return launch<false, false, false, EPI_STORE>("dgrad1", ta, ta, tb, to, to, p, ws.L.MT_max * p.n_tiles, st);
 }
 
 cudaError_t gemm_wgrad(const moe_config& c, const Ws& ws, const moe_sched& s,
@@ -850,8 +948,8 @@ cudaError_t gemm_wgrad(const moe_config& c, const Ws& ws, const moe_sched& s,
   const char* name = M == c.f ? "wgrad2" : "wgrad1";
   if (gemm_pair_enabled(c, kGemmWgrad))
     return launch<true, true, true, EPI_STORE, false, true>(
-        name, ta, tb, to, to, p, (long long)c.E * ((p.m_tiles_w + 1) / 2) * p.n_tiles, st);
-  return launch<true, true, true, EPI_STORE>(name, ta, tb, to, to, p,
+        name, ta, ta, tb, to, to, p, (long long)c.E * ((p.m_tiles_w + 1) / 2) * p.n_tiles, st);
+  return launch<true, true, true, EPI_STORE>(name, ta, ta, tb, to, to, p,
                                              (long long)c.E * p.m_tiles_w * p.n_tiles, st);
 }
 
@@ -880,7 +978,7 @@ cudaError_t gemm_fwd1_mx(const moe_config& c, const Ws& ws, const uint8_t* Xq, c
       !map3d(&tb, W1q, c.d, 2ull * c.f, c.E, 128, 128, true))
     return cudaErrorInvalidValue;
   to = tb;
-  return launch<false, false, false, EPI_SWIGLU, true>("gemm1_swiglu_mxfp8", ta, tb, to, to, p,
+  return launch<false, false, false, EPI_SWIGLU, true>("gemm1_swiglu_mxfp8", ta, ta, tb, to, to, p,
                                                        ws.L.MT_max * p.n_tiles, st);
 }
 
@@ -902,7 +1000,7 @@ cudaError_t gemm_fwd2_mx(const moe_config& c, const Ws& ws, const uint8_t* Aq, c
   if (!map2d(&ta, Aq, c.f, rows, 128, kBM, true) ||
       !map3d(&tb, W2q, c.f, c.d, c.E, 128, 256, true) || !map2d(&to, Yp, c.d, rows, 64, 32))
     return cudaErrorInvalidValue;
-  return launch<false, false, false, EPI_STORE, true>("gemm2_mxfp8", ta, tb, to, to, p,
+  return launch<false, false, false, EPI_STORE, true>("gemm2_mxfp8", ta, ta, tb, to, to, p,
                                                       ws.L.MT_max * p.n_tiles, st);
 }
 

@@ -388,6 +388,11 @@ MOE_DEV void tma_load_3d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar, 
 }
 
 // ---------------------------------------------------------------- misc
+// Barrier `id` (1..15) over `nthreads` threads of the CTA (whole warps).
+MOE_DEV void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 MOE_DEV uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
