@@ -217,7 +217,7 @@ moe_status moe_forward(const moe_config* cfg, const moe_bf16* x, const void* w1,
                                 nullptr, st);
   if (e == cudaSuccess)
     e = gemm_fwd1(c, W, sched.counts, Xp, static_cast<const __nv_bfloat16*>(w1), A, H, st);
-  if (e == cudaSuccess) e = gemm_fwd2(c, W, A, static_cast<const __nv_bfloat16*>(w2), Yp, st);
+  if (e == cudaSuccess) e = gemm_fwd2(c, W, sched.counts, A, static_cast<const __nv_bfloat16*>(w2), Yp, st);
   if (e == cudaSuccess)
     e = launch_merge(c, W, Yp, sched.topk_w, reinterpret_cast<__nv_bfloat16*>(out), st);
   return cuda_status(e);
@@ -258,7 +258,7 @@ moe_status moe_backward(const moe_config* cfg, const moe_bf16* dout, const moe_b
     e = gemm_wgrad(c, W, sched, gA, c.f, dYp, c.d, reinterpret_cast<__nv_bfloat16*>(dw2), st);
   if (e == cudaSuccess)
     e = gemm_wgrad(c, W, sched, Xp, c.d, dH, 2 * c.f, reinterpret_cast<__nv_bfloat16*>(dw1), st);
-  if (e == cudaSuccess) e = gemm_dgrad1(c, W, dH, bf(w1), dXp, st);
+  if (e == cudaSuccess) e = gemm_dgrad1(c, W, sched.counts, dH, bf(w1), dXp, st);
   if (e == cudaSuccess) e = launch_merge(c, W, dXp, nullptr, reinterpret_cast<__nv_bfloat16*>(dx), st);
   return cuda_status(e);
 }

@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
-    if (PAIR && EPI == EPI_SWIGLU) tma_prefetch_desc(&tmA2);
+    if (PAIR && !WGRAD) tma_prefetch_desc(&tmA2);
     tma_prefetch_desc(&tmB);
     if (Cfg::kOutBufs > 0) tma_prefetch_desc(&tmO);
     if (EPI == EPI_SWIGLU && !FP8) tma_prefetch_desc(&tmO2);
@@ -380,13 +380,22 @@ __global__ void __launch_bounds__(kThreads, 1)
               if constexpr (PAIR) tma_load_3d_pair(sa + off, m, fb, c0, c1, c2);
               else tma_load_3d(sa + off, m, fb, c0, c1, c2);
             };
-            if (PAIR && EPI == EPI_SWIGLU && t.thin) {
-              // thin pair unit: this CTA's 64 gate and 64 up weight columns
-              // (the MMA's A, MN-major), then its half of the rows in 16-row
-              // boxes (the MMA's B, K-major)
-              const int c0 = t.n * p.hn + rank * 64;
-              load3(0u, &tmB, c0, kb * BK, t.e);
-              load3(8192u, &tmB, p.f + c0, kb * BK, t.e);
+            if (PAIR && !WGRAD && t.thin) {
+              // thin pair unit: this CTA's weight columns as the MMA's A --
+              // SwiGLU: 64 gate and the matching 64 up columns; otherwise 128
+              // output columns (MN-major, or K-major rows for dgrad) -- then its
+              // half of the rows in 16-row boxes (the MMA's B, K-major)
+              if (EPI == EPI_SWIGLU) {
+                const int c0 = t.n * p.hn + rank * 64;
+                load3(0u, &tmB, c0, kb * BK, t.e);
+                load3(8192u, &tmB, p.f + c0, kb * BK, t.e);
+              } else if (B_MN) {
+                const int c0 = t.n * 256 + rank * 128;
+                load3(0u, &tmB, c0, kb * BK, t.e);
+                load3(8192u, &tmB, c0 + 64, kb * BK, t.e);
+              } else {
+                load3(0u, &tmB, kb * BK, t.n * 256 + rank * 128, t.e);
+              }
               const int nt2 = t.nt / 2;
               for (int i = 0; i < nt2; i += 16)
                 load2((uint32_t)(kABytes + i * 128), &tmA2, kb * BK, t.row0 + rank * nt2 + i);
@@ -465,14 +474,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issued = true;
               }
             }
-            if constexpr (PAIR && EPI == EPI_SWIGLU) {
+            if constexpr (PAIR && !WGRAD) {
               if (t.thin) {
-                // thin pair unit: D^T (weight columns on TMEM lanes: gate 0..63,
-                // up 64..127 in each CTA; tokens on TMEM columns) = W^T x rows^T
-                const uint32_t idt = idesc_bf16(2 * kBM, t.nt, true, false);
+                // thin pair unit: D^T (weight columns on TMEM lanes -- SwiGLU:
+                // gate 0..63, up 64..127 in each CTA; tokens on TMEM columns)
+                // = W^T x rows^T
+                constexpr bool kWmn = (EPI == EPI_SWIGLU) || B_MN;  // weights MN-major in smem
+                const uint32_t idt = idesc_bf16(2 * kBM, t.nt, kWmn, false);
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)
-                  tc_mma_f16_pair(dt, sdesc_sw128(sa + kk * 2048, 8192, 1024),
+                  tc_mma_f16_pair(dt, kWmn ? sdesc_sw128(sa + kk * 2048, 8192, 1024)
+                                           : sdesc_sw128(sa + kk * 32, 16, 1024),
                                   sdesc_sw128(sb + kk * 32, 16, 1024), idt,
                                   (kb > 0 || kk > 0) ? 1u : 0u);
                 issued = true;
@@ -548,6 +560,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       if (!t.valid) {
         // pair mode: the odd CTA's rows past the expert's last tile
+      } else if (EPI == EPI_STORE && PAIR && !WGRAD && t.thin) {
+        // thin pair unit: lane = output column, TMEM columns = tokens; rows
+        // [row0, row0 + nt) are written (zeros past the expert's rows)
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+        uint8_t* tr = staging + (size_t)(warp - 2) * Cfg::kOutBufs * kOutTile;
+        const int c0 = t.n * 256 + rank * 128 + q * 32;
+        if (c0 < p.out_cols) {
+          for (int t0 = 0; t0 < t.nt; t0 += 32) {
+            float v[32];
+            tmem_ld32(tb + t0, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = (t0 + i < t.rows) ? v[i] : 0.f;
+            store_cols_t(tr, v, p.out0 + ((size_t)t.row0 + t0) * p.out_cols + c0, p.out_cols, 32, lane);
+          }
+        }
       } else if constexpr (EPI == EPI_STORE) {
         const int row = (WGRAD ? t.m * kBM : t.row0) + q * 32;
         for (int c = 0; c < p.umma_n / 64; ++c) {
@@ -865,20 +893,24 @@ cudaError_t gemm_fwd1(const moe_config& c, const Ws& ws, const int* counts, cons
                                                 ws.L.MT_max * p.n_tiles, st);
 }
 
-cudaError_t gemm_fwd2(const moe_config& c, const Ws& ws, const __nv_bfloat16* A,
+cudaError_t gemm_fwd2(const moe_config& c, const Ws& ws, const int* counts, const __nv_bfloat16* A,
                       const __nv_bfloat16* W2, __nv_bfloat16* Yp, cudaStream_t st) {
-  CUtensorMap ta, tb, to;
+  CUtensorMap ta, ta16, tb, to;
   const uint64_t rows = (uint64_t)ws.L.Rp_max;
   Params p = base_params(c, ws);
   p.umma_n = 256;
   p.n_tiles = (c.d + 255) / 256;
   p.num_kb = c.f / BK;
   p.out_cols = c.d;
-  if (!map2d(&ta, A, c.f, rows, 64, kBM) || !map3d(&tb, W2, c.d, c.f, c.E, 64, 64) ||
-      !map2d(&to, Yp, c.d, rows, 64, 32))
+  p.out0 = Yp;
+  p.counts = counts;
+  const bool pair = gemm_pair_enabled(c, kGemmFwd2);
+  p.thin = pair ? 1 : 0;  // an expert's unpartnered last tile as a thin pair unit
+  if (!map2d(&ta, A, c.f, rows, 64, kBM) || !map2d(&ta16, A, c.f, rows, 64, 16) ||
+      !map3d(&tb, W2, c.d, c.f, c.E, 64, 64) || !map2d(&to, Yp, c.d, rows, 64, 32))
     return cudaErrorInvalidValue;
-  if (gemm_pair_enabled(c, kGemmFwd2))
-    return launch<false, false, true, EPI_STORE, false, true>("gemm2", ta, ta, tb, to, to, p,
+  if (pair)
+    return launch<false, false, true, EPI_STORE, false, true>("gemm2", ta, ta16, tb, to, to, p,
                                                               ws.L.MT_max * p.n_tiles, st);
   return launch<false, false, true, EPI_STORE>("gemm2", ta, ta, tb, to, to, p, ws.L.MT_max * p.n_tiles, st);
 }
@@ -910,22 +942,25 @@ cudaError_t gemm_dgrad2(const moe_config& c, const Ws& ws, const __nv_bfloat16* 
   return launch<false, false, false, EPI_DSWIGLU>("dgrad2_dswiglu", ta, ta, tb, to, to, p, ws.L.MT_max * p.n_tiles, st);
 }
 
-cudaError_t gemm_dgrad1(const moe_config& c, const Ws& ws, const __nv_bfloat16* dH,
+cudaError_t gemm_dgrad1(const moe_config& c, const Ws& ws, const int* counts, const __nv_bfloat16* dH,
                         const __nv_bfloat16* W1, __nv_bfloat16* dXp, cudaStream_t st) {
-  CUtensorMap ta, tb, to;
+  CUtensorMap ta, ta16, tb, to;
   const uint64_t rows = (uint64_t)ws.L.Rp_max;
   Params p = base_params(c, ws);
   p.umma_n = 256;
   p.n_tiles = (c.d + 255) / 256;
   p.num_kb = 2 * c.f / BK;
   p.out_cols = c.d;
+  p.out0 = dXp;
+  p.counts = counts;
   // B = W1[e]^T: K = 2f contiguous, N = d rows (box of 256 rows; pair: 128 a CTA)
   const bool pair = gemm_pair_enabled(c, kGemmDgrad1);
-  if (!map2d(&ta, dH, 2ull * c.f, rows, 64, kBM) ||
+  p.thin = pair ? 1 : 0;  // an expert's unpartnered last tile as a thin pair unit
+  if (!map2d(&ta, dH, 2ull * c.f, rows, 64, kBM) || !map2d(&ta16, dH, 2ull * c.f, rows, 64, 16) ||
       !map3d(&tb, W1, 2ull * c.f, c.d, c.E, 64, pair ? 128 : 256) || !map2d(&to, dXp, c.d, rows, 64, 32))
     return cudaErrorInvalidValue;
   if (pair)
-    return launch<false, false, false, EPI_STORE, false, true>("dgrad1", ta, ta, tb, to, to, p,
+    return launch<false, false, false, EPI_STORE, false, true>("dgrad1", ta, ta16, tb, to, to, p,
                                                                ws.L.MT_max * p.n_tiles, st);
   return launch<false, false, false, EPI_STORE>("dgrad1", ta, ta, tb, to, to, p, ws.L.MT_max * p.n_tiles, st);
 }

@@ -120,12 +120,12 @@ cudaError_t launch_quantize_mxfp8(const __nv_bfloat16* w, int64_t batch, int K, 
 // Grouped GEMMs on tcgen05 (gemm.cu).
 cudaError_t gemm_fwd1(const moe_config& c, const Ws& ws, const int* counts, const __nv_bfloat16* Xp,
                       const __nv_bfloat16* W1, __nv_bfloat16* A, __nv_bfloat16* H, cudaStream_t st);
-cudaError_t gemm_fwd2(const moe_config& c, const Ws& ws, const __nv_bfloat16* A,
+cudaError_t gemm_fwd2(const moe_config& c, const Ws& ws, const int* counts, const __nv_bfloat16* A,
                       const __nv_bfloat16* W2, __nv_bfloat16* Yp, cudaStream_t st);
 cudaError_t gemm_dgrad2(const moe_config& c, const Ws& ws, const __nv_bfloat16* dYp,
                         const __nv_bfloat16* W2, const __nv_bfloat16* Hs, const __nv_bfloat16* As,
                         __nv_bfloat16* dH, __nv_bfloat16* gA, float* dgp, cudaStream_t st);
-cudaError_t gemm_dgrad1(const moe_config& c, const Ws& ws, const __nv_bfloat16* dH,
+cudaError_t gemm_dgrad1(const moe_config& c, const Ws& ws, const int* counts, const __nv_bfloat16* dH,
                         const __nv_bfloat16* W1, __nv_bfloat16* dXp, cudaStream_t st);
 cudaError_t gemm_wgrad(const moe_config& c, const Ws& ws, const moe_sched& s,
                        const __nv_bfloat16* Amn, int M, const __nv_bfloat16* Bmn, int N,
