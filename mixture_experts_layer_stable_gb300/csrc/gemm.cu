@@ -64,7 +64,7 @@ struct KCfg {
   static constexpr int kStageBytes = kABytes + (PAIR ? kBHalfBytes : kBBytes);
   static constexpr int kStages = PAIR ? 6 : (FP8 && EPI == EPI_STORE) ? 3 : 4;
   // swizzled staging tiles per epilogue warp for the TMA-store epilogues
-  static constexpr int kOutBufs = (EPI == EPI_STORE || (EPI == EPI_SWIGLU && !FP8)) ? 2 : 0;
+  static constexpr int kOutBufs = (EPI == EPI_STORE || EPI == EPI_DSWIGLU || (EPI == EPI_SWIGLU && !FP8)) ? 2 : 0;
   static constexpr int kAcc = FP8 ? 1 : 2;
   // scale-tile region rounded to 1024 bytes: the swizzled staging tiles after
   // it must start on a 1024-byte boundary for the 128-byte swizzle pattern
@@ -311,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (PAIR && !WGRAD) tma_prefetch_desc(&tmA2);
     tma_prefetch_desc(&tmB);
     if (Cfg::kOutBufs > 0) tma_prefetch_desc(&tmO);
-    if (EPI == EPI_SWIGLU && !FP8) tma_prefetch_desc(&tmO2);
+    if (EPI == EPI_DSWIGLU || (EPI == EPI_SWIGLU && !FP8)) tma_prefetch_desc(&tmO2);
   }
   if (warp == 1) {
     if constexpr (PAIR) {
@@ -551,6 +551,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (++buf == Cfg::kOutBufs) buf = 0;
     };
+    // The same for 32 rows x 32 columns through 2 KB tiles with the 64-byte
+    // swizzle (16-byte chunk j of row r at r * 64 + ((j ^ ((r >> 1) & 3)) << 4)),
+    // four of them rotating in this warp's staging space.
+    int buf32 = 0;
+    auto put_tile32 = [&](const CUtensorMap* m, const float* v, int col, int row) {
+      if (lane == 0) bulk_wait_read<(Cfg::kOutBufs > 0 ? 2 * Cfg::kOutBufs - 1 : 0)>();
+      __syncwarp();
+      const uint32_t sbuf = stg + (uint32_t)buf32 * (kOutTile / 2);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        st_shared_v4(sbuf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), pack_bf16x2(v[8 * j + 0], v[8 * j + 1]),
+                     pack_bf16x2(v[8 * j + 2], v[8 * j + 3]), pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
+                     pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(m, sbuf, col, row);
+        bulk_commit();
+      }
+      if (++buf32 == 2 * Cfg::kOutBufs) buf32 = 0;
+    };
     for (int L = unit0; L < total; L += ustride) {
       const Tile t = decode<WGRAD, PAIR>(p, unit_at(L, total, ustride), rank);
       if (!mbar_wait(&tfull[acc], aph, abort_flag, p.status, 400 + acc)) break;
@@ -728,8 +750,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        // EPI_DSWIGLU: acc = dA' = dOut_p W2^T for f columns [n*256, n*256+256)
+        // EPI_DSWIGLU: acc = dA' = dOut_p W2^T for f columns [n*256, n*256+256);
+        // dH (gate, up) and g*A leave through TMA stores of 32 x 32 tiles
         const size_t row = (size_t)t.row0 + q * 32 + lane;
+        const int wrow = t.row0 + q * 32;
         const float gw = p.g_pad[row];
         float dg = 0.f;
         // fragments of A, H_gate, H_up for the next 32 columns are loaded while
@@ -768,9 +792,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             o2[i] = dA * hg[i] * sg;                                // d up
             o3[i] = gw * av[i];                                     // g * A (for dW2)
           }
-          store32_bf16(p.out0 + row * (2 * p.f) + col, o1);
-          store32_bf16(p.out0 + row * (2 * p.f) + p.f + col, o2);
-          store32_bf16(p.out1 + row * p.f + col, o3);
+          put_tile32(&tmO, o1, col, wrow);
+          put_tile32(&tmO, o2, p.f + col, wrow);
+          put_tile32(&tmO2, o3, col, wrow);
         }
         p.dgp[row * p.n_tiles + t.n] = dg;
       }
@@ -933,13 +957,17 @@ cudaError_t gemm_dgrad2(const moe_config& c, const Ws& ws, const __nv_bfloat16* 
   p.dgp = dgp;
   // B = W2[e]^T: K = d contiguous, N = f rows -> K-major box of 256 rows (pair: 128 a CTA)
   const bool pair = gemm_pair_enabled(c, kGemmDgrad2);
-  if (!map2d(&ta, dYp, c.d, rows, 64, kBM) || !map3d(&tb, W2, c.d, c.f, c.E, 64, pair ? 128 : 256))
+  // outputs dH [rows, 2f] and g*A [rows, f] as 32 x 32 tiles (64-byte swizzle)
+  CUtensorMap tg;
+  if (!map2d(&ta, dYp, c.d, rows, 64, kBM) || !map3d(&tb, W2, c.d, c.f, c.E, 64, pair ? 128 : 256) ||
+      !map2d(&to, dH, 2ull * c.f, rows, 32, 32, false, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !map2d(&tg, gA, c.f, rows, 32, 32, false, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
-  to = tb;
   if (pair)
-    return launch<false, false, false, EPI_DSWIGLU, false, true>("dgrad2_dswiglu", ta, ta, tb, to, to, p,
+    return launch<false, false, false, EPI_DSWIGLU, false, true>("dgrad2_dswiglu", ta, ta, tb, to, tg, p,
                                                                  ws.L.MT_max * p.n_tiles, st);
-  return launch<false, false, false, EPI_DSWIGLU>("dgrad2_dswiglu", ta, ta, tb, to, to, p, ws.L.MT_max * p.n_tiles, st);
+  return launch<false, false, false, EPI_DSWIGLU>("dgrad2_dswiglu", ta, ta, tb, to, tg, p,
+                                                 ws.L.MT_max * p.n_tiles, st);
 }
 
 cudaError_t gemm_dgrad1(const moe_config& c, const Ws& ws, const int* counts, const __nv_bfloat16* dH,

@@ -79,9 +79,11 @@ inline EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D map (bf16, or bytes for fp8): `cols` contiguous elements per row, `rows` rows.
+// 2-D map (bf16, or bytes for fp8): `cols` contiguous elements per row, `rows` rows;
+// 128-byte swizzle unless `swz` says otherwise.
 inline bool map2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-           uint32_t box_rows, bool bytes = false) {
+           uint32_t box_rows, bool bytes = false,
+           CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
@@ -89,7 +91,7 @@ inline bool map2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t es[2] = {1, 1};
   return fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
