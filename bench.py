@@ -29,25 +29,30 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE layer fwd/bwd ms, TFLOP/s and routed tokens/s; % of tensor peak and HBM BW"
 UNIT = "routed tokens/s"
 
-# kernel -> (unit kind, per-step algorithmic amount as a function of the workload)
-#   flop: 2*M*N*K of the real (unpadded) rows; bytes: one read of each input
-#   row and one write of each output row.
-def kernel_units(c):
-    R, T, d, f, k = c["T"] * c["k"], c["T"], c["d"], c["f"], c["k"]
+# kernel -> (flop kind, algorithmic FLOPs, algorithmic HBM bytes) per launch.
+#   FLOPs: 2*M*N*K over the real (unpadded) rows.  Bytes: each weight of the
+#   `touched` experts (those with rows) read once -- the weight gradients write
+#   every expert's dW -- plus one read of each input row and one write of each
+#   output row.  Memory-only kernels have no FLOPs.
+def kernel_units(c, touched):
+    R, T, d, f, k, E = c["T"] * c["k"], c["T"], c["d"], c["f"], c["k"], c["E"]
+    b = 2.0  # bf16
+    w1, w2 = touched * d * 2 * f * b, touched * f * d * b
     return {
-        "gemm1_swiglu": ("flop", 2.0 * R * d * 2 * f),
-        "gemm2": ("flop", 2.0 * R * f * d),
-        "dgrad2_dswiglu": ("flop", 2.0 * R * d * f),
-        "wgrad2": ("flop", 2.0 * R * f * d),
-        "wgrad1": ("flop", 2.0 * R * d * 2 * f),
-        "dgrad1": ("flop", 2.0 * R * 2 * f * d),
-        "gather": ("bytes", 2.0 * R * d * 2),
-        "gather_mxfp8": ("bytes", R * d * (2.0 + 1.0 + 1.0 / 32)),
-        "gemm1_swiglu_mxfp8": ("flop8", 2.0 * R * d * 2 * f),
-        "gemm2_mxfp8": ("flop8", 2.0 * R * f * d),
-        "gather_x_dy": ("bytes", 4.0 * R * d * 2),
-        "merge": ("bytes", T * (k + 1) * d * 2.0 + R * 4.0 * 2),
-        "reverse_dispatch": ("bytes", T * (k + 1) * d * 2.0 + R * 4.0),
+        "gemm1_swiglu": ("flop", 2.0 * R * d * 2 * f, w1 + R * d * b + R * 3 * f * b),
+        "gemm2": ("flop", 2.0 * R * f * d, w2 + R * f * b + R * d * b),
+        "dgrad2_dswiglu": ("flop", 2.0 * R * d * f, w2 + R * d * b + 2 * R * 3 * f * b),
+        "wgrad2": ("flop", 2.0 * R * f * d, E * f * d * b + R * f * b + R * d * b),
+        "wgrad1": ("flop", 2.0 * R * d * 2 * f, E * d * 2 * f * b + R * d * b + R * 2 * f * b),
+        "dgrad1": ("flop", 2.0 * R * 2 * f * d, w1 + R * 2 * f * b + R * d * b),
+        "gemm1_swiglu_mxfp8": ("flop8", 2.0 * R * d * 2 * f,
+                               touched * d * 2 * f * (1 + 1 / 32) + R * d * (1 + 1 / 32) + R * f * (1 + 1 / 32)),
+        "gemm2_mxfp8": ("flop8", 2.0 * R * f * d, touched * f * d * (1 + 1 / 32) + R * f * (1 + 1 / 32) + R * d * b),
+        "gather": (None, 0.0, 2.0 * R * d * b),
+        "gather_mxfp8": (None, 0.0, R * d * (2.0 + 1.0 + 1.0 / 32)),
+        "gather_x_dy": (None, 0.0, 4.0 * R * d * b),
+        "merge": (None, 0.0, T * (k + 1) * d * b + R * 4.0 * 2),
+        "reverse_dispatch": (None, 0.0, T * (k + 1) * d * b + R * 4.0),
     }
 
 
@@ -227,6 +232,21 @@ def parse():
     return ap.parse_args()
 
 
+def max_over_ranks(x, dist=None, device="cpu"):
+    """The largest x over all ranks (x itself without a process group)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(rows_per_step, steps, world, ms_max):
+    """Whole-job routed rows/s: every rank's rows over the slowest rank's time."""
+    return rows_per_step * steps * world / (ms_max / 1000.0)
+
+
 def dist_setup():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -352,13 +372,9 @@ def main():
     st = B.moe_read_status(ws)
     if st != 0:
         raise RuntimeError(f"device status after timed region: {B.moe_status_string(st)}")
-    ms_max = ms
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, dist, "cuda")
     R = cfg.T * cfg.k
-    value = R * args.steps * world / (ms_max / 1000.0)
+    value = job_throughput(R, args.steps, world, ms_max)
     ms_step = ms_max / args.steps
 
     # ---------------- end to end through the C ABI with host buffers
@@ -389,45 +405,47 @@ def main():
             e2e_step()
         e1.record()
         barrier()
-        ems = e0.elapsed_time(e1)
-        if dist is not None:
-            t = torch.tensor([ems], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": R * k_e2e * world / (ems / 1000.0), "unit": UNIT,
+        ems = max_over_ranks(e0.elapsed_time(e1), dist, "cuda")
+        e2e = {"value": job_throughput(R, k_e2e, world, ems), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": k_e2e}
 
     # ---------------- per-kernel roofline
+    # the binding resource of each kernel is the larger of FLOPs / tensor peak
+    # and algorithmic bytes / HBM bandwidth
     peaks = load_peaks()
-    units = kernel_units(workload_dict(cfg))
+    touched = int((sched["counts"] > 0).sum().item())
+    units = kernel_units(workload_dict(cfg), touched)
+
+    def roof_of(name, avg_ms):
+        kind, flop, nbytes = units[name]
+        fpeak = peaks["bf16_sustained"] * (2.0 if kind == "flop8" else 1.0)
+        t_f = flop / (fpeak * 1e12) if kind else 0.0
+        t_b = nbytes / (peaks["hbm_gbs"] * 1e9)
+        if t_f >= t_b:
+            src = (f"{peaks['source']} bf16 sustained (MEASURED_PEAKS.json)" if kind == "flop" else
+                   f"{peaks['source']} bf16 sustained x 2 (nominal fp8:bf16 dense ratio 4.5:2.25)")
+            ach = flop / (avg_ms / 1e3) / 1e12
+            return {"bound": "tensor", "achieved": ach, "peak": fpeak, "unit": "TFLOP/s",
+                    "frac": ach / fpeak, "algorithmic_per_launch": flop, "peak_source": src,
+                    "hbm_frac": nbytes / (avg_ms / 1e3) / 1e9 / peaks["hbm_gbs"]}
+        ach = nbytes / (avg_ms / 1e3) / 1e9
+        return {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"], "algorithmic_per_launch": nbytes,
+                "peak_source": f"{peaks['source']} hbm copy (MEASURED_PEAKS.json)",
+                "tensor_frac": (flop / (avg_ms / 1e3) / 1e12 / fpeak) if kind else None}
+
     kernels = {}
     for name, (cnt, tot) in per.items():
         avg = tot / cnt
         ent = {"launches": cnt, "ms_per_launch": avg, "share": tot / max(sum(v[1] for v in per.values()), 1e-9)}
         if name in units:
-            kind, amount = units[name]
-            if kind in ("flop", "flop8"):
-                ent["TFLOP/s"] = amount / (avg / 1e3) / 1e12
-            else:
-                ent["GB/s"] = amount / (avg / 1e3) / 1e9
+            r = roof_of(name, avg)
+            ent.update({"bound": r["bound"], "frac": r["frac"], r["unit"]: r["achieved"]})
         kernels[name] = ent
     dom = max(per.items(), key=lambda kv: kv[1][1])[0]
-    kind, amount = units.get(dom, ("flop", 0.0))
     avg = per[dom][1] / per[dom][0]
-    if kind in ("flop", "flop8"):
-        achieved = amount / (avg / 1e3) / 1e12
-        peak = peaks["bf16_sustained"] * (2.0 if kind == "flop8" else 1.0)
-        src = (f"{peaks['source']} bf16 sustained (MEASURED_PEAKS.json)" if kind == "flop" else
-               f"{peaks['source']} bf16 sustained x 2 (nominal fp8:bf16 dense ratio 4.5:2.25)")
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": ncu_traffic(cfg.name, dom), "kernel": dom,
-                "algorithmic_per_launch": amount, "peak_source": src}
-    else:
-        achieved = amount / (avg / 1e3) / 1e9
-        peak = peaks["hbm_gbs"]
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": ncu_traffic(cfg.name, dom), "kernel": dom,
-                "algorithmic_per_launch": amount, "peak_source": f"{peaks['source']} hbm"}
+    roof = roof_of(dom, avg) if dom in units else {"bound": None, "frac": None}
+    roof.update({"traffic": ncu_traffic(cfg.name, dom), "kernel": dom})
     fwd_names = ("gather", "gather_mxfp8", "gemm1_swiglu", "gemm2", "gemm1_swiglu_mxfp8",
                  "gemm2_mxfp8", "merge", "ring_forward")
     sched_names = ("sched_topk", "sched_hist", "sched_scatter")
