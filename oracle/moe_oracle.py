@@ -34,6 +34,8 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = [
+    "router_logits",
+    "router_backward",
     "route",
     "schedule",
     "silu",
@@ -54,6 +56,24 @@ __all__ = [
 
 def _f64(a) -> np.ndarray:
     return np.asarray(a, dtype=np.float64)
+
+
+# --------------------------------------------------------------------------
+# Router projection: the logits that routing reads come from the router of
+# [LP] 01 (it decides afresh every step which experts each token goes to).
+# Reading: a bias-free linear map of the token row, the router weight stored
+# expert by expert, logits[t, e] = sum_i x[t, i] * Wr[e, i]; and its backward.
+# --------------------------------------------------------------------------
+def router_logits(x, Wr):
+    """logits [T, E] = x [T, d] . Wr [E, d]^T, in fp64."""
+    return _f64(x) @ _f64(Wr).T
+
+
+def router_backward(x, Wr, dlogits):
+    """Backward of router_logits for an upstream gradient dlogits [T, E]:
+    dx [T, d] = dlogits . Wr and dWr [E, d] = dlogits^T . x, in fp64."""
+    dl = _f64(dlogits)
+    return dl @ _f64(Wr), dl.T @ _f64(x)
 
 
 # --------------------------------------------------------------------------
