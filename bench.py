@@ -53,6 +53,11 @@ def kernel_units(c, touched):
         "gather_x_dy": (None, 0.0, 4.0 * R * d * b),
         "merge": (None, 0.0, T * (k + 1) * d * b + R * 4.0 * 2),
         "reverse_dispatch": (None, 0.0, T * (k + 1) * d * b + R * 4.0),
+        # router projection (--router): x [T, d], Wr [E, d], logits / ids / weights
+        "router_logits": ("flop", 2.0 * T * d * E, T * d * b + E * d * b + R * 8.0),
+        "router_dlogits_bf16": (None, 0.0, T * E * 6.0),
+        "router_dx": ("flop", 2.0 * T * E * d, T * E * b + E * d * b + T * d * b),
+        "router_dw": ("flop", 2.0 * T * E * d, T * E * b + T * d * b + E * d * b),
     }
 
 
@@ -227,6 +232,9 @@ def parse():
     ap.add_argument("--minibatch-rows", type=int, default=0)
     ap.add_argument("--ring-slots", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--router", action="store_true",
+                    help="route from x and a router weight (moe_route, plus the router backward) "
+                         "instead of from the workload's synthetic logits")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
     return ap.parse_args()
@@ -326,11 +334,24 @@ def main():
         dtw = torch.empty(cfg.T * cfg.k, dtype=torch.float32, device="cuda")
         dlog = torch.empty(cfg.T, cfg.E, dtype=torch.float32, device="cuda")
 
+    if args.router:
+        gr = torch.Generator(device="cuda").manual_seed(5)
+        w_router = (torch.randn(cfg.E, cfg.d, device="cuda", generator=gr) / cfg.d ** 0.5).to(torch.bfloat16)
+        r_logits = None if cfg.E <= 256 else torch.empty(cfg.T, cfg.E, dtype=torch.float32, device="cuda")
+        if bwd:
+            dx_r = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device="cuda")
+            dw_r = torch.empty_like(w_router)
+
     def step(logits=inp["logits"], x=inp["x"], dOut=inp.get("dOut")):
-        B.moe_schedule(c, logits, sched, ws)
+        if args.router:
+            B.moe_route(c, x, w_router, r_logits, sched, ws)
+        else:
+            B.moe_schedule(c, logits, sched, ws)
         B.moe_forward(c, x, w1, w1s, w2, w2s, sched, out, saved, ws)
         if bwd:
             B.moe_backward(c, dOut, x, inp["W1"], inp["W2"], sched, saved, dx, dW1, dW2, dtw, dlog, ws)
+            if args.router:
+                B.moe_router_backward(c, x, w_router, dlog, dx_r, dw_r, ws)
 
     for _ in range(args.warmup):
         step()
@@ -448,11 +469,13 @@ def main():
     roof.update({"traffic": ncu_traffic(cfg.name, dom), "kernel": dom})
     fwd_names = ("gather", "gather_mxfp8", "gemm1_swiglu", "gemm2", "gemm1_swiglu_mxfp8",
                  "gemm2_mxfp8", "merge", "ring_forward")
-    sched_names = ("sched_topk", "sched_hist", "sched_scatter")
+    sched_names = ("sched_topk", "sched_hist", "sched_scatter", "router_logits")
     fwd_ms = sum(per[n][1] for n in per if n in fwd_names) / args.steps
     sch_ms = sum(per[n][1] for n in per if n in sched_names) / args.steps
     bwd_ms = sum(per[n][1] for n in per if n not in fwd_names + sched_names) / args.steps
     flops = (6.0 if not bwd else 18.0) * R * cfg.d * cfg.f
+    if args.router:
+        flops += (2.0 if not bwd else 6.0) * cfg.T * cfg.d * cfg.E
 
     # ---------------- CPU baseline: the oracle on a bounded sample
     cpu = None
@@ -471,6 +494,7 @@ def main():
         "data": "synthetic (seeded torch generators on device; no dataset, random-init weights)",
         "config": {"workload": cfg.name, **workload_dict(cfg), "passes": passes,
                    "minibatch_rows": args.minibatch_rows,
+                   "routing": "router projection (moe_route)" if args.router else "synthetic logits",
                    "l2": "inputs larger than L2 (weights %.2f GB per step)" % (
                        (inp["W1"].numel() + inp["W2"].numel()) * 2 / 1e9),
                    "parallelism": f"replicas x{world}"},

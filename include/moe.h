@@ -131,6 +131,34 @@ int32_t moe_min_minibatch(int32_t compute_sms, int32_t bm, int32_t bn, int32_t n
 moe_status moe_schedule(const moe_config* cfg, const float* logits, moe_sched sched,
                         void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* Router projection + routing + schedule table: the logits are computed from
+ * the token rows by the router ([LP] 01: the router decides every step which
+ * experts each token goes to), then routed and scheduled exactly as
+ * moe_schedule does.  Reading: a bias-free linear router,
+ *   logits[t, e] = sum_i x[t, i] * w_router[e, i]
+ * with bf16 products accumulated in fp32 on the tensor cores.
+ *   x: device bf16 [T, d]; w_router: device bf16 [E, d] (row e = expert e).
+ *   logits: device fp32 [T, E] output; may be NULL when E <= 256, where the
+ *   top-k and its weights are taken in the GEMM's epilogue and the logits are
+ *   never written (E > 256: required; the top-k runs on the stored logits).
+ *   The routing decisions are those of moe_schedule on the same fp32 logits,
+ *   bit for bit.  Writes every array of `sched` and the workspace as
+ *   moe_schedule does. */
+moe_status moe_route(const moe_config* cfg, const moe_bf16* x, const moe_bf16* w_router,
+                     float* logits, moe_sched sched, void* ws, size_t ws_bytes,
+                     moe_stream_t stream);
+
+/* Backward of the router projection for an upstream gradient dlogits (as
+ * moe_backward writes it):
+ *   dx_router[t, i] = sum_e dlogits[t, e] * w_router[e, i]   (add it to dx)
+ *   dw_router[e, i] = sum_t dlogits[t, e] * x[t, i]
+ * dlogits: device fp32 [T, E], rounded to bf16 for the tensor cores;
+ * dx_router: device bf16 [T, d] output; dw_router: device bf16 [E, d] output.
+ * Uses the workspace (not the schedule in it). */
+moe_status moe_router_backward(const moe_config* cfg, const moe_bf16* x, const moe_bf16* w_router,
+                               const float* dlogits, moe_bf16* dx_router, moe_bf16* dw_router,
+                               void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* moe_schedule without a workspace.  The pages have no counterpart: this is a
  * convenience for callers that cannot allocate device memory -- for example a
  * plugin running inside a host framework that hands it only its input and

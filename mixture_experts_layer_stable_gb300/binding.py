@@ -31,6 +31,7 @@ EXPORTED = [
     "moe_workspace_bytes", "moe_saved_rows", "moe_min_minibatch", "moe_schedule",
     "moe_quantize_mxfp8", "moe_forward", "moe_backward", "moe_read_status", "moe_status_string",
     "moe_trace_enable", "moe_trace_count", "moe_trace_read", "moe_schedule_noalloc",
+    "moe_route", "moe_router_backward",
 ]
 
 
@@ -95,6 +96,10 @@ def lib():
         L.moe_trace_read.restype = ctypes.c_int
         L.moe_schedule_noalloc.argtypes = [cfgp, vp, moe_sched, vp]
         L.moe_schedule_noalloc.restype = ctypes.c_int
+        L.moe_route.argtypes = [cfgp, vp, vp, vp, moe_sched, vp, sz, vp]
+        L.moe_route.restype = ctypes.c_int
+        L.moe_router_backward.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.moe_router_backward.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -147,6 +152,20 @@ def sched_struct(s):
 def moe_schedule(cfg, logits, sched, ws, stream=None):
     _check(lib().moe_schedule(ctypes.byref(cfg), _ptr(logits), sched_struct(sched), _ptr(ws),
                               ws.numel() * ws.element_size(), _stream(stream)), "moe_schedule")
+
+
+def moe_route(cfg, x, w_router, logits, sched, ws, stream=None):
+    """Router projection + routing + schedule (logits may be None when E <= 256)."""
+    _check(lib().moe_route(ctypes.byref(cfg), _ptr(x), _ptr(w_router),
+                           None if logits is None else _ptr(logits), sched_struct(sched), _ptr(ws),
+                           ws.numel() * ws.element_size(), _stream(stream)), "moe_route")
+
+
+def moe_router_backward(cfg, x, w_router, dlogits, dx_router, dw_router, ws, stream=None):
+    _check(lib().moe_router_backward(ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(dlogits),
+                                     _ptr(dx_router), _ptr(dw_router), _ptr(ws),
+                                     ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_router_backward")
 
 
 def moe_schedule_noalloc(cfg, logits, sched, stream=None):

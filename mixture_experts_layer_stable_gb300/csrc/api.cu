@@ -57,6 +57,7 @@ WsLayout ws_layout(const moe_config* c) {
   L.gA = take(rp * c->f * 2);
   L.dgp = take(rp * L.nt_dg * sizeof(float));
   L.Aq = take(c->prec == MOE_MXFP8 ? rp * c->f + rp * (c->f / 32) : 0);
+  L.dl16 = take((size_t)c->T * ((c->E + 63) / 64 * 64) * 2);
   if (c->minibatch_rows > 0) {
     L.ring = take((size_t)c->ring_slots * ring_window_rows(*c) * c->d * 2);
     L.ctr_bytes = (size_t)(2 * c->ring_slots + 2 + L.MT_max) * sizeof(int);
@@ -148,6 +149,51 @@ moe_status moe_schedule(const moe_config* cfg, const float* logits, moe_sched sc
   w.base = static_cast<uint8_t*>(ws);
   if (ws_bytes < w.L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   return cuda_status(launch_schedule(*cfg, logits, sched, w, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_route(const moe_config* cfg, const moe_bf16* x, const moe_bf16* w_router,
+                     float* logits, moe_sched sched, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!config_valid(cfg) || !aligned(x) || !aligned(w_router) || !sched_ok(sched) || !aligned(ws))
+    return MOE_ERR_INVALID_ARG;
+  if (logits == nullptr ? cfg->E > 256 : !aligned(logits)) return MOE_ERR_INVALID_ARG;
+  Ws w;
+  w.L = ws_layout(cfg);
+  w.base = static_cast<uint8_t*>(ws);
+  if (ws_bytes < w.L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const moe_config& c = *cfg;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const bool fused = c.E <= 256;
+  cudaError_t e = cudaMemsetAsync(w.hdr(), 0, kHdrWords * sizeof(int), st);
+  if (e == cudaSuccess)
+    e = router_gemm(c, w, reinterpret_cast<const __nv_bfloat16*>(x),
+                    reinterpret_cast<const __nv_bfloat16*>(w_router), logits,
+                    fused ? sched.topk_ids : nullptr, sched.topk_w, st);
+  if (e == cudaSuccess && !fused) e = launch_topk(c, logits, sched, st);
+  if (e == cudaSuccess) e = launch_schedule_tail(c, sched, w, st);
+  return cuda_status(e);
+}
+
+moe_status moe_router_backward(const moe_config* cfg, const moe_bf16* x, const moe_bf16* w_router,
+                               const float* dlogits, moe_bf16* dx_router, moe_bf16* dw_router,
+                               void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!config_valid(cfg) || !aligned(x) || !aligned(w_router) || !aligned(dlogits) ||
+      !aligned(dx_router) || !aligned(dw_router) || !aligned(ws))
+    return MOE_ERR_INVALID_ARG;
+  Ws w;
+  w.L = ws_layout(cfg);
+  w.base = static_cast<uint8_t*>(ws);
+  if (ws_bytes < w.L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const moe_config& c = *cfg;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int Epad = (c.E + 63) / 64 * 64;
+  auto* dl16 = static_cast<__nv_bfloat16*>(w.at(w.L.dl16));
+  cudaError_t e = launch_to_bf16_padded(dlogits, c.T, c.E, Epad, dl16, st);
+  if (e == cudaSuccess)
+    e = router_bwd(c, w, dl16, Epad, reinterpret_cast<const __nv_bfloat16*>(x),
+                   reinterpret_cast<const __nv_bfloat16*>(w_router),
+                   reinterpret_cast<__nv_bfloat16*>(dx_router),
+                   reinterpret_cast<__nv_bfloat16*>(dw_router), st);
+  return cuda_status(e);
 }
 
 moe_status moe_quantize_mxfp8(const moe_bf16* w, int64_t batch, int32_t K, int32_t N, uint8_t* q,

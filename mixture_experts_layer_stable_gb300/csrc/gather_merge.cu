@@ -229,4 +229,24 @@ cudaError_t launch_quantize_mxfp8(const __nv_bfloat16* w, int64_t batch, int K, 
   return cudaGetLastError();
 }
 
+namespace {
+__global__ void to_bf16_padded_kernel(const float* __restrict__ src, int T, int E, int Epad,
+                                      __nv_bfloat16* __restrict__ dst) {
+  const size_t n = (size_t)T * Epad;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / Epad), e = (int)(i % Epad);
+    dst[i] = __float2bfloat16_rn(e < E ? src[(size_t)t * E + e] : 0.f);
+  }
+}
+}  // namespace
+
+cudaError_t launch_to_bf16_padded(const float* src, int T, int E, int Epad, __nv_bfloat16* dst,
+                                  cudaStream_t st) {
+  const size_t n = (size_t)T * Epad;
+  const int blocks = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+  TraceScope ts("router_dlogits_bf16", st);
+  to_bf16_padded_kernel<<<blocks, 256, 0, st>>>(src, T, E, Epad, dst);
+  return cudaGetLastError();
+}
+
 }  // namespace moe

@@ -27,6 +27,7 @@
 // MOE_ERR_TIMEOUT in the workspace status word, stops, drains its in-flight
 // copies and MMAs, frees TMEM and returns.
 #include <cuda_bf16.h>
+#include <math.h>
 
 #include "moe_internal.h"
 #include "gemm_common.cuh"
@@ -51,7 +52,7 @@ constexpr int kTmemSf = 256;              // fp8: per-stage scale columns start 
 constexpr int kTmemSfStride = 16;         // fp8: TMEM columns per stage (A: 4, B: 8; 8-aligned)
 constexpr int kTrTile = 32 * 80;          // 32 rows x (64 + 16 pad) bytes: per-warp transpose tile
 
-enum Epi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2 };
+enum Epi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2, EPI_LOGITS = 3 };
 
 // Pipeline shape per variant.  The fp8 kernels keep one TMEM accumulator
 // (256 columns) and put the per-stage scale factors (16 columns a stage) in
@@ -103,6 +104,13 @@ struct Params {
   uint8_t* q_out;           // FP8 SWIGLU: E4M3 codes of A [rows, f]
   uint8_t* q_sf;            // FP8 SWIGLU: scale tiles of A
   int thin;                 // bf16 GEMM1: compute an expert's partial last tile swapped
+  // dense mode (router GEMMs): ROWS without mt_off walks dense_mt 128-row
+  // tiles of one matrix; WGRAD without counts contracts over dense_k rows
+  int dense_mt, dense_k, T;
+  float* logits;            // LOGITS: fp32 [T, E] output (may be null when the top-k is fused)
+  int* topk_ids;            // LOGITS: fused top-k (one N tile): ids [T, k] and weights [T, k]
+  float* topk_w;
+  int k;
   int* status;
 };
 
@@ -119,6 +127,7 @@ struct Tile {
 template <bool WGRAD, bool PAIR>
 __device__ __forceinline__ int total_units(const Params& p) {
   if (WGRAD) return p.E * (PAIR ? (p.m_tiles_w + 1) >> 1 : p.m_tiles_w) * p.n_tiles;
+  if (p.mt_off == nullptr) return p.dense_mt * p.n_tiles;
   return __ldg((PAIR ? p.pt_off : p.mt_off) + p.E) * p.n_tiles;
 }
 
@@ -141,7 +150,18 @@ template <bool WGRAD, bool PAIR>
 __device__ __forceinline__ Tile decode(const Params& p, int L, int rank) {
   Tile t;
   t.valid = true;
-  if (!WGRAD) {
+  if (!WGRAD && p.mt_off == nullptr) {
+    // dense: tile m of one [T, K] matrix
+    t.e = 0;
+    t.m = L / p.n_tiles;
+    t.n = L - t.m * p.n_tiles;
+    t.row0 = t.m * kBM;
+    t.kb_count = p.num_kb;
+    t.krow0 = 0;
+    t.rows = min(kBM, p.T - t.row0);
+    t.nt = 0;
+    t.thin = false;
+  } else if (!WGRAD) {
     const int* uoff = PAIR ? p.pt_off : p.mt_off;
     const int e = find_expert(uoff, p.E, L / p.n_tiles);
     const int u0 = __ldg(uoff + e);
@@ -189,8 +209,13 @@ __device__ __forceinline__ Tile decode(const Params& p, int L, int rank) {
     t.m = PAIR ? 2 * (loc % mu) + rank : loc % mu;
     t.n = loc / mu;
     t.valid = t.m < p.m_tiles_w;
-    t.kb_count = (__ldg(p.counts + t.e) + BK - 1) / BK;
-    t.krow0 = __ldg(p.poff + t.e);
+    if (p.counts != nullptr) {
+      t.kb_count = (__ldg(p.counts + t.e) + BK - 1) / BK;
+      t.krow0 = __ldg(p.poff + t.e);
+    } else {
+      t.kb_count = (p.dense_k + BK - 1) / BK;
+      t.krow0 = 0;
+    }
     t.row0 = 0;
     t.rows = kBM;
     t.thin = false;
@@ -749,6 +774,62 @@ __global__ void __launch_bounds__(kThreads, 1)
             store32_bf16(p.out1 + row * (2 * p.f) + p.f + col, u);
           }
         }
+      } else if constexpr (EPI == EPI_LOGITS) {
+        // router: this thread's row of fp32 logits for experts [n*256, n*256+256);
+        // with one N tile the row is complete here, and its top-k (value
+        // descending, ties to the lower expert id) and softmax weights over
+        // the selected logits are taken in the same fp32 steps as sched_topk
+        const int r = t.row0 + q * 32 + lane;
+        const bool fused = p.topk_ids != nullptr;
+        float bv[kMaxK];
+        int bi[kMaxK];
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+          bv[j] = -INFINITY;
+          bi[j] = 0x7fffffff;
+        }
+        for (int c = 0; c < p.umma_n; c += 32) {
+          float v[32];
+          tmem_ld32(tb + c, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int e = t.n * 256 + c + i;
+            if (r >= p.T || e >= p.E) continue;
+            if (p.logits != nullptr) p.logits[(size_t)r * p.E + e] = v[i];
+            if (fused) {
+              // insertion into the sorted top-k by compare-and-swap
+              float cv = v[i];
+              int ci = e;
+#pragma unroll
+              for (int j = 0; j < kMaxK; ++j) {
+                if (j < p.k && (cv > bv[j] || (cv == bv[j] && ci < bi[j]))) {
+                  const float tv = bv[j];
+                  const int ti = bi[j];
+                  bv[j] = cv;
+                  bi[j] = ci;
+                  cv = tv;
+                  ci = ti;
+                }
+              }
+            }
+          }
+        }
+        if (fused && r < p.T) {
+          float ex[kMaxK];
+          float ssum = 0.f;
+#pragma unroll
+          for (int j = 0; j < kMaxK; ++j) {
+            ex[j] = (j < p.k) ? expf(bv[j] - bv[0]) : 0.f;
+            if (j < p.k) ssum += ex[j];
+          }
+#pragma unroll
+          for (int j = 0; j < kMaxK; ++j) {
+            if (j < p.k) {
+              p.topk_ids[(size_t)r * p.k + j] = bi[j];
+              p.topk_w[(size_t)r * p.k + j] = ex[j] / ssum;
+            }
+          }
+        }
       } else {
         // EPI_DSWIGLU: acc = dA' = dOut_p W2^T for f columns [n*256, n*256+256);
         // dH (gate, up) and g*A leave through TMA stores of 32 x 32 tiles
@@ -1014,6 +1095,69 @@ cudaError_t gemm_wgrad(const moe_config& c, const Ws& ws, const moe_sched& s,
         name, ta, ta, tb, to, to, p, (long long)c.E * ((p.m_tiles_w + 1) / 2) * p.n_tiles, st);
   return launch<true, true, true, EPI_STORE>(name, ta, ta, tb, to, to, p,
                                              (long long)c.E * p.m_tiles_w * p.n_tiles, st);
+}
+
+// Router logits [T, E] = x [T, d] . Wr [E, d]^T (fp32 accumulation), one CTA
+// per 128 x 256 tile; with E <= 256 and topk_ids given the epilogue also takes
+// each row's top-k and weights.
+cudaError_t router_gemm(const moe_config& c, const Ws& ws, const __nv_bfloat16* x,
+                        const __nv_bfloat16* Wr, float* logits, int* topk_ids, float* topk_w,
+                        cudaStream_t st) {
+  CUtensorMap ta, tb;
+  Params p = base_params(c, ws);
+  p.mt_off = nullptr;
+  p.T = c.T;
+  p.dense_mt = (c.T + kBM - 1) / kBM;
+  p.n_tiles = (c.E + 255) / 256;
+  p.umma_n = p.n_tiles > 1 ? 256 : (c.E + 15) / 16 * 16;
+  p.num_kb = c.d / BK;
+  p.logits = logits;
+  p.topk_ids = p.n_tiles == 1 ? topk_ids : nullptr;
+  p.topk_w = topk_w;
+  p.k = c.k;
+  if (!map2d(&ta, x, c.d, (uint64_t)c.T, 64, kBM) || !map3d(&tb, Wr, c.d, c.E, 1, 64, 256))
+    return cudaErrorInvalidValue;
+  return launch<false, false, false, EPI_LOGITS>("router_logits", ta, ta, tb, ta, ta, p,
+                                                 (long long)p.dense_mt * p.n_tiles, st);
+}
+
+// Router backward: dx_r [T, d] = dlogits [T, Epad] . Wr [E, d] and
+// dWr [E, d] = dlogits^T . x; dlogits in bf16 with Epad (E rounded up to 64)
+// columns, zero past E.
+cudaError_t router_bwd(const moe_config& c, const Ws& ws, const __nv_bfloat16* dl16, int Epad,
+                       const __nv_bfloat16* x, const __nv_bfloat16* Wr, __nv_bfloat16* dx_r,
+                       __nv_bfloat16* dWr, cudaStream_t st) {
+  CUtensorMap ta, tb, to;
+  {
+    Params p = base_params(c, ws);
+    p.mt_off = nullptr;
+    p.T = c.T;
+    p.dense_mt = (c.T + kBM - 1) / kBM;
+    p.umma_n = 256;
+    p.n_tiles = (c.d + 255) / 256;
+    p.num_kb = Epad / BK;
+    p.out_cols = c.d;
+    if (!map2d(&ta, dl16, (uint64_t)Epad, (uint64_t)c.T, 64, kBM) ||
+        !map3d(&tb, Wr, c.d, c.E, 1, 64, 64) || !map2d(&to, dx_r, c.d, (uint64_t)c.T, 64, 32))
+      return cudaErrorInvalidValue;
+    const cudaError_t e = launch<false, false, true, EPI_STORE>("router_dx", ta, ta, tb, to, to, p,
+                                                                (long long)p.dense_mt * p.n_tiles, st);
+    if (e != cudaSuccess) return e;
+  }
+  Params p = base_params(c, ws);
+  p.E = 1;
+  p.counts = nullptr;
+  p.dense_k = c.T;
+  p.umma_n = 256;
+  p.m_tiles_w = (c.E + kBM - 1) / kBM;
+  p.n_tiles = (c.d + 255) / 256;
+  p.out_cols = c.d;
+  p.out_rows = c.E;
+  if (!map2d(&ta, dl16, (uint64_t)Epad, (uint64_t)c.T, 64, 64) || !map2d(&tb, x, c.d, (uint64_t)c.T, 64, 64) ||
+      !map3d(&to, dWr, c.d, c.E, 1, 64, 32))
+    return cudaErrorInvalidValue;
+  return launch<true, true, true, EPI_STORE>("router_dw", ta, ta, tb, to, to, p,
+                                             (long long)p.m_tiles_w * p.n_tiles, st);
 }
 
 // MXFP8 GEMM1: Xq [rows, d] E4M3 (+ scale tiles) x W1q [E, 2f, d] E4M3 (+ scale

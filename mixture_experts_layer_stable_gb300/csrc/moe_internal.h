@@ -61,6 +61,7 @@ struct WsLayout {
   int64_t R = 0, Rp_max = 0, MT_max = 0, nblk = 0, nt_dg = 0;
   size_t hdr = 0, hist = 0, poff = 0, mt_off = 0, pt_off = 0, pos_pad = 0, row_of_pad = 0, g_pad = 0;
   size_t Xp = 0, Abuf = 0, Yp = 0, dYp = 0, dH = 0, gA = 0, dgp = 0, Aq = 0, ring = 0;
+  size_t dl16 = 0;  // router backward: dlogits in bf16 [T, E rounded up to 64]
   size_t ctr = 0, ctr_bytes = 0;  // ring path: window counters
   size_t total = 0;
 };
@@ -102,6 +103,14 @@ struct TraceScope {
 // ---- launchers (return a cudaError_t from the launch) ----
 cudaError_t launch_schedule(const moe_config& c, const float* logits, const moe_sched& s,
                             const Ws& ws, cudaStream_t st);
+// The parts of it: top-k routing of fp32 logits, and the table from the ids
+// (histogram, scans, stable scatter; expects the header words zeroed).
+cudaError_t launch_topk(const moe_config& c, const float* logits, const moe_sched& s, cudaStream_t st);
+cudaError_t launch_schedule_tail(const moe_config& c, const moe_sched& s, const Ws& ws,
+                                 cudaStream_t st);
+// dst [T, Epad] bf16 = src [T, E] fp32 rounded, zero in columns [E, Epad).
+cudaError_t launch_to_bf16_padded(const float* src, int T, int E, int Epad, __nv_bfloat16* dst,
+                                  cudaStream_t st);
 // dst[pp] = src[row_of_pad[pp] / k] (zero rows for padding), pp < Rp_total.
 cudaError_t launch_gather(const moe_config& c, const Ws& ws, const __nv_bfloat16* src,
                           __nv_bfloat16* dst, const __nv_bfloat16* src2, __nv_bfloat16* dst2,
@@ -134,6 +143,14 @@ cudaError_t gemm_wgrad(const moe_config& c, const Ws& ws, const moe_sched& s,
 cudaError_t ring_forward(const moe_config& c, const Ws& ws, const int* counts, const __nv_bfloat16* x,
                          const __nv_bfloat16* W1, const __nv_bfloat16* W2, const float* topk_w,
                          __nv_bfloat16* A, __nv_bfloat16* H, __nv_bfloat16* out, cudaStream_t st);
+// Router projection (gemm.cu): logits = x Wr^T with the top-k fused when E <= 256,
+// and its backward (dx_r = dlogits Wr, dWr = dlogits^T x).
+cudaError_t router_gemm(const moe_config& c, const Ws& ws, const __nv_bfloat16* x,
+                        const __nv_bfloat16* Wr, float* logits, int* topk_ids, float* topk_w,
+                        cudaStream_t st);
+cudaError_t router_bwd(const moe_config& c, const Ws& ws, const __nv_bfloat16* dl16, int Epad,
+                       const __nv_bfloat16* x, const __nv_bfloat16* Wr, __nv_bfloat16* dx_r,
+                       __nv_bfloat16* dWr, cudaStream_t st);
 cudaError_t gemm_fwd1_mx(const moe_config& c, const Ws& ws, const uint8_t* Xq, const uint8_t* Xs,
                          const uint8_t* W1q, const uint8_t* W1s, uint8_t* Aq, uint8_t* As,
                          __nv_bfloat16* A, __nv_bfloat16* H, cudaStream_t st);

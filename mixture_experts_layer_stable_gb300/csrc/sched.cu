@@ -220,19 +220,11 @@ __global__ void __launch_bounds__(kSchedThreads) sched_scatter_kernel(
 
 }  // namespace
 
-cudaError_t launch_schedule(const moe_config& c, const float* logits, const moe_sched& s,
-                            const Ws& ws, cudaStream_t st) {
+cudaError_t launch_schedule_tail(const moe_config& c, const moe_sched& s, const Ws& ws,
+                                 cudaStream_t st) {
   const int R = c.T * c.k;
   const int nchunk = (int)ws.L.nblk;
-  cudaError_t err = cudaMemsetAsync(ws.hdr(), 0, kHdrWords * sizeof(int), st);
-  if (err != cudaSuccess) return err;
-  {
-    TraceScope ts("sched_topk", st);
-    sched_topk_kernel<<<(c.T + kWarps - 1) / kWarps, kSchedThreads, 0, st>>>(logits, c.T, c.E, c.k,
-                                                                            s.topk_ids, s.topk_w);
-    err = cudaGetLastError();
-  }
-  if (err != cudaSuccess) return err;
+  cudaError_t err;
   {
     TraceScope ts("sched_hist", st);
     sched_hist_kernel<<<nchunk, kSchedThreads, 0, st>>>(s.topk_ids, R, c.E, ws.hist(), ws.hdr(),
@@ -246,6 +238,21 @@ cudaError_t launch_schedule(const moe_config& c, const float* logits, const moe_
       s.topk_ids, s.topk_w, R, c.E, ws.hist(), s.counts, s.offsets, ws.poff(), s.perm, s.inv,
       ws.pos_pad(), ws.row_of_pad(), ws.g_pad());
   return cudaGetLastError();
+}
+
+cudaError_t launch_topk(const moe_config& c, const float* logits, const moe_sched& s, cudaStream_t st) {
+  TraceScope ts("sched_topk", st);
+  sched_topk_kernel<<<(c.T + kWarps - 1) / kWarps, kSchedThreads, 0, st>>>(logits, c.T, c.E, c.k,
+                                                                          s.topk_ids, s.topk_w);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_schedule(const moe_config& c, const float* logits, const moe_sched& s,
+                            const Ws& ws, cudaStream_t st) {
+  cudaError_t err = cudaMemsetAsync(ws.hdr(), 0, kHdrWords * sizeof(int), st);
+  if (err == cudaSuccess) err = launch_topk(c, logits, s, st);
+  if (err == cudaSuccess) err = launch_schedule_tail(c, s, ws, st);
+  return err;
 }
 
 }  // namespace moe
