@@ -775,60 +775,54 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else if constexpr (EPI == EPI_LOGITS) {
-        // router: this thread's row of fp32 logits for experts [n*256, n*256+256);
-        // with one N tile the row is complete here, and its top-k (value
-        // descending, ties to the lower expert id) and softmax weights over
-        // the selected logits are taken in the same fp32 steps as sched_topk
+        // router: this thread's row of fp32 logits for experts [n*256, n*256+256)
         const int r = t.row0 + q * 32 + lane;
-        const bool fused = p.topk_ids != nullptr;
-        float bv[kMaxK];
-        int bi[kMaxK];
+        if (p.logits != nullptr) {
+          for (int c = 0; c < p.umma_n; c += 32) {
+            float v[32];
+            tmem_ld32(tb + c, v);
 #pragma unroll
-        for (int j = 0; j < kMaxK; ++j) {
-          bv[j] = -INFINITY;
-          bi[j] = 0x7fffffff;
+            for (int i = 0; i < 32; ++i) {
+              const int e = t.n * 256 + c + i;
+              if (r < p.T && e < p.E) p.logits[(size_t)r * p.E + e] = v[i];
+            }
+          }
         }
-        for (int c = 0; c < p.umma_n; c += 32) {
-          float v[32];
-          tmem_ld32(tb + c, v);
+        if (p.topk_ids != nullptr) {
+          // one N tile holds the whole row: its top-k in k rounds, round j
+          // taking the best (value descending, id ascending) strictly after
+          // round j-1's pick; weights exp(z_j - z_0) summed in slot order and
+          // divided by the sum -- the same fp32 steps as sched_topk
+          float pv = INFINITY, z0 = 0.f, ssum = 0.f;
+          int pi = -1;
+          for (int j = 0; j < p.k; ++j) {
+            float bv = -INFINITY;
+            int bi = 0x7fffffff;
+            for (int c = 0; c < p.umma_n; c += 32) {
+              float v[32];
+              tmem_ld32(tb + c, v);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int e = t.n * 256 + c + i;
-            if (r >= p.T || e >= p.E) continue;
-            if (p.logits != nullptr) p.logits[(size_t)r * p.E + e] = v[i];
-            if (fused) {
-              // insertion into the sorted top-k by compare-and-swap
-              float cv = v[i];
-              int ci = e;
-#pragma unroll
-              for (int j = 0; j < kMaxK; ++j) {
-                if (j < p.k && (cv > bv[j] || (cv == bv[j] && ci < bi[j]))) {
-                  const float tv = bv[j];
-                  const int ti = bi[j];
-                  bv[j] = cv;
-                  bi[j] = ci;
-                  cv = tv;
-                  ci = ti;
+              for (int i = 0; i < 32; ++i) {
+                const int e = c + i;
+                const bool after = v[i] < pv || (v[i] == pv && e > pi);
+                if (e < p.E && after && (v[i] > bv || (v[i] == bv && e < bi))) {
+                  bv = v[i];
+                  bi = e;
                 }
               }
             }
-          }
-        }
-        if (fused && r < p.T) {
-          float ex[kMaxK];
-          float ssum = 0.f;
-#pragma unroll
-          for (int j = 0; j < kMaxK; ++j) {
-            ex[j] = (j < p.k) ? expf(bv[j] - bv[0]) : 0.f;
-            if (j < p.k) ssum += ex[j];
-          }
-#pragma unroll
-          for (int j = 0; j < kMaxK; ++j) {
-            if (j < p.k) {
-              p.topk_ids[(size_t)r * p.k + j] = bi[j];
-              p.topk_w[(size_t)r * p.k + j] = ex[j] / ssum;
+            if (j == 0) z0 = bv;
+            const float ex = expf(bv - z0);
+            ssum += ex;
+            if (r < p.T) {
+              p.topk_ids[(size_t)r * p.k + j] = bi;
+              p.topk_w[(size_t)r * p.k + j] = ex;
             }
+            pv = bv;
+            pi = bi;
           }
+          if (r < p.T)
+            for (int j = 0; j < p.k; ++j) p.topk_w[(size_t)r * p.k + j] /= ssum;
         }
       } else {
         // EPI_DSWIGLU: acc = dA' = dOut_p W2^T for f columns [n*256, n*256+256);
