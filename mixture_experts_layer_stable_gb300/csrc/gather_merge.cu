@@ -3,7 +3,9 @@
 //  * gather (dispatch by pull, leiphone "MoK..." section 02): the expert side
 //    reads each routed token row from its source position and lays rows out
 //    in expert order.  On one GPU this is an HBM row gather into the padded
-//    expert-ordered buffer (padding rows are written as zeros).
+//    expert-ordered buffer.  The forward's gather leaves padding rows alone
+//    (GEMM1 zeroes what it computes from them); the backward's writes them as
+//    zeros, which the weight gradients' K loop over padded rows relies on.
 //  * merge (combine + final weighted merge, leiphone section 03): each token
 //    sums its k expert outputs in slot order in fp32 and rounds once to bf16.
 //    The same kernel without weights is the backward's reverse dispatch.
@@ -23,13 +25,15 @@ namespace moe {
 
 namespace {
 
-// One warp per padded row; 16-byte vectors; up to 4 loads in flight per lane.
+// One warp per padded row; 16-byte vectors; up to 8 loads in flight per lane.
+// Padding rows are zero-filled when zero_pad, else skipped.
 __global__ void __launch_bounds__(256) gather_kernel(const __nv_bfloat16* __restrict__ src,
                                                      __nv_bfloat16* __restrict__ dst,
                                                      const __nv_bfloat16* __restrict__ src2,
                                                      __nv_bfloat16* __restrict__ dst2,
                                                      const int* __restrict__ row_of_pad,
-                                                     const int* __restrict__ hdr, int k, int d) {
+                                                     const int* __restrict__ hdr, int k, int d,
+                                                     int zero_pad) {
   const int rows = hdr[kHdrRpTotal];
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -37,21 +41,22 @@ __global__ void __launch_bounds__(256) gather_kernel(const __nv_bfloat16* __rest
   const int nvec = d >> 3;
   for (int pp = gw; pp < rows; pp += nw) {
     const int r = row_of_pad[pp];
+    if (r < 0 && !zero_pad) continue;
     for (int pass = 0; pass < 2; ++pass) {
       const __nv_bfloat16* s = pass ? src2 : src;
       __nv_bfloat16* o = pass ? dst2 : dst;
       if (o == nullptr) break;
       const uint4* sv = reinterpret_cast<const uint4*>(s + (size_t)(r < 0 ? 0 : r / k) * d);
       uint4* ov = reinterpret_cast<uint4*>(o + (size_t)pp * d);
-      for (int v0 = lane; v0 < nvec; v0 += 32 * 4) {
-        uint4 buf[4];
+      for (int v0 = lane; v0 < nvec; v0 += 32 * 8) {
+        uint4 buf[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < 8; ++u) {
           const int v = v0 + u * 32;
           buf[u] = (r >= 0 && v < nvec) ? ldg_nc_v4(sv + v) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < 8; ++u) {
           const int v = v0 + u * 32;
           if (v < nvec) stg_v4(ov + v, buf[u]);
         }
@@ -188,7 +193,9 @@ cudaError_t launch_gather(const moe_config& c, const Ws& ws, const __nv_bfloat16
                           cudaStream_t st) {
   const int grid = num_sms() * 8;
   TraceScope ts(dst2 ? "gather_x_dy" : "gather", st);
-  gather_kernel<<<grid, 256, 0, st>>>(src, dst, src2, dst2, ws.row_of_pad(), ws.hdr(), c.k, c.d);
+  // the backward's gather (two sources) zero-fills padding rows for the weight gradients
+  gather_kernel<<<grid, 256, 0, st>>>(src, dst, src2, dst2, ws.row_of_pad(), ws.hdr(), c.k, c.d,
+                                      dst2 != nullptr ? 1 : 0);
   return cudaGetLastError();
 }
 

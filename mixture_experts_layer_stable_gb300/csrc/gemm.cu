@@ -192,13 +192,11 @@ __device__ __forceinline__ Tile decode(const Params& p, int L, int rank) {
     t.row0 = t.m * kBM;
     t.kb_count = p.num_kb;
     t.krow0 = 0;
-    if (!PAIR && p.thin) {
+    if (!t.thin && p.counts != nullptr) {
+      // rows of this tile that hold routed rows (<= 0 past the expert's tiles)
       const int cnt = __ldg(p.counts + e);
-      const int rows = cnt - (t.m - m0) * kBM;
-      if (thin_tile(rows, cnt)) {
-        t.rows = rows;
-        t.thin = true;
-      }
+      t.rows = min(kBM, cnt - mrel * kBM);
+      if (!PAIR && p.thin && thin_tile(t.rows, cnt)) t.thin = true;
     }
   } else {
     t.nt = 0;
@@ -742,6 +740,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tb + p.hn + c, u);
           tmem_ld32(tb + p.hn + c + 32, u + 32);
           const int col = t.n * p.hn + c;
+          if (q * 32 + lane >= t.rows) {
+            // a padding row of the expert's last tile (its input row is not
+            // written by the gather): saved and passed on as zeros
+#pragma unroll
+            for (int i = 0; i < 64; ++i) g[i] = u[i] = 0.f;
+          }
           if (p.out1 != nullptr) {
             put_tile(&tmO2, g, col, row);
             put_tile(&tmO2, u, p.f + col, row);
