@@ -53,6 +53,11 @@ def kernel_units(c, touched):
         "gather_x_dy": (None, 0.0, 4.0 * R * d * b),
         "merge": (None, 0.0, T * (k + 1) * d * b + R * 4.0 * 2),
         "reverse_dispatch": (None, 0.0, T * (k + 1) * d * b + R * 4.0),
+        # persistent ring forward (gather + GEMM1 + SwiGLU + GEMM2 + merge in one launch):
+        # token rows in, weights of the touched experts, H and A saved, Y written and read
+        # back by the merge, out written
+        "ring_forward": ("flop", 2.0 * R * d * 2 * f + 2.0 * R * f * d,
+                         R * d * b + w1 + w2 + R * 3 * f * b + 2.0 * R * d * b + T * d * b),
         # router projection (--router): x [T, d], Wr [E, d], logits / ids / weights
         "router_logits": ("flop", 2.0 * T * d * E, T * d * b + E * d * b + R * 8.0),
         "router_dlogits_bf16": (None, 0.0, T * E * 6.0),
@@ -229,8 +234,12 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="balanced")
     ap.add_argument("--passes", default=None, help="fwd or fwd+bwd (default: fwd+bwd)")
-    ap.add_argument("--minibatch-rows", type=int, default=0)
-    ap.add_argument("--ring-slots", type=int, default=0)
+    ap.add_argument("--minibatch-rows", type=int, default=None,
+                    help="forward through the persistent ring kernel with windows of this many rows "
+                         "(default: the workload's first minibatch size, e.g. 1024 for balanced; "
+                         "0 = the kernel chain)")
+    ap.add_argument("--ring-slots", type=int, default=4)
+    ap.add_argument("--gather-ctas", type=int, default=0, help="ring gather CTAs (0 = the library default from d and f)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--router", action="store_true",
                     help="route from x and a router weight (moe_route, plus the router backward) "
@@ -308,8 +317,11 @@ def main():
         torch.cuda.synchronize()
 
     prec = B.MOE_MXFP8 if cfg.prec == "mxfp8" else B.MOE_BF16
+    if args.minibatch_rows is None:
+        # the ring kernel serves the BF16 forward only
+        args.minibatch_rows = cfg.minibatch_rows[0] if (cfg.minibatch_rows and cfg.prec == "bf16") else 0
     c = B.make_config(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, prec, args.minibatch_rows,
-                      args.ring_slots, 0)
+                      args.ring_slots if args.minibatch_rows > 0 else 0, args.gather_ctas)
     inp = make_inputs(cfg, device="cuda", seed=0, with_grad=(passes != "fwd"))
     w1, w1s, w2, w2s = inp["W1"], None, inp["W2"], None
     if cfg.prec == "mxfp8":
@@ -494,6 +506,8 @@ def main():
         "data": "synthetic (seeded torch generators on device; no dataset, random-init weights)",
         "config": {"workload": cfg.name, **workload_dict(cfg), "passes": passes,
                    "minibatch_rows": args.minibatch_rows,
+                   "forward": ("persistent ring kernel, %d-row windows, %d slots" % (args.minibatch_rows, args.ring_slots)
+                               if args.minibatch_rows > 0 else "kernel chain"),
                    "routing": "router projection (moe_route)" if args.router else "synthetic logits",
                    "l2": "inputs larger than L2 (weights %.2f GB per step)" % (
                        (inp["W1"].numel() + inp["W2"].numel()) * 2 / 1e9),

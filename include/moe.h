@@ -72,8 +72,10 @@ typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_precision;
  *     for every window size.  MXFP8 with minibatch_rows > 0 returns
  *     MOE_ERR_UNSUPPORTED; the backward always runs as a chain of kernels.
  *   ring_slots: ring depth, 2..64, when minibatch_rows > 0.
- *   gather_ctas: CTAs on the gather side of the SM split (0 = SMs / 8); must
- *     be below the SM count. */
+ *   gather_ctas: CTAs on the gather side of the SM split; must be below the
+ *     SM count.  0 picks it from d and f: the gather side's share of the
+ *     per-row work (2d bytes moved at ~30 GB/s per SM against 6df FLOPs at
+ *     ~8 TFLOP/s per SM) times 1.3, clamped to [2, SMs / 4]. */
 typedef struct {
   int32_t T, d, f, E, k;
   int32_t prec; /* moe_precision */

@@ -60,7 +60,7 @@ WsLayout ws_layout(const moe_config* c) {
   L.dl16 = take((size_t)c->T * ((c->E + 63) / 64 * 64) * 2);
   if (c->minibatch_rows > 0) {
     L.ring = take((size_t)c->ring_slots * ring_window_rows(*c) * c->d * 2);
-    L.ctr_bytes = (size_t)(2 * c->ring_slots + 2 + L.MT_max) * sizeof(int);
+    L.ctr_bytes = (size_t)(2 * c->ring_slots + 3 + L.MT_max) * sizeof(int);
     L.ctr = take(L.ctr_bytes);
   }
   L.total = off;

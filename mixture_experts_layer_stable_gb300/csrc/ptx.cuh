@@ -162,6 +162,28 @@ template <int N>
 MOE_DEV void bulk_wait() {
   asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
+// Wait until at most n (0..15, clamped) of this thread's most recent bulk
+// async-groups still read shared memory.
+MOE_DEV void bulk_wait_read_n(int n) {
+  switch (n < 0 ? 0 : n) {
+    case 0: bulk_wait_read<0>(); break;
+    case 1: bulk_wait_read<1>(); break;
+    case 2: bulk_wait_read<2>(); break;
+    case 3: bulk_wait_read<3>(); break;
+    case 4: bulk_wait_read<4>(); break;
+    case 5: bulk_wait_read<5>(); break;
+    case 6: bulk_wait_read<6>(); break;
+    case 7: bulk_wait_read<7>(); break;
+    case 8: bulk_wait_read<8>(); break;
+    case 9: bulk_wait_read<9>(); break;
+    case 10: bulk_wait_read<10>(); break;
+    case 11: bulk_wait_read<11>(); break;
+    case 12: bulk_wait_read<12>(); break;
+    case 13: bulk_wait_read<13>(); break;
+    case 14: bulk_wait_read<14>(); break;
+    default: bulk_wait_read<15>(); break;
+  }
+}
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (TMA stores, tcgen05 operand reads).
 MOE_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -300,6 +322,15 @@ MOE_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t b
           dst),
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
       : "memory");
+}
+
+// Plain bulk copy shared -> global (same alignment rules), in the thread's
+// current bulk async-group.
+MOE_DEV void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                   reinterpret_cast<uint64_t>(dst)),
+               "r"(src), "r"(bytes)
+               : "memory");
 }
 
 // ---------------------------------------------------------------- CTA pairs

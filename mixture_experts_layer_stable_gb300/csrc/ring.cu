@@ -11,11 +11,15 @@
 // Layout of one launch (cooperative, so every CTA is co-resident):
 //   CTAs [0, G)       gather side: for every window w of `mb` consecutive rows
 //                     of the padded expert order, wait until ring slot
-//                     w % S is free, copy the window's token rows into it,
-//                     then release ready[slot].
+//                     w % S is free, copy the window's token rows into it
+//                     (bulk copies staged through shared memory), then
+//                     release ready[slot].
 //   CTAs [G, grid)    compute side: the warp-specialised tcgen05 pipeline of
 //                     gemm.cu over a tile stream ordered
-//                     G1(0), [G1(1), G2(0)], [G1(2), G2(1)], ..., G2(last):
+//                     G1(0), [G1(1), G2(0)], [G1(2), G2(1)], ..., G2(last),
+//                     each CTA claiming the next tile from a global counter
+//                     when its loader is ready for one (tiles of mixed cost
+//                     balance themselves across CTAs):
 //                     GEMM1 + SwiGLU tiles of window w read the ring slot after
 //                     acquiring ready[slot] and release freed[slot] once their
 //                     loads have landed; GEMM2 tiles of a 128-row tile wait for
@@ -28,6 +32,9 @@
 // sets a global abort word, reports MOE_ERR_TIMEOUT in the workspace status
 // word and every CTA winds down (no trap).
 #include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cmath>
 
 #include "gemm_common.cuh"
 #include "moe_internal.h"
@@ -47,12 +54,15 @@ constexpr int kThreads = 192;
 constexpr int kEpiWarps = 4;
 constexpr int kOutTile = 32 * 128;
 constexpr int kTmemCols = 512;
+constexpr int kQ = 4;  // depth of the per-CTA queue of claimed tile indices
 constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kEpiWarps * 2 * kOutTile + 256;
 static_assert(kSmem <= 232448, "shared memory budget");
 
 struct RingParams {
   int T, d, f, E, k;
   int G, S, mb, mtw;          // gather CTAs, ring slots, rows per window, 128-row tiles per window
+  int gw, nbw;                // gather warps per CTA issuing bulk copies, row buffers per such warp
+  int lag;                    // windows between a window's GEMM1 and GEMM2 tiles in the stream
   int hn, nt1, nt2, kb1, kb2;  // GEMM1 half width, N tiles of GEMM1 / GEMM2, K blocks
   const int* mt_off;
   const int* counts;   // rows per expert: a partial last tile runs thin (swapped)
@@ -71,6 +81,7 @@ struct RingParams {
   int* freed;           // [S]  GEMM1 tiles done reading per slot
   int* a_ready;         // [MT] GEMM1 epilogue warps done per 128-row tile
   int* done2;           // GEMM2 epilogue warps done
+  int* tile_next;       // next unclaimed tile of the stream
   int* gabort;          // set once by the first wait that gives up
   int* status;
 };
@@ -117,30 +128,44 @@ __device__ __forceinline__ void ring_store_cols_t(uint8_t* tr, const float* v, _
   }
 }
 
-// Tile L of the stream G1(0), [G1(1) G2(0)], ..., [G1(nW-1) G2(nW-2)], G2(nW-1).
-// Inside a phase block, tiles run N-tile-major so that the tiles sharing an
-// expert's weight slice are adjacent.
+// Tile L of the stream G1(0), ..., G1(lag - 1), [G1(lag) G2(0)], [G1(lag + 1)
+// G2(1)], ..., [G1(nW - 1) G2(nW - 1 - lag)], G2(nW - lag), ..., G2(nW - 1):
+// GEMM2 of a window is claimed `lag` windows after its GEMM1, by when its
+// GEMM1 tiles are mostly done.  Inside a phase block, tiles run
+// N-tile-major so that the tiles sharing an expert's weight slice are
+// adjacent.  Only the last window can be short (mt_last tiles).
 __device__ __forceinline__ RTile ring_decode(const RingParams& p, const Geo& g, int L) {
   int phase, w, loc;
   const int t1l = g.mt_last * p.nt1;
-  if (g.nW == 1) {
-    if (L < t1l) { phase = 1; w = 0; loc = L; }
-    else { phase = 2; w = 0; loc = L - t1l; }
-  } else if (L < g.F1) {
-    phase = 1; w = 0; loc = L;
+  const int lag = min(p.lag, g.nW);
+  if (lag == g.nW) {
+    // every GEMM1 tile, then every GEMM2 tile
+    const int n1 = (g.nW - 1) * g.F1 + t1l;
+    phase = L < n1 ? 1 : 2;
+    const int l = L < n1 ? L : L - n1;
+    const int F = phase == 1 ? g.F1 : g.F2;
+    w = min(l / F, g.nW - 1);
+    loc = l - w * F;
+  } else if (L < lag * g.F1) {
+    phase = 1; w = L / g.F1; loc = L % g.F1;
   } else {
-    int l = L - g.F1;
+    int l = L - lag * g.F1;
     const int blk = g.F1 + g.F2;
-    const int nfull = g.nW - 2;
+    const int nfull = g.nW - 1 - lag;  // blocks [G1(b) G2(b - lag)] of full windows
     if (l < nfull * blk) {
-      const int b = 1 + l / blk, r = l % blk;
+      const int b = lag + l / blk, r = l % blk;
       if (r < g.F1) { phase = 1; w = b; loc = r; }
-      else { phase = 2; w = b - 1; loc = r - g.F1; }
+      else { phase = 2; w = b - lag; loc = r - g.F1; }
     } else {
       l -= nfull * blk;
       if (l < t1l) { phase = 1; w = g.nW - 1; loc = l; }
-      else if (l < t1l + g.F2) { phase = 2; w = g.nW - 2; loc = l - t1l; }
-      else { phase = 2; w = g.nW - 1; loc = l - t1l - g.F2; }
+      else if ((l -= t1l) < g.F2) { phase = 2; w = g.nW - 1 - lag; loc = l; }
+      else {
+        l -= g.F2;
+        phase = 2;
+        w = min(g.nW - lag + l / g.F2, g.nW - 1);
+        loc = l - (w - (g.nW - lag)) * g.F2;
+      }
     }
   }
   const int mtw = (w == g.nW - 1) ? g.mt_last : p.mtw;
@@ -170,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tmY, const RingParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_ok;
+  __shared__ int s_gab;
   __shared__ int s_pos[kMaxK];
   __shared__ float s_w[kMaxK];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -182,7 +208,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (blockIdx.x < (unsigned)p.G) {
     // ====================================================== gather side
-    const int nwarp = kThreads / 32;
+    // Warps [0, gw) each move their share of a window's rows with bulk
+    // copies: a row load lands in one of the warp's nbw row buffers (one
+    // mbarrier each) and leaves by a bulk store into the ring slot (padding
+    // rows of the expert order from a zero row).  A buffer is refilled once
+    // its store has read it, with up to nbw / 2 stores of a warp in flight,
+    // so that the wait for one store never stalls the next rows.
+    const uint32_t rb = (uint32_t)p.d * 2u;
+    const int nbw = p.nbw, depth = p.nbw / 2;
+    const bool issuer = warp < p.gw;
+    const uint32_t zrow = smem_u32(smem);
+    const uint32_t wbuf = zrow + rb + (uint32_t)(warp * nbw) * rb;
+    uint64_t* gfull = reinterpret_cast<uint64_t*>(smem + (size_t)(1 + p.gw * nbw) * rb) + warp * nbw;
+    for (uint32_t i = threadIdx.x; i < rb / 16; i += kThreads)
+      reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();  // the zero row is read by bulk stores
+    if (issuer && lane == 0) {
+      for (int b = 0; b < nbw; ++b) mbar_init(&gfull[b], 1);
+      fence_mbar_init();
+    }
+    if (threadIdx.x == 0) s_gab = 0;
+    __syncthreads();
+    const int gid = blockIdx.x * p.gw + warp, ni = p.G * p.gw;
+    uint32_t gph = 0, pend = 0;  // lane 0: buffer parities, buffers with a load in flight
     for (int w = 0; w < geo.nW; ++w) {
       const int s = w % p.S, gen = w / p.S;
       if (threadIdx.x == 0)
@@ -192,24 +240,70 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncthreads();  // everyone has read s_ok before thread 0 writes it again
       if (!ok) break;
       const int r0 = w * p.mb, r1 = min(r0 + p.mb, geo.rp);
-      const int nvec = p.d >> 3;
-      for (int pp = r0 + blockIdx.x * nwarp + warp; pp < r1; pp += p.G * nwarp) {
-        const int r = p.row_of_pad[pp];
-        const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)(r < 0 ? 0 : r / p.k) * p.d);
-        uint4* dst = reinterpret_cast<uint4*>(p.ring + ((size_t)s * p.mb + (pp - r0)) * p.d);
-        for (int v0 = lane; v0 < nvec; v0 += 32 * 4) {
-          uint4 buf[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int v = v0 + u * 32;
-            buf[u] = (r >= 0 && v < nvec) ? ldg_nc_v4(src + v) : make_uint4(0, 0, 0, 0);
+      const int n = (issuer && r0 + gid < r1) ? (r1 - r0 - gid + ni - 1) / ni : 0;
+      if (n > 0) {
+        __nv_bfloat16* slot = p.ring + (size_t)s * p.mb * p.d;
+        const int* rop = p.row_of_pad + r0 + gid;
+        // source rows of this warp's share, 32 at a time in two registers
+        // (rows [c0, c0 + 32) and [c0 + 32, c0 + 64)), read by shuffles
+        int c0 = 0;
+        int ia = (lane < n) ? __ldg(rop + (size_t)lane * ni) : -1;
+        int ib = (32 + lane < n) ? __ldg(rop + (size_t)(32 + lane) * ni) : -1;
+        auto row_at = [&](int i) { return __shfl_sync(0xffffffffu, (i - c0) < 32 ? ia : ib, (i - c0) & 31); };
+        // row i of this warp's share -> buffer i % nbw (warp-uniform call)
+        auto issue = [&](int i) {
+          const int r = row_at(i);
+          if (lane == 0 && r >= 0) {
+            const int b = i % nbw;
+            mbar_arrive_expect_tx(&gfull[b], rb);
+            bulk_load(wbuf + (uint32_t)b * rb, p.x + (size_t)(r / p.k) * p.d, rb, smem_u32(&gfull[b]));
+            pend |= 1u << b;
           }
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            if (v0 + u * 32 < nvec) stg_v4(dst + v0 + u * 32, buf[u]);
+        };
+        if (lane == 0) fence_proxy_async_global();  // the slot's earlier readers are done (freed acquired above)
+        for (int i = 0; i < min(nbw, n); ++i) issue(i);
+        for (int i = 0; i < n; ++i) {
+          if (i - c0 == 32) {
+            c0 += 32;
+            ia = ib;
+            ib = (c0 + 32 + lane < n) ? __ldg(rop + (size_t)(c0 + 32 + lane) * ni) : -1;
+          }
+          const int r = row_at(i);
+          int wok = 1;
+          if (lane == 0) {
+            const int b = i % nbw;
+            uint32_t src = zrow;
+            if (r >= 0) {
+              wok = mbar_wait(&gfull[b], (gph >> b) & 1u, &s_gab, p.status, 550);
+              gph ^= wok ? (1u << b) : 0u;
+              pend &= wok ? ~(1u << b) : ~0u;
+              src = wbuf + (uint32_t)b * rb;
+            }
+            if (wok) {
+              bulk_store(slot + (size_t)(r0 + gid + i * ni - r0) * p.d, src, rb);
+              bulk_commit();  // one group per row
+            }
+          }
+          if (!__shfl_sync(0xffffffffu, wok, 0)) break;
+          // refill the buffer of row i - depth once that row's store has read it
+          if (i >= depth && i - depth + nbw < n) {
+            if (lane == 0) bulk_wait_read_n(depth);
+            issue(i - depth + nbw);
+          }
         }
+        if (lane == 0) {
+          bulk_wait<0>();  // this warp's rows are in global memory
+          fence_proxy_async_global();
+          if (s_gab) {
+            atomicExch(p.gabort, 1);
+            for (int b = 0; b < nbw; ++b)  // no copy may still target shared memory at exit
+              if ((pend >> b) & 1u) mbar_wait_drain(&gfull[b], (gph >> b) & 1u);
+          }
+        }
+        __syncwarp();
       }
       __syncthreads();
+      if (s_gab) break;
       if (threadIdx.x == 0) {
         __threadfence();
         if (inject != w + 1) red_release_add(&p.ready[s], 1);
@@ -225,9 +319,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* tfull = empty + kStages;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* qfull = drain + 1;     // tile queue: claimed tile index published
+    uint64_t* qempty = qfull + kQ;   // tile queue: slot read by the MMA and epilogue warps
+    int* qtile = reinterpret_cast<int*>(qempty + kQ);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qtile + kQ);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    const int cta = blockIdx.x - p.G, ncta = gridDim.x - p.G;
 
     if (threadIdx.x == 0) {
       for (int s = 0; s < kStages; ++s) {
@@ -239,6 +335,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&tempty[a], kEpiWarps * 32);
       }
       mbar_init(drain, 1);
+      for (int i = 0; i < kQ; ++i) {
+        mbar_init(&qfull[i], 1);
+        mbar_init(&qempty[i], 1 + kEpiWarps);
+      }
       *abort_flag = 0;
       fence_mbar_init();
       tma_prefetch_desc(&tmX);
@@ -261,7 +361,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------ TMA producer
         int s = 0;
         uint32_t ph = 0, used = 0, last_par = 0;
-        for (int L = cta; L < geo.total; L += ncta) {
+        for (int j = 0;; ++j) {
+          // claim the next tile of the stream and hand its index to the other roles
+          if (!mbar_wait(&qempty[j % kQ], ((j / kQ) & 1) ^ 1, abort_flag, p.status, 150)) goto producer_done;
+          const int L = atomicAdd(p.tile_next, 1);
+          qtile[j % kQ] = L;
+          mbar_arrive(&qfull[j % kQ]);
+          if (L >= geo.total) break;
           const RTile t = ring_decode(p, geo, L);
           const bool g1 = (t.phase == 1);
           const int slot = t.w % p.S;
@@ -313,7 +419,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t idesc2 = idesc_bf16(kBM, 256, false, true);
         int s = 0, acc = 0;
         uint32_t ph = 0, aph = 0;
-        for (int L = cta; L < geo.total; L += ncta) {
+        for (int j = 0;; ++j) {
+          if (!mbar_wait(&qfull[j % kQ], (j / kQ) & 1, abort_flag, p.status, 160)) goto mma_done;
+          const int L = qtile[j % kQ];
+          mbar_arrive(&qempty[j % kQ]);
+          if (L >= geo.total) break;
           const RTile t = ring_decode(p, geo, L);
           const bool g1 = (t.phase == 1);
           const int nkb = g1 ? p.kb1 : p.kb2;
@@ -364,7 +474,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int acc = 0, buf = 0;
       uint32_t aph = 0;
       const uint32_t stg = smem_u32(staging) + (uint32_t)(warp - 2) * 2u * kOutTile;
-      for (int L = cta; L < geo.total; L += ncta) {
+      for (int j = 0;; ++j) {
+        if (!mbar_wait(&qfull[j % kQ], (j / kQ) & 1, abort_flag, p.status, 170)) break;
+        const int L = qtile[j % kQ];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&qempty[j % kQ]);
+        if (L >= geo.total) break;
         const RTile t = ring_decode(p, geo, L);
         if (!mbar_wait(&tfull[acc], aph, abort_flag, p.status, 400 + acc)) break;
         tc_fence_after();
@@ -508,13 +623,36 @@ cudaError_t ring_forward(const moe_config& c, const Ws& ws, const int* counts, c
   p.S = c.ring_slots;
   p.mb = ring_window_rows(c);
   p.mtw = p.mb / kBM;
-  p.G = c.gather_ctas > 0 ? c.gather_ctas : ring_default_gather_ctas(sms);
+  p.G = c.gather_ctas > 0 ? c.gather_ctas : ring_default_gather_ctas(c, sms);
   if (p.G >= sms) return cudaErrorInvalidValue;
+  {
+    // gather row buffers (after one zero row): up to 16 per warp in all six
+    // warps, at least two per issuing warp (fewer issuing warps for very wide
+    // rows)
+    const size_t rb = (size_t)c.d * 2;
+    if (kSmem <= 2048 + 3 * rb || rb >= (1u << 20)) return cudaErrorInvalidValue;
+    const size_t avail = kSmem - 2048 - rb;
+    p.gw = kThreads / 32;
+    p.nbw = (int)std::min<size_t>(16, avail / (p.gw * rb));
+    if (p.nbw < 2) {
+      p.nbw = 2;
+      p.gw = (int)(avail / (2 * rb));
+    }
+    if (p.gw < 1) return cudaErrorInvalidValue;
+  }
   p.hn = (c.f % 128 == 0) ? 128 : 64;
   p.nt1 = c.f / p.hn;
   p.nt2 = (c.d + 255) / 256;
   p.kb1 = c.d / BK;
   p.kb2 = c.f / BK;
+  {
+    // lag: enough windows that the tiles claimed between a window's GEMM1 and
+    // its GEMM2 keep every compute CTA busy for one GEMM1 tile (relative tile
+    // costs from their FLOPs: GEMM1 128 x 2hn x d, GEMM2 128 x 256 x f)
+    const double t1 = 2.0 * p.hn * c.d, t2 = 256.0 * c.f;
+    const double blk = p.mtw * (p.nt1 * t1 + p.nt2 * t2);
+    p.lag = std::max(1, std::min(4, (int)std::ceil((sms - p.G) * t1 / blk)));
+  }
   p.mt_off = ws.mt_off();
   p.counts = counts;
   p.thin = gemm1_thin_enabled(c) ? 1 : 0;
@@ -533,7 +671,8 @@ cudaError_t ring_forward(const moe_config& c, const Ws& ws, const int* counts, c
   p.freed = ctr + p.S;
   p.done2 = ctr + 2 * p.S;
   p.gabort = ctr + 2 * p.S + 1;
-  p.a_ready = ctr + 2 * p.S + 2;
+  p.tile_next = ctr + 2 * p.S + 2;
+  p.a_ready = ctr + 2 * p.S + 3;
   p.status = ws.hdr() + kHdrStatus;
 
   const uint64_t rows = (uint64_t)ws.L.Rp_max;
