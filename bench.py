@@ -239,7 +239,7 @@ def parse():
                          "(default: the workload's first minibatch size, e.g. 1024 for balanced; "
                          "0 = the kernel chain)")
     ap.add_argument("--ring-slots", type=int, default=4)
-    ap.add_argument("--gather-ctas", type=int, default=0, help="ring gather CTAs (0 = the library default from d and f)")
+    ap.add_argument("--gather-ctas", type=int, default=0, help="ring: 0 = a gather warp in every CTA, G > 0 = G gather-only CTAs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--router", action="store_true",
                     help="route from x and a router weight (moe_route, plus the router backward) "
@@ -506,7 +506,10 @@ def main():
         "data": "synthetic (seeded torch generators on device; no dataset, random-init weights)",
         "config": {"workload": cfg.name, **workload_dict(cfg), "passes": passes,
                    "minibatch_rows": args.minibatch_rows,
-                   "forward": ("persistent ring kernel, %d-row windows, %d slots" % (args.minibatch_rows, args.ring_slots)
+                   "forward": ("persistent ring kernel, %d-row windows, %d slots, %s" % (
+                                   args.minibatch_rows, args.ring_slots,
+                                   "%d gather CTAs" % args.gather_ctas if args.gather_ctas > 0
+                                   else "a gather warp in every CTA")
                                if args.minibatch_rows > 0 else "kernel chain"),
                    "routing": "router projection (moe_route)" if args.router else "synthetic logits",
                    "l2": "inputs larger than L2 (weights %.2f GB per step)" % (

@@ -65,17 +65,18 @@ typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_precision;
  *   minibatch_rows: 0 runs the layer as a chain of kernels over the whole
  *     expert-ordered buffer.  > 0 runs the BF16 forward as one persistent
  *     cooperative kernel that hands windows of this many expert-ordered rows
- *     (rounded up to a multiple of 128) from gather CTAs to GEMM CTAs through
- *     a ring of ring_slots slots, with GPU-side counters and the weighted
- *     merge at the end ([LP] 02: SM partition, local counters, minibatch,
- *     ring token buffer).  Results are bitwise identical to the chain path
+ *     (rounded up to a multiple of 128) from gather warps or CTAs to GEMM
+ *     warps through a ring of ring_slots slots, with GPU-side counters and
+ *     the weighted merge at the end ([LP] 02: SM partition, local counters,
+ *     minibatch, ring token buffer).  Results are bitwise identical to the chain path
  *     for every window size.  MXFP8 with minibatch_rows > 0 returns
  *     MOE_ERR_UNSUPPORTED; the backward always runs as a chain of kernels.
  *   ring_slots: ring depth, 2..64, when minibatch_rows > 0.
- *   gather_ctas: CTAs on the gather side of the SM split; must be below the
- *     SM count.  0 picks it from d and f: the gather side's share of the
- *     per-row work (2d bytes moved at ~30 GB/s per SM against 6df FLOPs at
- *     ~8 TFLOP/s per SM) times 1.3, clamped to [2, SMs / 4]. */
+ *   gather_ctas: how the work is split when minibatch_rows > 0.  0 (the
+ *     default): every CTA runs the GEMM warps and one gather warp, so all
+ *     SMs compute.  G > 0 (below the SM count): CTAs [0, G) only gather, with
+ *     bulk copies staged through shared memory, and the other CTAs only
+ *     compute. */
 typedef struct {
   int32_t T, d, f, E, k;
   int32_t prec; /* moe_precision */

@@ -86,18 +86,8 @@ struct Ws {
 
 int num_sms();
 
-// Ring path: rows per window (minibatch_rows rounded up to 128-row tiles) and
-// the default number of gather CTAs of the SM split.
+// Ring path: rows per window (minibatch_rows rounded up to 128-row tiles).
 inline int ring_window_rows(const moe_config& c) { return (c.minibatch_rows + kBM - 1) / kBM * kBM; }
-// The split follows the work per row: a gather SM moves about 30 GB/s of rows
-// (d * 2 bytes each) next to the GEMMs, a GEMM SM runs about 8 TFLOP/s of the
-// 6 * d * f FLOPs a row costs in the forward; the gather side gets 1.3 times
-// its share of that sum (it must stay ahead), between 2 and SMs / 4.
-inline int ring_default_gather_ctas(const moe_config& c, int sms) {
-  const double g = 2.0 * c.d / 30e9, m = 6.0 * c.d * c.f / 8e12;
-  const int G = (int)(1.3 * sms * g / (g + m)) + 1;
-  return G < 2 ? 2 : (G > sms / 4 ? sms / 4 : G);
-}
 
 // Tracing hooks around every kernel launch (no-ops unless moe_trace_enable).
 void trace_before(const char* name, cudaStream_t st);

@@ -50,8 +50,9 @@ constexpr int kStages = 4;
 constexpr int kABytes = kBM * BK * 2;          // 16 KB
 constexpr int kBBox = 64 * BK * 2;             // 8 KB: 64 columns x 64 K rows, MN-major
 constexpr int kStageBytes = kABytes + 4 * kBBox;
-constexpr int kThreads = 192;
 constexpr int kEpiWarps = 4;
+constexpr int kGatherWarps = 2;  // gather warps of a CTA in the warp split
+constexpr int kThreads = (2 + kEpiWarps + kGatherWarps) * 32;  // producer, MMA, epilogue, gather
 constexpr int kOutTile = 32 * 128;
 constexpr int kTmemCols = 512;
 constexpr int kQ = 4;  // depth of the per-CTA queue of claimed tile indices
@@ -60,7 +61,9 @@ static_assert(kSmem <= 232448, "shared memory budget");
 
 struct RingParams {
   int T, d, f, E, k;
-  int G, S, mb, mtw;          // gather CTAs, ring slots, rows per window, 128-row tiles per window
+  int G, S, mb, mtw;          // gather CTAs (0: a gather warp in every CTA), ring slots, rows per
+                              // window, 128-row tiles per window
+  int nrel;                   // arrivals that complete one window (gather CTAs or gather warps)
   int gw, nbw;                // gather warps per CTA issuing bulk copies, row buffers per such warp
   int lag;                    // windows between a window's GEMM1 and GEMM2 tiles in the stream
   int hn, nt1, nt2, kb1, kb2;  // GEMM1 half width, N tiles of GEMM1 / GEMM2, K blocks
@@ -373,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int slot = t.w % p.S;
           bool ok;
           if (g1)
-            ok = wait_counter(&p.ready[slot], p.G * (t.w / p.S + 1), p.gabort, p.status, 600 + slot, limit);
+            ok = wait_counter(&p.ready[slot], p.nrel * (t.w / p.S + 1), p.gabort, p.status, 600 + slot, limit);
           else
             ok = wait_counter(&p.a_ready[t.mt], kEpiWarps * p.nt1, p.gabort, p.status, 700, limit);
           if (!ok) {
@@ -468,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(smem_u32(drain));
         mbar_wait_drain(drain, 0);
       }
-    } else {
+    } else if (warp < 2 + kEpiWarps) {
       // -------------------------------------------- epilogue warps
       const int q = warp & 3;
       int acc = 0, buf = 0;
@@ -583,6 +586,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (lane == 0) bulk_wait<0>();
+    } else if (p.G == 0) {
+      // -------------------------------------------- gather warps (warp split)
+      // The last kGatherWarps warps of every CTA copy their share of each
+      // window (rows r0 + gwi + i * ncta, gwi this warp's global index, ncta
+      // the number of gather warps) into the ring slot with plain 16-byte
+      // loads and stores, two rows at a time, 8 loads per lane and row in
+      // flight; source-row indices are read 32 at a time and shuffled.
+      const int nvec = p.d >> 3, ncta = gridDim.x * kGatherWarps;
+      const int gwi = blockIdx.x * kGatherWarps + (warp - 2 - kEpiWarps);
+      for (int w = 0; w < geo.nW; ++w) {
+        const int s = w % p.S, gen = w / p.S;
+        int ok = 1;
+        if (lane == 0)
+          ok = (gen == 0) || wait_counter(&p.freed[s], gen * geo.F1, p.gabort, p.status, 500 + s, limit);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        const int r0 = w * p.mb, r1 = min(r0 + p.mb, geo.rp);
+        const int n = (r0 + gwi < r1) ? (r1 - r0 - gwi + ncta - 1) / ncta : 0;
+        __nv_bfloat16* slot = p.ring + (size_t)s * p.mb * p.d;
+        for (int c0 = 0; c0 < n; c0 += 32) {
+          const int my = (c0 + lane < n) ? __ldg(p.row_of_pad + r0 + gwi + (size_t)(c0 + lane) * ncta) : -1;
+          const int cn = min(32, n - c0);
+          for (int i = 0; i < cn; i += 2) {
+            const int ra = __shfl_sync(0xffffffffu, my, i);
+            const int rb = __shfl_sync(0xffffffffu, my, (i + 1) & 31);
+            const bool two = i + 1 < cn;
+            const int pa = gwi + (c0 + i) * ncta;  // row within the window
+            const uint4* sa = reinterpret_cast<const uint4*>(p.x + (size_t)(ra < 0 ? 0 : ra / p.k) * p.d);
+            const uint4* sb = reinterpret_cast<const uint4*>(p.x + (size_t)(rb < 0 ? 0 : rb / p.k) * p.d);
+            uint4* da = reinterpret_cast<uint4*>(slot + (size_t)pa * p.d);
+            uint4* db = reinterpret_cast<uint4*>(slot + (size_t)(pa + ncta) * p.d);
+            for (int v0 = lane; v0 < nvec; v0 += 32 * 8) {
+              uint4 a[8], b[8];
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const int v = v0 + 32 * u;
+                a[u] = (ra >= 0 && v < nvec) ? ldg_nc_v4(sa + v) : make_uint4(0, 0, 0, 0);
+                b[u] = (two && rb >= 0 && v < nvec) ? ldg_nc_v4(sb + v) : make_uint4(0, 0, 0, 0);
+              }
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const int v = v0 + 32 * u;
+                if (v < nvec) {
+                  stg_v4(da + v, a[u]);
+                  if (two) stg_v4(db + v, b[u]);
+                }
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence();
+          if (inject != w + 1) red_release_add(&p.ready[s], 1);
+        }
+      }
     }
     tc_fence_before();
     __syncthreads();
@@ -623,8 +681,9 @@ cudaError_t ring_forward(const moe_config& c, const Ws& ws, const int* counts, c
   p.S = c.ring_slots;
   p.mb = ring_window_rows(c);
   p.mtw = p.mb / kBM;
-  p.G = c.gather_ctas > 0 ? c.gather_ctas : ring_default_gather_ctas(c, sms);
-  if (p.G >= sms) return cudaErrorInvalidValue;
+  p.G = c.gather_ctas;
+  if (p.G < 0 || p.G >= sms) return cudaErrorInvalidValue;
+  p.nrel = p.G > 0 ? p.G : sms * kGatherWarps;
   {
     // gather row buffers (after one zero row): up to 16 per warp in all six
     // warps, at least two per issuing warp (fewer issuing warps for very wide
@@ -646,12 +705,13 @@ cudaError_t ring_forward(const moe_config& c, const Ws& ws, const int* counts, c
   p.kb1 = c.d / BK;
   p.kb2 = c.f / BK;
   {
-    // lag: enough windows that the tiles claimed between a window's GEMM1 and
-    // its GEMM2 keep every compute CTA busy for one GEMM1 tile (relative tile
-    // costs from their FLOPs: GEMM1 128 x 2hn x d, GEMM2 128 x 256 x f)
+    // lag: one window more than it takes for the tiles claimed between a
+    // window's GEMM1 and its GEMM2 to keep every compute CTA busy for one
+    // GEMM1 tile (relative tile costs from their FLOPs: GEMM1 128 x 2hn x d,
+    // GEMM2 128 x 256 x f); the extra window covers the spread of claim times
     const double t1 = 2.0 * p.hn * c.d, t2 = 256.0 * c.f;
     const double blk = p.mtw * (p.nt1 * t1 + p.nt2 * t2);
-    p.lag = std::max(1, std::min(4, (int)std::ceil((sms - p.G) * t1 / blk)));
+    p.lag = std::min(4, 1 + (int)std::ceil((sms - p.G) * t1 / blk));
   }
   p.mt_off = ws.mt_off();
   p.counts = counts;

@@ -62,7 +62,7 @@ def test_ring_equals_chain_bitwise(name, kw, mbs):
     dev = {k: v.cuda() for k, v in inp.items()}
     ref = _run(cfg, dev)
     for mb, slots in mbs:
-        for gather in (0, 3):
+        for gather in (0, 3):  # a gather warp in every CTA; three gather-only CTAs
             L = _run(cfg, dev, mb, slots, gather)
             assert _same(L.out, ref.out), (mb, slots, gather)
             rp = _rows_written(ref)
@@ -92,10 +92,11 @@ def test_ring_inference_without_saved():
     assert _same(L.out, ref.out)
 
 
-def test_ring_withheld_window_times_out_cleanly():
+@pytest.mark.parametrize("gather", [0, 8])
+def test_ring_withheld_window_times_out_cleanly(gather):
     cfg = with_config("balanced")
     dev = {k: v.cuda() for k, v in make_inputs(cfg, with_grad=False).items()}
-    c = cfg_struct(cfg, minibatch_rows=1024, ring_slots=2)
+    c = cfg_struct(cfg, minibatch_rows=1024, ring_slots=2, gather_ctas=gather)
     L = Layer(cfg, c)
     L.schedule(dev["logits"])
     hdr = L.ws[:64 * 4].view(torch.int32)
@@ -129,6 +130,6 @@ def test_kimi_zipf_ring_equals_chain():
     cfg = CONFIGS["kimi_zipf"]
     dev = make_inputs(cfg, device="cuda", with_grad=False)
     ref = _run(cfg, dev, save=False)
-    for mb in (512, 2368, 4096):
-        L = _run(cfg, dev, mb, 4, save=False)
-        assert _same(L.out, ref.out), mb
+    for mb, gather in ((512, 0), (2368, 0), (4096, 0), (1024, 9)):
+        L = _run(cfg, dev, mb, 4, gather, save=False)
+        assert _same(L.out, ref.out), (mb, gather)
