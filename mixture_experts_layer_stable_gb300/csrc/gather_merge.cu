@@ -17,6 +17,13 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
+#include <algorithm>
+
+#ifndef MOE_BULK_GATHER
+#define MOE_BULK_GATHER 1  // 0: the plain-load gather everywhere
+#endif
+
+#include "bulk_rows.cuh"
 #include "moe_internal.h"
 #include "mx.cuh"
 #include "rowops.cuh"
@@ -62,6 +69,66 @@ __global__ void __launch_bounds__(256) gather_kernel(const __nv_bfloat16* __rest
         }
       }
     }
+  }
+}
+
+// The same gather staged through shared memory with bulk copies: one CTA per
+// SM, warps [0, gw) each with nbw row buffers (bulk_rows.cuh).  Item i of a
+// warp is padded row gid + (i / npass) * ni, from src (pass 0) or src2
+// (pass 1).  The item code carries the pass in its low bit.
+__global__ void __launch_bounds__(256, 1) gather_bulk_kernel(
+    const __nv_bfloat16* __restrict__ src, __nv_bfloat16* __restrict__ dst,
+    const __nv_bfloat16* __restrict__ src2, __nv_bfloat16* __restrict__ dst2,
+    const int* __restrict__ row_of_pad, const int* __restrict__ hdr, int k, int d, int zero_pad,
+    int gw, int nbw, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int s_abort;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                             ~static_cast<uintptr_t>(127));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rb = (uint32_t)d * 2u;
+  RowPipe rp;
+  rp.zrow = smem_u32(smem);
+  rp.rb = rb;
+  rp.wbuf = rp.zrow + rb + (uint32_t)(warp * nbw) * rb;
+  rp.bars = reinterpret_cast<uint64_t*>(smem + (size_t)(1 + gw * nbw) * rb) + warp * nbw;
+  rp.nbw = nbw;
+  rp.depth = nbw / 2;
+  rp.ph = rp.pend = 0;
+  if (zero_pad) {
+    for (uint32_t i = threadIdx.x; i < rb / 16; i += blockDim.x)
+      reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();  // the zero row is read by bulk stores
+  }
+  if (warp < gw && lane == 0) {
+    for (int b = 0; b < nbw; ++b) mbar_init(&rp.bars[b], 1);
+    fence_mbar_init();
+  }
+  if (threadIdx.x == 0) s_abort = 0;
+  __syncthreads();
+  if (warp >= gw) return;
+  const int rows = hdr[kHdrRpTotal];
+  const int npass = dst2 != nullptr ? 2 : 1;
+  const int gid = blockIdx.x * gw + warp, ni = gridDim.x * gw;
+  const int n = gid < rows ? (rows - gid + ni - 1) / ni * npass : 0;
+  if (n == 0) return;
+  const bool done = bulk_rows(
+      rp, n,
+      [&](int i) {
+        const int r = __ldg(row_of_pad + gid + (size_t)(i / npass) * ni);
+        return r >= 0 ? r * npass + i % npass : (zero_pad ? kRowZero : kRowSkip);
+      },
+      [&](int code) {
+        const __nv_bfloat16* s = (code % npass) ? src2 : src;
+        return s + (size_t)(code / npass / k) * d;
+      },
+      [&](int i) { return ((i % npass) ? dst2 : dst) + (size_t)(gid + (i / npass) * ni) * d; },
+      &s_abort, status, 900);
+  if (lane == 0) {
+    bulk_wait<0>();
+    if (!done)
+      for (int b = 0; b < nbw; ++b)  // no copy may still target shared memory at exit
+        if ((rp.pend >> b) & 1u) mbar_wait_drain(&rp.bars[b], (rp.ph >> b) & 1u);
   }
 }
 
@@ -191,11 +258,31 @@ __global__ void __launch_bounds__(256) dg_reduce_kernel(
 cudaError_t launch_gather(const moe_config& c, const Ws& ws, const __nv_bfloat16* src,
                           __nv_bfloat16* dst, const __nv_bfloat16* src2, __nv_bfloat16* dst2,
                           cudaStream_t st) {
-  const int grid = num_sms() * 8;
   TraceScope ts(dst2 ? "gather_x_dy" : "gather", st);
   // the backward's gather (two sources) zero-fills padding rows for the weight gradients
-  gather_kernel<<<grid, 256, 0, st>>>(src, dst, src2, dst2, ws.row_of_pad(), ws.hdr(), c.k, c.d,
-                                      dst2 != nullptr ? 1 : 0);
+  const int zero_pad = dst2 != nullptr ? 1 : 0;
+  // bulk-copy gather: a zero row and up to 16 row buffers in each of 8 warps
+  // (fewer warps for wide rows, at least two buffers each), one CTA per SM
+  constexpr size_t kBudget = 227 * 1024 - 128 - 8 * 16 * 8;
+  const size_t rb = (size_t)c.d * 2;
+  if (kBudget >= 3 * rb && MOE_BULK_GATHER) {
+    int gw = 8;
+    int nbw = (int)std::min<size_t>(16, (kBudget - rb) / (gw * rb));
+    if (nbw < 2) {
+      nbw = 2;
+      gw = (int)((kBudget - rb) / (2 * rb));
+    }
+    const size_t smem = 128 + (1 + (size_t)gw * nbw) * rb + (size_t)gw * nbw * 8;
+    cudaError_t err = cudaFuncSetAttribute(gather_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)smem);
+    if (err != cudaSuccess) return err;
+    gather_bulk_kernel<<<num_sms(), 256, smem, st>>>(src, dst, src2, dst2, ws.row_of_pad(), ws.hdr(), c.k,
+                                                     c.d, zero_pad, gw, nbw, ws.hdr() + kHdrStatus);
+    return cudaGetLastError();
+  }
+  // rows too wide for two shared-memory buffers per warp: plain loads and stores
+  gather_kernel<<<num_sms() * 8, 256, 0, st>>>(src, dst, src2, dst2, ws.row_of_pad(), ws.hdr(), c.k, c.d,
+                                               zero_pad);
   return cudaGetLastError();
 }
 

@@ -39,6 +39,7 @@
 #include "gemm_common.cuh"
 #include "moe_internal.h"
 #include "ptx.cuh"
+#include "bulk_rows.cuh"
 #include "rowops.cuh"
 
 namespace moe {
@@ -211,29 +212,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (blockIdx.x < (unsigned)p.G) {
     // ====================================================== gather side
-    // Warps [0, gw) each move their share of a window's rows with bulk
-    // copies: a row load lands in one of the warp's nbw row buffers (one
-    // mbarrier each) and leaves by a bulk store into the ring slot (padding
-    // rows of the expert order from a zero row).  A buffer is refilled once
-    // its store has read it, with up to nbw / 2 stores of a warp in flight,
-    // so that the wait for one store never stalls the next rows.
+    // Warps [0, gw) each move their share of a window's rows with bulk copies
+    // staged through nbw row buffers of their own (bulk_rows.cuh); padding
+    // rows of the expert order leave from a zero row.
     const uint32_t rb = (uint32_t)p.d * 2u;
-    const int nbw = p.nbw, depth = p.nbw / 2;
     const bool issuer = warp < p.gw;
-    const uint32_t zrow = smem_u32(smem);
-    const uint32_t wbuf = zrow + rb + (uint32_t)(warp * nbw) * rb;
-    uint64_t* gfull = reinterpret_cast<uint64_t*>(smem + (size_t)(1 + p.gw * nbw) * rb) + warp * nbw;
+    RowPipe rp;
+    rp.zrow = smem_u32(smem);
+    rp.rb = rb;
+    rp.wbuf = rp.zrow + rb + (uint32_t)(warp * p.nbw) * rb;
+    rp.bars = reinterpret_cast<uint64_t*>(smem + (size_t)(1 + p.gw * p.nbw) * rb) + warp * p.nbw;
+    rp.nbw = p.nbw;
+    rp.depth = p.nbw / 2;
+    rp.ph = rp.pend = 0;
     for (uint32_t i = threadIdx.x; i < rb / 16; i += kThreads)
       reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();  // the zero row is read by bulk stores
     if (issuer && lane == 0) {
-      for (int b = 0; b < nbw; ++b) mbar_init(&gfull[b], 1);
+      for (int b = 0; b < p.nbw; ++b) mbar_init(&rp.bars[b], 1);
       fence_mbar_init();
     }
     if (threadIdx.x == 0) s_gab = 0;
     __syncthreads();
     const int gid = blockIdx.x * p.gw + warp, ni = p.G * p.gw;
-    uint32_t gph = 0, pend = 0;  // lane 0: buffer parities, buffers with a load in flight
     for (int w = 0; w < geo.nW; ++w) {
       const int s = w % p.S, gen = w / p.S;
       if (threadIdx.x == 0)
@@ -247,60 +248,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (n > 0) {
         __nv_bfloat16* slot = p.ring + (size_t)s * p.mb * p.d;
         const int* rop = p.row_of_pad + r0 + gid;
-        // source rows of this warp's share, 32 at a time in two registers
-        // (rows [c0, c0 + 32) and [c0 + 32, c0 + 64)), read by shuffles
-        int c0 = 0;
-        int ia = (lane < n) ? __ldg(rop + (size_t)lane * ni) : -1;
-        int ib = (32 + lane < n) ? __ldg(rop + (size_t)(32 + lane) * ni) : -1;
-        auto row_at = [&](int i) { return __shfl_sync(0xffffffffu, (i - c0) < 32 ? ia : ib, (i - c0) & 31); };
-        // row i of this warp's share -> buffer i % nbw (warp-uniform call)
-        auto issue = [&](int i) {
-          const int r = row_at(i);
-          if (lane == 0 && r >= 0) {
-            const int b = i % nbw;
-            mbar_arrive_expect_tx(&gfull[b], rb);
-            bulk_load(wbuf + (uint32_t)b * rb, p.x + (size_t)(r / p.k) * p.d, rb, smem_u32(&gfull[b]));
-            pend |= 1u << b;
-          }
-        };
         if (lane == 0) fence_proxy_async_global();  // the slot's earlier readers are done (freed acquired above)
-        for (int i = 0; i < min(nbw, n); ++i) issue(i);
-        for (int i = 0; i < n; ++i) {
-          if (i - c0 == 32) {
-            c0 += 32;
-            ia = ib;
-            ib = (c0 + 32 + lane < n) ? __ldg(rop + (size_t)(c0 + 32 + lane) * ni) : -1;
-          }
-          const int r = row_at(i);
-          int wok = 1;
-          if (lane == 0) {
-            const int b = i % nbw;
-            uint32_t src = zrow;
-            if (r >= 0) {
-              wok = mbar_wait(&gfull[b], (gph >> b) & 1u, &s_gab, p.status, 550);
-              gph ^= wok ? (1u << b) : 0u;
-              pend &= wok ? ~(1u << b) : ~0u;
-              src = wbuf + (uint32_t)b * rb;
-            }
-            if (wok) {
-              bulk_store(slot + (size_t)(r0 + gid + i * ni - r0) * p.d, src, rb);
-              bulk_commit();  // one group per row
-            }
-          }
-          if (!__shfl_sync(0xffffffffu, wok, 0)) break;
-          // refill the buffer of row i - depth once that row's store has read it
-          if (i >= depth && i - depth + nbw < n) {
-            if (lane == 0) bulk_wait_read_n(depth);
-            issue(i - depth + nbw);
-          }
-        }
+        const bool done = bulk_rows(
+            rp, n,
+            [&](int i) {
+              const int r = __ldg(rop + (size_t)i * ni);
+              return r >= 0 ? r : kRowZero;
+            },
+            [&](int r) { return p.x + (size_t)(r / p.k) * p.d; },
+            [&](int i) { return slot + (size_t)(gid + i * ni) * p.d; }, &s_gab, p.status, 550);
         if (lane == 0) {
           bulk_wait<0>();  // this warp's rows are in global memory
           fence_proxy_async_global();
-          if (s_gab) {
+          if (!done || s_gab) {
             atomicExch(p.gabort, 1);
-            for (int b = 0; b < nbw; ++b)  // no copy may still target shared memory at exit
-              if ((pend >> b) & 1u) mbar_wait_drain(&gfull[b], (gph >> b) & 1u);
+            for (int b = 0; b < p.nbw; ++b)  // no copy may still target shared memory at exit
+              if ((rp.pend >> b) & 1u) mbar_wait_drain(&rp.bars[b], (rp.ph >> b) & 1u);
           }
         }
         __syncwarp();
