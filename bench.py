@@ -77,10 +77,23 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
 
 
-def src_digest():
+# the translation unit that defines each traced kernel (every header counts for all)
+KERNEL_SOURCE = {"ring_forward": "ring.cu", "gather": "gather_merge.cu", "gather_x_dy": "gather_merge.cu",
+                 "gather_mxfp8": "gather_merge.cu", "merge": "gather_merge.cu",
+                 "reverse_dispatch": "gather_merge.cu", "dg_reduce": "gather_merge.cu",
+                 "sched_topk": "sched.cu", "sched_hist": "sched.cu", "sched_scatter": "sched.cu"}
+
+
+def src_digest(kernel=None):
+    """Digest of the CUDA sources a kernel is built from: its translation unit
+    (gemm.cu for the grouped GEMMs) and every header; all sources when kernel
+    is None."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mixture_experts_layer_stable_gb300", "csrc")
+    tu = KERNEL_SOURCE.get(kernel, "gemm.cu") if kernel else None
     for name in sorted(os.listdir(csrc)):
+        if tu is not None and name.endswith(".cu") and name != tu:
+            continue
         with open(os.path.join(csrc, name), "rb") as fh:
             h.update(name.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -95,7 +108,7 @@ def ncu_traffic(workload, kernel):
     with open(p) as fh:
         tab = json.load(fh)
     ent = tab.get(f"{workload}/{kernel}")
-    if not ent or ent.get("src_digest") != src_digest():
+    if not ent or ent.get("src_digest") != src_digest(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 
