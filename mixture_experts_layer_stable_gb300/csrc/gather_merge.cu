@@ -178,6 +178,89 @@ __global__ void __launch_bounds__(256) gather_mxfp8_kernel(const __nv_bfloat16* 
   }
 }
 
+// Gather + quantise staged through shared memory: warps [0, gw) each keep up
+// to nbw rows in flight as bulk copies into their own buffers; the 32 lanes
+// quantise a landed row's 32-element blocks from shared memory (lane = block
+// mod 32) and store codes and scales, then the buffer takes the row nbw
+// items later.  Padding rows give zero codes and the all-zero scale, as in
+// gather_mxfp8_kernel.
+__global__ void __launch_bounds__(256, 1) gather_mxfp8_bulk_kernel(
+    const __nv_bfloat16* __restrict__ src, uint8_t* __restrict__ q, uint8_t* __restrict__ sc,
+    const int* __restrict__ row_of_pad, const int* __restrict__ hdr, int k, int d, int gw, int nbw,
+    int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int s_abort;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                             ~static_cast<uintptr_t>(127));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rb = (uint32_t)d * 2u;
+  uint8_t* wbuf = smem + (size_t)warp * nbw * rb;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)gw * nbw * rb) + warp * nbw;
+  if (warp < gw && lane == 0) {
+    for (int b = 0; b < nbw; ++b) mbar_init(&bars[b], 1);
+    fence_mbar_init();
+  }
+  if (threadIdx.x == 0) s_abort = 0;
+  __syncthreads();
+  if (warp >= gw) return;
+  const int rows = hdr[kHdrRpTotal];
+  const int gid = blockIdx.x * gw + warp, ni = gridDim.x * gw;
+  const int n = gid < rows ? (rows - gid + ni - 1) / ni : 0;
+  const int nblk = d >> 5;
+  // source rows 32 items at a time in two registers, shuffled to every lane
+  int c0 = 0;
+  int ia = lane < n ? __ldg(row_of_pad + gid + (size_t)lane * ni) : -1;
+  int ib = 32 + lane < n ? __ldg(row_of_pad + gid + (size_t)(32 + lane) * ni) : -1;
+  auto row_at = [&](int i) { return __shfl_sync(0xffffffffu, (i - c0) < 32 ? ia : ib, (i - c0) & 31); };
+  uint32_t ph = 0, pend = 0;
+  auto issue = [&](int i) {
+    const int r = row_at(i);
+    if (lane == 0 && r >= 0) {
+      const int b = i % nbw;
+      mbar_arrive_expect_tx(&bars[b], rb);
+      bulk_load(smem_u32(wbuf + (size_t)b * rb), src + (size_t)(r / k) * d, rb, smem_u32(&bars[b]));
+      pend |= 1u << b;
+    }
+  };
+  for (int i = 0; i < min(nbw, n); ++i) issue(i);
+  bool ok = true;
+  for (int i = 0; i < n; ++i) {
+    if (i - c0 == 32) {
+      c0 += 32;
+      ia = ib;
+      ib = c0 + 32 + lane < n ? __ldg(row_of_pad + gid + (size_t)(c0 + 32 + lane) * ni) : -1;
+    }
+    const int r = row_at(i);
+    const int b = i % nbw;
+    if (r >= 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars[b], (ph >> b) & 1u, &s_abort, status, 910));
+      if (!ok) break;
+      ph ^= 1u << b;
+      pend &= ~(1u << b);
+    }
+    const size_t pp = (size_t)gid + (size_t)i * ni;
+    const uint4* row = reinterpret_cast<const uint4*>(wbuf + (size_t)b * rb);
+    for (int blk = lane; blk < nblk; blk += 32) {
+      uint4 in[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) in[u] = (r >= 0) ? row[blk * 4 + u] : make_uint4(0, 0, 0, 0);
+      uint4 out[2];
+      uint8_t s8;
+      quant32(in, out, s8);
+      uint4* qv = reinterpret_cast<uint4*>(q + pp * d + blk * 32);
+      stg_v4(qv, out[0]);
+      stg_v4(qv + 1, out[1]);
+      sc[mx_sf_offset(pp, blk, d >> 7)] = s8;
+    }
+    fence_proxy_async_smem();  // this lane's reads of the buffer come before the next copy into it
+    __syncwarp();
+    if (i + nbw < n) issue(i + nbw);
+  }
+  if (lane == 0 && !ok)
+    for (int b = 0; b < nbw; ++b)  // no copy may still target shared memory at exit
+      if ((pend >> b) & 1u) mbar_wait_drain(&bars[b], (ph >> b) & 1u);
+}
+
 // Weights [batch, K, N] bf16 -> codes [batch, N, K] and scale tiles over [batch*N, K].
 // One thread per (batch, n, 32-block of K): reads a strided column block.
 __global__ void __launch_bounds__(256) quant_weights_kernel(const __nv_bfloat16* __restrict__ w,
@@ -288,9 +371,27 @@ cudaError_t launch_gather(const moe_config& c, const Ws& ws, const __nv_bfloat16
 
 cudaError_t launch_gather_mxfp8(const moe_config& c, const Ws& ws, const __nv_bfloat16* src,
                                 uint8_t* q, uint8_t* sc, cudaStream_t st) {
-  const int grid = num_sms() * 8;
   TraceScope ts("gather_mxfp8", st);
-  gather_mxfp8_kernel<<<grid, 256, 0, st>>>(src, q, sc, ws.row_of_pad(), ws.hdr(), c.k, c.d);
+  // bf16 rows staged through shared memory: up to 16 buffers in each of 8
+  // warps (fewer warps for wide rows, at least two buffers each)
+  constexpr size_t kBudget = 227 * 1024 - 128 - 8 * 16 * 8;
+  const size_t rb = (size_t)c.d * 2;
+  if (kBudget >= 2 * rb && MOE_BULK_GATHER) {
+    int gw = 8;
+    int nbw = (int)std::min<size_t>(16, kBudget / (gw * rb));
+    if (nbw < 2) {
+      nbw = 2;
+      gw = (int)(kBudget / (2 * rb));
+    }
+    const size_t smem = 128 + (size_t)gw * nbw * rb + (size_t)gw * nbw * 8;
+    cudaError_t err = cudaFuncSetAttribute(gather_mxfp8_bulk_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    gather_mxfp8_bulk_kernel<<<num_sms(), 256, smem, st>>>(src, q, sc, ws.row_of_pad(), ws.hdr(), c.k,
+                                                           c.d, gw, nbw, ws.hdr() + kHdrStatus);
+    return cudaGetLastError();
+  }
+  gather_mxfp8_kernel<<<num_sms() * 8, 256, 0, st>>>(src, q, sc, ws.row_of_pad(), ws.hdr(), c.k, c.d);
   return cudaGetLastError();
 }
 
