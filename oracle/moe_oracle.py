@@ -51,6 +51,7 @@ __all__ = [
     "mxfp8_quantize",
     "mxfp8_dequantize",
     "forward_mxfp8",
+    "backward_mxfp8",
 ]
 
 
@@ -449,3 +450,79 @@ def forward_mxfp8(x, W1, W2, ids, g, tokens=None):
         for q, (i, t, j) in enumerate(lst):
             out[i] += gg[t, j] * Y[q]
     return out
+
+
+def _pad_rows(v, mult: int = 32):
+    """v [m, n] with zero rows appended up to a multiple of `mult` rows."""
+    m = v.shape[0]
+    pad = (-m) % mult
+    return np.concatenate([v, np.zeros((pad, v.shape[1]))], axis=0) if pad else v
+
+
+def backward_mxfp8(x, W1, W2, ids, g, dOut, qdq=None):
+    """Full backward with MXFP8 operands.
+
+    Reading (the pages name an MXFP8 mode for the layer, [MT] "BF16 and MXFP8
+    precision modes", and put the quantisation on the GEMMs' data path, [LP]
+    02, but do not say how the backward quantises): every GEMM quantises both
+    of its operands along its own contraction dimension, in blocks of 32 with
+    the scale rule above; for the weight-gradient GEMMs that dimension is the
+    expert's rows in the stable expert order, blocked from the start of the
+    expert's segment, the last block padded with zero rows.  Per expert e with
+    rows X (of x), weights g, upstream rows dO:
+      forward, as forward_mxfp8:  H = q_d(X) q_d(W1e),  A = silu(Hg) * Hu
+      dgrad2   (K = d):   dA' = q_d(dO) q_d(W2e)^T        (W2e [f, d])
+      routing-weight gradient fused into the SwiGLU backward: dg = <dA', A>
+      SwiGLU backward (fp64) on dA = g dA'  ->  dH = [dHg | dHu]
+      dgrad1   (K = 2f):  dX = q_2f(dH) q_2f(W1e)^T       (W1e [d, 2f])
+      wgrad1   (K = rows): dW1e = q_m(X)^T q_m(dH)
+      wgrad2   (K = rows): dW2e = q_m(g A)^T q_m(dO)
+    dx[t] sums its rows' dX in slot order; dlogits follows from dg as in
+    backward().  qdq(v, axis) is the quantise-dequantise step (MXFP8 by
+    default); the identity turns this into backward() (its dg_fused).
+    Returns dict: dx, dW1, dW2, dg (fused), dlogits."""
+    q = _qdq if qdq is None else qdq
+    x = _f64(x)
+    dOut = _f64(dOut)
+    ids = np.asarray(ids)
+    T, d = x.shape
+    k = ids.shape[1]
+    E = len(W1)
+    gg = _f64(g)
+    twof = np.asarray(W1[0]).shape[1]
+    f = twof // 2
+    counts, offsets, perm, inv = schedule(ids, E)
+    dx = np.zeros((T, d))
+    dW1 = np.zeros((E, d, twof))
+    dW2 = np.zeros((E, f, d))
+    dg = np.zeros(T * k)
+    dX_rows = np.zeros((T * k, d))
+    for e in range(E):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if a == b:
+            continue
+        rows = perm[a:b]
+        tok = rows // k
+        m = b - a
+        W1e = _f64(W1[e])
+        W2e = _f64(W2[e])
+        Xe = x[tok]
+        ge = gg.reshape(-1)[rows]
+        dOe = dOut[tok]
+        H = q(Xe, 1) @ q(W1e, 0)
+        Hg, Hu = H[:, :f], H[:, f:]
+        A = silu(Hg) * Hu
+        dAp = q(dOe, 1) @ q(W2e, 1).T
+        dg[rows] = np.einsum("mf,mf->m", dAp, A)
+        dA = ge[:, None] * dAp
+        sg = _sigmoid(Hg)
+        dH = np.concatenate([dA * Hu * sg * (1.0 + Hg * (1.0 - sg)), dA * (Hg * sg)], axis=1)
+        dX_rows[rows] = q(dH, 1) @ q(W1e, 1).T
+        dW1[e] = (q(_pad_rows(Xe), 0).T @ q(_pad_rows(dH), 0))
+        dW2[e] = (q(_pad_rows(ge[:, None] * A), 0).T @ q(_pad_rows(dOe), 0))
+        del m
+    for j in range(k):  # slot order
+        dx += dX_rows[np.arange(T) * k + j]
+    dg = dg.reshape(T, k)
+    return {"dx": dx, "dW1": dW1, "dW2": dW2, "dg": dg,
+            "dlogits": dlogits_from_dg(gg, ids, dg, E)}
