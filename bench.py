@@ -17,6 +17,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -84,18 +85,30 @@ KERNEL_SOURCE = {"ring_forward": "ring.cu", "gather": "gather_merge.cu", "gather
                  "sched_topk": "sched.cu", "sched_hist": "sched.cu", "sched_scatter": "sched.cu"}
 
 
-def src_digest(kernel=None):
-    """Digest of the CUDA sources a kernel is built from: its translation unit
-    (gemm.cu for the grouped GEMMs) and every header; all sources when kernel
-    is None."""
-    h = hashlib.sha256()
+def strip_comments(text):
+    """C++ source without // and /* */ comments and blank lines (string
+    literals in these sources hold no comment markers)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(ln.rstrip() for ln in text.splitlines() if ln.strip())
+
+
+def src_digest(kernel=None, read=None):
+    """Digest of the code (comments stripped) a kernel is built from: its
+    translation unit (gemm.cu for the grouped GEMMs) and every header; all
+    sources when kernel is None.  read(name) returns a source's text (default:
+    the working tree)."""
     csrc = os.path.join(ROOT, "mixture_experts_layer_stable_gb300", "csrc")
+    if read is None:
+        def read(name):
+            with open(os.path.join(csrc, name), encoding="utf-8") as fh:
+                return fh.read()
+    h = hashlib.sha256()
     tu = KERNEL_SOURCE.get(kernel, "gemm.cu") if kernel else None
     for name in sorted(os.listdir(csrc)):
         if tu is not None and name.endswith(".cu") and name != tu:
             continue
-        with open(os.path.join(csrc, name), "rb") as fh:
-            h.update(name.encode() + fh.read())
+        h.update(name.encode() + strip_comments(read(name)).encode())
     return h.hexdigest()[:16]
 
 

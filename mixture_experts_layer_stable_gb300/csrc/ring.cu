@@ -1,4 +1,4 @@
-// ring.cu -- the forward pass as one persistent kernel with an SM partition.
+// ring.cu -- the forward pass as one persistent kernel.
 //
 // The pages' megakernel splits the GPU's SMs into a side that moves tokens
 // (dispatch, combine, state) and a side that runs the expert FFN; the moving
@@ -8,25 +8,27 @@
 // CPU in the loop (leiphone "MoK..." section 02; Marktechpost "Cursor开源MoK..."
 // three design decisions).  On one GPU the moving side is an HBM gather.
 //
-// Layout of one launch (cooperative, so every CTA is co-resident):
-//   CTAs [0, G)       gather side: for every window w of `mb` consecutive rows
-//                     of the padded expert order, wait until ring slot
-//                     w % S is free, copy the window's token rows into it
-//                     (bulk copies staged through shared memory), then
-//                     release ready[slot].
-//   CTAs [G, grid)    compute side: the warp-specialised tcgen05 pipeline of
-//                     gemm.cu over a tile stream ordered
-//                     G1(0), [G1(1), G2(0)], [G1(2), G2(1)], ..., G2(last),
-//                     each CTA claiming the next tile from a global counter
-//                     when its loader is ready for one (tiles of mixed cost
-//                     balance themselves across CTAs):
-//                     GEMM1 + SwiGLU tiles of window w read the ring slot after
-//                     acquiring ready[slot] and release freed[slot] once their
-//                     loads have landed; GEMM2 tiles of a 128-row tile wait for
-//                     that tile's GEMM1 epilogues (a_ready) and store Y in
-//                     expert order.
-//   all CTAs          after the last GEMM2 store (done2), the fixed-order
-//                     weighted merge of every token.
+// Layout of one launch (cooperative, so every CTA is co-resident), for
+// windows w of `mb` consecutive rows of the padded expert order held in ring
+// slot w % S:
+//   gather         either (G = 0, the default) the last kGatherWarps warps of
+//                  every CTA, each copying its share of a window with plain
+//                  loads and stores, or (G > 0) CTAs [0, G), whose warps stage
+//                  rows through shared memory with bulk copies; each waits
+//                  until the slot is free (freed), copies the window's token
+//                  rows in and releases ready[slot].
+//   compute        the warp-specialised tcgen05 pipeline of gemm.cu (TMA
+//                  producer, MMA issuer, four epilogue warps) in every CTA that
+//                  is not a gather CTA, over the tile stream G1(0) ... G1(lag-1),
+//                  [G1(lag), G2(0)], ..., G2(last); each CTA claims the next
+//                  tile from a global counter when its producer is ready for
+//                  one, so tiles of mixed cost balance themselves.  GEMM1 +
+//                  SwiGLU tiles of window w read the ring slot after acquiring
+//                  ready[slot] and release freed[slot] once their loads have
+//                  landed; GEMM2 tiles of a 128-row tile wait for that tile's
+//                  GEMM1 epilogues (a_ready) and store Y in expert order.
+//   all CTAs       after the last GEMM2 store (done2), the fixed-order
+//                  weighted merge of every token.
 // Every tile waits only on tiles and windows earlier in the stream, so the
 // stream always makes progress.  Every wait is bounded: on expiry the kernel
 // sets a global abort word, reports MOE_ERR_TIMEOUT in the workspace status

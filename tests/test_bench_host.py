@@ -87,3 +87,20 @@ def test_roofline_units_pick_the_binding_resource():
     assert flop / peak_f > nbytes / peak_b
     # memory-only kernels carry no FLOPs
     assert u["merge"][0] is None and u["merge"][1] == 0.0
+
+
+def test_recorded_traffic_follows_the_kernel_code_not_its_comments():
+    real = {n: open(os.path.join(ROOT, "mixture_experts_layer_stable_gb300", "csrc", n)).read()
+            for n in os.listdir(os.path.join(ROOT, "mixture_experts_layer_stable_gb300", "csrc"))}
+    base = bench.src_digest("ring_forward", real.__getitem__)
+    # a comment edit keeps the digest (and so the recorded ncu bytes)
+    commented = dict(real, **{"ring.cu": "// note\n" + real["ring.cu"].replace("\n", "  // x\n", 3)})
+    assert bench.src_digest("ring_forward", commented.__getitem__) == base
+    # a code edit in the kernel's own translation unit or in a header does not
+    for name in ("ring.cu", "ptx.cuh"):
+        edited = dict(real, **{name: real[name] + "\nstatic int moe_digest_probe;\n"})
+        assert bench.src_digest("ring_forward", edited.__getitem__) != base
+    # another translation unit does not matter to this kernel
+    other = dict(real, **{"sched.cu": real["sched.cu"] + "\nstatic int moe_digest_probe;\n"})
+    assert bench.src_digest("ring_forward", other.__getitem__) == base
+    assert bench.src_digest("wgrad1", other.__getitem__) == bench.src_digest("wgrad1", real.__getitem__)
