@@ -102,3 +102,25 @@ def test_tile_boundary_counts_forward_backward(d, f):
     pad_t = torch.from_numpy(pad).cuda()
     assert torch.count_nonzero(H[pad_t]) == 0
     assert torch.count_nonzero(A[pad_t]) == 0
+
+
+def test_rows_wider_than_the_bulk_gather_buffers():
+    # d = 40960: a bf16 row (80 KB) leaves no room for two shared-memory row
+    # buffers per warp, so both gathers take their plain-load kernel; the
+    # grouped GEMMs run K = 40960 (GEMM1, dgrad2) and N = 40960 (GEMM2)
+    cfg = with_config("tiny", T=96, d=40960, f=64, E=4, k=2)
+    inp = make_inputs(cfg, x_std=1.0)
+    dev = {k: v.cuda() for k, v in inp.items()}
+    L = Layer(cfg)
+    L.schedule(dev["logits"])
+    out = L.forward(dev["x"], dev["W1"], dev["W2"], save=True)
+    L.backward(dev["dOut"], dev["x"], dev["W1"], dev["W2"])
+    torch.cuda.synchronize()
+    assert L.status() == 0
+    ids, g = O.route(inp["logits"].numpy(), 2)
+    x, W1, W2, dO = to_np(inp["x"]), ExpertView(inp["W1"]), ExpertView(inp["W2"]), to_np(inp["dOut"])
+    want, _ = O.forward(x, W1, W2, ids, g)
+    assert rel_err(out.float().cpu().numpy(), want) <= TOL_BF16
+    wb = O.backward(x, W1, W2, ids, g, dO)
+    for name, got in (("dx", L.dx), ("dW1", L.dW1), ("dW2", L.dW2)):
+        assert rel_err(got.float().cpu().numpy(), wb[name]) <= TOL_BF16, name
