@@ -78,7 +78,7 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
 
 
-# the translation unit that defines each traced kernel (every header counts for all)
+# the translation unit that defines each traced kernel
 KERNEL_SOURCE = {"ring_forward": "ring.cu", "gather": "gather_merge.cu", "gather_x_dy": "gather_merge.cu",
                  "gather_mxfp8": "gather_merge.cu", "merge": "gather_merge.cu",
                  "reverse_dispatch": "gather_merge.cu", "dg_reduce": "gather_merge.cu",
@@ -95,19 +95,28 @@ def strip_comments(text):
 
 def src_digest(kernel=None, read=None):
     """Digest of the code (comments stripped) a kernel is built from: its
-    translation unit (gemm.cu for the grouped GEMMs) and every header; all
-    sources when kernel is None.  read(name) returns a source's text (default:
-    the working tree)."""
+    translation unit (gemm.cu for the grouped GEMMs) and the library headers
+    it includes, directly or not; all sources when kernel is None.
+    read(name) returns a source's text (default: the working tree)."""
     csrc = os.path.join(ROOT, "mixture_experts_layer_stable_gb300", "csrc")
+    names = set(os.listdir(csrc))
     if read is None:
         def read(name):
             with open(os.path.join(csrc, name), encoding="utf-8") as fh:
                 return fh.read()
+    if kernel is None:
+        files = sorted(names)
+    else:
+        files, todo = set(), [KERNEL_SOURCE.get(kernel, "gemm.cu")]
+        while todo:
+            name = todo.pop()
+            if name in files or name not in names:
+                continue
+            files.add(name)
+            todo += [os.path.basename(i) for i in re.findall(r'#include\s+"([^"]+)"', read(name))]
+        files = sorted(files)
     h = hashlib.sha256()
-    tu = KERNEL_SOURCE.get(kernel, "gemm.cu") if kernel else None
-    for name in sorted(os.listdir(csrc)):
-        if tu is not None and name.endswith(".cu") and name != tu:
-            continue
+    for name in files:
         h.update(name.encode() + strip_comments(read(name)).encode())
     return h.hexdigest()[:16]
 

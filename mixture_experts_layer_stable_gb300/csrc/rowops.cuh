@@ -48,20 +48,32 @@ __device__ __forceinline__ void merge_token(const __nv_bfloat16* __restrict__ ro
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const void* src = rows + (size_t)sp[j] * d + (size_t)v * 8;
-      const uint4 y = COHERENT ? ldcg_v4(src) : ldg_nc_v4(src);
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&y);
-      const float g = sw[j];
+    // the slots' rows 8 at a time: loads first (in flight together), then
+    // the sums in slot order
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      uint4 y[8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(h[i]);
-        if (weighted) {
-          acc[2 * i] = fmaf(g, f.x, acc[2 * i]);
-          acc[2 * i + 1] = fmaf(g, f.y, acc[2 * i + 1]);
-        } else {
-          acc[2 * i] += f.x;
-          acc[2 * i + 1] += f.y;
+      for (int u = 0; u < 8; ++u) {
+        if (j0 + u < k) {
+          const void* src = rows + (size_t)sp[j0 + u] * d + (size_t)v * 8;
+          y[u] = COHERENT ? ldcg_v4(src) : ldg_nc_v4(src);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (j0 + u >= k) break;
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&y[u]);
+        const float g = sw[j0 + u];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __bfloat1622float2(h[i]);
+          if (weighted) {
+            acc[2 * i] = fmaf(g, f.x, acc[2 * i]);
+            acc[2 * i + 1] = fmaf(g, f.y, acc[2 * i + 1]);
+          } else {
+            acc[2 * i] += f.x;
+            acc[2 * i + 1] += f.y;
+          }
         }
       }
     }

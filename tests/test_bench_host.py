@@ -96,10 +96,14 @@ def test_recorded_traffic_follows_the_kernel_code_not_its_comments():
     # a comment edit keeps the digest (and so the recorded ncu bytes)
     commented = dict(real, **{"ring.cu": "// note\n" + real["ring.cu"].replace("\n", "  // x\n", 3)})
     assert bench.src_digest("ring_forward", commented.__getitem__) == base
-    # a code edit in the kernel's own translation unit or in a header does not
-    for name in ("ring.cu", "ptx.cuh"):
+    # a code edit in the kernel's own translation unit or in a header it
+    # includes does not
+    for name in ("ring.cu", "ptx.cuh", "rowops.cuh"):
         edited = dict(real, **{name: real[name] + "\nstatic int moe_digest_probe;\n"})
         assert bench.src_digest("ring_forward", edited.__getitem__) != base
+    # a header the grouped GEMMs do not include does not matter to them
+    edited = dict(real, **{"rowops.cuh": real["rowops.cuh"] + "\nstatic int moe_digest_probe;\n"})
+    assert bench.src_digest("wgrad1", edited.__getitem__) == bench.src_digest("wgrad1", real.__getitem__)
     # another translation unit does not matter to this kernel
     other = dict(real, **{"sched.cu": real["sched.cu"] + "\nstatic int moe_digest_probe;\n"})
     assert bench.src_digest("ring_forward", other.__getitem__) == base
