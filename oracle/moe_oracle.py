@@ -422,33 +422,61 @@ def _qdq(v, axis):
     return mxfp8_dequantize(c, s, axis)
 
 
-def forward_mxfp8(x, W1, W2, ids, g, tokens=None):
+# Names of the quantised GEMM operands, "<GEMM>.<operand>".  The MXFP8 forward
+# and backward below quantise every one of them by default; `quantise` may
+# name a subset (the others pass through unchanged) so that each operand's
+# quantisation axis can be checked on its own.
+FORWARD_OPERANDS = ("fwd.x", "fwd.W1", "fwd.A", "fwd.W2")
+BACKWARD_OPERANDS = ("fwd.x", "fwd.W1", "dgrad2.dO", "dgrad2.W2", "dgrad1.dH", "dgrad1.W1",
+                     "wgrad1.X", "wgrad1.dH", "wgrad2.gA", "wgrad2.dO")
+
+
+def _quantiser(qdq, quantise, names):
+    """apply(v, axis, name): qdq(v, axis) (MXFP8 by default) when `name` is
+    among `quantise` (all of `names` when None), else v unchanged."""
+    q = _qdq if qdq is None else qdq
+    chosen = set(names if quantise is None else quantise)
+    unknown = chosen - set(names)
+    if unknown:
+        raise ValueError(f"unknown operands {sorted(unknown)}")
+
+    def apply(v, axis, name):
+        return q(v, axis) if name in chosen else v
+    return apply
+
+
+def forward_mxfp8(x, W1, W2, ids, g, tokens=None, qdq=None, quantise=None):
     """Per-token forward with MXFP8 operands ([LP] 02: activation quantisation
-    fused into dispatch and into the SwiGLU data path).  x is quantised along
-    d, W1[e] along its K dim d, the SwiGLU output A along f, W2[e] along its K
-    dim f; every product is then exact in fp64.  Returns out for `tokens`."""
+    fused into dispatch and into the SwiGLU data path).  Each GEMM quantises
+    both operands along its contraction dimension: x along d and W1[e] [d, 2f]
+    along d (GEMM1), the SwiGLU output A along f and W2[e] [f, d] along f
+    (GEMM2); every product is then exact in fp64.  qdq(v, axis) is the
+    quantise-dequantise step (MXFP8 by default; the identity gives the
+    unquantised layer); `quantise` names the operands it applies to
+    (FORWARD_OPERANDS; all by default).  Returns out for `tokens`."""
+    q = _quantiser(qdq, quantise, FORWARD_OPERANDS)
     x = _f64(x)
     ids = np.asarray(ids)
     T, k = ids.shape
     tokens = np.arange(T) if tokens is None else np.asarray(tokens)
     gg = _f64(g)
-    xq = _qdq(x[tokens], axis=1)
+    xq = q(x[tokens], 1, "fwd.x")
     out = np.zeros((len(tokens), x.shape[1]))
     pairs = {}
     for i, t in enumerate(tokens):
         for j in range(k):
             pairs.setdefault(int(ids[t, j]), []).append((i, int(t), j))
     for e, lst in pairs.items():
-        W1q = _qdq(W1[e], axis=0)
-        W2q = _qdq(W2[e], axis=0)
+        W1q = q(_f64(W1[e]), 0, "fwd.W1")
+        W2q = q(_f64(W2[e]), 0, "fwd.W2")
         f = W2q.shape[0]
         Xe = xq[[i for (i, _, _) in lst]]
         H = Xe @ W1q
         A = silu(H[:, :f]) * H[:, f:]
-        Aq = _qdq(A, axis=1)
+        Aq = q(A, 1, "fwd.A")
         Y = Aq @ W2q
-        for q, (i, t, j) in enumerate(lst):
-            out[i] += gg[t, j] * Y[q]
+        for r, (i, t, j) in enumerate(lst):
+            out[i] += gg[t, j] * Y[r]
     return out
 
 
@@ -459,7 +487,7 @@ def _pad_rows(v, mult: int = 32):
     return np.concatenate([v, np.zeros((pad, v.shape[1]))], axis=0) if pad else v
 
 
-def backward_mxfp8(x, W1, W2, ids, g, dOut, qdq=None):
+def backward_mxfp8(x, W1, W2, ids, g, dOut, qdq=None, quantise=None):
     """Full backward with MXFP8 operands.
 
     Reading (the pages name an MXFP8 mode for the layer, [MT] "BF16 and MXFP8
@@ -480,8 +508,9 @@ def backward_mxfp8(x, W1, W2, ids, g, dOut, qdq=None):
     dx[t] sums its rows' dX in slot order; dlogits follows from dg as in
     backward().  qdq(v, axis) is the quantise-dequantise step (MXFP8 by
     default); the identity turns this into backward() (its dg_fused).
-    Returns dict: dx, dW1, dW2, dg (fused), dlogits."""
-    q = _qdq if qdq is None else qdq
+    `quantise` names the operands qdq applies to (BACKWARD_OPERANDS; all by
+    default).  Returns dict: dx, dW1, dW2, dg (fused), dlogits."""
+    q = _quantiser(qdq, quantise, BACKWARD_OPERANDS)
     x = _f64(x)
     dOut = _f64(dOut)
     ids = np.asarray(ids)
@@ -509,17 +538,17 @@ def backward_mxfp8(x, W1, W2, ids, g, dOut, qdq=None):
         Xe = x[tok]
         ge = gg.reshape(-1)[rows]
         dOe = dOut[tok]
-        H = q(Xe, 1) @ q(W1e, 0)
+        H = q(Xe, 1, "fwd.x") @ q(W1e, 0, "fwd.W1")
         Hg, Hu = H[:, :f], H[:, f:]
         A = silu(Hg) * Hu
-        dAp = q(dOe, 1) @ q(W2e, 1).T
+        dAp = q(dOe, 1, "dgrad2.dO") @ q(W2e, 1, "dgrad2.W2").T
         dg[rows] = np.einsum("mf,mf->m", dAp, A)
         dA = ge[:, None] * dAp
         sg = _sigmoid(Hg)
         dH = np.concatenate([dA * Hu * sg * (1.0 + Hg * (1.0 - sg)), dA * (Hg * sg)], axis=1)
-        dX_rows[rows] = q(dH, 1) @ q(W1e, 1).T
-        dW1[e] = (q(_pad_rows(Xe), 0).T @ q(_pad_rows(dH), 0))
-        dW2[e] = (q(_pad_rows(ge[:, None] * A), 0).T @ q(_pad_rows(dOe), 0))
+        dX_rows[rows] = q(dH, 1, "dgrad1.dH") @ q(W1e, 1, "dgrad1.W1").T
+        dW1[e] = (q(_pad_rows(Xe), 0, "wgrad1.X").T @ q(_pad_rows(dH), 0, "wgrad1.dH"))
+        dW2[e] = (q(_pad_rows(ge[:, None] * A), 0, "wgrad2.gA").T @ q(_pad_rows(dOe), 0, "wgrad2.dO"))
         del m
     for j in range(k):  # slot order
         dx += dX_rows[np.arange(T) * k + j]

@@ -20,10 +20,13 @@ operands along its own contraction dimension).
    the matching gate and up columns of dW1: wgrad1 quantises dH along the
    rows.
 
-Not pinned separately: dgrad1's quantisation axis of W1, wgrad1's of X,
-wgrad2's of g*A (each also enters the forward), and where the
-weight-gradient row blocks start (the start of each expert's segment, a
-reading).
+6. Every operand on its own (the tests at the end): quantising one operand
+   alone reproduces the unquantised backward exactly on inputs that are
+   blockwise exact along that operand's contraction axis, and loses bits when
+   the same operand is blocked along its other axis -- all ten operands,
+   including dgrad1's W1, wgrad1's X and wgrad2's g*A.  The weight-gradient
+   row blocks start at each expert's segment (a reading): an input exact
+   under that anchoring is lossy under blocks keyed to the global position.
 """
 import numpy as np
 import pytest
@@ -174,3 +177,154 @@ def test_wgrad1_blocks_dh_along_the_rows():
     np.testing.assert_array_equal(b["dW1"][:, :, cols], a["dW1"][:, :, cols])
     np.testing.assert_array_equal(b["dW1"][:, :, ~cols], 2.0 ** 12 * a["dW1"][:, :, ~cols])
     np.testing.assert_array_equal(b["dW2"], a["dW2"])
+
+
+# ---------------------------------------------------------------------------
+# Every operand on its own.  For each quantised operand of the backward, an
+# input on which that operand holds one power-of-two scale per 32-block along
+# its contraction axis (and small integers) quantises losslessly there, so
+# quantising only it reproduces the unquantised backward exactly; blocked
+# along its other axis it mixes magnitudes 16 binades apart and loses bits.
+# dH and g*A are computed, so their cases are built from one-hot token rows
+# (x[t] = c_t e_i(t), dOut[t] = e_l(t)), top-1 routing (g = 1) and gate
+# weights of at least 2^6, where sigmoid(H_gate) is exactly 1 in fp64: then
+# SiLU(H_gate) = H_gate, dH_gate = dA * H_up and dH_up = dA * H_gate exactly.
+# ---------------------------------------------------------------------------
+def _ident(v, axis):
+    return v
+
+
+def _swapped(v, axis):
+    return _qdq_any(v, 1 - axis)
+
+
+def _binades(rng, shape):
+    return np.ldexp(1.0, 8 * rng.choice([-1, 1], size=shape))
+
+
+def _pow2(rng, shape, top=2):
+    """+-2^j, j in [0, top]: products of a few stay exact in E4M3."""
+    return rng.choice([-1, 1], size=shape) * np.ldexp(1.0, rng.integers(0, top + 1, size=shape))
+
+
+def _onehot_rows(rng, T, n, scale):
+    v = np.zeros((T, n))
+    v[np.arange(T), rng.integers(0, n, size=T)] = scale
+    return v
+
+
+def _operand_case(op, seed):
+    rng = np.random.default_rng(seed)
+    T, d, f, E = 96, 64, 64, 3
+    k = 2
+    x = rng.standard_normal((T, d))
+    W1 = [rng.standard_normal((d, 2 * f)) / 8 for _ in range(E)]
+    W2 = [rng.standard_normal((f, d)) / 8 for _ in range(E)]
+    dO = rng.standard_normal((T, d))
+    if op == "fwd.x":          # [m, d] along d: a scale per row
+        x = _grid(rng, (T, d)) * _binades(rng, (T, 1))
+    elif op == "fwd.W1":       # [d, 2f] along d: a scale per column
+        W1 = [_grid(rng, (d, 2 * f)) * _binades(rng, (1, 2 * f)) for _ in range(E)]
+    elif op == "dgrad2.dO":    # [m, d] along d: a scale per row
+        dO = _grid(rng, (T, d)) * _binades(rng, (T, 1))
+    elif op == "dgrad2.W2":    # W2e [f, d] along d: a scale per row
+        W2 = [_grid(rng, (f, d)) * _binades(rng, (f, 1)) for _ in range(E)]
+    elif op == "dgrad1.W1":    # W1e [d, 2f] along 2f: a scale per row
+        W1 = [_grid(rng, (d, 2 * f)) * _binades(rng, (d, 1)) for _ in range(E)]
+    elif op == "wgrad1.X":     # [m, d] along the rows: a scale per column
+        x = _grid(rng, (T, d)) * _binades(rng, (1, d))
+    elif op == "wgrad2.dO":    # [m, d] along the rows: a scale per column
+        dO = _grid(rng, (T, d)) * _binades(rng, (1, d))
+    else:
+        k = 1
+        dO = _onehot_rows(rng, T, d, 1.0)
+        W2 = [_pow2(rng, (f, d), 1) for _ in range(E)]
+        if op == "wgrad2.gA":
+            # A[t, j] = n[i, j] 2^s_j: a scale per column of g*A
+            x = _onehot_rows(rng, T, d, 1.0)
+            W1 = [np.concatenate([np.full((d, f), 64.0),
+                                  _grid(rng, (d, f)) * _binades(rng, (1, f)) / 64.0], axis=1)
+                  for _ in range(E)]
+        elif op == "dgrad1.dH":
+            # x[t] = c_t e_i with c_t = 2^8 or 2^-8, gate weights 2^14, up
+            # weights +-2^j 2^-14, W2 +-2^j: dH_gate = c_t W2 up and dH_up =
+            # c_t W2 2^14 (gate and up in separate 32-blocks): one scale per
+            # row in each half
+            c = _binades(rng, T)
+            x = _onehot_rows(rng, T, d, 1.0) * c[:, None]
+            W1 = [np.concatenate([np.full((d, f), 2.0 ** 14), _pow2(rng, (d, f)) * 2.0 ** -14], axis=1)
+                  for _ in range(E)]
+        elif op == "wgrad1.dH":
+            # one scale per column: gate columns 2^(14 + 16 b_j), up columns
+            # +-2^j 2^(-14 + 8 s_j); token rows all of scale 1
+            x = _onehot_rows(rng, T, d, 1.0)
+            gate = np.ldexp(1.0, 14 + 16 * rng.integers(0, 2, size=(1, f)))
+            W1 = [np.concatenate([np.ones((d, 1)) * gate,
+                                  _pow2(rng, (d, f)) * 2.0 ** -14 * _binades(rng, (1, f))], axis=1)
+                  for _ in range(E)]
+        else:
+            raise ValueError(op)
+    z = rng.standard_normal((T, E)).astype(np.float32)
+    ids, g = O.route(z, k)
+    return x, W1, W2, ids, g, dO
+
+
+def _worst(got, ref):
+    """Largest relative deviation over every output (exact zeros must stay)."""
+    w = 0.0
+    for name in ("dx", "dW1", "dW2", "dg"):
+        a, b = got[name], ref[name]
+        nz = b != 0
+        if np.any(nz):
+            w = max(w, float(np.max(np.abs(a[nz] - b[nz]) / np.abs(b[nz]))))
+        if np.any(~nz):
+            w = max(w, float(np.max(np.abs(a[~nz]))) / max(float(np.max(np.abs(b))), 1e-300))
+    return w
+
+
+@pytest.mark.filterwarnings("ignore:overflow encountered in exp")  # sigmoid / SiLU limits, exact
+@pytest.mark.parametrize("op", O.BACKWARD_OPERANDS)
+def test_quantisation_axis_of_each_backward_operand(op):
+    x, W1, W2, ids, g, dO = _operand_case(op, seed=30 + O.BACKWARD_OPERANDS.index(op))
+    ref = O.backward_mxfp8(x, W1, W2, ids, g, dO, qdq=_ident)
+    assert all(np.all(np.isfinite(ref[n])) for n in ("dx", "dW1", "dW2", "dg"))
+    got = O.backward_mxfp8(x, W1, W2, ids, g, dO, quantise=[op])
+    assert _worst(got, ref) < 1e-12, op
+    bad = O.backward_mxfp8(x, W1, W2, ids, g, dO, qdq=_swapped, quantise=[op])
+    assert _worst(bad, ref) > 1e-2, op
+
+
+def test_weight_gradient_row_blocks_start_at_each_expert_segment():
+    # Reading: the weight gradients' 32-row blocks run from the start of each
+    # expert's rows (in the stable expert order).  Top-1 routing with segment
+    # lengths that are not multiples of 32; x scaled 2^8 / 2^-8 by the block
+    # parity of its row's position in its expert's segment quantises
+    # losslessly under that reading -- and the same construction keyed to the
+    # global expert-ordered position (blocks straddling segments) does not.
+    rng = np.random.default_rng(40)
+    T, d, f, E = 150, 64, 32, 3
+    z = rng.standard_normal((T, E)).astype(np.float32)
+    ids, g = O.route(z, 1)
+    counts, offsets, perm, inv = O.schedule(ids, E)
+    assert np.any(offsets[1:E] % 32 != 0) and np.any(counts % 32 != 0)
+    pos = np.empty(T, np.int64)
+    seg = np.empty(T, np.int64)
+    pos[perm] = np.arange(T)
+    e_of = ids[:, 0]
+    seg = pos - offsets[e_of]
+    base = _grid(rng, (T, d))
+    W1 = [rng.standard_normal((d, 2 * f)) / 8 for _ in range(E)]
+    W2 = [rng.standard_normal((f, d)) / 8 for _ in range(E)]
+    dO = rng.standard_normal((T, d))
+
+    def dev(blockpos):
+        x = base * np.ldexp(1.0, 8 * np.where((blockpos // 32) % 2 == 0, 1, -1))[:, None]
+        ref = O.backward_mxfp8(x, W1, W2, ids, g, dO, qdq=_ident)["dW1"]
+        got = O.backward_mxfp8(x, W1, W2, ids, g, dO, quantise=["wgrad1.X"])["dW1"]
+        return float(np.max(np.abs(got - ref)) / np.max(np.abs(ref)))
+
+    # lossless: the quantised X is X itself, so dW1 is the same bits; lossy:
+    # the 2^-8 rows lose bits, visible far above fp64 rounding although they
+    # weigh 2^-16 of the 2^8 rows in each sum
+    assert dev(seg) == 0.0
+    assert dev(pos) > 1e-13
