@@ -2,16 +2,23 @@
 """Benchmark of the single-GPU MoE layer (routing -> schedule -> gather ->
 grouped SwiGLU FFN -> weighted merge, forward and backward) on GB300.
 
-One step = moe_schedule + moe_forward (saving activations) + moe_backward on
-one batch of seeded synthetic input already resident in HBM.  Prints ONE JSON
-line (rank 0).  `--impl reference` times the fp64 CPU oracle instead, on a
-bounded sample of the same workload.
+Default workload: the Kimi-like layer (hidden 7168, expert intermediate 2048,
+256 experts, top-8, 4,096 tokens, Zipf(1.2)-skewed routing), BF16 forward.
+One step = moe_schedule + moe_forward on one batch of seeded synthetic input
+already resident in HBM (fwd+bwd workloads add moe_backward).  Prints ONE
+JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle instead, on
+a bounded sample of the same workload.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload balanced]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload kimi_zipf]
   python -m torch.distributed.run --nproc-per-node N bench.py --gpus N ...
 
-With N > 1 every rank runs an independent replica of the layer (the layer has
-no exchange step on one GPU); value = routed tokens of all ranks / max time.
+Timing: W warm-up steps, then about a second of further untimed steps with
+the GPU clocks sampled (so the samples see the GPU under load), then K timed
+steps between CUDA events with a barrier and a synchronise on both sides and
+no other work in between.  Per-kernel times come from a separate traced pass
+afterwards.  With N > 1 every rank runs an independent replica of the layer
+(the layer has no exchange step on one GPU); value = routed tokens of all
+ranks / the slowest rank's time.
 """
 import argparse
 import hashlib
@@ -35,12 +42,13 @@ UNIT = "routed tokens/s"
 #   `touched` experts (those with rows) read once -- the weight gradients write
 #   every expert's dW -- plus one read of each input row and one write of each
 #   output row.  Memory-only kernels have no FLOPs.
-def kernel_units(c, touched):
+def kernel_units(c, touched, saved=True):
     R, T, d, f, k, E = c["T"] * c["k"], c["T"], c["d"], c["f"], c["k"], c["E"]
     b = 2.0  # bf16
     w1, w2 = touched * d * 2 * f * b, touched * f * d * b
+    a_out = 3 if saved else 1  # GEMM1 writes A, and H when saving
     return {
-        "gemm1_swiglu": ("flop", 2.0 * R * d * 2 * f, w1 + R * d * b + R * 3 * f * b),
+        "gemm1_swiglu": ("flop", 2.0 * R * d * 2 * f, w1 + R * d * b + R * a_out * f * b),
         "gemm2": ("flop", 2.0 * R * f * d, w2 + R * f * b + R * d * b),
         "dgrad2_dswiglu": ("flop", 2.0 * R * d * f, w2 + R * d * b + 2 * R * 3 * f * b),
         "wgrad2": ("flop", 2.0 * R * f * d, E * f * d * b + R * f * b + R * d * b),
@@ -49,16 +57,19 @@ def kernel_units(c, touched):
         "gemm1_swiglu_mxfp8": ("flop8", 2.0 * R * d * 2 * f,
                                touched * d * 2 * f * (1 + 1 / 32) + R * d * (1 + 1 / 32) + R * f * (1 + 1 / 32)),
         "gemm2_mxfp8": ("flop8", 2.0 * R * f * d, touched * f * d * (1 + 1 / 32) + R * f * (1 + 1 / 32) + R * d * b),
-        "gather": (None, 0.0, 2.0 * R * d * b),
-        "gather_mxfp8": (None, 0.0, R * d * (2.0 + 1.0 + 1.0 / 32)),
-        "gather_x_dy": (None, 0.0, 4.0 * R * d * b),
+        # gathers: one read per distinct token (its k reads after the first hit
+        # L2) and one write per routed row
+        "gather": (None, 0.0, T * d * b + R * d * b),
+        "gather_mxfp8": (None, 0.0, T * d * b + R * d * (1.0 + 1.0 / 32)),
+        "gather_x_dy": (None, 0.0, 2.0 * (T * d * b + R * d * b)),
         "merge": (None, 0.0, T * (k + 1) * d * b + R * 4.0 * 2),
+        "recompute_gemm1": ("flop", 2.0 * R * d * 2 * f, w1 + R * d * b + R * 3 * f * b),
         "reverse_dispatch": (None, 0.0, T * (k + 1) * d * b + R * 4.0),
         # persistent ring forward (gather + GEMM1 + SwiGLU + GEMM2 + merge in one launch):
         # token rows in, weights of the touched experts, H and A saved, Y written and read
         # back by the merge, out written
         "ring_forward": ("flop", 2.0 * R * d * 2 * f + 2.0 * R * f * d,
-                         R * d * b + w1 + w2 + R * 3 * f * b + 2.0 * R * d * b + T * d * b),
+                         T * d * b + w1 + w2 + R * a_out * f * b + 2.0 * R * d * b + T * d * b),
         # router projection (--router): x [T, d], Wr [E, d], logits / ids / weights
         "router_logits": ("flop", 2.0 * T * d * E, T * d * b + E * d * b + R * 8.0),
         "router_dlogits_bf16": (None, 0.0, T * E * 6.0),
@@ -136,7 +147,9 @@ def ncu_traffic(workload, kernel):
 
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples of the SM clock and throttle reasons every 100 ms;
+    stop(since) keeps the samples taken after wall time `since`."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -153,7 +166,34 @@ class ClockSampler:
         except (OSError, ValueError):
             self.proc = None
 
-    def stop(self):
+    @staticmethod
+    def parse(lines, since=None):
+        """Summary of sample lines (timestamp first; local time as nvidia-smi
+        prints it); samples before wall time `since` are dropped."""
+        sm, mx, pw, reasons = [], 0.0, [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in lines:
+            r = [c.strip() for c in line.split(",")]
+            try:
+                ts = time.mktime(time.strptime(r[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + r[0].split(".")[1]) if "." in r[0] else 0.0
+                if since is not None and ts < since:
+                    continue
+                sm.append(float(r[2]))
+                mx = max(mx, float(r[3]))
+                pw.append(float(r[4]))
+                for nm, v in zip(names, r[6:10]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "sm_mhz_min": min(sm),
+                "power_w_median": statistics.median(pw), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+    def stop(self, since=None):
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -163,23 +203,9 @@ class ClockSampler:
             self.proc.kill()
         self.out.flush()
         self.out.seek(0)
-        rows = [l.strip().split(", ") for l in self.out.read().splitlines() if l.strip()]
+        lines = [l for l in self.out.read().splitlines() if l.strip()]
         os.unlink(self.out.name)
-        sm, mx, reasons = [], 0.0, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            try:
-                sm.append(float(r[1]))
-                mx = max(mx, float(r[2]))
-                for nm, v in zip(names, r[5:9]):
-                    if v.strip().lower() == "active":
-                        reasons.add(nm)
-            except (ValueError, IndexError):
-                continue
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return self.parse(lines, since)
 
 
 def workload_dict(cfg):
@@ -198,29 +224,35 @@ def oracle_sample(cfg, n_experts, seed=0):
     return inp
 
 
-def oracle_step(cfg, inp, experts):
+def oracle_step(cfg, inp, experts, passes="fwd+bwd"):
     """One oracle pass over a sample: routing + schedule for every token,
-    then forward + backward of every row routed to `experts`.  Returns the
-    number of routed rows processed."""
-    import numpy as np
+    then the forward (and, for fwd+bwd, the backward) of every row routed to
+    `experts`.  Returns the number of routed rows processed."""
     import torch
     from oracle import moe_oracle as O
-
-    class View:
-        def __init__(self, t):
-            self.t = t
-
-        def __len__(self):
-            return cfg.E
-
-        def __getitem__(self, e):
-            return self.t[e].to(torch.float64).numpy()
 
     ids, g = O.route(inp["logits"].numpy(), cfg.k)
     counts, offsets, perm, inv = O.schedule(ids, cfg.E)
     x = inp["x"].to(torch.float64).numpy()
-    dO = inp["dOut"].to(torch.float64).numpy()
-    O.backward_experts(x, View(inp["W1"]), View(inp["W2"]), ids, g, dO, list(experts))
+    W1 = lambda e: inp["W1"][e].to(torch.float64).numpy()
+    W2 = lambda e: inp["W2"][e].to(torch.float64).numpy()
+    if passes == "fwd":
+        for e in experts:
+            a, b = int(offsets[e]), int(offsets[e + 1])
+            if a < b:
+                O.expert_ffn(x[perm[a:b] // cfg.k], W1(e), W2(e))
+    else:
+        class View:
+            def __len__(self):
+                return cfg.E
+
+            def __getitem__(self, e):
+                return W1(e) if self.which == 1 else W2(e)
+
+        v1, v2 = View(), View()
+        v1.which, v2.which = 1, 2
+        dO = inp["dOut"].to(torch.float64).numpy()
+        O.backward_experts(x, v1, v2, ids, g, dO, list(experts))
     return int(sum(int(counts[e]) for e in experts))
 
 
@@ -235,28 +267,38 @@ def blas_threads():
     return os.cpu_count()
 
 
-def time_oracle(cfg, budget_s, steps=1, warmup=0):
-    """Pick the sample (first n experts) so that one oracle pass takes about
-    budget_s, run warmup + steps passes, return (rows/s, sample description)."""
-    inp = oracle_sample(cfg, 2)
-    oracle_step(cfg, inp, range(1))           # first call: BLAS start-up
+def time_oracle(cfg, budget_s, steps=1, warmup=0, passes="fwd+bwd"):
+    """Pick the sample -- the rows of experts 0..n-1 -- so that one oracle
+    pass takes about budget_s, run warmup + steps passes, return (rows/s,
+    sample description, seconds)."""
+    import numpy as np
+    from oracle import moe_oracle as O
+    inp = oracle_sample(cfg, 1)
+    ids, _ = O.route(inp["logits"].numpy(), cfg.k)
+    counts = np.bincount(ids.reshape(-1), minlength=cfg.E)
+    # cost of one row: from the first nonempty expert's rows (at most 256 of them)
+    e0 = int(np.argmax(counts > 0))
+    inp = oracle_sample(cfg, e0 + 1)
+    oracle_step(cfg, inp, [e0], passes)             # first call: BLAS start-up
     t0 = time.perf_counter()
-    rows1 = oracle_step(cfg, inp, range(2))
-    t1 = max(time.perf_counter() - t0, 1e-3)
-    per_row = t1 / max(rows1, 1)
-    avg_rows = cfg.T * cfg.k / cfg.E
-    n = int(max(1, min(cfg.E, budget_s / (per_row * avg_rows))))
+    rows1 = oracle_step(cfg, inp, [e0], passes)
+    per_row = max(time.perf_counter() - t0, 1e-4) / max(rows1, 1)
+    n = 1
+    while n < cfg.E and (np.cumsum(counts)[n] * per_row) <= budget_s:
+        n += 1
     inp = oracle_sample(cfg, n)
     experts = range(n)
     for _ in range(warmup):
-        oracle_step(cfg, inp, experts)
+        oracle_step(cfg, inp, experts, passes)
     rows = 0
     t0 = time.perf_counter()
     for _ in range(steps):
-        rows += oracle_step(cfg, inp, experts)
+        rows += oracle_step(cfg, inp, experts, passes)
     dt = time.perf_counter() - t0
-    desc = (f"routing + schedule of all {cfg.T} tokens, then forward+backward (fp64 numpy) of the "
-            f"rows routed to experts 0..{n - 1} of {cfg.E}; {rows // max(steps, 1)} routed rows per pass")
+    what = "forward" if passes == "fwd" else "forward+backward"
+    desc = (f"routing + schedule of all {cfg.T} tokens, then {what} (fp64 numpy) of the rows "
+            f"routed to experts 0..{n - 1} of {cfg.E}; {rows // max(steps, 1)} of {cfg.T * cfg.k} "
+            f"routed rows per pass")
     return rows / dt, desc, dt
 
 
@@ -264,17 +306,20 @@ def time_oracle(cfg, budget_s, steps=1, warmup=0):
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="balanced")
-    ap.add_argument("--passes", default=None, help="fwd or fwd+bwd (default: fwd+bwd)")
-    ap.add_argument("--minibatch-rows", type=int, default=None,
-                    help="forward through the persistent ring kernel with windows of this many rows "
-                         "(default: the workload's first minibatch size, e.g. 1024 for balanced; "
-                         "0 = the kernel chain)")
+    ap.add_argument("--workload", default="kimi_zipf")
+    ap.add_argument("--passes", default=None, help="fwd or fwd+bwd (default: the workload's)")
+    ap.add_argument("--save", action="store_true",
+                    help="forward-only passes: also save H and A for a later backward")
+    ap.add_argument("--minibatch-rows", type=int, default=0,
+                    help="0 = the kernel chain; > 0 = the forward through the persistent ring "
+                         "kernel with windows of this many expert-ordered rows")
     ap.add_argument("--ring-slots", type=int, default=4)
-    ap.add_argument("--gather-ctas", type=int, default=0, help="ring: 0 = a gather warp in every CTA, G > 0 = G gather-only CTAs")
+    ap.add_argument("--gather-ctas", type=int, default=0, help="ring: 0 = gather warps in every CTA, G > 0 = G gather-only CTAs")
+    ap.add_argument("--settle-s", type=float, default=1.0,
+                    help="seconds of untimed steps after the warm-up, clocks sampled")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--router", action="store_true",
                     help="route from x and a router weight (moe_route, plus the router backward) "
@@ -309,15 +354,16 @@ def dist_setup():
 def run_reference(args, cfg, rank):
     if rank != 0:
         return
+    passes = args.passes or cfg.passes
     budget = 0.5 if args.steps + args.warmup <= 200 else max(0.05, 100.0 / (args.steps + args.warmup))
-    v, desc, dt = time_oracle(cfg, budget, steps=args.steps, warmup=args.warmup)
+    v, desc, dt = time_oracle(cfg, budget, steps=args.steps, warmup=args.warmup, passes=passes)
     cores = blas_threads()
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * dt / max(args.steps, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded torch generators; no dataset)",
-        "config": {"workload": cfg.name, **workload_dict(cfg), "passes": "fwd+bwd"},
+        "config": {"workload": cfg.name, **workload_dict(cfg), "passes": passes},
         "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -329,7 +375,7 @@ def main():
     world, rank, local = dist_setup()
     from mixture_experts_layer_stable_gb300.configs import CONFIGS
     cfg = CONFIGS[args.workload]
-    passes = args.passes or ("fwd" if cfg.prec == "mxfp8" else "fwd+bwd")
+    passes = args.passes or cfg.passes
     if args.impl == "reference":
         run_reference(args, cfg, rank)
         return
@@ -352,16 +398,14 @@ def main():
         torch.cuda.synchronize()
 
     prec = B.MOE_MXFP8 if cfg.prec == "mxfp8" else B.MOE_BF16
-    if args.minibatch_rows is None:
-        # the ring kernel serves the BF16 forward only
-        args.minibatch_rows = cfg.minibatch_rows[0] if (cfg.minibatch_rows and cfg.prec == "bf16") else 0
-    c = B.make_config(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, prec, args.minibatch_rows,
-                      args.ring_slots if args.minibatch_rows > 0 else 0, args.gather_ctas)
-    inp = make_inputs(cfg, device="cuda", seed=0, with_grad=(passes != "fwd"))
+    bwd = passes != "fwd"
+    save = bwd or args.save
+    mb = args.minibatch_rows
+    c = B.make_config(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, prec, mb,
+                      args.ring_slots if mb > 0 else 0, args.gather_ctas)
+    inp = make_inputs(cfg, device="cuda", seed=0, with_grad=bwd)
     w1, w1s, w2, w2s = inp["W1"], None, inp["W2"], None
     if cfg.prec == "mxfp8":
-        if passes != "fwd":
-            raise SystemExit("the MXFP8 backward is not implemented (BF16 backward only)")
         # weights pre-quantised once along K (E4M3 + UE8M0 per 32), outside the timed region
         w1 = torch.empty(cfg.E, 2 * cfg.f, cfg.d, dtype=torch.uint8, device="cuda")
         w1s = torch.empty(cfg.E * 2 * cfg.f * cfg.d // 32, dtype=torch.uint8, device="cuda")
@@ -371,9 +415,8 @@ def main():
         B.moe_quantize_mxfp8(inp["W2"], cfg.E, cfg.f, cfg.d, w2, w2s)
     sched = B.alloc_sched(c)
     ws = B.alloc_workspace(c)
-    saved = B.alloc_saved(c) if passes != "fwd" else None
+    saved = B.alloc_saved(c) if save else None
     out = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device="cuda")
-    bwd = passes != "fwd"
     if bwd:
         dx = torch.empty_like(out)
         dW1 = torch.empty_like(inp["W1"])
@@ -396,20 +439,22 @@ def main():
             B.moe_schedule(c, logits, sched, ws)
         B.moe_forward(c, x, w1, w1s, w2, w2s, sched, out, saved, ws)
         if bwd:
-            B.moe_backward(c, dOut, x, inp["W1"], inp["W2"], sched, saved, dx, dW1, dW2, dtw, dlog, ws)
+            B.moe_backward(c, dOut, x, w1, w2, sched, saved, dx, dW1, dW2, dtw, dlog, ws)
             if args.router:
                 B.moe_router_backward(c, x, w_router, dlog, dx_r, dw_r, ws)
 
-    for _ in range(args.warmup):
+    # ---------------- warm-up, then untimed steps with the clocks sampled
+    wa, wb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(max(args.warmup, 1)):
         step()
+        if i == 0:
+            wa.record()
+    wb.record()
     torch.cuda.synchronize()
     st = B.moe_read_status(ws)
     if st != 0:
         raise RuntimeError(f"device status after warm-up: {B.moe_status_string(st)}")
-
-    # ---------------- timed region (device-resident inputs)
-    B.moe_trace_enable(0)
-    B.moe_trace_enable(64 * args.steps + 64)
+    est_ms = wa.elapsed_time(wb) / max(args.warmup - 1, 1) if args.warmup > 1 else 5.0
     gpu_idx = local
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     if vis:
@@ -419,7 +464,13 @@ def main():
             pass
     clocks = ClockSampler(gpu_idx)
     clocks.start()
-    time.sleep(0.3)
+    time.sleep(0.2)  # the sampler's first line comes after nvidia-smi starts up
+    t_load = time.time()
+    n_settle = int(min(20000, max(0, args.settle_s * 1000.0 / max(est_ms, 1e-3))))
+    for _ in range(n_settle):
+        step()
+
+    # ---------------- timed region (device-resident inputs, no tracing)
     barrier()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record()
@@ -427,16 +478,10 @@ def main():
         step()
     ev1.record()
     barrier()
-    clk = clocks.stop()
+    clk = clocks.stop(since=t_load)
+    if clk is not None:
+        clk["window"] = "%d untimed steps (%.2f s) + the timed region" % (n_settle, n_settle * est_ms / 1e3)
     ms = ev0.elapsed_time(ev1)
-    n_launch = B.moe_trace_count()
-    per = {}
-    for i in range(n_launch):
-        name, kms = B.moe_trace_read(i)
-        a = per.setdefault(name, [0, 0.0])
-        a[0] += 1
-        a[1] += kms
-    B.moe_trace_enable(0)
     st = B.moe_read_status(ws)
     if st != 0:
         raise RuntimeError(f"device status after timed region: {B.moe_status_string(st)}")
@@ -445,10 +490,28 @@ def main():
     value = job_throughput(R, args.steps, world, ms_max)
     ms_step = ms_max / args.steps
 
+    # ---------------- per-kernel times: a separate traced pass
+    n_tr = max(3, min(args.steps, 20))
+    B.moe_trace_enable(0)
+    B.moe_trace_enable(64 * n_tr + 64)
+    for _ in range(n_tr):
+        step()
+    torch.cuda.synchronize()
+    n_launch = B.moe_trace_count()
+    per = {}
+    for i in range(n_launch):
+        name, kms = B.moe_trace_read(i)
+        a = per.setdefault(name, [0, 0.0])
+        a[0] += 1
+        a[1] += kms
+    B.moe_trace_enable(0)
+    launches_per_step = n_launch / n_tr
+
     # ---------------- end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e:
-        host = {k: inp[k].cpu().pin_memory() for k in (("logits", "x", "dOut") if bwd else ("logits", "x"))}
+        names = ("logits", "x", "dOut") if bwd else ("logits", "x")
+        host = {k: inp[k].cpu().pin_memory() for k in names}
         dev_in = {k: torch.empty_like(inp[k]) for k in host}
         h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
         h_dx = torch.empty(out.shape, dtype=out.dtype, pin_memory=True) if bwd else None
@@ -479,60 +542,88 @@ def main():
 
     # ---------------- per-kernel roofline
     # the binding resource of each kernel is the larger of FLOPs / tensor peak
-    # and algorithmic bytes / HBM bandwidth
+    # and algorithmic bytes / HBM bandwidth; kernels run inside a long loop of
+    # steps, so the tensor peak is the sustained one
     peaks = load_peaks()
     touched = int((sched["counts"] > 0).sum().item())
-    units = kernel_units(workload_dict(cfg), touched)
+    units = kernel_units(workload_dict(cfg), touched, saved=save)
 
     def roof_of(name, avg_ms):
         kind, flop, nbytes = units[name]
         fpeak = peaks["bf16_sustained"] * (2.0 if kind == "flop8" else 1.0)
         t_f = flop / (fpeak * 1e12) if kind else 0.0
         t_b = nbytes / (peaks["hbm_gbs"] * 1e9)
+        tr = ncu_traffic(cfg.name, name)
+        dram = None if tr is None else tr / (avg_ms / 1e3) / 1e9 / peaks["hbm_gbs"]
         if t_f >= t_b:
             src = (f"{peaks['source']} bf16 sustained (MEASURED_PEAKS.json)" if kind == "flop" else
                    f"{peaks['source']} bf16 sustained x 2 (nominal fp8:bf16 dense ratio 4.5:2.25)")
             ach = flop / (avg_ms / 1e3) / 1e12
             return {"bound": "tensor", "achieved": ach, "peak": fpeak, "unit": "TFLOP/s",
                     "frac": ach / fpeak, "algorithmic_per_launch": flop, "peak_source": src,
-                    "hbm_frac": nbytes / (avg_ms / 1e3) / 1e9 / peaks["hbm_gbs"]}
+                    "hbm_frac": nbytes / (avg_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                    "dram_frac_ncu": dram}
         ach = nbytes / (avg_ms / 1e3) / 1e9
         return {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": ach / peaks["hbm_gbs"], "algorithmic_per_launch": nbytes,
                 "peak_source": f"{peaks['source']} hbm copy (MEASURED_PEAKS.json)",
-                "tensor_frac": (flop / (avg_ms / 1e3) / 1e12 / fpeak) if kind else None}
+                "tensor_frac": (flop / (avg_ms / 1e3) / 1e12 / fpeak) if kind else None,
+                "dram_frac_ncu": dram}
 
     kernels = {}
+    tot_all = max(sum(v[1] for v in per.values()), 1e-9)
     for name, (cnt, tot) in per.items():
         avg = tot / cnt
-        ent = {"launches": cnt, "ms_per_launch": avg, "share": tot / max(sum(v[1] for v in per.values()), 1e-9)}
+        ent = {"launches": cnt, "ms_per_launch": avg, "share": tot / tot_all}
         if name in units:
             r = roof_of(name, avg)
             ent.update({"bound": r["bound"], "frac": r["frac"], r["unit"]: r["achieved"]})
+            if r.get("dram_frac_ncu") is not None:
+                ent["dram_frac_ncu"] = r["dram_frac_ncu"]
         kernels[name] = ent
     dom = max(per.items(), key=lambda kv: kv[1][1])[0]
     avg = per[dom][1] / per[dom][0]
     roof = roof_of(dom, avg) if dom in units else {"bound": None, "frac": None}
-    roof.update({"traffic": ncu_traffic(cfg.name, dom), "kernel": dom})
+    tr = ncu_traffic(cfg.name, dom)
+    roof.update({"traffic": tr, "kernel": dom,
+                 "timing": "CUDA events around each launch on its stream, traced pass of %d steps "
+                           "after the timed region" % n_tr})
     fwd_names = ("gather", "gather_mxfp8", "gemm1_swiglu", "gemm2", "gemm1_swiglu_mxfp8",
                  "gemm2_mxfp8", "merge", "ring_forward")
     sched_names = ("sched_topk", "sched_hist", "sched_scatter", "router_logits")
-    fwd_ms = sum(per[n][1] for n in per if n in fwd_names) / args.steps
-    sch_ms = sum(per[n][1] for n in per if n in sched_names) / args.steps
-    bwd_ms = sum(per[n][1] for n in per if n not in fwd_names + sched_names) / args.steps
+    fwd_ms = sum(per[n][1] for n in per if n in fwd_names) / n_tr
+    sch_ms = sum(per[n][1] for n in per if n in sched_names) / n_tr
+    bwd_ms = sum(per[n][1] for n in per if n not in fwd_names + sched_names) / n_tr
     flops = (6.0 if not bwd else 18.0) * R * cfg.d * cfg.f
     if args.router:
         flops += (2.0 if not bwd else 6.0) * cfg.T * cfg.d * cfg.E
+    tflops = flops / (ms_step / 1e3) / 1e12
+    fpk = 2.0 if cfg.prec == "mxfp8" else 1.0
+    # the layer's own bound: its FLOPs at the tensor peak against streaming
+    # the touched experts' weights once (bf16: 6 d f bytes each; mxfp8: 3 d f
+    # plus scales) at the HBM bandwidth
+    wbytes = touched * 3.0 * cfg.d * cfg.f * (2.0 if cfg.prec == "bf16" else (1 + 1 / 32))
+    if bwd:
+        wbytes += cfg.E * 6.0 * cfg.d * cfg.f  # every dW written once
+    layer = {"tflops": tflops,
+             "tensor_frac_sustained": tflops / (peaks["bf16_sustained"] * fpk),
+             "tensor_frac_burst": tflops / (peaks["bf16"] * fpk),
+             "weight_stream_ms": wbytes / (peaks["hbm_gbs"] * 1e9) * 1e3,
+             "flop_ms_burst": flops / (peaks["bf16"] * fpk * 1e12) * 1e3,
+             "experts_touched": touched}
 
     # ---------------- CPU baseline: the oracle on a bounded sample
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, desc, dt = time_oracle(cfg, 12.0, steps=1)
+        v, desc, dt = time_oracle(cfg, 12.0, steps=1, passes=passes)
         cpu = {"value": v, "unit": UNIT, "cores": blas_threads(), "kind": "oracle", "sample": desc,
                "seconds": dt}
 
     if rank != 0:
         return
+    fwd_desc = ("persistent ring kernel, %d-row windows, %d slots, %s" % (
+        mb, args.ring_slots, "%d gather CTAs" % args.gather_ctas if args.gather_ctas > 0
+        else "gather warps in every CTA") if mb > 0 else "kernel chain")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -540,21 +631,17 @@ def main():
         "dtype": "e4m3 (mxfp8)" if cfg.prec == "mxfp8" else "bf16",
         "data": "synthetic (seeded torch generators on device; no dataset, random-init weights)",
         "config": {"workload": cfg.name, **workload_dict(cfg), "passes": passes,
-                   "minibatch_rows": args.minibatch_rows,
-                   "forward": ("persistent ring kernel, %d-row windows, %d slots, %s" % (
-                                   args.minibatch_rows, args.ring_slots,
-                                   "%d gather CTAs" % args.gather_ctas if args.gather_ctas > 0
-                                   else "a gather warp in every CTA")
-                               if args.minibatch_rows > 0 else "kernel chain"),
+                   "minibatch_rows": mb, "forward": fwd_desc,
+                   "saved_activations": "H and A" if save else "none",
                    "routing": "router projection (moe_route)" if args.router else "synthetic logits",
                    "l2": "inputs larger than L2 (weights %.2f GB per step)" % (
                        (inp["W1"].numel() + inp["W2"].numel()) * 2 / 1e9),
                    "parallelism": f"replicas x{world}"},
-        "tflops": flops / (ms_step / 1e3) / 1e12,
+        "tflops": tflops, "layer": layer,
         "sched_ms": sch_ms, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
         "roofline": roof, "kernels": kernels,
         "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": int(n_launch), "clocks": clk,
+        "gpu_launches": int(round(launches_per_step * args.steps)), "clocks": clk,
     }
     print(json.dumps(line), flush=True)
     if dist is not None:

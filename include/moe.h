@@ -175,7 +175,10 @@ moe_status moe_router_backward(const moe_config* cfg, const moe_bf16* x, const m
  * Limit: configurations whose schedule scratch exceeds 1.5 MiB return
  * MOE_ERR_INVALID_ARG; T <= 16384, E <= 256 and T*k <= 65536 always fit.
  * The first call on each device looks up the array's device address (with
- * that device current); make that first call before any stream capture.
+ * that device current); make that first call before any stream capture.  The
+ * address is kept for as long as the device's CUDA context stays the same; a
+ * call after a device reset (or in a new context) looks it up again, and that
+ * call too should come before any stream capture.
  * All calls share the one array and leave their contents in it: calls that
  * overlap on the GPU (different streams, or different host threads, without
  * ordering between them) race and give undefined results.  The result does
@@ -226,6 +229,29 @@ moe_status moe_backward(const moe_config* cfg, const moe_bf16* dout, const moe_b
                         const moe_saved* saved, moe_bf16* dx, moe_bf16* dw1, moe_bf16* dw2,
                         float* dtopk_w, float* dlogits, void* ws, size_t ws_bytes,
                         moe_stream_t stream);
+
+/* Where an intermediate buffer of the layer lies inside the workspace, for
+ * tests and debugging (the pages describe no such call).  Pure host
+ * arithmetic: writes the byte offset from the workspace start and the size
+ * in bytes, or returns MOE_ERR_INVALID_ARG for an invalid cfg, an unknown
+ * region, a null pointer, or a region the configuration does not have.
+ *   MOE_WS_XQ_CODES   MXFP8: E4M3 codes of the gathered token rows,
+ *                     [moe_saved_rows(cfg), d] in the padded expert order
+ *                     (written by moe_forward for rows below the padded
+ *                     total; padding rows hold zero codes)
+ *   MOE_WS_XQ_SCALES  their UE8M0 scales in 512-byte tiles (the layout
+ *                     moe_quantize_mxfp8 documents, K = d)
+ *   MOE_WS_AQ_CODES   MXFP8: E4M3 codes of the SwiGLU output A that GEMM1's
+ *                     epilogue quantises for GEMM2, [moe_saved_rows(cfg), f]
+ *   MOE_WS_AQ_SCALES  their scales in 512-byte tiles (K = f) */
+typedef enum {
+  MOE_WS_XQ_CODES = 0,
+  MOE_WS_XQ_SCALES = 1,
+  MOE_WS_AQ_CODES = 2,
+  MOE_WS_AQ_SCALES = 3
+} moe_ws_region;
+moe_status moe_workspace_region(const moe_config* cfg, int32_t region, size_t* offset,
+                                size_t* bytes);
 
 /* Synchronises `stream` and returns the device status word of `ws` (MOE_OK,
  * MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK).  Test / debug use. */

@@ -31,8 +31,13 @@ EXPORTED = [
     "moe_workspace_bytes", "moe_saved_rows", "moe_min_minibatch", "moe_schedule",
     "moe_quantize_mxfp8", "moe_forward", "moe_backward", "moe_read_status", "moe_status_string",
     "moe_trace_enable", "moe_trace_count", "moe_trace_read", "moe_schedule_noalloc",
-    "moe_route", "moe_router_backward",
+    "moe_route", "moe_router_backward", "moe_workspace_region",
 ]
+
+MOE_WS_XQ_CODES = 0
+MOE_WS_XQ_SCALES = 1
+MOE_WS_AQ_CODES = 2
+MOE_WS_AQ_SCALES = 3
 
 
 class MoeError(RuntimeError):
@@ -100,6 +105,8 @@ def lib():
         L.moe_route.restype = ctypes.c_int
         L.moe_router_backward.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.moe_router_backward.restype = ctypes.c_int
+        L.moe_workspace_region.argtypes = [cfgp, i32, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+        L.moe_workspace_region.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -193,6 +200,14 @@ def moe_backward(cfg, dout, x, w1, w2, sched, saved, dx, dw1, dw2, dtopk_w, dlog
                               sched_struct(sched), sv, _ptr(dx), _ptr(dw1), _ptr(dw2),
                               _ptr(dtopk_w), _ptr(dlogits), _ptr(ws),
                               ws.numel() * ws.element_size(), _stream(stream)), "moe_backward")
+
+
+def moe_workspace_region(cfg, region):
+    """(byte offset, bytes) of an intermediate buffer inside the workspace."""
+    off, n = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().moe_workspace_region(ctypes.byref(cfg), int(region), ctypes.byref(off),
+                                      ctypes.byref(n)), "moe_workspace_region")
+    return int(off.value), int(n.value)
 
 
 def moe_read_status(ws, stream=None):

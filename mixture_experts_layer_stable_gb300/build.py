@@ -15,8 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe.so")
-SOURCES = ["api.cu", "sched.cu", "gather_merge.cu", "gemm.cu", "ring.cu", "mxfp8_gemm.cu",
-           "noalloc.cu"]
+SOURCES = ["api.cu", "sched.cu", "gather_merge.cu", "gemm.cu", "ring.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xcompiler", "-Wall", "-DNDEBUG"]
@@ -48,7 +47,7 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
         return LIB
     nvcc = _nvcc()
     os.makedirs(OBJDIR, exist_ok=True)
-    srcs = [s for s in SOURCES if os.path.exists(os.path.join(CSRC, s))]
+    srcs = list(SOURCES)
 
     def compile_one(src):
         obj = os.path.join(OBJDIR, src.replace(".cu", ".o"))

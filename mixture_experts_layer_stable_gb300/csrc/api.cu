@@ -309,6 +309,21 @@ moe_status moe_backward(const moe_config* cfg, const moe_bf16* dout, const moe_b
   return cuda_status(e);
 }
 
+moe_status moe_workspace_region(const moe_config* cfg, int32_t region, size_t* offset,
+                                size_t* bytes) {
+  if (!config_valid(cfg) || offset == nullptr || bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  if (cfg->prec != MOE_MXFP8) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(cfg);
+  const size_t rp = (size_t)L.Rp_max;
+  switch (region) {
+    case MOE_WS_XQ_CODES: *offset = L.Xp; *bytes = rp * cfg->d; return MOE_OK;
+    case MOE_WS_XQ_SCALES: *offset = L.Xp + rp * cfg->d; *bytes = rp * (cfg->d / 32); return MOE_OK;
+    case MOE_WS_AQ_CODES: *offset = L.Aq; *bytes = rp * cfg->f; return MOE_OK;
+    case MOE_WS_AQ_SCALES: *offset = L.Aq + rp * cfg->f; *bytes = rp * (cfg->f / 32); return MOE_OK;
+    default: return MOE_ERR_INVALID_ARG;
+  }
+}
+
 moe_status moe_read_status(const void* ws, moe_stream_t stream) {
   if (!aligned(ws)) return MOE_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)

@@ -51,6 +51,14 @@ constexpr int kTmemCols = 512;
 constexpr int kTmemSf = 256;              // fp8: per-stage scale columns start here
 constexpr int kTmemSfStride = 16;         // fp8: TMEM columns per stage (A: 4, B: 8; 8-aligned)
 constexpr int kTrTile = 32 * 80;          // 32 rows x (64 + 16 pad) bytes: per-warp transpose tile
+// Thin pair units (an expert's lone last tile, mostly experts with a few rows)
+// stream their weight slice from HBM with little to compute, so they are
+// bound by the bytes a CTA has in flight; they also prefetch the slice's
+// k-block this many blocks ahead into L2.  0 turns the prefetch off.
+#ifndef MOE_THIN_PREFETCH
+#define MOE_THIN_PREFETCH 8
+#endif
+constexpr int kThinPrefetch = MOE_THIN_PREFETCH;
 
 enum Epi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2, EPI_LOGITS = 3 };
 
@@ -408,6 +416,24 @@ __global__ void __launch_bounds__(kThreads, 1)
               // SwiGLU: 64 gate and the matching 64 up columns; otherwise 128
               // output columns (MN-major, or K-major rows for dgrad) -- then its
               // half of the rows in 16-row boxes (the MMA's B, K-major)
+              if constexpr (kThinPrefetch > 0) {
+                auto pf = [&](int kk) {
+                  if (EPI == EPI_SWIGLU) {
+                    const int c0 = t.n * p.hn + rank * 64;
+                    tma_prefetch_3d(&tmB, c0, kk * BK, t.e);
+                    tma_prefetch_3d(&tmB, p.f + c0, kk * BK, t.e);
+                  } else if (B_MN) {
+                    const int c0 = t.n * 256 + rank * 128;
+                    tma_prefetch_3d(&tmB, c0, kk * BK, t.e);
+                    tma_prefetch_3d(&tmB, c0 + 64, kk * BK, t.e);
+                  } else {
+                    tma_prefetch_3d(&tmB, kk * BK, t.n * 256 + rank * 128, t.e);
+                  }
+                };
+                if (kb == 0)
+                  for (int j = kStages; j < kThinPrefetch && j < t.kb_count; ++j) pf(j);
+                if (kb + kThinPrefetch < t.kb_count && kThinPrefetch >= kStages) pf(kb + kThinPrefetch);
+              }
               if (EPI == EPI_SWIGLU) {
                 const int c0 = t.n * p.hn + rank * 64;
                 load3(0u, &tmB, c0, kb * BK, t.e);

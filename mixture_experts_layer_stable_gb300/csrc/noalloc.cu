@@ -19,20 +19,53 @@ static __device__ __align__(256) unsigned char g_sched_scratch[kNoAllocScratchBy
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {nullptr};
+unsigned long long g_scratch_ctx[kMaxDevices] = {0};  // context id the address belongs to
 
-// Device address of g_sched_scratch on the current device (looked up once per
-// device, with that device current).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current CUDA context (ids are never
+// reused within a process, unlike context handles), or 0 if unknown.
+unsigned long long current_ctx_id() {
+  static CtxGetCurrentFn get_cur = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static bool looked = false;
+  if (!looked) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<CtxGetCurrentFn>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+    looked = true;
+  }
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_cur == nullptr || get_id == nullptr || get_cur(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of g_sched_scratch on the current device, looked up with
+// that device current and cached per device for as long as the device's
+// context stays the same (a device reset or a new primary context loads the
+// module again, and the array may then sit elsewhere).
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+  const unsigned long long id = current_ctx_id();  // 0 before the first runtime call made one
+  if (g_scratch_ptr[dev] == nullptr || id == 0 || id != g_scratch_ctx[dev]) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_sched_scratch);
+    e = cudaGetSymbolAddress(&p, g_sched_scratch);  // makes the device's context current
     if (e != cudaSuccess) return e;
     g_scratch_ptr[dev] = p;
+    g_scratch_ctx[dev] = current_ctx_id();
   }
   *out = g_scratch_ptr[dev];
   return cudaSuccess;

@@ -91,3 +91,21 @@ def test_status_strings(B):
     for code in range(7):
         assert B.moe_status_string(code) not in ("", "unknown status")
     assert B.moe_status_string(99) == "unknown status"
+
+
+def test_workspace_regions_lie_inside_the_workspace(B):
+    c = B.make_config(300, 256, 128, 6, 3, B.MOE_MXFP8)
+    total = B.moe_workspace_bytes(c)
+    rows = B.moe_saved_rows(c)
+    spans = []
+    for region, want in ((B.MOE_WS_XQ_CODES, rows * 256), (B.MOE_WS_XQ_SCALES, rows * 256 // 32),
+                         (B.MOE_WS_AQ_CODES, rows * 128), (B.MOE_WS_AQ_SCALES, rows * 128 // 32)):
+        off, n = B.moe_workspace_region(c, region)
+        assert n == want and off % 128 == 0 and off + n <= total
+        spans.append((off, off + n))
+    spans.sort()
+    assert all(a[1] <= b[0] for a, b in zip(spans, spans[1:]))  # no overlap
+    with pytest.raises(B.MoeError):
+        B.moe_workspace_region(c, 7)
+    with pytest.raises(B.MoeError):  # a BF16 layer has no quantised buffers
+        B.moe_workspace_region(B.make_config(300, 256, 128, 6, 3), B.MOE_WS_XQ_CODES)

@@ -108,3 +108,17 @@ def test_recorded_traffic_follows_the_kernel_code_not_its_comments():
     other = dict(real, **{"sched.cu": real["sched.cu"] + "\nstatic int moe_digest_probe;\n"})
     assert bench.src_digest("ring_forward", other.__getitem__) == base
     assert bench.src_digest("wgrad1", other.__getitem__) == bench.src_digest("wgrad1", real.__getitem__)
+
+
+def test_clock_sampler_keeps_samples_of_the_load_window():
+    import time as _t
+    t0 = _t.mktime(_t.strptime("2026/12/03 05:39:00", "%Y/%m/%d %H:%M:%S"))
+    lines = ["2026/12/03 05:39:00.100, 0, 300, 2070, 150.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+             "2026/12/03 05:39:01.200, 0, 1980, 2070, 900.5, 0x4, Not Active, Not Active, Not Active, Active",
+             "2026/12/03 05:39:01.300, 0, 2000, 2070, 910.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+             "garbage line"]
+    all_ = bench.ClockSampler.parse(lines)
+    assert all_["samples"] == 3 and all_["sm_mhz"] == 1980
+    win = bench.ClockSampler.parse(lines, since=t0 + 1.0)
+    assert win["samples"] == 2 and win["sm_mhz"] == 1990 and win["sm_max_mhz"] == 2070
+    assert win["reasons"] == ["sw_power_cap"]

@@ -249,3 +249,18 @@ def test_kimi_backward_sampled():
     if len(empty):
         assert torch.count_nonzero(L.dW1[int(empty[0])]) == 0
         assert torch.count_nonzero(L.dW2[int(empty[0])]) == 0
+
+
+@pytest.mark.slow
+def test_kimi_zipf_forward_bitwise_deterministic():
+    cfg = CONFIGS["kimi_zipf"]
+    dev = make_inputs(cfg, device="cuda", with_grad=False)
+    L = Layer(cfg)
+    ref = None
+    for _ in range(5):
+        L.schedule(dev["logits"])
+        out = L.forward(dev["x"], dev["W1"], dev["W2"], save=False).clone()
+        if ref is None:
+            ref = out
+        assert torch.equal(ref.view(torch.int16), out.view(torch.int16))
+    assert L.status() == 0

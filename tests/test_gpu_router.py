@@ -119,3 +119,26 @@ def test_route_kimi_shape():
     np.testing.assert_allclose(s["topk_w"], g, rtol=TOL_W, atol=0)
     counts, offsets, perm, inv = O.schedule(ids, cfg.E)
     assert np.array_equal(s["perm"], perm) and np.array_equal(s["counts"], counts)
+
+
+@pytest.mark.parametrize("T,d,E", [(2048, 2048, 64), (300, 256, 300)])
+def test_route_and_router_backward_bitwise_deterministic_over_10_runs(T, d, E):
+    cfg = with_config("tiny", T=T, d=d, f=64, E=E, k=8)
+    x, Wr = _router_inputs(T, d, E, seed=9, skew=0.03)
+    x, Wr = x.cuda(), Wr.cuda()
+    dl = torch.randn(T, E, generator=torch.Generator().manual_seed(6)).cuda()
+    L = Layer(cfg)
+    logits = torch.empty(T, E, dtype=torch.float32, device="cuda")
+    dx = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    dW = torch.empty(E, d, dtype=torch.bfloat16, device="cuda")
+    ref = None
+    for _ in range(10):
+        B.moe_route(L.c, x, Wr, logits, L.sched, L.ws)
+        B.moe_router_backward(L.c, x, Wr, dl, dx, dW, L.ws)
+        got = [logits.clone(), dx.clone().view(torch.int16), dW.clone().view(torch.int16)]
+        got += [L.sched[n].clone() for n in ("topk_ids", "topk_w", "perm")]
+        if ref is None:
+            ref = got
+        for a, b in zip(ref, got):
+            assert torch.equal(a, b)
+    assert L.status() == 0

@@ -36,12 +36,22 @@ def test_noalloc_schedule_equals_workspace_schedule_twice(cuda_lib):
         c = cfg_struct(cfg)
         logits = make_inputs(cfg, parts=("logits",))["logits"].cuda()
         want = _reference(c, logits)
-        for _ in range(2):  # two calls in a row on the shared scratch
-            got = B.alloc_sched(c)
+        outs = [B.alloc_sched(c) for _ in range(2)]
+        for got in outs:
             for t in got.values():
                 t.fill_(-7)
-            B.moe_schedule_noalloc(c, logits, got)
-            torch.cuda.synchronize()
+        B.moe_schedule_noalloc(c, logits, outs[0])  # first call on this device: address lookup
+        torch.cuda.synchronize()
+        # the second call allocates nothing: neither device memory nor through torch
+        free0 = torch.cuda.mem_get_info()[0]
+        stats0 = torch.cuda.memory_stats()
+        B.moe_schedule_noalloc(c, logits, outs[1])
+        torch.cuda.synchronize()
+        assert torch.cuda.mem_get_info()[0] == free0
+        stats1 = torch.cuda.memory_stats()
+        for key in ("allocation.all.allocated", "segment.all.allocated", "reserved_bytes.all.current"):
+            assert stats1.get(key) == stats0.get(key), key
+        for got in outs:  # two calls in a row on the shared scratch
             for n in NAMES:
                 assert torch.equal(got[n], want[n]), (cfg.name, n)
 
