@@ -64,6 +64,18 @@ def kernel_units(c, touched, saved=True):
         "gather_x_dy": (None, 0.0, 2.0 * (T * d * b + R * d * b)),
         "merge": (None, 0.0, T * (k + 1) * d * b + R * 4.0 * 2),
         "recompute_gemm1": ("flop", 2.0 * R * d * 2 * f, w1 + R * d * b + R * 3 * f * b),
+        "ring_forward_mxfp8": ("flop8", 2.0 * R * d * 2 * f + 2.0 * R * f * d,
+                               T * d * b + (touched * 3 * d * f + R * f + R * d) * (1 + 1 / 32)
+                               + 2.0 * R * d * b + T * d * b),
+        "dgrad2_dswiglu_mxfp8": ("flop8", 2.0 * R * d * f,
+                                 (touched * f * d + R * d) * (1 + 1 / 32) + R * 3 * f * b
+                                 + (2 * R * 2 * f + R * f) * (1 + 1 / 32)),
+        "dgrad1_mxfp8": ("flop8", 2.0 * R * 2 * f * d, (touched * d * 2 * f + R * 2 * f) * (1 + 1 / 32) + R * d * b),
+        "wgrad1_mxfp8": ("flop8", 2.0 * R * d * 2 * f, E * d * 2 * f * b + (R * d + R * 2 * f) * (1 + 1 / 32)),
+        "wgrad2_mxfp8": ("flop8", 2.0 * R * f * d, E * f * d * b + (R * f + R * d) * (1 + 1 / 32)),
+        "quant_dy_rows": (None, 0.0, R * d * b + R * d * (1 + 1 / 32)),
+        "quant_x_cols": (None, 0.0, R * d * b + R * d * (1 + 1 / 32)),
+        "quant_dy_cols": (None, 0.0, R * d * b + R * d * (1 + 1 / 32)),
         "reverse_dispatch": (None, 0.0, T * (k + 1) * d * b + R * 4.0),
         # persistent ring forward (gather + GEMM1 + SwiGLU + GEMM2 + merge in one launch):
         # token rows in, weights of the touched experts, H and A saved, Y written and read
@@ -311,6 +323,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="kimi_zipf")
     ap.add_argument("--passes", default=None, help="fwd or fwd+bwd (default: the workload's)")
+    ap.add_argument("--prec", choices=["bf16", "mxfp8"], default=None,
+                    help="precision (default: the workload's)")
     ap.add_argument("--save", action="store_true",
                     help="forward-only passes: also save H and A for a later backward")
     ap.add_argument("--minibatch-rows", type=int, default=0,
@@ -375,6 +389,9 @@ def main():
     world, rank, local = dist_setup()
     from mixture_experts_layer_stable_gb300.configs import CONFIGS
     cfg = CONFIGS[args.workload]
+    if args.prec and args.prec != cfg.prec:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, prec=args.prec)
     passes = args.passes or cfg.passes
     if args.impl == "reference":
         run_reference(args, cfg, rank)
@@ -413,6 +430,14 @@ def main():
         w2s = torch.empty(cfg.E * cfg.d * cfg.f // 32, dtype=torch.uint8, device="cuda")
         B.moe_quantize_mxfp8(inp["W1"], cfg.E, cfg.d, 2 * cfg.f, w1, w1s)
         B.moe_quantize_mxfp8(inp["W2"], cfg.E, cfg.f, cfg.d, w2, w2s)
+        if bwd:
+            # the backward's copies, quantised along the other dimension
+            w1r = torch.empty(cfg.E, cfg.d, 2 * cfg.f, dtype=torch.uint8, device="cuda")
+            w1rs = torch.empty(cfg.E * cfg.d * 2 * cfg.f // 32, dtype=torch.uint8, device="cuda")
+            w2r = torch.empty(cfg.E, cfg.f, cfg.d, dtype=torch.uint8, device="cuda")
+            w2rs = torch.empty(cfg.E * cfg.f * cfg.d // 32, dtype=torch.uint8, device="cuda")
+            B.moe_quantize_mxfp8_rows(inp["W1"], cfg.E * cfg.d, 2 * cfg.f, w1r, w1rs)
+            B.moe_quantize_mxfp8_rows(inp["W2"], cfg.E * cfg.f, cfg.d, w2r, w2rs)
     sched = B.alloc_sched(c)
     ws = B.alloc_workspace(c)
     saved = B.alloc_saved(c) if save else None
@@ -438,7 +463,9 @@ def main():
         else:
             B.moe_schedule(c, logits, sched, ws)
         B.moe_forward(c, x, w1, w1s, w2, w2s, sched, out, saved, ws)
-        if bwd:
+        if bwd and cfg.prec == "mxfp8":
+            B.moe_backward_mxfp8(c, dOut, x, w1r, w1rs, w2r, w2rs, sched, saved, dx, dW1, dW2, dtw, dlog, ws)
+        elif bwd:
             B.moe_backward(c, dOut, x, w1, w2, sched, saved, dx, dW1, dW2, dtw, dlog, ws)
             if args.router:
                 B.moe_router_backward(c, x, w_router, dlog, dx_r, dw_r, ws)
@@ -589,7 +616,7 @@ def main():
                  "timing": "CUDA events around each launch on its stream, traced pass of %d steps "
                            "after the timed region" % n_tr})
     fwd_names = ("gather", "gather_mxfp8", "gemm1_swiglu", "gemm2", "gemm1_swiglu_mxfp8",
-                 "gemm2_mxfp8", "merge", "ring_forward")
+                 "gemm2_mxfp8", "merge", "ring_forward", "ring_forward_mxfp8")
     sched_names = ("sched_topk", "sched_hist", "sched_scatter", "router_logits")
     fwd_ms = sum(per[n][1] for n in per if n in fwd_names) / n_tr
     sch_ms = sum(per[n][1] for n in per if n in sched_names) / n_tr
@@ -608,6 +635,8 @@ def main():
     layer = {"tflops": tflops,
              "tensor_frac_sustained": tflops / (peaks["bf16_sustained"] * fpk),
              "tensor_frac_burst": tflops / (peaks["bf16"] * fpk),
+            "peak_note": ("MXFP8 against 2x the bf16 peaks (nominal fp8:bf16 dense ratio 4.5:2.25)"
+                          if cfg.prec == "mxfp8" else "bf16 peaks of MEASURED_PEAKS.json"),
              "weight_stream_ms": wbytes / (peaks["hbm_gbs"] * 1e9) * 1e3,
              "flop_ms_burst": flops / (peaks["bf16"] * fpk * 1e12) * 1e3,
              "experts_touched": touched}
@@ -630,7 +659,7 @@ def main():
         "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 (mxfp8)" if cfg.prec == "mxfp8" else "bf16",
         "data": "synthetic (seeded torch generators on device; no dataset, random-init weights)",
-        "config": {"workload": cfg.name, **workload_dict(cfg), "passes": passes,
+        "config": {"workload": cfg.name, **workload_dict(cfg), "passes": passes, "prec": cfg.prec,
                    "minibatch_rows": mb, "forward": fwd_desc,
                    "saved_activations": "H and A" if save else "none",
                    "routing": "router projection (moe_route)" if args.router else "synthetic logits",

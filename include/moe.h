@@ -70,7 +70,8 @@ typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_precision;
  *     the weighted merge at the end ([LP] 02: SM partition, local counters,
  *     minibatch, ring token buffer).  Results are bitwise identical to the chain path
  *     for every window size.  MXFP8 with minibatch_rows > 0 returns
- *     MOE_ERR_UNSUPPORTED; the backward always runs as a chain of kernels.
+ *     MOE_ERR_UNSUPPORTED.  The backward runs as a chain of kernels; it
+ *     reuses the rows the ring still holds (see moe_backward).
  *   ring_slots: ring depth, 2..64, when minibatch_rows > 0.
  *   gather_ctas: how the work is split when minibatch_rows > 0.  0 (the
  *     default): every CTA runs the GEMM warps and one gather warp, so all
@@ -201,6 +202,17 @@ moe_status moe_schedule_noalloc(const moe_config* cfg, const float* logits, moe_
 moe_status moe_quantize_mxfp8(const moe_bf16* w, int64_t batch, int32_t K, int32_t N,
                               uint8_t* q, uint8_t* scales, moe_stream_t stream);
 
+/* MXFP8 quantisation along the contiguous dimension (the weights of the MXFP8
+ * backward, whose GEMMs contract over the weights' other dimension): w [rows,
+ * K] bf16 -> q [rows, K] E4M3 and one UE8M0 scale per 32 consecutive K
+ * elements, with the scale rule, rounding and 512-byte tile layout of
+ * moe_quantize_mxfp8 (row r, block kb at byte 16*(r%32) + 4*((r%128)/32) +
+ * kb%4 of tile (r/128, kb/4)).  rows and K multiples of 128.  W1 [E, d, 2f]
+ * for the MXFP8 backward: rows = E*d, K = 2f; W2 [E, f, d]: rows = E*f,
+ * K = d. */
+moe_status moe_quantize_mxfp8_rows(const moe_bf16* w, int64_t rows, int32_t K, uint8_t* q,
+                                   uint8_t* scales, moe_stream_t stream);
+
 /* Forward: Dispatch -> Expert FFN -> Combine -> weighted merge ([LP] 03;
  * dispatch by pull, combine by push, [LP] 02).
  *   x [T, d] bf16.  BF16 mode: w1 = W1 bf16 [E, d, 2f], w2 = W2 bf16 [E, f, d],
@@ -217,13 +229,23 @@ moe_status moe_forward(const moe_config* cfg, const moe_bf16* x, const void* w1,
 /* Backward (BF16): reverse combine, expert FFN dgrad / wgrad, SwiGLU backward
  * fused with the routing-weight gradient, reverse dispatch ([LP] 02: pull
  * reverse-combine, push reverse-dispatch; [MT] three design decisions: the
- * routing-weight gradient is fused into the SwiGLU backward).
+ * routing-weight gradient is fused into the SwiGLU backward, and the ring
+ * buffer is traversed in reverse to replay as few forward activations as
+ * possible).
  *   dout [T, d] bf16 upstream gradient; x, w1, w2 as in the forward; saved
- *   as written by moe_forward with the same sched and ws.
+ *   as written by moe_forward with the same sched and ws, or NULL: then H and
+ *   A are recomputed from the re-gathered rows by the forward's GEMM1 (the
+ *   same bits as the saved ones) in workspace buffers.
+ *   The token rows are re-gathered into expert order walking the rows from
+ *   the last to the first; after a ring forward (minibatch_rows > 0, same
+ *   ws) the rows of its last ring_slots windows, still held in the ring, are
+ *   taken from there instead of from x.
  *   dx [T, d] bf16; dw1 [E, d, 2f] bf16; dw2 [E, f, d] bf16 (experts with no
  *   rows get exact zeros); dtopk_w [T*k] fp32 = d loss / d topk_w;
  *   dlogits [T, E] fp32 or NULL: gradient through the renormalised softmax
- *   (zero for unselected experts). */
+ *   (zero for unselected experts).
+ *   An MXFP8 configuration returns MOE_ERR_UNSUPPORTED: its backward is
+ *   moe_backward_mxfp8. */
 moe_status moe_backward(const moe_config* cfg, const moe_bf16* dout, const moe_bf16* x,
                         const moe_bf16* w1, const moe_bf16* w2, moe_sched sched,
                         const moe_saved* saved, moe_bf16* dx, moe_bf16* dw1, moe_bf16* dw2,
@@ -243,15 +265,60 @@ moe_status moe_backward(const moe_config* cfg, const moe_bf16* dout, const moe_b
  *                     moe_quantize_mxfp8 documents, K = d)
  *   MOE_WS_AQ_CODES   MXFP8: E4M3 codes of the SwiGLU output A that GEMM1's
  *                     epilogue quantises for GEMM2, [moe_saved_rows(cfg), f]
- *   MOE_WS_AQ_SCALES  their scales in 512-byte tiles (K = f) */
+ *   MOE_WS_AQ_SCALES  their scales in 512-byte tiles (K = f)
+ * The operands moe_backward_mxfp8 quantises, each a codes region followed by
+ * its scales region (tiles as above; Rp = moe_saved_rows(cfg)):
+ *   MOE_WS_DYQ_*      dOut rows in expert order, blocks along d: [Rp, d]
+ *   MOE_WS_XQT_*      x rows in expert order, transposed, blocks of 32 rows
+ *                     from each expert's segment start: [d, Rp]
+ *   MOE_WS_DYQT_*     dOut rows the same way: [d, Rp]
+ *   MOE_WS_DHQ_*      dH, blocks along 2f: [Rp, 2f]
+ *   MOE_WS_DHQT_*     dH transposed, blocks of 32 rows: [2f, Rp]
+ *   MOE_WS_GAQT_*     g*A transposed, blocks of 32 rows: [f, Rp] */
 typedef enum {
   MOE_WS_XQ_CODES = 0,
   MOE_WS_XQ_SCALES = 1,
   MOE_WS_AQ_CODES = 2,
-  MOE_WS_AQ_SCALES = 3
+  MOE_WS_AQ_SCALES = 3,
+  MOE_WS_DYQ_CODES = 4,
+  MOE_WS_DYQ_SCALES = 5,
+  MOE_WS_XQT_CODES = 6,
+  MOE_WS_XQT_SCALES = 7,
+  MOE_WS_DYQT_CODES = 8,
+  MOE_WS_DYQT_SCALES = 9,
+  MOE_WS_DHQ_CODES = 10,
+  MOE_WS_DHQ_SCALES = 11,
+  MOE_WS_DHQT_CODES = 12,
+  MOE_WS_DHQT_SCALES = 13,
+  MOE_WS_GAQT_CODES = 14,
+  MOE_WS_GAQT_SCALES = 15
 } moe_ws_region;
 moe_status moe_workspace_region(const moe_config* cfg, int32_t region, size_t* offset,
                                 size_t* bytes);
+
+/* Backward in MXFP8 ([MT] three design decisions: BF16 and MXFP8 precision
+ * modes; [LP] 03: the MXFP8 backward is among the layer's measured passes).
+ * The pages do not say how the backward quantises; reading: every backward
+ * GEMM quantises both operands along its own contraction dimension, with the
+ * forward's block format --
+ *   dgrad2 (K = d):   dOut rows and W2 along d
+ *   dgrad1 (K = 2f):  dH and W1 along 2f
+ *   wgrad2 (K = the expert's rows): g*A and dOut along the rows
+ *   wgrad1 (K = the expert's rows): x rows and dH along the rows
+ * the row blocks of 32 counted from the start of each expert's rows (the
+ * padded expert order; the last block holds zero rows).  The SwiGLU backward
+ * and the routing-weight gradient run in fp32 in dgrad2's epilogue, which
+ * also quantises dH (both ways) and g*A.
+ *   cfg->prec must be MOE_MXFP8.  dout, x: as moe_backward.  w1q / w1s: W1
+ *   quantised by moe_quantize_mxfp8_rows(W1, E*d, 2f); w2q / w2s: W2 by
+ *   moe_quantize_mxfp8_rows(W2, E*f, d).  saved: required, written by the
+ *   MXFP8 moe_forward (H and A in bf16) with the same sched and ws.
+ *   Outputs as moe_backward (dx, dw1, dw2 bf16; dtopk_w, dlogits fp32). */
+moe_status moe_backward_mxfp8(const moe_config* cfg, const moe_bf16* dout, const moe_bf16* x,
+                              const uint8_t* w1q, const uint8_t* w1s, const uint8_t* w2q,
+                              const uint8_t* w2s, moe_sched sched, const moe_saved* saved, moe_bf16* dx,
+                              moe_bf16* dw1, moe_bf16* dw2, float* dtopk_w, float* dlogits, void* ws,
+                              size_t ws_bytes, moe_stream_t stream);
 
 /* Synchronises `stream` and returns the device status word of `ws` (MOE_OK,
  * MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK).  Test / debug use. */

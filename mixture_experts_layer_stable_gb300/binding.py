@@ -31,13 +31,20 @@ EXPORTED = [
     "moe_workspace_bytes", "moe_saved_rows", "moe_min_minibatch", "moe_schedule",
     "moe_quantize_mxfp8", "moe_forward", "moe_backward", "moe_read_status", "moe_status_string",
     "moe_trace_enable", "moe_trace_count", "moe_trace_read", "moe_schedule_noalloc",
-    "moe_route", "moe_router_backward", "moe_workspace_region",
+    "moe_route", "moe_router_backward", "moe_workspace_region", "moe_quantize_mxfp8_rows",
+    "moe_backward_mxfp8",
 ]
 
 MOE_WS_XQ_CODES = 0
 MOE_WS_XQ_SCALES = 1
 MOE_WS_AQ_CODES = 2
 MOE_WS_AQ_SCALES = 3
+MOE_WS_DYQ_CODES, MOE_WS_DYQ_SCALES = 4, 5
+MOE_WS_XQT_CODES, MOE_WS_XQT_SCALES = 6, 7
+MOE_WS_DYQT_CODES, MOE_WS_DYQT_SCALES = 8, 9
+MOE_WS_DHQ_CODES, MOE_WS_DHQ_SCALES = 10, 11
+MOE_WS_DHQT_CODES, MOE_WS_DHQT_SCALES = 12, 13
+MOE_WS_GAQT_CODES, MOE_WS_GAQT_SCALES = 14, 15
 
 
 class MoeError(RuntimeError):
@@ -107,6 +114,11 @@ def lib():
         L.moe_router_backward.restype = ctypes.c_int
         L.moe_workspace_region.argtypes = [cfgp, i32, ctypes.POINTER(sz), ctypes.POINTER(sz)]
         L.moe_workspace_region.restype = ctypes.c_int
+        L.moe_quantize_mxfp8_rows.argtypes = [vp, i64, i32, vp, vp, vp]
+        L.moe_quantize_mxfp8_rows.restype = ctypes.c_int
+        L.moe_backward_mxfp8.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, moe_sched, savp, vp, vp, vp, vp,
+                                         vp, vp, sz, vp]
+        L.moe_backward_mxfp8.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -195,7 +207,8 @@ def moe_forward(cfg, x, w1, w1_scales, w2, w2_scales, sched, out, saved, ws, str
 
 
 def moe_backward(cfg, dout, x, w1, w2, sched, saved, dx, dw1, dw2, dtopk_w, dlogits, ws, stream=None):
-    sv = ctypes.byref(moe_saved(_ptr(saved["H"]), _ptr(saved["A"])))
+    """saved: the dict moe_forward filled, or None (H and A are recomputed)."""
+    sv = None if saved is None else ctypes.byref(moe_saved(_ptr(saved["H"]), _ptr(saved["A"])))
     _check(lib().moe_backward(ctypes.byref(cfg), _ptr(dout), _ptr(x), _ptr(w1), _ptr(w2),
                               sched_struct(sched), sv, _ptr(dx), _ptr(dw1), _ptr(dw2),
                               _ptr(dtopk_w), _ptr(dlogits), _ptr(ws),
@@ -208,6 +221,20 @@ def moe_workspace_region(cfg, region):
     _check(lib().moe_workspace_region(ctypes.byref(cfg), int(region), ctypes.byref(off),
                                       ctypes.byref(n)), "moe_workspace_region")
     return int(off.value), int(n.value)
+
+
+def moe_quantize_mxfp8_rows(w, rows, K, q, scales, stream=None):
+    _check(lib().moe_quantize_mxfp8_rows(_ptr(w), rows, K, _ptr(q), _ptr(scales), _stream(stream)),
+           "moe_quantize_mxfp8_rows")
+
+
+def moe_backward_mxfp8(cfg, dout, x, w1q, w1s, w2q, w2s, sched, saved, dx, dw1, dw2, dtopk_w, dlogits,
+                       ws, stream=None):
+    sv = None if saved is None else ctypes.byref(moe_saved(_ptr(saved["H"]), _ptr(saved["A"])))
+    _check(lib().moe_backward_mxfp8(ctypes.byref(cfg), _ptr(dout), _ptr(x), _ptr(w1q), _ptr(w1s),
+                                    _ptr(w2q), _ptr(w2s), sched_struct(sched), sv, _ptr(dx), _ptr(dw1),
+                                    _ptr(dw2), _ptr(dtopk_w), _ptr(dlogits), _ptr(ws),
+                                    ws.numel() * ws.element_size(), _stream(stream)), "moe_backward_mxfp8")
 
 
 def moe_read_status(ws, stream=None):

@@ -58,6 +58,11 @@ WsLayout ws_layout(const moe_config* c) {
   L.dgp = take(rp * L.nt_dg * sizeof(float));
   L.Aq = take(c->prec == MOE_MXFP8 ? rp * c->f + rp * (c->f / 32) : 0);
   L.dl16 = take((size_t)c->T * ((c->E + 63) / 64 * 64) * 2);
+  L.Hrc = take(c->prec == MOE_BF16 ? rp * 2 * c->f * 2 : 0);
+  // MXFP8 backward: dY along d [rp, d], X and dY transposed [d, rp] each, dH
+  // along 2f [rp, 2f] and transposed [2f, rp], g*A transposed [f, rp]; codes
+  // followed by their scale tiles (1/32 of the codes)
+  L.bq = take(c->prec == MOE_MXFP8 ? (rp * c->d * 3 + rp * 2 * c->f * 2 + rp * c->f) / 32 * 33 : 0);
   if (c->minibatch_rows > 0) {
     L.ring = take((size_t)c->ring_slots * ring_window_rows(*c) * c->d * 2);
     L.ctr_bytes = (size_t)(2 * c->ring_slots + 3 + L.MT_max) * sizeof(int);
@@ -205,6 +210,15 @@ moe_status moe_quantize_mxfp8(const moe_bf16* w, int64_t batch, int32_t K, int32
                                            q, scales, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_quantize_mxfp8_rows(const moe_bf16* w, int64_t rows, int32_t K, uint8_t* q,
+                                   uint8_t* scales, moe_stream_t stream) {
+  if (!aligned(w) || !aligned(q) || !aligned(scales) || rows < 128 || rows % 128 || K < 128 || K % 128)
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_quant_rows(reinterpret_cast<const __nv_bfloat16*>(w), rows, K, nullptr, q,
+                                       scales, reinterpret_cast<cudaStream_t>(stream),
+                                       "quantize_weight_rows"));
+}
+
 moe_status moe_forward(const moe_config* cfg, const moe_bf16* x, const void* w1,
                        const uint8_t* w1_scales, const void* w2, const uint8_t* w2_scales,
                        moe_sched sched, moe_bf16* out, const moe_saved* saved, void* ws,
@@ -219,9 +233,21 @@ moe_status moe_forward(const moe_config* cfg, const moe_bf16* x, const void* w1,
   if (ws_bytes < W.L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   const moe_config& c = *cfg;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (c.minibatch_rows > 0 && c.prec == MOE_MXFP8) {
+    // persistent kernel with MXFP8 operands
+    if (!aligned(w1_scales) || !aligned(w2_scales)) return MOE_ERR_INVALID_ARG;
+    if (c.gather_ctas >= num_sms()) return MOE_ERR_INVALID_ARG;
+    const cudaError_t e = ring_forward_mx(
+        c, W, sched.counts, reinterpret_cast<const __nv_bfloat16*>(x), static_cast<const uint8_t*>(w1),
+        w1_scales, static_cast<const uint8_t*>(w2), w2_scales, sched.topk_w,
+        saved ? reinterpret_cast<__nv_bfloat16*>(saved->A) : nullptr,
+        saved ? reinterpret_cast<__nv_bfloat16*>(saved->H) : nullptr, reinterpret_cast<__nv_bfloat16*>(out), st);
+    if (e == cudaErrorCooperativeLaunchTooLarge) return MOE_ERR_UNSUPPORTED;
+    return cuda_status(e);
+  }
   if (c.minibatch_rows > 0) {
     // persistent kernel: SM split, ring of windows, device counters
-    if (c.prec != MOE_BF16 || w1_scales != nullptr || w2_scales != nullptr) return MOE_ERR_UNSUPPORTED;
+    if (w1_scales != nullptr || w2_scales != nullptr) return MOE_ERR_INVALID_ARG;
     if (c.gather_ctas >= num_sms()) return MOE_ERR_INVALID_ARG;
     auto* A = saved ? reinterpret_cast<__nv_bfloat16*>(saved->A)
                     : static_cast<__nv_bfloat16*>(W.at(W.L.Abuf));
@@ -279,7 +305,7 @@ moe_status moe_backward(const moe_config* cfg, const moe_bf16* dout, const moe_b
       !aligned(ws))
     return MOE_ERR_INVALID_ARG;
   if (dlogits != nullptr && !aligned(dlogits)) return MOE_ERR_INVALID_ARG;
-  if (saved == nullptr || !aligned(saved->H) || !aligned(saved->A)) return MOE_ERR_INVALID_ARG;
+  if (saved != nullptr && (!aligned(saved->H) || !aligned(saved->A))) return MOE_ERR_INVALID_ARG;
   if (cfg->prec != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   Ws W;
   W.L = ws_layout(cfg);
@@ -294,10 +320,22 @@ moe_status moe_backward(const moe_config* cfg, const moe_bf16* dout, const moe_b
   auto* gA = static_cast<__nv_bfloat16*>(W.at(W.L.gA));
   auto* dXp = static_cast<__nv_bfloat16*>(W.at(W.L.Yp));
   auto* dgp = static_cast<float*>(W.at(W.L.dgp));
-  const auto* Hs = reinterpret_cast<const __nv_bfloat16*>(saved->H);
-  const auto* As = reinterpret_cast<const __nv_bfloat16*>(saved->A);
+  // without saved activations H and A are recomputed from the re-gathered
+  // rows by the forward's own GEMM1 (same tiles, same K order: the same bits)
+  auto* Hrc = static_cast<__nv_bfloat16*>(W.at(W.L.Hrc));
+  auto* Arc = static_cast<__nv_bfloat16*>(W.at(W.L.Abuf));
+  const auto* Hs = saved ? reinterpret_cast<const __nv_bfloat16*>(saved->H) : Hrc;
+  const auto* As = saved ? reinterpret_cast<const __nv_bfloat16*>(saved->A) : Arc;
 
-  cudaError_t e = launch_gather(c, W, bf(x), Xp, bf(dout), dYp, st);
+  // after a ring forward its last windows are still in the ring: the
+  // re-gather walks the rows in reverse and takes those from the ring
+  RingSrc rs;
+  rs.ring = static_cast<const __nv_bfloat16*>(W.at(W.L.ring));
+  rs.mb = ring_window_rows(c);
+  rs.slots = c.ring_slots;
+  cudaError_t e = launch_gather(c, W, bf(x), Xp, bf(dout), dYp, st, c.minibatch_rows > 0 ? &rs : nullptr);
+  if (e == cudaSuccess && saved == nullptr)
+    e = gemm_fwd1(c, W, sched.counts, Xp, bf(w1), Arc, Hrc, st, "recompute_gemm1");
   if (e == cudaSuccess) e = gemm_dgrad2(c, W, dYp, bf(w2), Hs, As, dH, gA, dgp, st);
   if (e == cudaSuccess) e = launch_dg_reduce(c, W, sched, dtopk_w, dlogits, st);
   if (e == cudaSuccess)
@@ -320,8 +358,87 @@ moe_status moe_workspace_region(const moe_config* cfg, int32_t region, size_t* o
     case MOE_WS_XQ_SCALES: *offset = L.Xp + rp * cfg->d; *bytes = rp * (cfg->d / 32); return MOE_OK;
     case MOE_WS_AQ_CODES: *offset = L.Aq; *bytes = rp * cfg->f; return MOE_OK;
     case MOE_WS_AQ_SCALES: *offset = L.Aq + rp * cfg->f; *bytes = rp * (cfg->f / 32); return MOE_OK;
-    default: return MOE_ERR_INVALID_ARG;
+    default: break;
   }
+  // the MXFP8 backward's operands, in the order moe_backward_mxfp8 carves them
+  const size_t d = cfg->d, f = cfg->f;
+  const size_t sizes[6] = {rp * d, d * rp, d * rp, rp * 2 * f, 2 * f * rp, f * rp};
+  const int first = MOE_WS_DYQ_CODES;
+  if (region < first || region >= first + 12) return MOE_ERR_INVALID_ARG;
+  size_t off = L.bq;
+  const int i = (region - first) / 2;
+  for (int j = 0; j < i; ++j) off += sizes[j] + sizes[j] / 32;
+  if ((region - first) % 2 == 0) {
+    *offset = off;
+    *bytes = sizes[i];
+  } else {
+    *offset = off + sizes[i];
+    *bytes = sizes[i] / 32;
+  }
+  return MOE_OK;
+}
+
+moe_status moe_backward_mxfp8(const moe_config* cfg, const moe_bf16* dout, const moe_bf16* x,
+                              const uint8_t* w1q, const uint8_t* w1s, const uint8_t* w2q,
+                              const uint8_t* w2s, moe_sched sched, const moe_saved* saved, moe_bf16* dx,
+                              moe_bf16* dw1, moe_bf16* dw2, float* dtopk_w, float* dlogits, void* ws,
+                              size_t ws_bytes, moe_stream_t stream) {
+  if (!config_valid(cfg) || cfg->prec != MOE_MXFP8) return MOE_ERR_INVALID_ARG;
+  if (!aligned(dout) || !aligned(x) || !aligned(w1q) || !aligned(w1s) || !aligned(w2q) || !aligned(w2s) ||
+      !sched_ok(sched) || !aligned(dx) || !aligned(dw1) || !aligned(dw2) || !aligned(dtopk_w) ||
+      !aligned(ws))
+    return MOE_ERR_INVALID_ARG;
+  if (dlogits != nullptr && !aligned(dlogits)) return MOE_ERR_INVALID_ARG;
+  if (saved == nullptr || !aligned(saved->H) || !aligned(saved->A)) return MOE_ERR_INVALID_ARG;
+  Ws W;
+  W.L = ws_layout(cfg);
+  W.base = static_cast<uint8_t*>(ws);
+  if (ws_bytes < W.L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const moe_config& c = *cfg;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  auto bf = [](const moe_bf16* p) { return reinterpret_cast<const __nv_bfloat16*>(p); };
+  const size_t rp = (size_t)W.L.Rp_max, d = c.d, f = c.f;
+  auto* Xp = static_cast<__nv_bfloat16*>(W.at(W.L.Xp));
+  auto* dYp = static_cast<__nv_bfloat16*>(W.at(W.L.dYp));
+  auto* dXp = static_cast<__nv_bfloat16*>(W.at(W.L.Yp));
+  auto* dgp = static_cast<float*>(W.at(W.L.dgp));
+  // quantised operands, codes then scale tiles
+  uint8_t* b = static_cast<uint8_t*>(W.at(W.L.bq));
+  auto carve = [&](size_t n) {
+    uint8_t* q = b;
+    b += n + n / 32;
+    return q;
+  };
+  uint8_t* dYq = carve(rp * d);
+  uint8_t* XqT = carve(d * rp);
+  uint8_t* dYqT = carve(d * rp);
+  uint8_t* dHq = carve(rp * 2 * f);
+  uint8_t* dHqT = carve(2 * f * rp);
+  uint8_t* gAqT = carve(f * rp);
+  auto sc = [](uint8_t* q, size_t n) { return q + n; };
+  const int* rows = W.hdr() + kHdrRpTotal;
+  const auto* Hs = reinterpret_cast<const __nv_bfloat16*>(saved->H);
+  const auto* As = reinterpret_cast<const __nv_bfloat16*>(saved->A);
+
+  cudaError_t e = launch_gather(c, W, bf(x), Xp, bf(dout), dYp, st);
+  if (e == cudaSuccess) e = launch_quant_rows(dYp, (int64_t)rp, c.d, rows, dYq, sc(dYq, rp * d), st, "quant_dy_rows");
+  if (e == cudaSuccess)
+    e = launch_quant_cols(Xp, (int64_t)rp, c.d, rows, XqT, sc(XqT, d * rp), (int)rp, st, "quant_x_cols");
+  if (e == cudaSuccess)
+    e = launch_quant_cols(dYp, (int64_t)rp, c.d, rows, dYqT, sc(dYqT, d * rp), (int)rp, st, "quant_dy_cols");
+  if (e == cudaSuccess)
+    e = gemm_dgrad2_mx(c, W, dYq, sc(dYq, rp * d), w2q, w2s, Hs, As, dHq, sc(dHq, rp * 2 * f), dHqT,
+                       sc(dHqT, 2 * f * rp), gAqT, sc(gAqT, f * rp), dgp, st);
+  if (e == cudaSuccess) e = launch_dg_reduce(c, W, sched, dtopk_w, dlogits, st);
+  if (e == cudaSuccess)
+    e = gemm_wgrad_mx(c, W, sched, gAqT, sc(gAqT, f * rp), c.f, dYqT, sc(dYqT, d * rp), c.d,
+                      reinterpret_cast<__nv_bfloat16*>(dw2), "wgrad2_mxfp8", st);
+  if (e == cudaSuccess)
+    e = gemm_wgrad_mx(c, W, sched, XqT, sc(XqT, d * rp), c.d, dHqT, sc(dHqT, 2 * f * rp), 2 * c.f,
+                      reinterpret_cast<__nv_bfloat16*>(dw1), "wgrad1_mxfp8", st);
+  if (e == cudaSuccess) e = gemm_dgrad1_mx(c, W, dHq, sc(dHq, rp * 2 * f), w1q, w1s, dXp, st);
+  if (e == cudaSuccess) e = launch_merge(c, W, dXp, nullptr, reinterpret_cast<__nv_bfloat16*>(dx), st);
+  return cuda_status(e);
 }
 
 moe_status moe_read_status(const void* ws, moe_stream_t stream) {

@@ -32,28 +32,51 @@ namespace moe {
 
 namespace {
 
+// First padded row that a completed ring forward left in its ring (its last
+// `slots` windows of mb rows), or `rows` when there is no such ring.
+__device__ __forceinline__ int ring_first_row(const __nv_bfloat16* ring, const int* hdr, int rows,
+                                              int mb, int slots) {
+  if (ring == nullptr || hdr[kHdrRingValid] == 0) return rows;
+  const int nw = (rows + mb - 1) / mb;
+  return max(0, nw - slots) * mb;
+}
+
+// Ring slot row that holds padded row pp (pp at or past ring_first_row).
+__device__ __forceinline__ const __nv_bfloat16* ring_row(const __nv_bfloat16* ring, int pp, int mb,
+                                                         int slots, int d) {
+  const int w = pp / mb;
+  return ring + ((size_t)(w % slots) * mb + (pp - w * mb)) * d;
+}
+
 // One warp per padded row; 16-byte vectors; up to 8 loads in flight per lane.
-// Padding rows are zero-filled when zero_pad, else skipped.
+// Padding rows are zero-filled when zero_pad, else skipped.  With a ring
+// (backward), rows are walked from the last to the first and the first
+// source's rows that the ring still holds are read from it.
 __global__ void __launch_bounds__(256) gather_kernel(const __nv_bfloat16* __restrict__ src,
                                                      __nv_bfloat16* __restrict__ dst,
                                                      const __nv_bfloat16* __restrict__ src2,
                                                      __nv_bfloat16* __restrict__ dst2,
                                                      const int* __restrict__ row_of_pad,
                                                      const int* __restrict__ hdr, int k, int d,
-                                                     int zero_pad) {
+                                                     int zero_pad, const __nv_bfloat16* __restrict__ ring,
+                                                     int ring_mb, int ring_slots) {
   const int rows = hdr[kHdrRpTotal];
+  const int rb = ring_first_row(ring, hdr, rows, ring_mb, ring_slots);
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
   const int nvec = d >> 3;
-  for (int pp = gw; pp < rows; pp += nw) {
+  for (int q = gw; q < rows; q += nw) {
+    const int pp = ring != nullptr ? rows - 1 - q : q;
     const int r = row_of_pad[pp];
     if (r < 0 && !zero_pad) continue;
     for (int pass = 0; pass < 2; ++pass) {
       const __nv_bfloat16* s = pass ? src2 : src;
       __nv_bfloat16* o = pass ? dst2 : dst;
       if (o == nullptr) break;
-      const uint4* sv = reinterpret_cast<const uint4*>(s + (size_t)(r < 0 ? 0 : r / k) * d);
+      const __nv_bfloat16* srow = (pass == 0 && r >= 0 && pp >= rb) ? ring_row(ring, pp, ring_mb, ring_slots, d)
+                                                                    : s + (size_t)(r < 0 ? 0 : r / k) * d;
+      const uint4* sv = reinterpret_cast<const uint4*>(srow);
       uint4* ov = reinterpret_cast<uint4*>(o + (size_t)pp * d);
       for (int v0 = lane; v0 < nvec; v0 += 32 * 8) {
         uint4 buf[8];
@@ -74,13 +97,16 @@ __global__ void __launch_bounds__(256) gather_kernel(const __nv_bfloat16* __rest
 
 // The same gather staged through shared memory with bulk copies: one CTA per
 // SM, warps [0, gw) each with nbw row buffers (bulk_rows.cuh).  Item i of a
-// warp is padded row gid + (i / npass) * ni, from src (pass 0) or src2
-// (pass 1).  The item code carries the pass in its low bit.
+// warp is the q-th padded row, q = gid + (i / npass) * ni (walked from the
+// last row down when a ring is given), from src (pass 0) or src2 (pass 1).
+// Item codes: r * npass + pass for row r of a source, R * npass + pp for
+// padded row pp read from the ring.
 __global__ void __launch_bounds__(256, 1) gather_bulk_kernel(
     const __nv_bfloat16* __restrict__ src, __nv_bfloat16* __restrict__ dst,
     const __nv_bfloat16* __restrict__ src2, __nv_bfloat16* __restrict__ dst2,
     const int* __restrict__ row_of_pad, const int* __restrict__ hdr, int k, int d, int zero_pad,
-    int gw, int nbw, int* status) {
+    int gw, int nbw, int* status, int R, const __nv_bfloat16* __restrict__ ring, int ring_mb,
+    int ring_slots) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_abort;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
@@ -108,21 +134,31 @@ __global__ void __launch_bounds__(256, 1) gather_bulk_kernel(
   __syncthreads();
   if (warp >= gw) return;
   const int rows = hdr[kHdrRpTotal];
+  const int ring0 = ring_first_row(ring, hdr, rows, ring_mb, ring_slots);
+  const bool rev = ring != nullptr;
   const int npass = dst2 != nullptr ? 2 : 1;
   const int gid = blockIdx.x * gw + warp, ni = gridDim.x * gw;
   const int n = gid < rows ? (rows - gid + ni - 1) / ni * npass : 0;
   if (n == 0) return;
+  auto pad_of = [&](int i) {
+    const int q = gid + (i / npass) * ni;
+    return rev ? rows - 1 - q : q;
+  };
   const bool done = bulk_rows(
       rp, n,
       [&](int i) {
-        const int r = __ldg(row_of_pad + gid + (size_t)(i / npass) * ni);
-        return r >= 0 ? r * npass + i % npass : (zero_pad ? kRowZero : kRowSkip);
+        const int pp = pad_of(i);
+        const int r = __ldg(row_of_pad + pp);
+        if (r < 0) return zero_pad ? kRowZero : kRowSkip;
+        if (i % npass == 0 && pp >= ring0) return R * npass + pp;
+        return r * npass + i % npass;
       },
       [&](int code) {
+        if (code >= R * npass) return ring_row(ring, code - R * npass, ring_mb, ring_slots, d);
         const __nv_bfloat16* s = (code % npass) ? src2 : src;
         return s + (size_t)(code / npass / k) * d;
       },
-      [&](int i) { return ((i % npass) ? dst2 : dst) + (size_t)(gid + (i / npass) * ni) * d; },
+      [&](int i) { return ((i % npass) ? dst2 : dst) + (size_t)pad_of(i) * d; },
       &s_abort, status, 900);
   if (lane == 0) {
     bulk_wait<0>();
@@ -291,6 +327,72 @@ __global__ void __launch_bounds__(256) quant_weights_kernel(const __nv_bfloat16*
   }
 }
 
+// Rows [rows, K] bf16 (K contiguous) -> E4M3 codes [rows, K] and scale tiles,
+// blocks of 32 along K: one thread per (row, block), consecutive threads on
+// consecutive blocks of a row.  rows_dev (optional) caps the rows at a
+// device-side count (the padded row total of the schedule).
+__global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16* __restrict__ w,
+                                                         int64_t rows, int K, const int* rows_dev,
+                                                         uint8_t* __restrict__ q, uint8_t* __restrict__ sc) {
+  const int nkb = K >> 5;
+  const int64_t nr = rows_dev ? (int64_t)*rows_dev : rows;
+  const int64_t total = nr * nkb;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / nkb;
+    const int kb = (int)(i - r * nkb);
+    const uint4* src = reinterpret_cast<const uint4*>(w + r * K + (int64_t)kb * 32);
+    uint4 in[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) in[u] = ldg_nc_v4(src + u);
+    uint4 out[2];
+    uint8_t s8;
+    quant32(in, out, s8);
+    uint4* qv = reinterpret_cast<uint4*>(q + r * K + (int64_t)kb * 32);
+    stg_v4(qv, out[0]);
+    stg_v4(qv + 1, out[1]);
+    sc[mx_sf_offset((size_t)r, kb, K >> 7)] = s8;
+  }
+}
+
+// Transposing quantiser: src [rows, K] bf16 (rows of the padded expert order,
+// K contiguous) -> codes qt [K, ld] (row k holds column k of src, rows
+// contiguous) and scale tiles over [K, ld], blocks of 32 rows: the K-major
+// operand of a weight-gradient GEMM that contracts over the rows.  A CTA
+// stages 32 rows x 256 columns through shared memory; thread c then holds
+// column c's 32 values, one block.  Rows past the device-side count
+// (*rows_dev) are left alone.
+__global__ void __launch_bounds__(256) quant_cols_kernel(const __nv_bfloat16* __restrict__ src, int K,
+                                                         const int* __restrict__ rows_dev, int ld,
+                                                         uint8_t* __restrict__ qt, uint8_t* __restrict__ sct) {
+  __shared__ __nv_bfloat16 tile[32][256 + 8];
+  const int rows = *rows_dev;
+  const int r0 = blockIdx.x * 32, c0 = blockIdx.y * 256;
+  if (r0 >= rows) return;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // each warp loads 4 rows of 256 columns: 32 lanes x 8 columns (16 bytes)
+  for (int rr = warp; rr < 32; rr += 8) {
+    const int c = c0 + lane * 8;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (c < K) v = ldg_nc_v4(src + (size_t)(r0 + rr) * K + c);
+    const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) tile[rr][lane * 8 + j] = h[j];
+  }
+  __syncthreads();
+  const int c = c0 + tid;
+  if (c >= K) return;
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __bfloat162float(tile[i][tid]);
+  uint4 lo, hi;
+  const uint8_t s8 = mx_quant32(v, lo, hi);
+  uint4* qv = reinterpret_cast<uint4*>(qt + (size_t)c * ld + r0);
+  stg_v4(qv, lo);
+  stg_v4(qv + 1, hi);
+  sct[mx_sf_offset((size_t)c, r0 >> 5, ld >> 7)] = s8;
+}
+
 // One CTA per token (grid-stride); each thread owns 8-column vectors.
 __global__ void __launch_bounds__(128) merge_kernel(const __nv_bfloat16* __restrict__ rows,
                                                     const int* __restrict__ pos_pad,
@@ -340,10 +442,12 @@ __global__ void __launch_bounds__(256) dg_reduce_kernel(
 
 cudaError_t launch_gather(const moe_config& c, const Ws& ws, const __nv_bfloat16* src,
                           __nv_bfloat16* dst, const __nv_bfloat16* src2, __nv_bfloat16* dst2,
-                          cudaStream_t st) {
+                          cudaStream_t st, const RingSrc* ring) {
   TraceScope ts(dst2 ? "gather_x_dy" : "gather", st);
   // the backward's gather (two sources) zero-fills padding rows for the weight gradients
   const int zero_pad = dst2 != nullptr ? 1 : 0;
+  const __nv_bfloat16* rg = ring ? ring->ring : nullptr;
+  const int rmb = ring ? ring->mb : 1, rsl = ring ? ring->slots : 1;
   // bulk-copy gather: a zero row and up to 16 row buffers in each of 8 warps
   // (fewer warps for wide rows, at least two buffers each), one CTA per SM
   constexpr size_t kBudget = 227 * 1024 - 128 - 8 * 16 * 8;
@@ -360,12 +464,13 @@ cudaError_t launch_gather(const moe_config& c, const Ws& ws, const __nv_bfloat16
                                            (int)smem);
     if (err != cudaSuccess) return err;
     gather_bulk_kernel<<<num_sms(), 256, smem, st>>>(src, dst, src2, dst2, ws.row_of_pad(), ws.hdr(), c.k,
-                                                     c.d, zero_pad, gw, nbw, ws.hdr() + kHdrStatus);
+                                                     c.d, zero_pad, gw, nbw, ws.hdr() + kHdrStatus,
+                                                     c.T * c.k, rg, rmb, rsl);
     return cudaGetLastError();
   }
   // rows too wide for two shared-memory buffers per warp: plain loads and stores
   gather_kernel<<<num_sms() * 8, 256, 0, st>>>(src, dst, src2, dst2, ws.row_of_pad(), ws.hdr(), c.k, c.d,
-                                               zero_pad);
+                                               zero_pad, rg, rmb, rsl);
   return cudaGetLastError();
 }
 
@@ -421,6 +526,26 @@ cudaError_t launch_quantize_mxfp8(const __nv_bfloat16* w, int64_t batch, int K, 
   if (blocks > cap) blocks = cap;
   TraceScope ts("quantize_weights", st);
   quant_weights_kernel<<<(int)blocks, 256, 0, st>>>(w, batch, K, N, q, sc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_rows(const __nv_bfloat16* w, int64_t rows, int K, const int* rows_dev,
+                              uint8_t* q, uint8_t* sc, cudaStream_t st, const char* name) {
+  const int64_t total = rows * (K / 32);
+  int64_t blocks = (total + 255) / 256;
+  const int64_t cap = (int64_t)num_sms() * 16;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  TraceScope ts(name, st);
+  quant_rows_kernel<<<(int)blocks, 256, 0, st>>>(w, rows, K, rows_dev, q, sc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_cols(const __nv_bfloat16* src, int64_t max_rows, int K, const int* rows_dev,
+                              uint8_t* qt, uint8_t* sct, int ld, cudaStream_t st, const char* name) {
+  dim3 grid((unsigned)((max_rows + 31) / 32), (unsigned)((K + 255) / 256));
+  TraceScope ts(name, st);
+  quant_cols_kernel<<<grid, 256, 0, st>>>(src, K, rows_dev, ld, qt, sct);
   return cudaGetLastError();
 }
 

@@ -51,14 +51,6 @@ constexpr int kTmemCols = 512;
 constexpr int kTmemSf = 256;              // fp8: per-stage scale columns start here
 constexpr int kTmemSfStride = 16;         // fp8: TMEM columns per stage (A: 4, B: 8; 8-aligned)
 constexpr int kTrTile = 32 * 80;          // 32 rows x (64 + 16 pad) bytes: per-warp transpose tile
-// Thin pair units (an expert's lone last tile, mostly experts with a few rows)
-// stream their weight slice from HBM with little to compute, so they are
-// bound by the bytes a CTA has in flight; they also prefetch the slice's
-// k-block this many blocks ahead into L2.  0 turns the prefetch off.
-#ifndef MOE_THIN_PREFETCH
-#define MOE_THIN_PREFETCH 8
-#endif
-constexpr int kThinPrefetch = MOE_THIN_PREFETCH;
 
 enum Epi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2, EPI_LOGITS = 3 };
 
@@ -73,7 +65,7 @@ struct KCfg {
   static constexpr int kStageBytes = kABytes + (PAIR ? kBHalfBytes : kBBytes);
   static constexpr int kStages = PAIR ? 6 : (FP8 && EPI == EPI_STORE) ? 3 : 4;
   // swizzled staging tiles per epilogue warp for the TMA-store epilogues
-  static constexpr int kOutBufs = (EPI == EPI_STORE || EPI == EPI_DSWIGLU || (EPI == EPI_SWIGLU && !FP8)) ? 2 : 0;
+  static constexpr int kOutBufs = (EPI == EPI_STORE || (EPI != EPI_LOGITS && !FP8)) ? 2 : 0;
   static constexpr int kAcc = FP8 ? 1 : 2;
   // scale-tile region rounded to 1024 bytes: the swizzled staging tiles after
   // it must start on a 1024-byte boundary for the 128-byte swizzle pattern
@@ -109,8 +101,14 @@ struct Params {
   const uint8_t* sfb;       // FP8: scale tiles of the weight stack [E * b_rows, K]
   int k_groups;             // FP8: K / 128
   int b_rows;               // FP8: rows (N) of one expert's weight
-  uint8_t* q_out;           // FP8 SWIGLU: E4M3 codes of A [rows, f]
-  uint8_t* q_sf;            // FP8 SWIGLU: scale tiles of A
+  uint8_t* q_out;           // FP8 SWIGLU: E4M3 codes of A [rows, f]; DSWIGLU: of dH [rows, 2f]
+  uint8_t* q_sf;            // FP8 SWIGLU: scale tiles of A; DSWIGLU: of dH (blocks along 2f)
+  uint8_t* qt0;             // FP8 DSWIGLU: dH transposed [2f, ldt], blocks of 32 rows
+  uint8_t* qt0_sf;
+  uint8_t* qt1;             // FP8 DSWIGLU: g*A transposed [f, ldt], blocks of 32 rows
+  uint8_t* qt1_sf;
+  int ldt;                  // FP8: row length (K) of the transposed operands (the padded row capacity)
+  int kstep;                // WGRAD: expert rows per K step (64 bf16, 128 fp8)
   int thin;                 // bf16 GEMM1: compute an expert's partial last tile swapped
   // dense mode (router GEMMs): ROWS without mt_off walks dense_mt 128-row
   // tiles of one matrix; WGRAD without counts contracts over dense_k rows
@@ -216,10 +214,10 @@ __device__ __forceinline__ Tile decode(const Params& p, int L, int rank) {
     t.n = loc / mu;
     t.valid = t.m < p.m_tiles_w;
     if (p.counts != nullptr) {
-      t.kb_count = (__ldg(p.counts + t.e) + BK - 1) / BK;
+      t.kb_count = (__ldg(p.counts + t.e) + p.kstep - 1) / p.kstep;
       t.krow0 = __ldg(p.poff + t.e);
     } else {
-      t.kb_count = (p.dense_k + BK - 1) / BK;
+      t.kb_count = (p.dense_k + p.kstep - 1) / p.kstep;
       t.krow0 = 0;
     }
     t.row0 = 0;
@@ -385,23 +383,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!PAIR || rank == 0) mbar_arrive_expect_tx(&full[s], tx);
           if constexpr (FP8) {
             // K-major E4M3 tiles (128 bytes of K per row) plus their scale tiles
+            // ROWS: A rows at row0, K from 0; WGRAD: A = the transposed
+            // operand's rows m*128 (output rows), K = the expert's rows from
+            // krow0 (a multiple of 128), the same for B (one matrix, e = 0)
             const int nbt = p.b_rows >> 7;  // 128-row scale tiles per expert
+            const int kc = (WGRAD ? t.krow0 : 0) + kb * BK8;
+            const int kg = kc >> 7;          // K group of the scale tiles
+            const int arow = WGRAD ? t.m * kBM : t.row0;
+            const int be = WGRAD ? 0 : t.e;
             int nb0, nb1;
-            tma_load_2d(sa, &tmA, fb, kb * BK8, t.row0);
+            tma_load_2d(sa, &tmA, fb, kc, arow);
             if (EPI == EPI_SWIGLU) {
-              tma_load_3d(sb, &tmB, fb, kb * BK8, t.n * 128, t.e);
-              tma_load_3d(sb + 16384, &tmB, fb, kb * BK8, p.f + t.n * 128, t.e);
+              tma_load_3d(sb, &tmB, fb, kc, t.n * 128, be);
+              tma_load_3d(sb + 16384, &tmB, fb, kc, p.f + t.n * 128, be);
               nb0 = t.n;
               nb1 = (p.f >> 7) + t.n;
             } else {
-              tma_load_3d(sb, &tmB, fb, kb * BK8, t.n * 256, t.e);
+              tma_load_3d(sb, &tmB, fb, kc, t.n * 256, be);
               nb0 = 2 * t.n;
               nb1 = min(2 * t.n + 1, nbt - 1);  // rows past N are zero-filled; any finite scale
             }
             const uint32_t sf = smem_u32(sfbuf + (size_t)s * kSfBytes);
-            bulk_load(sf, p.sfa + ((size_t)(t.row0 >> 7) * p.k_groups + kb) * 512u, 512u, fb);
-            bulk_load(sf + 512, p.sfb + (((size_t)t.e * nbt + nb0) * p.k_groups + kb) * 512u, 512u, fb);
-            bulk_load(sf + 1024, p.sfb + (((size_t)t.e * nbt + nb1) * p.k_groups + kb) * 512u, 512u, fb);
+            bulk_load(sf, p.sfa + ((size_t)(arow >> 7) * p.k_groups + kg) * 512u, 512u, fb);
+            bulk_load(sf + 512, p.sfb + (((size_t)be * nbt + nb0) * p.k_groups + kg) * 512u, 512u, fb);
+            bulk_load(sf + 1024, p.sfb + (((size_t)be * nbt + nb1) * p.k_groups + kg) * 512u, 512u, fb);
           } else {
             auto load2 = [&](uint32_t off, const CUtensorMap* m, int c0, int c1) {
               if constexpr (PAIR) tma_load_2d_pair(sa + off, m, fb, c0, c1);
@@ -416,24 +421,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               // SwiGLU: 64 gate and the matching 64 up columns; otherwise 128
               // output columns (MN-major, or K-major rows for dgrad) -- then its
               // half of the rows in 16-row boxes (the MMA's B, K-major)
-              if constexpr (kThinPrefetch > 0) {
-                auto pf = [&](int kk) {
-                  if (EPI == EPI_SWIGLU) {
-                    const int c0 = t.n * p.hn + rank * 64;
-                    tma_prefetch_3d(&tmB, c0, kk * BK, t.e);
-                    tma_prefetch_3d(&tmB, p.f + c0, kk * BK, t.e);
-                  } else if (B_MN) {
-                    const int c0 = t.n * 256 + rank * 128;
-                    tma_prefetch_3d(&tmB, c0, kk * BK, t.e);
-                    tma_prefetch_3d(&tmB, c0 + 64, kk * BK, t.e);
-                  } else {
-                    tma_prefetch_3d(&tmB, kk * BK, t.n * 256 + rank * 128, t.e);
-                  }
-                };
-                if (kb == 0)
-                  for (int j = kStages; j < kThinPrefetch && j < t.kb_count; ++j) pf(j);
-                if (kb + kThinPrefetch < t.kb_count && kThinPrefetch >= kStages) pf(kb + kThinPrefetch);
-              }
               if (EPI == EPI_SWIGLU) {
                 const int c0 = t.n * p.hn + rank * 64;
                 load3(0u, &tmB, c0, kb * BK, t.e);
@@ -854,6 +841,62 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (r < p.T)
             for (int j = 0; j < p.k; ++j) p.topk_w[(size_t)r * p.k + j] /= ssum;
         }
+      } else if constexpr (EPI == EPI_DSWIGLU && FP8) {
+        // MXFP8 SwiGLU backward: acc = dA' for f columns [n*256, n*256+256).
+        // dH is quantised along 2f for dgrad1 (this lane's 32 gate and 32 up
+        // values are one block each), and dH and g*A along the rows for the
+        // weight gradients (the warp's 32 lanes are one 32-row block of every
+        // column), written transposed.
+        const size_t row = (size_t)t.row0 + q * 32 + lane;
+        const int rblk = (t.row0 + q * 32) >> 5;
+        const int kq = (2 * p.f) >> 7, kt = p.ldt >> 7;
+        const float gw = p.g_pad[row];
+        float dg = 0.f;
+        for (int c = 0; c < 256; c += 32) {
+          const int col = t.n * 256 + c;
+          if (col >= p.f) break;
+          float da[32], av[32], hg[32], hu[32], o1[32], o2[32], o3[32];
+          load32_bf16(p.As + row * p.f + col, av);
+          load32_bf16(p.Hs + row * (2 * p.f) + col, hg);
+          load32_bf16(p.Hs + row * (2 * p.f) + p.f + col, hu);
+          tmem_ld32(tb + c, da);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            dg = fmaf(da[i], av[i], dg);
+            const float dA = gw * da[i];
+            const float sg = sigmoid_f(hg[i]);
+            o1[i] = dA * hu[i] * sg * (1.0f + hg[i] * (1.0f - sg));  // d gate
+            o2[i] = dA * hg[i] * sg;                                // d up
+            o3[i] = gw * av[i];                                     // g * A (for dW2)
+          }
+          uint4 lo, hi;
+          uint8_t sc = mx_quant32(o1, lo, hi);
+          uint4* qd = reinterpret_cast<uint4*>(p.q_out + row * (2 * p.f) + col);
+          qd[0] = lo;
+          qd[1] = hi;
+          p.q_sf[mx_sf_offset(row, col >> 5, kq)] = sc;
+          sc = mx_quant32(o2, lo, hi);
+          qd = reinterpret_cast<uint4*>(p.q_out + row * (2 * p.f) + p.f + col);
+          qd[0] = lo;
+          qd[1] = hi;
+          p.q_sf[mx_sf_offset(row, (p.f + col) >> 5, kq)] = sc;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            uint8_t s1, s2, s3;
+            const uint8_t c1 = mx_quant_lane(o1[i], &s1);
+            const uint8_t c2 = mx_quant_lane(o2[i], &s2);
+            const uint8_t c3 = mx_quant_lane(o3[i], &s3);
+            p.qt0[(size_t)(col + i) * p.ldt + row] = c1;
+            p.qt0[(size_t)(p.f + col + i) * p.ldt + row] = c2;
+            p.qt1[(size_t)(col + i) * p.ldt + row] = c3;
+            if (lane == 0) {
+              p.qt0_sf[mx_sf_offset((size_t)(col + i), rblk, kt)] = s1;
+              p.qt0_sf[mx_sf_offset((size_t)(p.f + col + i), rblk, kt)] = s2;
+              p.qt1_sf[mx_sf_offset((size_t)(col + i), rblk, kt)] = s3;
+            }
+          }
+        }
+        p.dgp[row * p.n_tiles + t.n] = dg;
       } else {
         // EPI_DSWIGLU: acc = dA' = dOut_p W2^T for f columns [n*256, n*256+256);
         // dH (gate, up) and g*A leave through TMA stores of 32 x 32 tiles
@@ -982,6 +1025,7 @@ Params base_params(const moe_config& c, const Ws& ws) {
   Params p{};
   p.E = c.E;
   p.f = c.f;
+  p.kstep = BK;
   p.mt_off = ws.mt_off();
   p.pt_off = ws.pt_off();
   p.poff = ws.poff();
@@ -992,7 +1036,8 @@ Params base_params(const moe_config& c, const Ws& ws) {
 }  // namespace
 
 cudaError_t gemm_fwd1(const moe_config& c, const Ws& ws, const int* counts, const __nv_bfloat16* Xp,
-                      const __nv_bfloat16* W1, __nv_bfloat16* A, __nv_bfloat16* H, cudaStream_t st) {
+                      const __nv_bfloat16* W1, __nv_bfloat16* A, __nv_bfloat16* H, cudaStream_t st,
+                      const char* name) {
   CUtensorMap ta, tb, to;
   const uint64_t rows = (uint64_t)ws.L.Rp_max;
   Params p = base_params(c, ws);
@@ -1016,10 +1061,9 @@ cudaError_t gemm_fwd1(const moe_config& c, const Ws& ws, const int* counts, cons
     return cudaErrorInvalidValue;
   if (H == nullptr) th = to;
   if (pair)
-    return launch<false, false, true, EPI_SWIGLU, false, true>("gemm1_swiglu", ta, ta16, tb, to, th, p,
+    return launch<false, false, true, EPI_SWIGLU, false, true>(name, ta, ta16, tb, to, th, p,
                                                                ws.L.MT_max * p.n_tiles, st);
-  return launch<false, false, true, EPI_SWIGLU>("gemm1_swiglu", ta, ta, tb, to, th, p,
-                                                ws.L.MT_max * p.n_tiles, st);
+  return launch<false, false, true, EPI_SWIGLU>(name, ta, ta, tb, to, th, p, ws.L.MT_max * p.n_tiles, st);
 }
 
 cudaError_t gemm_fwd2(const moe_config& c, const Ws& ws, const int* counts, const __nv_bfloat16* A,
@@ -1233,6 +1277,94 @@ cudaError_t gemm_fwd2_mx(const moe_config& c, const Ws& ws, const uint8_t* Aq, c
     return cudaErrorInvalidValue;
   return launch<false, false, false, EPI_STORE, true>("gemm2_mxfp8", ta, ta, tb, to, to, p,
                                                       ws.L.MT_max * p.n_tiles, st);
+}
+
+// ---------------------------------------------------------------- MXFP8 backward
+// dgrad2: dYq [rows, d] E4M3 (blocks along d) x W2 quantised along d
+// (W2q [E, f, d], its scale tiles over [E*f, d]) -> SwiGLU backward with the
+// routing-weight gradient; dH quantised along 2f (dHq, dHs), dH and g*A
+// quantised along the rows and written transposed (dHqT [2f, ldt], gAqT
+// [f, ldt], ldt = the padded row capacity), dg partials.
+cudaError_t gemm_dgrad2_mx(const moe_config& c, const Ws& ws, const uint8_t* dYq, const uint8_t* dYs,
+                           const uint8_t* W2q, const uint8_t* W2s, const __nv_bfloat16* Hs,
+                           const __nv_bfloat16* As, uint8_t* dHq, uint8_t* dHs, uint8_t* dHqT,
+                           uint8_t* dHsT, uint8_t* gAqT, uint8_t* gAsT, float* dgp, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  const uint64_t rows = (uint64_t)ws.L.Rp_max;
+  Params p = base_params(c, ws);
+  p.umma_n = 256;
+  p.n_tiles = (int)ws.L.nt_dg;
+  p.num_kb = c.d / BK8;
+  p.out_cols = c.f;
+  p.Hs = Hs;
+  p.As = As;
+  p.g_pad = ws.g_pad();
+  p.dgp = dgp;
+  p.sfa = dYs;
+  p.sfb = W2s;
+  p.k_groups = c.d / 128;
+  p.b_rows = c.f;
+  p.q_out = dHq;
+  p.q_sf = dHs;
+  p.qt0 = dHqT;
+  p.qt0_sf = dHsT;
+  p.qt1 = gAqT;
+  p.qt1_sf = gAsT;
+  p.ldt = (int)ws.L.Rp_max;
+  if (!map2d(&ta, dYq, c.d, rows, 128, kBM, true) || !map3d(&tb, W2q, c.d, c.f, c.E, 128, 256, true))
+    return cudaErrorInvalidValue;
+  return launch<false, false, false, EPI_DSWIGLU, true>("dgrad2_dswiglu_mxfp8", ta, ta, tb, ta, ta, p,
+                                                        ws.L.MT_max * p.n_tiles, st);
+}
+
+// dgrad1: dHq [rows, 2f] (blocks along 2f) x W1 quantised along 2f (W1q
+// [E, d, 2f], scale tiles over [E*d, 2f]) -> dX [rows, d] bf16 in expert order.
+cudaError_t gemm_dgrad1_mx(const moe_config& c, const Ws& ws, const uint8_t* dHq, const uint8_t* dHs,
+                           const uint8_t* W1q, const uint8_t* W1s, __nv_bfloat16* dXp, cudaStream_t st) {
+  CUtensorMap ta, tb, to;
+  const uint64_t rows = (uint64_t)ws.L.Rp_max;
+  Params p = base_params(c, ws);
+  p.umma_n = 256;
+  p.n_tiles = (c.d + 255) / 256;
+  p.num_kb = 2 * c.f / BK8;
+  p.out_cols = c.d;
+  p.sfa = dHs;
+  p.sfb = W1s;
+  p.k_groups = 2 * c.f / 128;
+  p.b_rows = c.d;
+  if (!map2d(&ta, dHq, 2ull * c.f, rows, 128, kBM, true) ||
+      !map3d(&tb, W1q, 2ull * c.f, c.d, c.E, 128, 256, true) || !map2d(&to, dXp, c.d, rows, 64, 32))
+    return cudaErrorInvalidValue;
+  return launch<false, false, false, EPI_STORE, true>("dgrad1_mxfp8", ta, ta, tb, to, to, p,
+                                                      ws.L.MT_max * p.n_tiles, st);
+}
+
+// Weight gradient dW[e] [M, N] = A_e^T B_e over expert e's rows with both
+// operands quantised along the rows and stored transposed: AqT [M, ldt],
+// BqT [N, ldt] (scale tiles over them, blocks of 32 rows from each expert's
+// padded segment start), K steps of 128 rows.
+cudaError_t gemm_wgrad_mx(const moe_config& c, const Ws& ws, const moe_sched& s, const uint8_t* AqT,
+                          const uint8_t* AsT, int M, const uint8_t* BqT, const uint8_t* BsT, int N,
+                          __nv_bfloat16* dW, const char* name, cudaStream_t st) {
+  CUtensorMap ta, tb, to;
+  const uint64_t ldt = (uint64_t)ws.L.Rp_max;
+  Params p = base_params(c, ws);
+  p.umma_n = 256;
+  p.m_tiles_w = (M + kBM - 1) / kBM;
+  p.n_tiles = (N + 255) / 256;
+  p.out_cols = N;
+  p.out_rows = M;
+  p.counts = s.counts;
+  p.kstep = BK8;
+  p.sfa = AsT;
+  p.sfb = BsT;
+  p.k_groups = (int)(ldt / 128);
+  p.b_rows = N;
+  if (!map2d(&ta, AqT, ldt, (uint64_t)M, 128, kBM, true) || !map3d(&tb, BqT, ldt, (uint64_t)N, 1, 128, 256, true) ||
+      !map3d(&to, dW, N, M, c.E, 64, 32))
+    return cudaErrorInvalidValue;
+  return launch<true, false, false, EPI_STORE, true>(name, ta, ta, tb, to, to, p,
+                                                     (long long)c.E * p.m_tiles_w * p.n_tiles, st);
 }
 
 }  // namespace moe

@@ -53,7 +53,8 @@ enum HdrWord {
   kHdrDone = 2,       // schedule: blocks finished (last-block ticket)
   kHdrRpTotal = 4,    // padded rows of all experts (multiple of kBM)
   kHdrMtTotal = 5,    // kRpTotal / kBM
-  kHdrInject = 8,     // fault-injection word for tests of the bounded waits
+  kHdrInject = 8,     // fault-injection words for tests of the bounded waits (8 and 9)
+  kHdrRingValid = 12, // set by the ring forward once every window has passed through the ring
   kHdrWords = 64
 };
 
@@ -61,6 +62,8 @@ struct WsLayout {
   int64_t R = 0, Rp_max = 0, MT_max = 0, nblk = 0, nt_dg = 0;
   size_t hdr = 0, hist = 0, poff = 0, mt_off = 0, pt_off = 0, pos_pad = 0, row_of_pad = 0, g_pad = 0;
   size_t Xp = 0, Abuf = 0, Yp = 0, dYp = 0, dH = 0, gA = 0, dgp = 0, Aq = 0, ring = 0;
+  size_t Hrc = 0;   // backward without saved activations: H recomputed [Rp, 2f]
+  size_t bq = 0;    // MXFP8 backward: quantised operands (see ws_layout)
   size_t dl16 = 0;  // router backward: dlogits in bf16 [T, E rounded up to 64]
   size_t ctr = 0, ctr_bytes = 0;  // ring path: window counters
   size_t total = 0;
@@ -109,10 +112,20 @@ cudaError_t launch_schedule_tail(const moe_config& c, const moe_sched& s, const 
 // dst [T, Epad] bf16 = src [T, E] fp32 rounded, zero in columns [E, Epad).
 cudaError_t launch_to_bf16_padded(const float* src, int T, int E, int Epad, __nv_bfloat16* dst,
                                   cudaStream_t st);
+// The ring of windows a ring forward leaves behind: once it completed (header
+// word kHdrRingValid), slot w % slots still holds the rows of each of the
+// last `slots` windows w of `mb` padded rows (padding rows zero).
+struct RingSrc {
+  const __nv_bfloat16* ring;
+  int mb, slots;
+};
 // dst[pp] = src[row_of_pad[pp] / k] (zero rows for padding), pp < Rp_total.
+// With `ring`, the rows of src that the last windows of a completed ring
+// forward still hold are read from the ring instead, and the padded rows are
+// walked from the last to the first (the backward's reverse traversal).
 cudaError_t launch_gather(const moe_config& c, const Ws& ws, const __nv_bfloat16* src,
                           __nv_bfloat16* dst, const __nv_bfloat16* src2, __nv_bfloat16* dst2,
-                          cudaStream_t st);
+                          cudaStream_t st, const RingSrc* ring = nullptr);
 // MXFP8 gather: E4M3 codes [Rp, d] and UE8M0 scale tiles (mx.cuh layout).
 cudaError_t launch_gather_mxfp8(const moe_config& c, const Ws& ws, const __nv_bfloat16* src,
                                 uint8_t* q, uint8_t* sc, cudaStream_t st);
@@ -124,9 +137,19 @@ cudaError_t launch_dg_reduce(const moe_config& c, const Ws& ws, const moe_sched&
 cudaError_t launch_quantize_mxfp8(const __nv_bfloat16* w, int64_t batch, int K, int N, uint8_t* q,
                                   uint8_t* sc, cudaStream_t st);
 
+// MXFP8 along the contiguous dimension: w [rows, K] -> codes [rows, K] and
+// scale tiles (mx.cuh layout, k_groups = K / 128); rows_dev (nullable) caps
+// the rows at a device-side count.
+cudaError_t launch_quant_rows(const __nv_bfloat16* w, int64_t rows, int K, const int* rows_dev,
+                              uint8_t* q, uint8_t* sc, cudaStream_t st, const char* name);
+// Transposed: src [*rows_dev, K] -> codes [K, ld] (rows contiguous) and scale
+// tiles over [K, ld] (blocks of 32 rows; ld a multiple of 128 >= max_rows).
+cudaError_t launch_quant_cols(const __nv_bfloat16* src, int64_t max_rows, int K, const int* rows_dev,
+                              uint8_t* qt, uint8_t* sct, int ld, cudaStream_t st, const char* name);
 // Grouped GEMMs on tcgen05 (gemm.cu).
 cudaError_t gemm_fwd1(const moe_config& c, const Ws& ws, const int* counts, const __nv_bfloat16* Xp,
-                      const __nv_bfloat16* W1, __nv_bfloat16* A, __nv_bfloat16* H, cudaStream_t st);
+                      const __nv_bfloat16* W1, __nv_bfloat16* A, __nv_bfloat16* H, cudaStream_t st,
+                      const char* name = "gemm1_swiglu");
 cudaError_t gemm_fwd2(const moe_config& c, const Ws& ws, const int* counts, const __nv_bfloat16* A,
                       const __nv_bfloat16* W2, __nv_bfloat16* Yp, cudaStream_t st);
 cudaError_t gemm_dgrad2(const moe_config& c, const Ws& ws, const __nv_bfloat16* dYp,
@@ -137,10 +160,29 @@ cudaError_t gemm_dgrad1(const moe_config& c, const Ws& ws, const int* counts, co
 cudaError_t gemm_wgrad(const moe_config& c, const Ws& ws, const moe_sched& s,
                        const __nv_bfloat16* Amn, int M, const __nv_bfloat16* Bmn, int N,
                        __nv_bfloat16* dW, cudaStream_t st);
+// MXFP8 backward GEMMs (gemm.cu): dgrad2 with the SwiGLU backward and the
+// quantisation of dH (along 2f, and transposed along the rows) and of g*A
+// (transposed), dgrad1, and the weight gradients over transposed operands.
+cudaError_t gemm_dgrad2_mx(const moe_config& c, const Ws& ws, const uint8_t* dYq, const uint8_t* dYs,
+                           const uint8_t* W2q, const uint8_t* W2s, const __nv_bfloat16* Hs,
+                           const __nv_bfloat16* As, uint8_t* dHq, uint8_t* dHs, uint8_t* dHqT,
+                           uint8_t* dHsT, uint8_t* gAqT, uint8_t* gAsT, float* dgp, cudaStream_t st);
+cudaError_t gemm_dgrad1_mx(const moe_config& c, const Ws& ws, const uint8_t* dHq, const uint8_t* dHs,
+                           const uint8_t* W1q, const uint8_t* W1s, __nv_bfloat16* dXp, cudaStream_t st);
+cudaError_t gemm_wgrad_mx(const moe_config& c, const Ws& ws, const moe_sched& s, const uint8_t* AqT,
+                          const uint8_t* AsT, int M, const uint8_t* BqT, const uint8_t* BsT, int N,
+                          __nv_bfloat16* dW, const char* name, cudaStream_t st);
 // Persistent forward with an SM split and a ring of windows (ring.cu).
 cudaError_t ring_forward(const moe_config& c, const Ws& ws, const int* counts, const __nv_bfloat16* x,
                          const __nv_bfloat16* W1, const __nv_bfloat16* W2, const float* topk_w,
                          __nv_bfloat16* A, __nv_bfloat16* H, __nv_bfloat16* out, cudaStream_t st);
+// The same with MXFP8 operands: the gather quantises rows in the ring, the
+// weights come as E4M3 codes and scale tiles (moe_quantize_mxfp8); A is saved
+// in bf16 only when A / H are given.
+cudaError_t ring_forward_mx(const moe_config& c, const Ws& ws, const int* counts, const __nv_bfloat16* x,
+                            const uint8_t* W1q, const uint8_t* W1s, const uint8_t* W2q, const uint8_t* W2s,
+                            const float* topk_w, __nv_bfloat16* A, __nv_bfloat16* H, __nv_bfloat16* out,
+                            cudaStream_t st);
 // Router projection (gemm.cu): logits = x Wr^T with the top-k fused when E <= 256,
 // and its backward (dx_r = dlogits Wr, dWr = dlogits^T x).
 cudaError_t router_gemm(const moe_config& c, const Ws& ws, const __nv_bfloat16* x,

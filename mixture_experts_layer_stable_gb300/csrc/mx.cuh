@@ -68,4 +68,19 @@ __device__ __forceinline__ uint8_t mx_quant32(const float* v, uint4& lo, uint4& 
   return (uint8_t)(s + 127);
 }
 
+// Quantise one value per lane of a warp whose 32 lanes form one block (a
+// column of 32 rows): the block's scale from the warp-wide maximum, each
+// lane's E4M3 code (same rounding and scale steps as mx_quant32).  Returns
+// the code; *scale gets the scale byte (s + 127) in every lane.
+__device__ __forceinline__ uint8_t mx_quant_lane(float v, uint8_t* scale) {
+  float amax = fabsf(v);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const int s = mx_scale_exp(amax);
+  const int s1 = -s / 2, s2 = -s - s1;
+  const float y = v * mx_exp2i(s1) * mx_exp2i(s2);
+  *scale = (uint8_t)(s + 127);
+  return (uint8_t)(__nv_cvt_float2_to_fp8x2(make_float2(y, 0.f), __NV_SATFINITE, __NV_E4M3) & 0xFFu);
+}
+
 }  // namespace moe

@@ -29,6 +29,12 @@
 //                  GEMM1 epilogues (a_ready) and store Y in expert order.
 //   all CTAs       after the last GEMM2 store (done2), the fixed-order
 //                  weighted merge of every token.
+// MXFP8 mode: the gather quantises each row into E4M3 codes and UE8M0 scale
+// tiles in the ring slot (one scale per 32 elements along d), GEMM1 and GEMM2
+// are block-scaled (tcgen05.mma kind::mxf8f6f4, scales staged into TMEM),
+// GEMM1's epilogue quantises A along f for GEMM2 -- the same tiles in the
+// same order as the kernel chain's MXFP8 GEMMs, so the results are the
+// chain's bit for bit.
 // Every tile waits only on tiles and windows earlier in the stream, so the
 // stream always makes progress.  Every wait is bounded: on expiry the kernel
 // sets a global abort word, reports MOE_ERR_TIMEOUT in the workspace status
@@ -40,6 +46,7 @@
 
 #include "gemm_common.cuh"
 #include "moe_internal.h"
+#include "mx.cuh"
 #include "ptx.cuh"
 #include "bulk_rows.cuh"
 #include "rowops.cuh"
@@ -49,18 +56,27 @@ namespace moe {
 namespace {
 
 constexpr int BK = 64;
+constexpr int BK8 = 128;                       // MXFP8: K elements (bytes) per stage
 constexpr int kStages = 4;
-constexpr int kABytes = kBM * BK * 2;          // 16 KB
+constexpr int kABytes = kBM * BK * 2;          // 16 KB (MXFP8: 128 rows x 128 bytes, the same)
 constexpr int kBBox = 64 * BK * 2;             // 8 KB: 64 columns x 64 K rows, MN-major
-constexpr int kStageBytes = kABytes + 4 * kBBox;
+constexpr int kStageBytes = kABytes + 4 * kBBox;  // MXFP8: 16 KB of A + 256 rows x 128 bytes of B
+constexpr int kSfBytes = 1536;                 // MXFP8: A scale tile + two B scale tiles a stage
 constexpr int kEpiWarps = 4;
 constexpr int kGatherWarps = 2;  // gather warps of a CTA in the warp split
 constexpr int kThreads = (2 + kEpiWarps + kGatherWarps) * 32;  // producer, MMA, epilogue, gather
 constexpr int kOutTile = 32 * 128;
 constexpr int kTmemCols = 512;
+constexpr int kTmemSf = 256;                   // MXFP8: scale columns of stage s at 256 + 16 s
 constexpr int kQ = 4;  // depth of the per-CTA queue of claimed tile indices
-constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kEpiWarps * 2 * kOutTile + 256;
-static_assert(kSmem <= 232448, "shared memory budget");
+// bf16: staging tiles for the Y stores (and the thin tiles' transposes);
+// MXFP8: per-stage scale tiles instead (Y leaves with direct stores)
+template <bool FP8>
+struct RingCfg {
+  static constexpr size_t kExtra = FP8 ? (size_t)kStages * kSfBytes : (size_t)kEpiWarps * 2 * kOutTile;
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + (kExtra + 1023) / 1024 * 1024 + 256;
+  static_assert(kSmem <= 232448, "shared memory budget");
+};
 
 struct RingParams {
   int T, d, f, E, k;
@@ -78,7 +94,12 @@ struct RingParams {
   const int* pos_pad;
   const float* topk_w;
   const __nv_bfloat16* x;
-  __nv_bfloat16* ring;  // [S * mb, d]
+  __nv_bfloat16* ring;  // [S * mb, d]  (MXFP8: E4M3 codes [S * mb, d], then their scale tiles)
+  uint8_t* ring_sf;     // MXFP8: scale tiles of the ring rows
+  uint8_t* Aq;          // MXFP8: E4M3 codes of A [Rp, f] and their scale tiles
+  uint8_t* As;
+  const uint8_t* W1s;   // MXFP8: scale tiles of the quantised weights
+  const uint8_t* W2s;
   __nv_bfloat16* A;     // [Rp, f]
   __nv_bfloat16* H;     // [Rp, 2f] or null
   __nv_bfloat16* Y;     // [Rp, d]
@@ -90,6 +111,7 @@ struct RingParams {
   int* tile_next;       // next unclaimed tile of the stream
   int* gabort;          // set once by the first wait that gives up
   int* status;
+  int* ring_valid;      // header word: set once every window has passed through the ring
 };
 
 // Window geometry of this call (from the padded row total the schedule wrote).
@@ -195,6 +217,27 @@ __device__ __forceinline__ RTile ring_decode(const RingParams& p, const Geo& g, 
   return t;
 }
 
+// MXFP8: one warp quantises the source row of routed row r (zeros for a
+// padding row, r < 0) into ring row rr -- E4M3 codes and one UE8M0 scale per
+// 32 elements along d, lane b taking blocks b, b + 32, ... -- with the
+// quantiser of the chain's gather (the same codes, bit for bit).
+__device__ __forceinline__ void ring_quant_row(const RingParams& p, int r, size_t rr, int lane) {
+  const int nblk = p.d >> 5;
+  const uint4* sv = reinterpret_cast<const uint4*>(p.x + (size_t)(r < 0 ? 0 : r / p.k) * p.d);
+  uint8_t* q = reinterpret_cast<uint8_t*>(p.ring) + rr * p.d;
+  for (int b = lane; b < nblk; b += 32) {
+    float v[32];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) unpack8(r >= 0 ? ldg_nc_v4(sv + b * 4 + u) : make_uint4(0, 0, 0, 0), v + 8 * u);
+    uint4 lo, hi;
+    const uint8_t sc = mx_quant32(v, lo, hi);
+    stg_v4(q + b * 32, lo);
+    stg_v4(q + b * 32 + 16, hi);
+    p.ring_sf[mx_sf_offset(rr, b, p.d >> 7)] = sc;
+  }
+}
+
+template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     ring_forward_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW1,
                         const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW2,
@@ -207,6 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kAcc = FP8 ? 1 : 2;  // MXFP8: one accumulator, the scales in TMEM columns 256..
   const Geo geo = make_geo(p);
   const int inject = p.hdr[kHdrInject];        // test hook: window + 1 whose arrival is withheld
   const int lim_ms = p.hdr[kHdrInject + 1];    // test hook: wait limit in ms (0: default)
@@ -217,6 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Warps [0, gw) each move their share of a window's rows with bulk copies
     // staged through nbw row buffers of their own (bulk_rows.cuh); padding
     // rows of the expert order leave from a zero row.
+    // (MXFP8: warps quantise rows from registers; no row buffers)
     const uint32_t rb = (uint32_t)p.d * 2u;
     const bool issuer = warp < p.gw;
     RowPipe rp;
@@ -227,12 +272,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     rp.nbw = p.nbw;
     rp.depth = p.nbw / 2;
     rp.ph = rp.pend = 0;
-    for (uint32_t i = threadIdx.x; i < rb / 16; i += kThreads)
-      reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
-    fence_proxy_async_smem();  // the zero row is read by bulk stores
-    if (issuer && lane == 0) {
-      for (int b = 0; b < p.nbw; ++b) mbar_init(&rp.bars[b], 1);
-      fence_mbar_init();
+    if constexpr (!FP8) {
+      for (uint32_t i = threadIdx.x; i < rb / 16; i += kThreads)
+        reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+      fence_proxy_async_smem();  // the zero row is read by bulk stores
+      if (issuer && lane == 0) {
+        for (int b = 0; b < p.nbw; ++b) mbar_init(&rp.bars[b], 1);
+        fence_mbar_init();
+      }
     }
     if (threadIdx.x == 0) s_gab = 0;
     __syncthreads();
@@ -246,6 +293,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncthreads();  // everyone has read s_ok before thread 0 writes it again
       if (!ok) break;
       const int r0 = w * p.mb, r1 = min(r0 + p.mb, geo.rp);
+      if constexpr (FP8) {
+        // every warp of the CTA quantises its share of the window's rows
+        const int gq = blockIdx.x * (kThreads / 32) + warp, nq = p.G * (kThreads / 32);
+        for (int pp = r0 + gq; pp < r1; pp += nq)
+          ring_quant_row(p, __ldg(p.row_of_pad + pp), (size_t)s * p.mb + (pp - r0), lane);
+        __syncthreads();
+        if (threadIdx.x == 0) {
+          __threadfence();
+          if (inject != w + 1) red_release_add(&p.ready[s], 1);
+        }
+        continue;
+      }
       const int n = (issuer && r0 + gid < r1) ? (r1 - r0 - gid + ni - 1) / ni : 0;
       if (n > 0) {
         __nv_bfloat16* slot = p.ring + (size_t)s * p.mb * p.d;
@@ -280,8 +339,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ====================================================== compute side
     uint8_t* stages = smem;
-    uint8_t* staging = smem + (size_t)kStages * kStageBytes;
-    uint8_t* ctrl = staging + kEpiWarps * 2 * kOutTile;
+    uint8_t* staging = smem + (size_t)kStages * kStageBytes;  // MXFP8: the stages' scale tiles
+    uint8_t* sfbuf = staging;
+    uint8_t* ctrl = staging + (RingCfg<FP8>::kExtra + 1023) / 1024 * 1024;
     uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
     uint64_t* empty = full + kStages;
     uint64_t* tfull = empty + kStages;
@@ -356,6 +416,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t sa = smem_u32(stages + (size_t)s * kStageBytes);
             const uint32_t sb = sa + kABytes;
             const uint32_t fb = smem_u32(&full[s]);
+            if constexpr (FP8) {
+              // K-major E4M3 tiles (128 bytes of K per row) and their scale
+              // tiles, as the chain's MXFP8 GEMMs load them
+              mbar_arrive_expect_tx(&full[s], (uint32_t)(kABytes + 32768 + kSfBytes));
+              const uint32_t sf = smem_u32(sfbuf + (size_t)s * kSfBytes);
+              if (g1) {
+                const int ring_row = slot * p.mb + t.mloc * kBM;
+                const int kg = p.d >> 7, nbt = (2 * p.f) >> 7;
+                tma_load_2d(sa, &tmX, fb, kb * BK8, ring_row);
+                tma_load_3d(sb, &tmW1, fb, kb * BK8, t.n * 128, t.e);
+                tma_load_3d(sb + 16384, &tmW1, fb, kb * BK8, p.f + t.n * 128, t.e);
+                bulk_load(sf, p.ring_sf + ((size_t)(ring_row >> 7) * kg + kb) * 512u, 512u, fb);
+                bulk_load(sf + 512, p.W1s + (((size_t)t.e * nbt + t.n) * kg + kb) * 512u, 512u, fb);
+                bulk_load(sf + 1024, p.W1s + (((size_t)t.e * nbt + (p.f >> 7) + t.n) * kg + kb) * 512u, 512u, fb);
+              } else {
+                const int kg = p.f >> 7, nbt = p.d >> 7;
+                const int nb1 = min(2 * t.n + 1, nbt - 1);  // rows past d are zero-filled; any finite scale
+                tma_load_2d(sa, &tmA, fb, kb * BK8, t.mt * kBM);
+                tma_load_3d(sb, &tmW2, fb, kb * BK8, t.n * 256, t.e);
+                bulk_load(sf, p.As + ((size_t)t.mt * kg + kb) * 512u, 512u, fb);
+                bulk_load(sf + 512, p.W2s + (((size_t)t.e * nbt + 2 * t.n) * kg + kb) * 512u, 512u, fb);
+                bulk_load(sf + 1024, p.W2s + (((size_t)t.e * nbt + nb1) * kg + kb) * 512u, 512u, fb);
+              }
+            } else {
             mbar_arrive_expect_tx(&full[s], (uint32_t)kABytes + (uint32_t)nbox * kBBox);
             if (g1) {
               tma_load_2d(sa, &tmX, fb, kb * BK, slot * p.mb + t.mloc * kBM);
@@ -367,6 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
               tma_load_2d(sa, &tmA, fb, kb * BK, t.mt * kBM);
               for (int i = 0; i < 4; ++i) tma_load_3d(sb + i * kBBox, &tmW2, fb, t.n * 256 + 64 * i, kb * BK, t.e);
+            }
             }
             used |= 1u << s;
             last_par = (last_par & ~(1u << s)) | (ph << s);
@@ -404,7 +489,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (g1 && kb == nkb - 1) red_release_add(&p.freed[t.w % p.S], 1);  // ring rows landed
             const uint32_t sa = smem_u32(stages + (size_t)s * kStageBytes);
             const uint32_t sb = sa + kABytes;
-            if (t.thin) {
+            if constexpr (FP8) {
+              // stage the scale tiles into this stage's TMEM columns, then 4
+              // block-scaled MMAs of K = 32, each reading its block's scale byte
+              const uint32_t sf = smem_u32(sfbuf + (size_t)s * kSfBytes);
+              const uint32_t tsa = tmem_base + kTmemSf + (uint32_t)s * 16u;
+              const uint32_t tsb = tsa + 8u;
+              tc_cp_32x128b_warpx4(tsa, sdesc_plain(sf, 16, 128));
+              tc_cp_32x128b_warpx4(tsb, sdesc_plain(sf + 512, 16, 128));
+              tc_cp_32x128b_warpx4(tsb + 4u, sdesc_plain(sf + 1024, 16, 128));
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                tc_mma_mxf8(dt, sdesc_sw128(sa + kk * 32, 16, 1024), sdesc_sw128(sb + kk * 32, 16, 1024),
+                            idesc_mxf8(kBM, 256, kk), tsa, tsb, (kb > 0 || kk > 0) ? 1u : 0u);
+            } else if (t.thin) {
               // weight slices (MN-major) x tile rows (K-major, N = rows rounded to 16)
               const uint32_t idt = idesc_bf16(kBM, (t.rows + 15) & ~15, true, false);
 #pragma unroll
@@ -427,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           tc_commit(smem_u32(&tfull[acc]));
-          if (++acc == 2) {
+          if (++acc == kAcc) {
             acc = 0;
             aph ^= 1u;
           }
@@ -452,7 +550,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&tfull[acc], aph, abort_flag, p.status, 400 + acc)) break;
         tc_fence_after();
         const uint32_t tb = tmem_base + (uint32_t)acc * 256u + ((uint32_t)(q * 32) << 16);
-        if (t.thin) {
+        if (FP8 && t.phase == 1) {
+          // SwiGLU; A quantised along f for GEMM2 (each lane's 32 columns are
+          // one block), A and H in bf16 when saving
+          const size_t row = (size_t)t.mt * kBM + q * 32 + lane;
+          for (int c = 0; c < p.hn; c += 32) {
+            float g[32], u[32], a[32];
+            tmem_ld32(tb + c, g);
+            tmem_ld32(tb + p.hn + c, u);
+            const int col = t.n * p.hn + c;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) a[i] = silu_f(g[i]) * u[i];
+            uint4 lo, hi;
+            const uint8_t sc = mx_quant32(a, lo, hi);
+            uint4* qd = reinterpret_cast<uint4*>(p.Aq + row * p.f + col);
+            qd[0] = lo;
+            qd[1] = hi;
+            p.As[mx_sf_offset(row, col >> 5, p.f >> 7)] = sc;
+            if (p.A != nullptr) store32_bf16(p.A + row * p.f + col, a);
+            if (p.H != nullptr) {
+              store32_bf16(p.H + row * (2 * p.f) + col, g);
+              store32_bf16(p.H + row * (2 * p.f) + p.f + col, u);
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(&tempty[acc]);
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) red_release_add(&p.a_ready[t.mt], 1);
+        } else if (FP8) {
+          // Y rows in expert order with direct stores
+          const size_t row = (size_t)t.mt * kBM + q * 32 + lane;
+          for (int c = 0; c < 256; c += 32) {
+            const int col = t.n * 256 + c;
+            if (col >= p.d) break;
+            float v[32];
+            tmem_ld32(tb + c, v);
+            store32_bf16(p.Y + row * p.d + col, v);
+          }
+          tc_fence_before();
+          mbar_arrive(&tempty[acc]);
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) red_release_add(p.done2, 1);
+        } else if (t.thin) {
           // thin GEMM1 tile: lanes hold gate / up columns, TMEM columns hold
           // tokens; rows go out through the warp's drained staging area used as
           // a transpose tile (all 128 rows: zeros past the expert's rows)
@@ -545,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           __syncwarp();
         }
-        if (++acc == 2) {
+        if (++acc == kAcc) {
           acc = 0;
           aph ^= 1u;
         }
@@ -569,6 +710,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r0 = w * p.mb, r1 = min(r0 + p.mb, geo.rp);
         const int n = (r0 + gwi < r1) ? (r1 - r0 - gwi + ncta - 1) / ncta : 0;
         __nv_bfloat16* slot = p.ring + (size_t)s * p.mb * p.d;
+        if constexpr (FP8) {
+          for (int i = 0; i < n; ++i) {
+            const int pa = gwi + i * ncta;  // row within the window
+            ring_quant_row(p, __ldg(p.row_of_pad + r0 + pa), (size_t)s * p.mb + pa, lane);
+          }
+        } else
         for (int c0 = 0; c0 < n; c0 += 32) {
           const int my = (c0 + lane < n) ? __ldg(p.row_of_pad + r0 + gwi + (size_t)(c0 + lane) * ncta) : -1;
           const int cn = min(32, n - c0);
@@ -620,6 +767,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_ok = wait_counter(p.done2, kEpiWarps * geo.total2, p.gabort, p.status, 800, limit);
   __syncthreads();
   if (!s_ok) return;
+  // every window's GEMM1 tiles acquired its rows before GEMM2 could finish:
+  // the ring now holds the last ring_slots windows for the (BF16) backward
+  if (!FP8 && blockIdx.x == 0 && threadIdx.x == 0) *p.ring_valid = 1;
   for (int t = blockIdx.x; t < p.T; t += gridDim.x) {
     if (threadIdx.x < p.k) {
       s_pos[threadIdx.x] = p.pos_pad[(size_t)t * p.k + threadIdx.x];
@@ -633,9 +783,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t ring_forward(const moe_config& c, const Ws& ws, const int* counts, const __nv_bfloat16* x,
-                         const __nv_bfloat16* W1, const __nv_bfloat16* W2, const float* topk_w,
-                         __nv_bfloat16* A, __nv_bfloat16* H, __nv_bfloat16* out, cudaStream_t st) {
+namespace {
+
+// Launch of the ring kernel; W1 / W2 are bf16, or (FP8) E4M3 codes with
+// their scale tiles W1s / W2s as moe_quantize_mxfp8 writes them.
+template <bool FP8>
+cudaError_t ring_launch(const moe_config& c, const Ws& ws, const int* counts, const __nv_bfloat16* x,
+                        const void* W1, const uint8_t* W1s, const void* W2, const uint8_t* W2s,
+                        const float* topk_w, __nv_bfloat16* A, __nv_bfloat16* H, __nv_bfloat16* out,
+                        cudaStream_t st) {
+  constexpr size_t kSmem = RingCfg<FP8>::kSmem;
   const int sms = num_sms();
   RingParams p{};
   p.T = c.T;
@@ -652,7 +809,7 @@ cudaError_t ring_forward(const moe_config& c, const Ws& ws, const int* counts, c
   {
     // gather row buffers (after one zero row): up to 16 per warp in all six
     // warps, at least two per issuing warp (fewer issuing warps for very wide
-    // rows)
+    // rows); MXFP8 gathers use none
     const size_t rb = (size_t)c.d * 2;
     if (kSmem <= 2048 + 3 * rb || rb >= (1u << 20)) return cudaErrorInvalidValue;
     const size_t avail = kSmem - 2048 - rb;
@@ -667,8 +824,8 @@ cudaError_t ring_forward(const moe_config& c, const Ws& ws, const int* counts, c
   p.hn = (c.f % 128 == 0) ? 128 : 64;
   p.nt1 = c.f / p.hn;
   p.nt2 = (c.d + 255) / 256;
-  p.kb1 = c.d / BK;
-  p.kb2 = c.f / BK;
+  p.kb1 = FP8 ? c.d / BK8 : c.d / BK;
+  p.kb2 = FP8 ? c.f / BK8 : c.f / BK;
   {
     // lag: one window more than it takes for the tiles claimed between a
     // window's GEMM1 and its GEMM2 to keep every compute CTA busy for one
@@ -680,17 +837,24 @@ cudaError_t ring_forward(const moe_config& c, const Ws& ws, const int* counts, c
   }
   p.mt_off = ws.mt_off();
   p.counts = counts;
-  p.thin = gemm1_thin_enabled(c) ? 1 : 0;
+  p.thin = (!FP8 && gemm1_thin_enabled(c)) ? 1 : 0;
   p.hdr = ws.hdr();
   p.row_of_pad = ws.row_of_pad();
   p.pos_pad = ws.pos_pad();
   p.topk_w = topk_w;
   p.x = x;
   p.ring = static_cast<__nv_bfloat16*>(ws.at(ws.L.ring));
+  p.ring_sf = static_cast<uint8_t*>(ws.at(ws.L.ring)) + (size_t)p.S * p.mb * c.d;
   p.A = A;
   p.H = H;
   p.Y = static_cast<__nv_bfloat16*>(ws.at(ws.L.Yp));
   p.out = out;
+  p.W1s = W1s;
+  p.W2s = W2s;
+  if (FP8) {
+    p.Aq = static_cast<uint8_t*>(ws.at(ws.L.Aq));
+    p.As = p.Aq + (size_t)ws.L.Rp_max * c.f;
+  }
   int* ctr = static_cast<int*>(ws.at(ws.L.ctr));
   p.ready = ctr;
   p.freed = ctr + p.S;
@@ -699,26 +863,50 @@ cudaError_t ring_forward(const moe_config& c, const Ws& ws, const int* counts, c
   p.tile_next = ctr + 2 * p.S + 2;
   p.a_ready = ctr + 2 * p.S + 3;
   p.status = ws.hdr() + kHdrStatus;
+  p.ring_valid = ws.hdr() + kHdrRingValid;
 
   const uint64_t rows = (uint64_t)ws.L.Rp_max;
   CUtensorMap tmX, tmW1, tmA, tmW2, tmY;
-  if (!map2d(&tmX, p.ring, c.d, (uint64_t)p.S * p.mb, 64, kBM) ||
-      !map3d(&tmW1, W1, 2ull * c.f, c.d, c.E, 64, 64) || !map2d(&tmA, A, c.f, rows, 64, kBM) ||
-      !map3d(&tmW2, W2, c.d, c.f, c.E, 64, 64) || !map2d(&tmY, p.Y, c.d, rows, 64, 32))
+  if (FP8) {
+    // K-major E4M3: 128-byte K boxes of 128 rows (W2: 256 rows)
+    if (!map2d(&tmX, p.ring, c.d, (uint64_t)p.S * p.mb, 128, kBM, true) ||
+        !map3d(&tmW1, W1, c.d, 2ull * c.f, c.E, 128, 128, true) ||
+        !map2d(&tmA, p.Aq, c.f, rows, 128, kBM, true) || !map3d(&tmW2, W2, c.f, c.d, c.E, 128, 256, true))
+      return cudaErrorInvalidValue;
+    tmY = tmX;  // Y leaves with direct stores
+  } else if (!map2d(&tmX, p.ring, c.d, (uint64_t)p.S * p.mb, 64, kBM) ||
+             !map3d(&tmW1, W1, 2ull * c.f, c.d, c.E, 64, 64) || !map2d(&tmA, A, c.f, rows, 64, kBM) ||
+             !map3d(&tmW2, W2, c.d, c.f, c.E, 64, 64) || !map2d(&tmY, p.Y, c.d, rows, 64, 32)) {
     return cudaErrorInvalidValue;
+  }
 
   cudaError_t err = cudaMemsetAsync(ctr, 0, ws.L.ctr_bytes, st);
   if (err != cudaSuccess) return err;
-  err = cudaFuncSetAttribute(ring_forward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+  auto kern = ring_forward_kernel<FP8>;
+  err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
   if (err != cudaSuccess) return err;
   int per_sm = 0;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ring_forward_kernel, kThreads, kSmem);
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, kSmem);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
   void* args[] = {&tmX, &tmW1, &tmA, &tmW2, &tmY, &p};
-  TraceScope ts("ring_forward", st);
-  return cudaLaunchCooperativeKernel((const void*)ring_forward_kernel, dim3(sms), dim3(kThreads), args,
-                                     kSmem, st);
+  TraceScope ts(FP8 ? "ring_forward_mxfp8" : "ring_forward", st);
+  return cudaLaunchCooperativeKernel((const void*)kern, dim3(sms), dim3(kThreads), args, kSmem, st);
+}
+
+}  // namespace
+
+cudaError_t ring_forward(const moe_config& c, const Ws& ws, const int* counts, const __nv_bfloat16* x,
+                         const __nv_bfloat16* W1, const __nv_bfloat16* W2, const float* topk_w,
+                         __nv_bfloat16* A, __nv_bfloat16* H, __nv_bfloat16* out, cudaStream_t st) {
+  return ring_launch<false>(c, ws, counts, x, W1, nullptr, W2, nullptr, topk_w, A, H, out, st);
+}
+
+cudaError_t ring_forward_mx(const moe_config& c, const Ws& ws, const int* counts, const __nv_bfloat16* x,
+                            const uint8_t* W1q, const uint8_t* W1s, const uint8_t* W2q, const uint8_t* W2s,
+                            const float* topk_w, __nv_bfloat16* A, __nv_bfloat16* H, __nv_bfloat16* out,
+                            cudaStream_t st) {
+  return ring_launch<true>(c, ws, counts, x, W1q, W1s, W2q, W2s, topk_w, A, H, out, st);
 }
 
 }  // namespace moe

@@ -39,6 +39,7 @@ __all__ = [
     "route",
     "schedule",
     "silu",
+    "swiglu_backward",
     "expert_ffn",
     "forward",
     "forward_tokens",
@@ -52,6 +53,7 @@ __all__ = [
     "mxfp8_dequantize",
     "forward_mxfp8",
     "backward_mxfp8",
+    "backward_mxfp8_experts",
 ]
 
 
@@ -219,6 +221,13 @@ def forward_tokens(x, W1, W2, ids, g, tokens=None):
 # reverse-dispatch) with the routing-weight gradient taken from the SwiGLU
 # backward ([MT] three design decisions, last paragraph).
 # --------------------------------------------------------------------------
+def swiglu_backward(Hg, Hu, dA):
+    """Gradient of A = silu(Hg) * Hu for an upstream dA: returns (dHg, dHu),
+    dHg = dA * Hu * s (1 + Hg (1 - s)) with s = sigmoid(Hg), dHu = dA * silu(Hg)."""
+    sg = _sigmoid(Hg)
+    return dA * Hu * sg * (1.0 + Hg * (1.0 - sg)), dA * (Hg * sg)
+
+
 def _expert_backward(Xe, W1e, W2e, ge, dOe):
     """Backward of one expert over its rows.
 
@@ -234,9 +243,7 @@ def _expert_backward(Xe, W1e, W2e, ge, dOe):
     dAp = dOe @ W2e.T                                  # dOut_t W2^T
     dg_fused = np.einsum("mf,mf->m", dAp, A)           # <dOut_t W2^T, A>
     dA = ge[:, None] * dAp
-    sg = _sigmoid(Hg)
-    dHg = dA * Hu * sg * (1.0 + Hg * (1.0 - sg))
-    dHu = dA * (Hg * sg)
+    dHg, dHu = swiglu_backward(Hg, Hu, dA)
     dH = np.concatenate([dHg, dHu], axis=1)
     dW2e = A.T @ (ge[:, None] * dOe)
     dW1e = _f64(Xe).T @ dH
@@ -487,6 +494,25 @@ def _pad_rows(v, mult: int = 32):
     return np.concatenate([v, np.zeros((pad, v.shape[1]))], axis=0) if pad else v
 
 
+def _expert_backward_mxfp8(Xe, W1e, W2e, ge, dOe, q):
+    """One expert's MXFP8 backward over its rows (in the stable expert order):
+    q(v, axis, name) quantises operand `name`.  Returns dict dg, dX, dW1, dW2."""
+    W1e = _f64(W1e)
+    W2e = _f64(W2e)
+    f = W2e.shape[0]
+    H = q(Xe, 1, "fwd.x") @ q(W1e, 0, "fwd.W1")
+    Hg, Hu = H[:, :f], H[:, f:]
+    A = silu(Hg) * Hu
+    dAp = q(dOe, 1, "dgrad2.dO") @ q(W2e, 1, "dgrad2.W2").T
+    dg = np.einsum("mf,mf->m", dAp, A)
+    dA = ge[:, None] * dAp
+    dH = np.concatenate(swiglu_backward(Hg, Hu, dA), axis=1)
+    return {"dg": dg,
+            "dX": q(dH, 1, "dgrad1.dH") @ q(W1e, 1, "dgrad1.W1").T,
+            "dW1": q(_pad_rows(Xe), 0, "wgrad1.X").T @ q(_pad_rows(dH), 0, "wgrad1.dH"),
+            "dW2": q(_pad_rows(ge[:, None] * A), 0, "wgrad2.gA").T @ q(_pad_rows(dOe), 0, "wgrad2.dO")}
+
+
 def backward_mxfp8(x, W1, W2, ids, g, dOut, qdq=None, quantise=None):
     """Full backward with MXFP8 operands.
 
@@ -532,26 +558,37 @@ def backward_mxfp8(x, W1, W2, ids, g, dOut, qdq=None, quantise=None):
             continue
         rows = perm[a:b]
         tok = rows // k
-        m = b - a
-        W1e = _f64(W1[e])
-        W2e = _f64(W2[e])
-        Xe = x[tok]
-        ge = gg.reshape(-1)[rows]
-        dOe = dOut[tok]
-        H = q(Xe, 1, "fwd.x") @ q(W1e, 0, "fwd.W1")
-        Hg, Hu = H[:, :f], H[:, f:]
-        A = silu(Hg) * Hu
-        dAp = q(dOe, 1, "dgrad2.dO") @ q(W2e, 1, "dgrad2.W2").T
-        dg[rows] = np.einsum("mf,mf->m", dAp, A)
-        dA = ge[:, None] * dAp
-        sg = _sigmoid(Hg)
-        dH = np.concatenate([dA * Hu * sg * (1.0 + Hg * (1.0 - sg)), dA * (Hg * sg)], axis=1)
-        dX_rows[rows] = q(dH, 1, "dgrad1.dH") @ q(W1e, 1, "dgrad1.W1").T
-        dW1[e] = (q(_pad_rows(Xe), 0, "wgrad1.X").T @ q(_pad_rows(dH), 0, "wgrad1.dH"))
-        dW2[e] = (q(_pad_rows(ge[:, None] * A), 0, "wgrad2.gA").T @ q(_pad_rows(dOe), 0, "wgrad2.dO"))
-        del m
+        r = _expert_backward_mxfp8(x[tok], W1[e], W2[e], gg.reshape(-1)[rows], dOut[tok], q)
+        dg[rows] = r["dg"]
+        dX_rows[rows] = r["dX"]
+        dW1[e] = r["dW1"]
+        dW2[e] = r["dW2"]
     for j in range(k):  # slot order
         dx += dX_rows[np.arange(T) * k + j]
     dg = dg.reshape(T, k)
     return {"dx": dx, "dW1": dW1, "dW2": dW2, "dg": dg,
             "dlogits": dlogits_from_dg(gg, ids, dg, E)}
+
+
+def backward_mxfp8_experts(x, W1, W2, ids, g, dOut, experts):
+    """dW1[e], dW2[e] and the routing-weight gradient of expert e's rows, with
+    MXFP8 operands as in backward_mxfp8, for the listed experts only (each
+    needs only its own rows).  Returns {e: (dW1e, dW2e, rows, dg_rows)}."""
+    q = _quantiser(None, None, BACKWARD_OPERANDS)
+    x = _f64(x)
+    ids = np.asarray(ids)
+    k = ids.shape[1]
+    flat = ids.reshape(-1)
+    gflat = _f64(g).reshape(-1)
+    res = {}
+    for e in experts:
+        rows = np.nonzero(flat == e)[0]          # ascending r, as perm orders them
+        W2e = _f64(W2[e])
+        f, d = W2e.shape
+        if rows.size == 0:
+            res[int(e)] = (np.zeros((d, 2 * f)), np.zeros((f, d)), rows, np.zeros(0))
+            continue
+        tok = rows // k
+        r = _expert_backward_mxfp8(x[tok], W1[e], W2e, gflat[rows], _f64(dOut[tok]), q)
+        res[int(e)] = (r["dW1"], r["dW2"], rows, r["dg"])
+    return res

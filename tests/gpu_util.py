@@ -37,12 +37,13 @@ class Layer:
                       self.saved if save else None, self.ws)
         return self.out
 
-    def backward(self, dOut, x, W1, W2, dlogits=True):
+    def backward(self, dOut, x, W1, W2, dlogits=True, recompute=False):
         if self.dW1 is None:
             self.dW1 = torch.empty_like(W1)
             self.dW2 = torch.empty_like(W2)
-        B.moe_backward(self.c, dOut, x, W1, W2, self.sched, self.saved, self.dx, self.dW1,
-                       self.dW2, self.dtopk_w, self.dlogits if dlogits else None, self.ws)
+        B.moe_backward(self.c, dOut, x, W1, W2, self.sched, None if recompute else self.saved,
+                       self.dx, self.dW1, self.dW2, self.dtopk_w, self.dlogits if dlogits else None,
+                       self.ws)
 
     def status(self):
         return B.moe_read_status(self.ws)

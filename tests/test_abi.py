@@ -80,8 +80,11 @@ def test_host_validation_returns_before_any_gpu_work(B):
     assert L.moe_schedule(ctypes.byref(bad), fake, s, fake, need, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_forward(ctypes.byref(c), fake, fake, None, fake, None, s, None, None, fake, need,
                          None) == B.MOE_ERR_INVALID_ARG
-    # backward needs saved activations
-    assert L.moe_backward(ctypes.byref(c), fake, fake, fake, fake, s, None, fake, fake, fake, fake,
+    # saved activations, when given, must be aligned (NULL asks for a recompute)
+    bad_saved = ctypes.byref(B.moe_saved(fake + 2, fake))
+    assert L.moe_backward(ctypes.byref(c), fake, fake, fake, fake, s, bad_saved, fake, fake, fake, fake,
+                          None, fake, need, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_backward(ctypes.byref(c), fake, fake, fake, fake, null_s, None, fake, fake, fake, fake,
                           None, fake, need, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_quantize_mxfp8(fake, 1, 100, 64, fake, fake, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_read_status(fake + 1, None) == B.MOE_ERR_INVALID_ARG
@@ -97,15 +100,23 @@ def test_workspace_regions_lie_inside_the_workspace(B):
     c = B.make_config(300, 256, 128, 6, 3, B.MOE_MXFP8)
     total = B.moe_workspace_bytes(c)
     rows = B.moe_saved_rows(c)
+    d, f = 256, 128
+    want = {B.MOE_WS_XQ_CODES: rows * d, B.MOE_WS_XQ_SCALES: rows * d // 32,
+            B.MOE_WS_AQ_CODES: rows * f, B.MOE_WS_AQ_SCALES: rows * f // 32,
+            B.MOE_WS_DYQ_CODES: rows * d, B.MOE_WS_DYQ_SCALES: rows * d // 32,
+            B.MOE_WS_XQT_CODES: d * rows, B.MOE_WS_XQT_SCALES: d * rows // 32,
+            B.MOE_WS_DYQT_CODES: d * rows, B.MOE_WS_DYQT_SCALES: d * rows // 32,
+            B.MOE_WS_DHQ_CODES: rows * 2 * f, B.MOE_WS_DHQ_SCALES: rows * 2 * f // 32,
+            B.MOE_WS_DHQT_CODES: 2 * f * rows, B.MOE_WS_DHQT_SCALES: 2 * f * rows // 32,
+            B.MOE_WS_GAQT_CODES: f * rows, B.MOE_WS_GAQT_SCALES: f * rows // 32}
     spans = []
-    for region, want in ((B.MOE_WS_XQ_CODES, rows * 256), (B.MOE_WS_XQ_SCALES, rows * 256 // 32),
-                         (B.MOE_WS_AQ_CODES, rows * 128), (B.MOE_WS_AQ_SCALES, rows * 128 // 32)):
+    for region, n_want in want.items():
         off, n = B.moe_workspace_region(c, region)
-        assert n == want and off % 128 == 0 and off + n <= total
+        assert n == n_want and off % 16 == 0 and off + n <= total, region
         spans.append((off, off + n))
     spans.sort()
     assert all(a[1] <= b[0] for a, b in zip(spans, spans[1:]))  # no overlap
     with pytest.raises(B.MoeError):
-        B.moe_workspace_region(c, 7)
+        B.moe_workspace_region(c, 16)
     with pytest.raises(B.MoeError):  # a BF16 layer has no quantised buffers
         B.moe_workspace_region(B.make_config(300, 256, 128, 6, 3), B.MOE_WS_XQ_CODES)

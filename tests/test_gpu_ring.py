@@ -113,16 +113,30 @@ def test_ring_withheld_window_times_out_cleanly(gather):
     assert _same(L.out, ref.out)
 
 
-def test_ring_rejects_unsupported_combinations():
+def test_ring_argument_errors_return_before_gpu_work():
+    # rejected on the host: an MXFP8 ring forward without weight scales, a
+    # BF16 one with scales, an SM split that leaves no compute CTA
     cfg = with_config("tiny", f=128, prec="mxfp8")
+    dev = {k: v.cuda() for k, v in make_inputs(cfg, with_grad=False).items()}
     c = cfg_struct(cfg, minibatch_rows=128, ring_slots=2)
     L = Layer(cfg, c)
-    dev = {k: v.cuda() for k, v in make_inputs(cfg, with_grad=False).items()}
     L.schedule(dev["logits"])
-    w = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    w = torch.zeros(64, dtype=torch.uint8, device="cuda")  # never read: the checks come first
     with pytest.raises(B.MoeError) as ei:
-        B.moe_forward(c, dev["x"], w, w, w, w, L.sched, L.out, None, L.ws)
-    assert ei.value.code == B.MOE_ERR_UNSUPPORTED
+        B.moe_forward(c, dev["x"], w, None, w, None, L.sched, L.out, None, L.ws)
+    assert ei.value.code == B.MOE_ERR_INVALID_ARG
+    cb = with_config("tiny", f=128)
+    c2 = cfg_struct(cb, minibatch_rows=128, ring_slots=2)
+    L2 = Layer(cb, c2)
+    with pytest.raises(B.MoeError) as ei:
+        B.moe_forward(c2, dev["x"], w, w, w, w, L2.sched, L2.out, None, L2.ws)
+    assert ei.value.code == B.MOE_ERR_INVALID_ARG
+    c3 = cfg_struct(cb, minibatch_rows=128, ring_slots=2, gather_ctas=100000)
+    L3 = Layer(cb, c3)
+    with pytest.raises(B.MoeError) as ei:
+        B.moe_forward(c3, dev["x"], w, None, w, None, L3.sched, L3.out, None, L3.ws)
+    assert ei.value.code == B.MOE_ERR_INVALID_ARG
+    torch.cuda.synchronize()
 
 
 @pytest.mark.slow
@@ -132,4 +146,79 @@ def test_kimi_zipf_ring_equals_chain():
     ref = _run(cfg, dev, save=False)
     for mb, gather in ((512, 0), (2368, 0), (4096, 0), (1024, 9)):
         L = _run(cfg, dev, mb, 4, gather, save=False)
+        assert _same(L.out, ref.out), (mb, gather)
+
+
+# ---------------------------------------------------------------- MXFP8
+def _quantized(dev):
+    out = {}
+    for name in ("W1", "W2"):
+        W = dev[name]
+        E, K, N = W.shape
+        q = torch.empty(E, N, K, dtype=torch.uint8, device="cuda")
+        s = torch.empty(E * N * K // 32, dtype=torch.uint8, device="cuda")
+        B.moe_quantize_mxfp8(W, E, K, N, q, s)
+        out[name] = (q, s)
+    return out
+
+
+def _run_mx(cfg, dev, wq, mb=0, slots=0, gather=0, save=True):
+    L = Layer(cfg, cfg_struct(cfg, prec="mxfp8", minibatch_rows=mb, ring_slots=slots, gather_ctas=gather))
+    L.schedule(dev["logits"])
+    L.forward(dev["x"], wq["W1"][0], wq["W2"][0], save=save, w1s=wq["W1"][1], w2s=wq["W2"][1])
+    torch.cuda.synchronize()
+    assert L.status() == 0
+    return L
+
+
+@pytest.mark.parametrize("name,kw,mbs", [
+    ("tiny", dict(f=128, d=256, T=300, E=6, k=3), [(128, 2), (256, 3)]),
+    ("tiny", dict(f=256, d=384, T=1, k=8), [(128, 2)]),
+    ("balanced", {}, [(1024, 2), (512, 4), (2368, 2), (8192, 2)]),
+])
+def test_mxfp8_ring_equals_chain_bitwise(name, kw, mbs):
+    cfg = with_config(name, prec="mxfp8", **kw)
+    inp = make_inputs(cfg, with_grad=False, x_std=1.0 if name == "tiny" else None)
+    dev = {k: v.cuda() for k, v in inp.items()}
+    wq = _quantized(dev)
+    ref = _run_mx(cfg, dev, wq)
+    rp = _rows_written(ref)
+    for mb, slots in mbs:
+        for gather in (0, 3):
+            L = _run_mx(cfg, dev, wq, mb, slots, gather)
+            assert _same(L.out, ref.out), (mb, slots, gather)
+            assert _same(L.saved["H"][:rp], ref.saved["H"][:rp])
+            assert _same(L.saved["A"][:rp], ref.saved["A"][:rp])
+    L = _run_mx(cfg, dev, wq, mbs[0][0], mbs[0][1], save=False)  # inference: no bf16 A / H
+    assert _same(L.out, ref.out)
+    ids, g = O.route(inp["logits"].numpy(), cfg.k)
+    toks = np.arange(0, cfg.T, max(1, cfg.T // 128))
+    want = O.forward_mxfp8(to_np(inp["x"]), ExpertView(inp["W1"]), ExpertView(inp["W2"]), ids, g, toks)
+    assert rel_err(ref.out.float().cpu().numpy()[toks], want) <= 6e-2
+
+
+def test_mxfp8_ring_bitwise_deterministic_over_10_runs():
+    cfg = with_config("balanced", prec="mxfp8")
+    dev = make_inputs(cfg, device="cuda", with_grad=False)
+    wq = _quantized(dev)
+    L = Layer(cfg, cfg_struct(cfg, prec="mxfp8", minibatch_rows=1024, ring_slots=4))
+    ref = None
+    for _ in range(10):
+        L.schedule(dev["logits"])
+        L.forward(dev["x"], wq["W1"][0], wq["W2"][0], save=False, w1s=wq["W1"][1], w2s=wq["W2"][1])
+        out = L.out.clone()
+        if ref is None:
+            ref = out
+        assert _same(out, ref)
+    assert L.status() == 0
+
+
+@pytest.mark.slow
+def test_kimi_mxfp8_ring_equals_chain():
+    cfg = CONFIGS["kimi_mxfp8"]
+    dev = make_inputs(cfg, device="cuda", with_grad=False)
+    wq = _quantized(dev)
+    ref = _run_mx(cfg, dev, wq, save=False)
+    for mb, gather in ((1024, 0), (2368, 0), (1024, 9)):
+        L = _run_mx(cfg, dev, wq, mb, 4, gather, save=False)
         assert _same(L.out, ref.out), (mb, gather)

@@ -328,3 +328,13 @@ def test_weight_gradient_row_blocks_start_at_each_expert_segment():
     # weigh 2^-16 of the 2^8 rows in each sum
     assert dev(seg) == 0.0
     assert dev(pos) > 1e-13
+
+
+def test_per_expert_variant_matches_the_full_backward():
+    x, W1, W2, ids, g, dO = _case(T=50, d=64, f=32, E=4, k=2, seed=9)
+    full = O.backward_mxfp8(x, W1, W2, ids, g, dO)
+    part = O.backward_mxfp8_experts(x, W1, W2, ids, g, dO, [0, 2, 3])
+    for e, (dW1, dW2, rows, dg_rows) in part.items():
+        np.testing.assert_array_equal(dW1, full["dW1"][e])
+        np.testing.assert_array_equal(dW2, full["dW2"][e])
+        np.testing.assert_array_equal(dg_rows, full["dg"].reshape(-1)[rows])
