@@ -105,7 +105,7 @@ def load_peaks():
 KERNEL_SOURCE = {"ring_forward": "ring.cu", "gather": "gather_merge.cu", "gather_x_dy": "gather_merge.cu",
                  "gather_mxfp8": "gather_merge.cu", "merge": "gather_merge.cu",
                  "reverse_dispatch": "gather_merge.cu", "dg_reduce": "gather_merge.cu",
-                 "sched_topk": "sched.cu", "sched_hist": "sched.cu", "sched_scatter": "sched.cu"}
+                 "sched_topk_hist": "sched.cu", "sched_hist": "sched.cu", "sched_scatter": "sched.cu"}
 
 
 def strip_comments(text):
@@ -617,7 +617,7 @@ def main():
                            "after the timed region" % n_tr})
     fwd_names = ("gather", "gather_mxfp8", "gemm1_swiglu", "gemm2", "gemm1_swiglu_mxfp8",
                  "gemm2_mxfp8", "merge", "ring_forward", "ring_forward_mxfp8")
-    sched_names = ("sched_topk", "sched_hist", "sched_scatter", "router_logits")
+    sched_names = ("sched_topk_hist", "sched_hist", "sched_scatter", "router_logits")
     fwd_ms = sum(per[n][1] for n in per if n in fwd_names) / n_tr
     sch_ms = sum(per[n][1] for n in per if n in sched_names) / n_tr
     bwd_ms = sum(per[n][1] for n in per if n not in fwd_names + sched_names) / n_tr
@@ -635,7 +635,7 @@ def main():
     layer = {"tflops": tflops,
              "tensor_frac_sustained": tflops / (peaks["bf16_sustained"] * fpk),
              "tensor_frac_burst": tflops / (peaks["bf16"] * fpk),
-            "peak_note": ("MXFP8 against 2x the bf16 peaks (nominal fp8:bf16 dense ratio 4.5:2.25)"
+             "peak_note": ("MXFP8 against 2x the bf16 peaks (nominal fp8:bf16 dense ratio 4.5:2.25)"
                           if cfg.prec == "mxfp8" else "bf16 peaks of MEASURED_PEAKS.json"),
              "weight_stream_ms": wbytes / (peaks["hbm_gbs"] * 1e9) * 1e3,
              "flop_ms_burst": flops / (peaks["bf16"] * fpk * 1e12) * 1e3,

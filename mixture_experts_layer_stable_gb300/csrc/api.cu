@@ -31,7 +31,7 @@ WsLayout ws_layout(const moe_config* c) {
   const int64_t nonempty = c->E < L.R ? c->E : L.R;
   L.Rp_max = (int64_t)align_up((size_t)(L.R + nonempty * (kBM - 1)), kBM);
   L.MT_max = L.Rp_max / kBM;
-  L.nblk = (L.R + kSchedChunk - 1) / kSchedChunk;
+  L.nblk = (c->T + sched_chunk_tokens(c->k) - 1) / sched_chunk_tokens(c->k);
   L.nt_dg = (c->f + 255) / 256;
   const size_t A = 1024;
   size_t off = 0;
@@ -173,8 +173,8 @@ moe_status moe_route(const moe_config* cfg, const moe_bf16* x, const moe_bf16* w
     e = router_gemm(c, w, reinterpret_cast<const __nv_bfloat16*>(x),
                     reinterpret_cast<const __nv_bfloat16*>(w_router), logits,
                     fused ? sched.topk_ids : nullptr, sched.topk_w, st);
-  if (e == cudaSuccess && !fused) e = launch_topk(c, logits, sched, st);
-  if (e == cudaSuccess) e = launch_schedule_tail(c, sched, w, st);
+  if (e == cudaSuccess)
+    e = fused ? launch_schedule_tail(c, sched, w, st) : launch_schedule_from_logits(c, logits, sched, w, st);
   return cuda_status(e);
 }
 

@@ -41,7 +41,10 @@ inline bool gemm_pair_enabled(const moe_config&, GemmKind k) {
   return k != kGemmWgrad;
 }
 
-constexpr int kSchedChunk = 1024;  // flat routed rows per histogram / scatter block
+constexpr int kSchedChunk = 1024;  // at most this many routed rows per histogram / scatter block
+// Tokens per schedule chunk: whole tokens (their k rows each), at most
+// kSchedChunk rows.
+__host__ __device__ inline int sched_chunk_tokens(int k) { return kSchedChunk / k > 0 ? kSchedChunk / k : 1; }
 constexpr int kSchedThreads = 256;
 constexpr int kMaxE = 1024;
 constexpr int kMaxK = 32;
@@ -104,9 +107,11 @@ struct TraceScope {
 // ---- launchers (return a cudaError_t from the launch) ----
 cudaError_t launch_schedule(const moe_config& c, const float* logits, const moe_sched& s,
                             const Ws& ws, cudaStream_t st);
-// The parts of it: top-k routing of fp32 logits, and the table from the ids
-// (histogram, scans, stable scatter; expects the header words zeroed).
-cudaError_t launch_topk(const moe_config& c, const float* logits, const moe_sched& s, cudaStream_t st);
+// The parts of it (both expect the header words zeroed): the table from
+// fp32 logits (top-k with the histograms, then the stable scatter), and the
+// table from ids chosen elsewhere (histograms, scans, stable scatter).
+cudaError_t launch_schedule_from_logits(const moe_config& c, const float* logits, const moe_sched& s,
+                                        const Ws& ws, cudaStream_t st);
 cudaError_t launch_schedule_tail(const moe_config& c, const moe_sched& s, const Ws& ws,
                                  cudaStream_t st);
 // dst [T, Epad] bf16 = src [T, E] fp32 rounded, zero in columns [E, Epad).

@@ -6,18 +6,21 @@
 // (same section; Marktechpost "Cursor开源MoK..." three design decisions:
 // one table serves all four transfer modes, at < 3 % of the MoE runtime).
 //
-// Three kernels, no host synchronisation:
-//  1. sched_topk: one warp per token, k rounds of a warp arg-max over the E
-//     fp32 logits (value descending, id ascending); weights = softmax over the
-//     k selected logits in fp32, summed in slot order.
-//  2. sched_hist: per chunk of kSchedChunk flat rows, an integer histogram
-//     over experts; the last block to finish (atomic ticket) turns the chunk
+// Two kernels after a clear of the header words, no host synchronisation.
+// Rows are handled in chunks of sched_chunk_tokens(k) tokens (their k rows
+// each, at most kSchedChunk rows):
+//  1. sched_topk_hist: per chunk, one warp per token runs k rounds of a warp
+//     arg-max over the E fp32 logits (value descending, id ascending);
+//     weights = softmax over the k selected logits in fp32, summed in slot
+//     order; the chunk's integer histogram over experts is counted in shared
+//     memory.  The last block to finish (atomic ticket) turns the chunk
 //     histograms into per-chunk exclusive prefixes and computes counts,
 //     offsets and the padded layout (each expert's segment rounded up to 128
 //     rows; prefixes over experts of their 128-row tiles and of their pairs
 //     of tiles).  Integer sums do not depend on order, so the table is
-//     deterministic.
-//  3. sched_scatter: every chunk re-walks its rows in index order and ranks
+//     deterministic.  (sched_hist does the histogram part alone, for ids
+//     chosen elsewhere: the router GEMM's fused top-k.)
+//  2. sched_scatter: every chunk re-walks its rows in index order and ranks
 //     each row among the earlier rows of the same expert (warp match + prefix
 //     over warps), which makes the permutation stable without atomics.
 #include <cuda_bf16.h>
@@ -35,20 +38,18 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
   return (v > bv) || (v == bv && i < bi);
 }
 
-__global__ void __launch_bounds__(kSchedThreads) sched_topk_kernel(
-    const float* __restrict__ logits, int T, int E, int k, int* __restrict__ ids,
-    float* __restrict__ wts) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
-  if (t >= T) return;
-  const int nchunk = (E + 31) >> 5;
-  float v[kMaxE / 32];
+// Top-k of token t by one warp, NCH chunks of 32 logits per lane (E <= 32 NCH):
+// lane j < k returns the j-th pick in *id and its weight in *w.
+template <int NCH>
+__device__ __forceinline__ void topk_token(const float* __restrict__ logits, int t, int E, int k,
+                                           int lane, int* id, float* w) {
+  float v[NCH];
   uint32_t taken = 0;
   const float* zrow = logits + (size_t)t * E;
 #pragma unroll
-  for (int c = 0; c < kMaxE / 32; ++c) {
+  for (int c = 0; c < NCH; ++c) {
     const int e = c * 32 + lane;
-    const bool in = c < nchunk && e < E;
+    const bool in = e < E;
     v[c] = in ? __ldg(zrow + e) : 0.f;
     if (!in) taken |= 1u << c;
   }
@@ -58,8 +59,8 @@ __global__ void __launch_bounds__(kSchedThreads) sched_topk_kernel(
     float bv = -INFINITY;
     int bi = 0x7fffffff;
 #pragma unroll
-    for (int c = 0; c < kMaxE / 32; ++c) {
-      if (c < nchunk && !((taken >> c) & 1u) && better(v[c], c * 32 + lane, bv, bi)) {
+    for (int c = 0; c < NCH; ++c) {
+      if (!((taken >> c) & 1u) && better(v[c], c * 32 + lane, bv, bi)) {
         bv = v[c];
         bi = c * 32 + lane;
       }
@@ -84,35 +85,18 @@ __global__ void __launch_bounds__(kSchedThreads) sched_topk_kernel(
   const float ex = (lane < k) ? expf(my_v - z0) : 0.f;
   float s = 0.f;
   for (int j = 0; j < k; ++j) s += __shfl_sync(0xffffffffu, ex, j);
-  if (lane < k) {
-    ids[(size_t)t * k + lane] = my_id;
-    wts[(size_t)t * k + lane] = ex / s;
-  }
+  *id = my_id;
+  *w = ex / s;
 }
 
-__global__ void __launch_bounds__(kSchedThreads) sched_hist_kernel(
-    const int* __restrict__ ids, int R, int E, int* __restrict__ hist, int* __restrict__ hdr,
-    int* __restrict__ counts, int* __restrict__ offsets, int* __restrict__ poff,
-    int* __restrict__ mt_off, int* __restrict__ pt_off) {
-  __shared__ int sh[kMaxE];
-  __shared__ int sh_last;
+// The last block of a chunked histogram pass: per-expert exclusive prefixes
+// over the chunks (in place), counts, offsets and the padded layout.
+__device__ void finish_histograms(int* __restrict__ hist, int nb, int E, int* __restrict__ hdr,
+                                  int* __restrict__ counts, int* __restrict__ offsets,
+                                  int* __restrict__ poff, int* __restrict__ mt_off,
+                                  int* __restrict__ pt_off, int* sh) {
   const int tid = threadIdx.x;
-  for (int e = tid; e < E; e += blockDim.x) sh[e] = 0;
-  __syncthreads();
-  const int r0 = blockIdx.x * kSchedChunk, r1 = min(R, r0 + kSchedChunk);
-  for (int r = r0 + tid; r < r1; r += blockDim.x) atomicAdd(&sh[ids[r]], 1);
-  __syncthreads();
-  for (int e = tid; e < E; e += blockDim.x) hist[(size_t)blockIdx.x * E + e] = sh[e];
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) sh_last = (atomicAdd(hdr + kHdrDone, 1) == (int)gridDim.x - 1);
-  __syncthreads();
-  if (!sh_last) return;
-  __threadfence();
-
-  // Last block: per-expert exclusive prefix over chunks (loads issued in
-  // batches so they overlap), then the scans over experts.
-  const int nb = gridDim.x;
+  // per-expert exclusive prefix over chunks (loads issued in batches so they overlap)
   for (int e = tid; e < E; e += blockDim.x) {
     int run = 0;
     for (int b0 = 0; b0 < nb; b0 += 8) {
@@ -153,16 +137,73 @@ __global__ void __launch_bounds__(kSchedThreads) sched_hist_kernel(
   }
 }
 
+// Top-k of the chunk's tokens (one warp per token) with the chunk's
+// histogram, then the table in the last block (see the file comment).
+template <int NCH>
+__global__ void __launch_bounds__(kSchedThreads) sched_topk_hist_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int tb, int* __restrict__ ids,
+    float* __restrict__ wts, int* __restrict__ hist, int* __restrict__ hdr, int* __restrict__ counts,
+    int* __restrict__ offsets, int* __restrict__ poff, int* __restrict__ mt_off,
+    int* __restrict__ pt_off) {
+  __shared__ int sh[kMaxE];
+  __shared__ int sh_last;
+  const int tid = threadIdx.x, lane = tid & 31;
+  for (int e = tid; e < E; e += blockDim.x) sh[e] = 0;
+  __syncthreads();
+  const int t0 = blockIdx.x * tb, t1 = min(T, t0 + tb);
+  for (int t = t0 + (tid >> 5); t < t1; t += kWarps) {
+    int id;
+    float w;
+    topk_token<NCH>(logits, t, E, k, lane, &id, &w);
+    if (lane < k) {
+      ids[(size_t)t * k + lane] = id;
+      wts[(size_t)t * k + lane] = w;
+      atomicAdd(&sh[id], 1);
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) hist[(size_t)blockIdx.x * E + e] = sh[e];
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) sh_last = (atomicAdd(hdr + kHdrDone, 1) == (int)gridDim.x - 1);
+  __syncthreads();
+  if (!sh_last) return;
+  __threadfence();
+  finish_histograms(hist, gridDim.x, E, hdr, counts, offsets, poff, mt_off, pt_off, sh);
+}
+
+__global__ void __launch_bounds__(kSchedThreads) sched_hist_kernel(
+    const int* __restrict__ ids, int R, int E, int cr, int* __restrict__ hist, int* __restrict__ hdr,
+    int* __restrict__ counts, int* __restrict__ offsets, int* __restrict__ poff,
+    int* __restrict__ mt_off, int* __restrict__ pt_off) {
+  __shared__ int sh[kMaxE];
+  __shared__ int sh_last;
+  const int tid = threadIdx.x;
+  for (int e = tid; e < E; e += blockDim.x) sh[e] = 0;
+  __syncthreads();
+  const int r0 = blockIdx.x * cr, r1 = min(R, r0 + cr);
+  for (int r = r0 + tid; r < r1; r += blockDim.x) atomicAdd(&sh[ids[r]], 1);
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) hist[(size_t)blockIdx.x * E + e] = sh[e];
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) sh_last = (atomicAdd(hdr + kHdrDone, 1) == (int)gridDim.x - 1);
+  __syncthreads();
+  if (!sh_last) return;
+  __threadfence();
+  finish_histograms(hist, gridDim.x, E, hdr, counts, offsets, poff, mt_off, pt_off, sh);
+}
+
 __global__ void __launch_bounds__(kSchedThreads) sched_scatter_kernel(
     const int* __restrict__ ids, const float* __restrict__ wts, int R, int E,
     const int* __restrict__ hist_prefix, const int* __restrict__ counts,
     const int* __restrict__ offsets, const int* __restrict__ poff, int* __restrict__ perm,
     int* __restrict__ inv, int* __restrict__ pos_pad, int* __restrict__ row_of_pad,
-    float* __restrict__ g_pad) {
+    float* __restrict__ g_pad, int cr) {
   __shared__ int wcnt[kWarps][kMaxE];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int r_begin = blockIdx.x * kSchedChunk;
-  const int r_end = min(R, r_begin + kSchedChunk);
+  const int r_begin = blockIdx.x * cr;
+  const int r_end = min(R, r_begin + cr);
   const int per_warp = (r_end - r_begin + kWarps - 1) / kWarps;
   const int w_begin = r_begin + warp * per_warp;
   const int w_end = min(r_end, w_begin + per_warp);
@@ -220,38 +261,58 @@ __global__ void __launch_bounds__(kSchedThreads) sched_scatter_kernel(
 
 }  // namespace
 
+namespace {
+cudaError_t launch_scatter(const moe_config& c, const moe_sched& s, const Ws& ws, cudaStream_t st) {
+  const int R = c.T * c.k;
+  TraceScope ts("sched_scatter", st);
+  sched_scatter_kernel<<<(int)ws.L.nblk, kSchedThreads, 0, st>>>(
+      s.topk_ids, s.topk_w, R, c.E, ws.hist(), s.counts, s.offsets, ws.poff(), s.perm, s.inv,
+      ws.pos_pad(), ws.row_of_pad(), ws.g_pad(), sched_chunk_tokens(c.k) * c.k);
+  return cudaGetLastError();
+}
+}  // namespace
+
 cudaError_t launch_schedule_tail(const moe_config& c, const moe_sched& s, const Ws& ws,
                                  cudaStream_t st) {
   const int R = c.T * c.k;
-  const int nchunk = (int)ws.L.nblk;
   cudaError_t err;
   {
     TraceScope ts("sched_hist", st);
-    sched_hist_kernel<<<nchunk, kSchedThreads, 0, st>>>(s.topk_ids, R, c.E, ws.hist(), ws.hdr(),
-                                                        s.counts, s.offsets, ws.poff(), ws.mt_off(),
-                                                        ws.pt_off());
+    sched_hist_kernel<<<(int)ws.L.nblk, kSchedThreads, 0, st>>>(
+        s.topk_ids, R, c.E, sched_chunk_tokens(c.k) * c.k, ws.hist(), ws.hdr(), s.counts, s.offsets,
+        ws.poff(), ws.mt_off(), ws.pt_off());
     err = cudaGetLastError();
   }
   if (err != cudaSuccess) return err;
-  TraceScope ts("sched_scatter", st);
-  sched_scatter_kernel<<<nchunk, kSchedThreads, 0, st>>>(
-      s.topk_ids, s.topk_w, R, c.E, ws.hist(), s.counts, s.offsets, ws.poff(), s.perm, s.inv,
-      ws.pos_pad(), ws.row_of_pad(), ws.g_pad());
-  return cudaGetLastError();
+  return launch_scatter(c, s, ws, st);
 }
 
-cudaError_t launch_topk(const moe_config& c, const float* logits, const moe_sched& s, cudaStream_t st) {
-  TraceScope ts("sched_topk", st);
-  sched_topk_kernel<<<(c.T + kWarps - 1) / kWarps, kSchedThreads, 0, st>>>(logits, c.T, c.E, c.k,
-                                                                          s.topk_ids, s.topk_w);
-  return cudaGetLastError();
+cudaError_t launch_schedule_from_logits(const moe_config& c, const float* logits, const moe_sched& s,
+                                        const Ws& ws, cudaStream_t st) {
+  const int nb = (int)ws.L.nblk, tb = sched_chunk_tokens(c.k);
+  cudaError_t err;
+  {
+    TraceScope ts("sched_topk_hist", st);
+    auto args = [&](auto kern) {
+      kern<<<nb, kSchedThreads, 0, st>>>(logits, c.T, c.E, c.k, tb, s.topk_ids, s.topk_w, ws.hist(),
+                                         ws.hdr(), s.counts, s.offsets, ws.poff(), ws.mt_off(),
+                                         ws.pt_off());
+    };
+    if (c.E <= 32) args(sched_topk_hist_kernel<1>);
+    else if (c.E <= 64) args(sched_topk_hist_kernel<2>);
+    else if (c.E <= 128) args(sched_topk_hist_kernel<4>);
+    else if (c.E <= 256) args(sched_topk_hist_kernel<8>);
+    else args(sched_topk_hist_kernel<kMaxE / 32>);
+    err = cudaGetLastError();
+  }
+  if (err != cudaSuccess) return err;
+  return launch_scatter(c, s, ws, st);
 }
 
 cudaError_t launch_schedule(const moe_config& c, const float* logits, const moe_sched& s,
                             const Ws& ws, cudaStream_t st) {
   cudaError_t err = cudaMemsetAsync(ws.hdr(), 0, kHdrWords * sizeof(int), st);
-  if (err == cudaSuccess) err = launch_topk(c, logits, s, st);
-  if (err == cudaSuccess) err = launch_schedule_tail(c, s, ws, st);
+  if (err == cudaSuccess) err = launch_schedule_from_logits(c, logits, s, ws, st);
   return err;
 }
 
