@@ -334,6 +334,8 @@ def parse():
     ap.add_argument("--gather-ctas", type=int, default=0, help="ring: 0 = gather warps in every CTA, G > 0 = G gather-only CTAs")
     ap.add_argument("--settle-s", type=float, default=1.0,
                     help="seconds of untimed steps after the warm-up, clocks sampled")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch every step's calls eagerly instead of replaying them as one CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--router", action="store_true",
                     help="route from x and a router weight (moe_route, plus the router backward) "
@@ -470,10 +472,34 @@ def main():
             if args.router:
                 B.moe_router_backward(c, x, w_router, dlog, dx_r, dw_r, ws)
 
+    # ---------------- the step as one CUDA graph: the library's calls are
+    # capturable (no synchronisation, no allocation); replaying the graph
+    # removes the host's per-call launch work from the step
+    graph = None
+    graph_note = "eager launches"
+    if not args.no_graph:
+        step()  # first calls outside capture: kernel attributes, occupancy queries
+        torch.cuda.synchronize()
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                step()
+            graph_note = "one CUDA graph per step (captured library calls)"
+        except Exception as ex:  # pragma: no cover - depends on the driver
+            graph = None
+            graph_note = f"eager launches (graph capture failed: {type(ex).__name__})"
+            torch.cuda.synchronize()
+
+    def run_step():
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
+
     # ---------------- warm-up, then untimed steps with the clocks sampled
     wa, wb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for i in range(max(args.warmup, 1)):
-        step()
+        run_step()
         if i == 0:
             wa.record()
     wb.record()
@@ -495,14 +521,14 @@ def main():
     t_load = time.time()
     n_settle = int(min(20000, max(0, args.settle_s * 1000.0 / max(est_ms, 1e-3))))
     for _ in range(n_settle):
-        step()
+        run_step()
 
     # ---------------- timed region (device-resident inputs, no tracing)
     barrier()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record()
     for _ in range(args.steps):
-        step()
+        run_step()
     ev1.record()
     barrier()
     clk = clocks.stop(since=t_load)
@@ -547,9 +573,15 @@ def main():
         k_e2e = args.e2e_steps or max(10, args.steps // 4)
 
         def e2e_step():
-            for k_, t in host.items():
-                dev_in[k_].copy_(t, non_blocking=True)
-            step(dev_in["logits"], dev_in["x"], dev_in.get("dOut"))
+            if graph is not None:
+                # the graph reads the inputs where it was captured
+                for k_, t in host.items():
+                    inp[k_].copy_(t, non_blocking=True)
+                graph.replay()
+            else:
+                for k_, t in host.items():
+                    dev_in[k_].copy_(t, non_blocking=True)
+                step(dev_in["logits"], dev_in["x"], dev_in.get("dOut"))
             h_out.copy_(out, non_blocking=True)
             if bwd:
                 h_dx.copy_(dx, non_blocking=True)
@@ -660,7 +692,7 @@ def main():
         "dtype": "e4m3 (mxfp8)" if cfg.prec == "mxfp8" else "bf16",
         "data": "synthetic (seeded torch generators on device; no dataset, random-init weights)",
         "config": {"workload": cfg.name, **workload_dict(cfg), "passes": passes, "prec": cfg.prec,
-                   "minibatch_rows": mb, "forward": fwd_desc,
+                   "minibatch_rows": mb, "forward": fwd_desc, "launch": graph_note,
                    "saved_activations": "H and A" if save else "none",
                    "routing": "router projection (moe_route)" if args.router else "synthetic logits",
                    "l2": "inputs larger than L2 (weights %.2f GB per step)" % (

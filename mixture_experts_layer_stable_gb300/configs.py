@@ -42,4 +42,9 @@ CONFIGS = {
                               logit_std=0.1, prec="mxfp8"),
     "kimi_bwd": LayerConfig("kimi_bwd", T=2048, d=7168, f=2048, E=256, k=8,
                             logit_std=1.0, zipf=1.2, passes="fwd+bwd"),
+    # the Kimi-like expert shape at a size whose profiler captures stay within
+    # a few GB of device memory (2.8 GB of weights, 22 of 32 experts with
+    # fewer than 128 rows, as most experts of the Zipf-routed layer)
+    "kimi_small": LayerConfig("kimi_small", T=512, d=7168, f=2048, E=32, k=8,
+                              logit_std=1.0, zipf=1.2),
 }
