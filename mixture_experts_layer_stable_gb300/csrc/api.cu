@@ -45,7 +45,8 @@ WsLayout ws_layout(const moe_config* c) {
   L.hist = take((size_t)L.nblk * c->E * sizeof(int));
   L.poff = take((size_t)(c->E + 1) * sizeof(int));
   L.mt_off = take((size_t)(c->E + 1) * sizeof(int));
-  L.pt_off = take((size_t)(c->E + 1) * sizeof(int));
+  L.E = c->E;
+  L.pt_off = take((size_t)3 * (c->E + 1) * sizeof(int));  // pairs, then heavy and light units
   L.pos_pad = take((size_t)L.R * sizeof(int));
   L.row_of_pad = take(rp * sizeof(int));
   L.g_pad = take(rp * sizeof(float));

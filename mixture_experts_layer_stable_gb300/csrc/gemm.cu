@@ -59,19 +59,47 @@ enum Epi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2, EPI_LOGITS = 3 };
 // the other half; the fp8 store variant has 3 stages to leave room for the
 // store staging tiles.  In pair mode a stage holds the CTA's 128 rows of A
 // and its half (128 columns) of B: 32 KB, so six stages fit.
-template <int EPI, bool FP8, bool WGRAD, bool PAIR>
+// Unit sets of the pair GEMMs: all units, or (split) the heavy units and
+// the light units as two kernels running side by side on every SM -- the
+// heavy kernel leaves room (shared memory, TMEM) for one light CTA per SM.
+// Their pipeline depths (stages) share one SM's shared memory.
+enum UnitSet { UNITS_ALL = 0, UNITS_HEAVY = 1, UNITS_LIGHT = 2 };
+#ifndef MOE_SPLIT_HEAVY_STAGES
+#define MOE_SPLIT_HEAVY_STAGES 3
+#endif
+#ifndef MOE_SPLIT_LIGHT_STAGES
+#define MOE_SPLIT_LIGHT_STAGES 4
+#endif
+
+template <int EPI, bool FP8, bool WGRAD, bool PAIR, int UM = UNITS_ALL>
 struct KCfg {
   static_assert(!(PAIR && FP8), "pair mode is bf16 only");
-  static constexpr int kStageBytes = kABytes + (PAIR ? kBHalfBytes : kBBytes);
-  static constexpr int kStages = PAIR ? 6 : (FP8 && EPI == EPI_STORE) ? 3 : 4;
+  static_assert(UM == UNITS_ALL || (PAIR && !WGRAD), "unit sets split the row pair GEMMs");
+  // a light unit's stage: its weight slice (MMA A) and at most 16 of its rows
+  // per CTA (MMA B, nt <= kLightRows)
+  static constexpr int kStageBytes = UM == UNITS_LIGHT ? kABytes + 16 * 128
+                                                       : kABytes + (PAIR ? kBHalfBytes : kBBytes);
+  static constexpr int kStages = UM == UNITS_HEAVY ? MOE_SPLIT_HEAVY_STAGES
+                                 : UM == UNITS_LIGHT ? MOE_SPLIT_LIGHT_STAGES
+                                 : PAIR ? 6 : (FP8 && EPI == EPI_STORE) ? 3 : 4;
   // swizzled staging tiles per epilogue warp for the TMA-store epilogues
-  static constexpr int kOutBufs = (EPI == EPI_STORE || (EPI != EPI_LOGITS && !FP8)) ? 2 : 0;
-  static constexpr int kAcc = FP8 ? 1 : 2;
+  // (light units only need their transpose tiles)
+  static constexpr int kOutBufs = (UM == UNITS_LIGHT && EPI == EPI_STORE) ? 1
+                                  : (EPI == EPI_STORE || (EPI != EPI_LOGITS && !FP8)) ? 2 : 0;
+  static constexpr int kAcc = (FP8 || UM == UNITS_HEAVY) ? 1 : 2;
+  // TMEM columns and the distance between accumulators
+  static constexpr uint32_t kTmemAlloc = UM == UNITS_HEAVY ? 256u : UM == UNITS_LIGHT ? 64u : 512u;
+  static constexpr uint32_t kAccStride = UM == UNITS_LIGHT ? (uint32_t)kLightRows : 256u;
   // scale-tile region rounded to 1024 bytes: the swizzled staging tiles after
   // it must start on a 1024-byte boundary for the 128-byte swizzle pattern
   static constexpr size_t kSfRegion = FP8 ? ((size_t)kStages * kSfBytes + 1023) / 1024 * 1024 : 0;
-  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kSfRegion +
-                                  (size_t)kEpiWarps * kOutBufs * kOutTile + 256;
+  // epilogue staging: kOutBufs swizzled tiles per warp; light SwiGLU units
+  // need only the gate warps' exchange buffers (32 x 32 fp32) and a
+  // transpose tile per warp
+  static constexpr bool kLightSwiglu = UM == UNITS_LIGHT && EPI == EPI_SWIGLU;
+  static constexpr size_t kStaging = kLightSwiglu ? 2 * 4096 + (size_t)kEpiWarps * kTrTile
+                                                  : (size_t)kEpiWarps * kOutBufs * kOutTile;
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kSfRegion + kStaging + 256;
   // the thin tiles' transpose tile lives in the warp's staging tiles
   static_assert(EPI != EPI_SWIGLU || FP8 || kOutBufs * kOutTile >= kTrTile, "transpose tile");
   static_assert(kSmem <= 232448, "shared memory budget");
@@ -89,6 +117,8 @@ struct Params {
   int out_rows;    // WGRAD: output height
   const int* mt_off;  // ROWS: [E+1] prefix of 128-row tiles per expert
   const int* pt_off;  // ROWS, pair mode: [E+1] prefix of tile pairs per expert
+  const int* hv_off;  // ROWS, pair mode: [E+1] prefix of heavy units per expert
+  const int* lt_off;  // ROWS, pair mode: [E+1] prefix of light units per expert
   const int* counts;  // WGRAD: [E] rows per expert
   const int* poff;    // WGRAD: [E+1] padded row prefix
   __nv_bfloat16* out0;  // SWIGLU: A [rows, f]      DSWIGLU: dH [rows, 2f]
@@ -130,11 +160,16 @@ struct Tile {
 
 // Work units: tiles, or in pair mode pairs of M-adjacent tiles of one expert
 // (the even CTA of the pair takes M tile 2j, the odd one 2j + 1).
-template <bool WGRAD, bool PAIR>
+template <int UM>
+__device__ __forceinline__ const int* pair_units(const Params& p) {
+  return UM == UNITS_HEAVY ? p.hv_off : UM == UNITS_LIGHT ? p.lt_off : p.pt_off;
+}
+
+template <bool WGRAD, bool PAIR, int UM = UNITS_ALL>
 __device__ __forceinline__ int total_units(const Params& p) {
   if (WGRAD) return p.E * (PAIR ? (p.m_tiles_w + 1) >> 1 : p.m_tiles_w) * p.n_tiles;
   if (p.mt_off == nullptr) return p.dense_mt * p.n_tiles;
-  return __ldg((PAIR ? p.pt_off : p.mt_off) + p.E) * p.n_tiles;
+  return __ldg((PAIR ? pair_units<UM>(p) : p.mt_off) + p.E) * p.n_tiles;
 }
 
 // Position L of a CTA's (cluster's) walk -> work unit.  Units are numbered
@@ -152,7 +187,7 @@ __device__ __forceinline__ int unit_at(int L, int total, int stride) {
   return back ? total - 1 - h : h;
 }
 
-template <bool WGRAD, bool PAIR>
+template <bool WGRAD, bool PAIR, int UM = UNITS_ALL>
 __device__ __forceinline__ Tile decode(const Params& p, int L, int rank) {
   Tile t;
   t.valid = true;
@@ -168,7 +203,7 @@ __device__ __forceinline__ Tile decode(const Params& p, int L, int rank) {
     t.nt = 0;
     t.thin = false;
   } else if (!WGRAD) {
-    const int* uoff = PAIR ? p.pt_off : p.mt_off;
+    const int* uoff = PAIR ? pair_units<UM>(p) : p.mt_off;
     const int e = find_expert(uoff, p.E, L / p.n_tiles);
     const int u0 = __ldg(uoff + e);
     const int ue = __ldg(uoff + e + 1) - u0;
@@ -180,7 +215,8 @@ __device__ __forceinline__ Tile decode(const Params& p, int L, int rank) {
     t.thin = false;
     if (PAIR) {
       const int me = __ldg(p.mt_off + e + 1) - m0;
-      mrel *= 2;
+      // a light unit is its expert's last tile; other units are pairs 2j, 2j+1
+      mrel = UM == UNITS_LIGHT ? me - 1 : 2 * mrel;
       if (p.thin && mrel + 1 == me) {
         // thin pair unit: the expert's last tile has no partner; both CTAs
         // compute it, each with half of the weight columns on M
@@ -291,14 +327,19 @@ __device__ __forceinline__ void for_each_box(const Params& p, const Tile& t, int
   }
 }
 
-template <bool WGRAD, bool A_MN, bool B_MN, int EPI, bool FP8, bool PAIR>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool WGRAD, bool A_MN, bool B_MN, int EPI, bool FP8, bool PAIR, int UM = UNITS_ALL>
+__global__ void __launch_bounds__(kThreads, UM == UNITS_ALL ? 1 : 2)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmA2,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmO,
                         const __grid_constant__ CUtensorMap tmO2, const Params p) {
-  using Cfg = KCfg<EPI, FP8, WGRAD, PAIR>;
+  using Cfg = KCfg<EPI, FP8, WGRAD, PAIR, UM>;
+  constexpr uint32_t kTmemAlloc = Cfg::kTmemAlloc;
+  constexpr uint32_t kAccStride = Cfg::kAccStride;
+  // split units: once every heavy CTA is resident, the light kernel queued
+  // behind this one in the stream may start on the room left on each SM
+  if constexpr (UM == UNITS_HEAVY) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int kStages = Cfg::kStages;
   constexpr int kAcc = Cfg::kAcc;
   constexpr int kStageB = Cfg::kStageBytes;
@@ -308,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* stages = smem;
   uint8_t* sfbuf = smem + (size_t)kStages * kStageB;  // fp8 scale tiles, kSfBytes a stage
   uint8_t* staging = sfbuf + Cfg::kSfRegion;
-  uint8_t* ctrl = staging + (size_t)kEpiWarps * Cfg::kOutBufs * kOutTile;
+  uint8_t* ctrl = staging + Cfg::kStaging;
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
@@ -344,10 +385,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 1) {
     if constexpr (PAIR) {
-      tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);  // both CTAs, collectively
+      tmem_alloc_pair(smem_u32(tmem_slot), kTmemAlloc);  // both CTAs, collectively
       tmem_relinquish_pair();
     } else {
-      tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+      tmem_alloc(smem_u32(tmem_slot), kTmemAlloc);
       tmem_relinquish();
     }
   }
@@ -356,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if constexpr (PAIR) cluster_sync();  // the peer's barriers exist before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int total = total_units<WGRAD, PAIR>(p);
+  const int total = total_units<WGRAD, PAIR, UM>(p);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -369,12 +410,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0, used = 0, last_par = 0;
       for (int L = unit0; L < total; L += ustride) {
         const int U = unit_at(L, total, ustride);
-        const Tile t = decode<WGRAD, PAIR>(p, U, rank);
+        const Tile t = decode<WGRAD, PAIR, UM>(p, U, rank);
         // bytes landing on this stage's "full" barrier (pair: both CTAs' copies)
         uint32_t tx = (t.valid ? (uint32_t)kABytes : 0u) + b_bytes + (FP8 ? (uint32_t)kSfBytes : 0u);
         if (PAIR && t.thin) tx = 16384u + (uint32_t)(t.nt / 2) * 128u;  // weights + half the rows
         if (PAIR && rank == 0)
-          tx += t.thin ? tx : (decode<WGRAD, PAIR>(p, U, 1).valid ? (uint32_t)kABytes : 0u) + b_bytes;
+          tx += t.thin ? tx : (decode<WGRAD, PAIR, UM>(p, U, 1).valid ? (uint32_t)kABytes : 0u) + b_bytes;
         for (int kb = 0; kb < t.kb_count; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status, 100 + s)) goto producer_done;
           const uint32_t sa = smem_u32(stages + (size_t)s * kStageB);
@@ -468,10 +509,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int s = 0, acc = 0;
       uint32_t ph = 0, aph = 0;
       for (int L = unit0; L < total; L += ustride) {
-        const Tile t = decode<WGRAD, PAIR>(p, unit_at(L, total, ustride), 0);
+        const Tile t = decode<WGRAD, PAIR, UM>(p, unit_at(L, total, ustride), 0);
         if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, p.status, 200 + acc)) goto mma_done;
         tc_fence_after();
-        const uint32_t dt = tmem_base + (uint32_t)acc * 256u;
+        const uint32_t dt = tmem_base + (uint32_t)acc * kAccStride;
         for (int kb = 0; kb < t.kb_count; ++kb) {
           if (!mbar_wait(&full[s], ph, abort_flag, p.status, 300 + s)) goto mma_done;
           tc_fence_after();
@@ -610,10 +651,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (++buf32 == 2 * Cfg::kOutBufs) buf32 = 0;
     };
     for (int L = unit0; L < total; L += ustride) {
-      const Tile t = decode<WGRAD, PAIR>(p, unit_at(L, total, ustride), rank);
+      const Tile t = decode<WGRAD, PAIR, UM>(p, unit_at(L, total, ustride), rank);
       if (!mbar_wait(&tfull[acc], aph, abort_flag, p.status, 400 + acc)) break;
       tc_fence_after();
-      const uint32_t tb = tmem_base + (uint32_t)acc * 256u + ((uint32_t)(q * 32) << 16);
+      const uint32_t tb = tmem_base + (uint32_t)acc * kAccStride + ((uint32_t)(q * 32) << 16);
       const bool zero = (t.kb_count == 0);
 
       if (!t.valid) {
@@ -713,8 +754,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
         const bool is_gate = q < 2;
-        uint8_t* tr = staging + (size_t)(warp - 2) * Cfg::kOutBufs * kOutTile + 4096;
-        float* xb = reinterpret_cast<float*>(staging + (size_t)(is_gate ? q : q - 2) * Cfg::kOutBufs * kOutTile);
+        uint8_t* tr = Cfg::kLightSwiglu ? staging + 2 * 4096 + (size_t)(warp - 2) * kTrTile
+                                        : staging + (size_t)(warp - 2) * Cfg::kOutBufs * kOutTile + 4096;
+        float* xb = reinterpret_cast<float*>(
+            staging + (size_t)(is_gate ? q : q - 2) * (Cfg::kLightSwiglu ? 4096 : Cfg::kOutBufs * kOutTile));
         const int c0 = t.n * p.hn + rank * 64 + (q & 1) * 32;
         for (int t0 = 0; t0 < kBM; t0 += 32) {
           float v[32];
@@ -967,18 +1010,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   if constexpr (PAIR) cluster_sync();  // the pair's MMAs and remote arrivals are done
   if (warp == 1) {
     tc_fence_after();
-    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, kTmemCols);
-    else tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, kTmemAlloc);
+    else tmem_dealloc(tmem_base, kTmemAlloc);
   }
+  // split units: the light kernel ends after the heavy one it runs beside,
+  // so the next kernel in the stream sees both finished
+  if constexpr (UM == UNITS_LIGHT) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ host side
-template <bool WGRAD, bool A_MN, bool B_MN, int EPI, bool FP8 = false, bool PAIR = false>
+template <bool WGRAD, bool A_MN, bool B_MN, int EPI, bool FP8 = false, bool PAIR = false, int UM = UNITS_ALL>
 cudaError_t launch(const char* name, const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b,
                    const CUtensorMap& o, const CUtensorMap& o2, const Params& p, long long max_units,
                    cudaStream_t st) {
-  auto kern = grouped_gemm_kernel<WGRAD, A_MN, B_MN, EPI, FP8, PAIR>;
-  const size_t smem = KCfg<EPI, FP8, WGRAD, PAIR>::kSmem;
+  auto kern = grouped_gemm_kernel<WGRAD, A_MN, B_MN, EPI, FP8, PAIR, UM>;
+  const size_t smem = KCfg<EPI, FP8, WGRAD, PAIR, UM>::kSmem;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   if constexpr (!PAIR) {
@@ -1002,6 +1048,21 @@ cudaError_t launch(const char* name, const CUtensorMap& a, const CUtensorMap& a2
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if constexpr (UM == UNITS_LIGHT) {
+      // beside the heavy kernel queued just before it: one CTA per SM, started
+      // as soon as every heavy CTA is resident (programmatic dependent launch)
+      cudaLaunchAttribute attr2[2] = {attr[0], {}};
+      attr2[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr2[1].val.programmaticStreamSerializationAllowed = 1;
+      long long clusters = num_sms() / 2;
+      if (max_units < clusters) clusters = max_units;
+      if (clusters < 1) clusters = 1;
+      cfg.gridDim = dim3((unsigned)(2 * clusters));
+      cfg.attrs = attr2;
+      cfg.numAttrs = 2;
+      TraceScope ts(name, st);
+      return cudaLaunchKernelEx(&cfg, kern, a, a2, b, o, o2, p);
+    }
     static int resident[64] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
@@ -1028,6 +1089,8 @@ Params base_params(const moe_config& c, const Ws& ws) {
   p.kstep = BK;
   p.mt_off = ws.mt_off();
   p.pt_off = ws.pt_off();
+  p.hv_off = ws.hv_off();
+  p.lt_off = ws.lt_off();
   p.poff = ws.poff();
   p.status = ws.hdr() + kHdrStatus;
   return p;
@@ -1060,6 +1123,16 @@ cudaError_t gemm_fwd1(const moe_config& c, const Ws& ws, const int* counts, cons
       !map2d(&to, A, c.f, rows, 64, 32) || (H != nullptr && !map2d(&th, H, 2ull * c.f, rows, 64, 32)))
     return cudaErrorInvalidValue;
   if (H == nullptr) th = to;
+  static_assert(KCfg<EPI_SWIGLU, false, false, true, UNITS_HEAVY>::kSmem +
+                    KCfg<EPI_SWIGLU, false, false, true, UNITS_LIGHT>::kSmem + 2048 <= 233472,
+                "heavy and light GEMM1 CTAs share an SM");
+  if (pair && p.thin && gemm_split_units(c)) {
+    const cudaError_t e = launch<false, false, true, EPI_SWIGLU, false, true, UNITS_HEAVY>(
+        name, ta, ta16, tb, to, th, p, ws.L.MT_max * p.n_tiles, st);
+    if (e != cudaSuccess) return e;
+    return launch<false, false, true, EPI_SWIGLU, false, true, UNITS_LIGHT>(
+        "gemm1_light", ta, ta16, tb, to, th, p, (long long)c.E * p.n_tiles, st);
+  }
   if (pair)
     return launch<false, false, true, EPI_SWIGLU, false, true>(name, ta, ta16, tb, to, th, p,
                                                                ws.L.MT_max * p.n_tiles, st);
@@ -1082,6 +1155,16 @@ cudaError_t gemm_fwd2(const moe_config& c, const Ws& ws, const int* counts, cons
   if (!map2d(&ta, A, c.f, rows, 64, kBM) || !map2d(&ta16, A, c.f, rows, 64, 16) ||
       !map3d(&tb, W2, c.d, c.f, c.E, 64, 64) || !map2d(&to, Yp, c.d, rows, 64, 32))
     return cudaErrorInvalidValue;
+  static_assert(KCfg<EPI_STORE, false, false, true, UNITS_HEAVY>::kSmem +
+                    KCfg<EPI_STORE, false, false, true, UNITS_LIGHT>::kSmem + 2048 <= 233472,
+                "heavy and light GEMM2 CTAs share an SM");
+  if (pair && p.thin && gemm_split_units(c)) {
+    const cudaError_t e = launch<false, false, true, EPI_STORE, false, true, UNITS_HEAVY>(
+        "gemm2", ta, ta16, tb, to, to, p, ws.L.MT_max * p.n_tiles, st);
+    if (e != cudaSuccess) return e;
+    return launch<false, false, true, EPI_STORE, false, true, UNITS_LIGHT>(
+        "gemm2_light", ta, ta16, tb, to, to, p, (long long)c.E * p.n_tiles, st);
+  }
   if (pair)
     return launch<false, false, true, EPI_STORE, false, true>("gemm2", ta, ta16, tb, to, to, p,
                                                               ws.L.MT_max * p.n_tiles, st);

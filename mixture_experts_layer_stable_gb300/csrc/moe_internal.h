@@ -41,6 +41,22 @@ inline bool gemm_pair_enabled(const moe_config&, GemmKind k) {
   return k != kGemmWgrad;
 }
 
+// Split units: a pair GEMM runs as two kernels side by side on every SM --
+// the heavy units (pairs of full tiles) with fewer pipeline stages and one
+// accumulator, and the light units (an expert's lone last tile of at most
+// kLightRows rows, which mostly streams its weight slice from HBM) in the
+// shared memory and TMEM left over -- so that the light units' weight
+// streaming overlaps the heavy units' tensor work.  MOE_SPLIT_UNITS=1 at
+// build time turns it on.
+#ifndef MOE_SPLIT_UNITS
+#define MOE_SPLIT_UNITS 0
+#endif
+inline bool gemm_split_units(const moe_config&) { return MOE_SPLIT_UNITS != 0; }
+
+// A light unit: an expert's lone last 128-row tile with at most this many
+// rows (the thin pair unit of an expert with a few rows), which streams its
+// weight slice with little to compute.
+constexpr int kLightRows = 32;
 constexpr int kSchedChunk = 1024;  // at most this many routed rows per histogram / scatter block
 // Tokens per schedule chunk: whole tokens (their k rows each), at most
 // kSchedChunk rows.
@@ -62,7 +78,7 @@ enum HdrWord {
 };
 
 struct WsLayout {
-  int64_t R = 0, Rp_max = 0, MT_max = 0, nblk = 0, nt_dg = 0;
+  int64_t R = 0, Rp_max = 0, MT_max = 0, nblk = 0, nt_dg = 0, E = 0;
   size_t hdr = 0, hist = 0, poff = 0, mt_off = 0, pt_off = 0, pos_pad = 0, row_of_pad = 0, g_pad = 0;
   size_t Xp = 0, Abuf = 0, Yp = 0, dYp = 0, dH = 0, gA = 0, dgp = 0, Aq = 0, ring = 0;
   size_t Hrc = 0;   // backward without saved activations: H recomputed [Rp, 2f]
@@ -84,6 +100,8 @@ struct Ws {
   int* poff() const { return reinterpret_cast<int*>(base + L.poff); }
   int* mt_off() const { return reinterpret_cast<int*>(base + L.mt_off); }
   int* pt_off() const { return reinterpret_cast<int*>(base + L.pt_off); }
+  int* hv_off() const { return pt_off() + (L.E + 1); }   // heavy units per expert (prefix)
+  int* lt_off() const { return pt_off() + 2 * (L.E + 1); }  // light units per expert (prefix)
   int* pos_pad() const { return reinterpret_cast<int*>(base + L.pos_pad); }
   int* row_of_pad() const { return reinterpret_cast<int*>(base + L.row_of_pad); }
   float* g_pad() const { return reinterpret_cast<float*>(base + L.g_pad); }

@@ -116,21 +116,33 @@ __device__ void finish_histograms(int* __restrict__ hist, int nb, int E, int* __
   }
   __syncthreads();
   if (tid == 0) {
-    int o = 0, po = 0, pt = 0;
+    // pt_off: work units of the CTA-pair GEMMs per expert (pairs of 128-row
+    // tiles, an odd last tile alone); hv_off / lt_off split them into heavy
+    // units and light ones (an odd last tile of at most kLightRows rows)
+    int* hv_off = pt_off + (E + 1);
+    int* lt_off = hv_off + (E + 1);
+    int o = 0, po = 0, pt = 0, hv = 0, lt = 0;
     for (int e = 0; e < E; ++e) {
       offsets[e] = o;
       poff[e] = po;
       mt_off[e] = po / kBM;
       pt_off[e] = pt;
+      hv_off[e] = hv;
+      lt_off[e] = lt;
       const int mt = (sh[e] + kBM - 1) / kBM;
+      const int light = ((mt & 1) && sh[e] - (mt - 1) * kBM <= kLightRows) ? 1 : 0;
       o += sh[e];
       po += mt * kBM;
       pt += (mt + 1) >> 1;
+      hv += ((mt + 1) >> 1) - light;
+      lt += light;
     }
     offsets[E] = o;
     poff[E] = po;
     mt_off[E] = po / kBM;
     pt_off[E] = pt;
+    hv_off[E] = hv;
+    lt_off[E] = lt;
     hdr[kHdrRpTotal] = po;
     hdr[kHdrMtTotal] = po / kBM;
     hdr[kHdrDone] = 0;
