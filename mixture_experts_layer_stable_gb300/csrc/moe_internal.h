@@ -57,7 +57,7 @@ inline bool gemm_split_units(const moe_config&) { return MOE_SPLIT_UNITS != 0; }
 // rows (the thin pair unit of an expert with a few rows), which streams its
 // weight slice with little to compute.
 constexpr int kLightRows = 32;
-constexpr int kSchedChunk = 1024;  // at most this many routed rows per histogram / scatter block
+constexpr int kSchedChunk = 256;  // at most this many routed rows per histogram / scatter block
 // Tokens per schedule chunk: whole tokens (their k rows each), at most
 // kSchedChunk rows.
 __host__ __device__ inline int sched_chunk_tokens(int k) { return kSchedChunk / k > 0 ? kSchedChunk / k : 1; }
