@@ -334,6 +334,8 @@ def parse():
     ap.add_argument("--gather-ctas", type=int, default=0, help="ring: 0 = gather warps in every CTA, G > 0 = G gather-only CTAs")
     ap.add_argument("--settle-s", type=float, default=1.0,
                     help="seconds of untimed steps after the warm-up, clocks sampled")
+    ap.add_argument("--tile-scheduler", choices=["static", "clc"], default=None,
+                    help="how the one-CTA weight-gradient GEMMs take their tiles (default: the library's)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every step's calls eagerly instead of replaying them as one CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -416,6 +418,8 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
+    if args.tile_scheduler is not None:
+        B.moe_set_tile_scheduler(1 if args.tile_scheduler == "clc" else 0)
     prec = B.MOE_MXFP8 if cfg.prec == "mxfp8" else B.MOE_BF16
     bwd = passes != "fwd"
     save = bwd or args.save
@@ -693,6 +697,7 @@ def main():
         "data": "synthetic (seeded torch generators on device; no dataset, random-init weights)",
         "config": {"workload": cfg.name, **workload_dict(cfg), "passes": passes, "prec": cfg.prec,
                    "minibatch_rows": mb, "forward": fwd_desc, "launch": graph_note,
+                   "tile_scheduler": ["static walk", "cluster launch control"][B.moe_get_tile_scheduler()],
                    "saved_activations": "H and A" if save else "none",
                    "routing": "router projection (moe_route)" if args.router else "synthetic logits",
                    "l2": "inputs larger than L2 (weights %.2f GB per step)" % (

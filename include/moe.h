@@ -124,7 +124,7 @@ int64_t moe_saved_rows(const moe_config* cfg);
 /* Smallest minibatch (rows) that gives the grouped GEMM at least two full
  * waves of tiles on compute_sms SMs: ceil(2 * compute_sms * bm * bn / n_cols)
  * with n_cols the GEMM's output width ([LP] 02 and [MT] three design
- * decisions: "at least two full SM waves"; for hidden 7168 / intermediate
+ * decisions: two full waves of tiles at least; for hidden 7168 / intermediate
  * 2048 the pages quote ~2,368 tokens).  Returns 0 on non-positive input. */
 int32_t moe_min_minibatch(int32_t compute_sms, int32_t bm, int32_t bn, int32_t n_cols);
 
@@ -189,7 +189,7 @@ moe_status moe_schedule_noalloc(const moe_config* cfg, const float* logits, moe_
                                 moe_stream_t stream);
 
 /* MXFP8 quantisation of weights for the MXFP8 forward ([LP] 02 MXFP8
- * paragraph; [MT] "BF16 and MXFP8 modes").  w: device bf16 [batch, K, N]
+ * paragraph; [MT] on the BF16 and MXFP8 modes).  w: device bf16 [batch, K, N]
  * (a W1 or W2 stack).  Writes q: e4m3 [batch, N, K] (K contiguous) and
  * scales: one UE8M0 byte per 32 consecutive K elements (batch*N*K/32 bytes;
  * scale 2^s with s the smallest exponent such that the block's max |v| <=
@@ -326,6 +326,20 @@ moe_status moe_read_status(const void* ws, moe_stream_t stream);
 
 /* Static English name of a status code. */
 const char* moe_status_string(moe_status s);
+
+/* How the one-CTA weight-gradient GEMMs (moe_backward, moe_backward_mxfp8)
+ * hand out their work units ([MT] three design decisions, last paragraph:
+ * the megakernel schedules its tiles with Blackwell's Cluster Launch
+ * Control).  0: a static walk -- a persistent grid of one CTA per SM, CTA i
+ * taking units i, i + grid, ...  1: cluster launch control -- a grid of one
+ * CTA per unit; each running CTA, while it works on a unit, has the hardware
+ * cancel the launch of a CTA that has not started yet and takes over that
+ * CTA's unit, so the units go to whichever SM frees up first.  Both give
+ * bitwise identical results (the same tiles, each computed whole by one
+ * CTA).  Process-wide, not thread-safe; takes effect for later calls.
+ * Returns MOE_ERR_INVALID_ARG for another mode. */
+moe_status moe_set_tile_scheduler(int32_t mode);
+int32_t moe_get_tile_scheduler(void);
 
 /* Tracing (profiling aid; the pages describe none).  moe_trace_enable(n)
  * creates 2n CUDA events on the current device; from then on every kernel the

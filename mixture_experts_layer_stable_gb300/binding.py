@@ -32,7 +32,7 @@ EXPORTED = [
     "moe_quantize_mxfp8", "moe_forward", "moe_backward", "moe_read_status", "moe_status_string",
     "moe_trace_enable", "moe_trace_count", "moe_trace_read", "moe_schedule_noalloc",
     "moe_route", "moe_router_backward", "moe_workspace_region", "moe_quantize_mxfp8_rows",
-    "moe_backward_mxfp8",
+    "moe_backward_mxfp8", "moe_set_tile_scheduler", "moe_get_tile_scheduler",
 ]
 
 MOE_WS_XQ_CODES = 0
@@ -119,6 +119,10 @@ def lib():
         L.moe_backward_mxfp8.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, moe_sched, savp, vp, vp, vp, vp,
                                          vp, vp, sz, vp]
         L.moe_backward_mxfp8.restype = ctypes.c_int
+        L.moe_set_tile_scheduler.argtypes = [i32]
+        L.moe_set_tile_scheduler.restype = ctypes.c_int
+        L.moe_get_tile_scheduler.argtypes = []
+        L.moe_get_tile_scheduler.restype = i32
         _lib = L
     return _lib
 
@@ -235,6 +239,15 @@ def moe_backward_mxfp8(cfg, dout, x, w1q, w1s, w2q, w2s, sched, saved, dx, dw1, 
                                     _ptr(w2q), _ptr(w2s), sched_struct(sched), sv, _ptr(dx), _ptr(dw1),
                                     _ptr(dw2), _ptr(dtopk_w), _ptr(dlogits), _ptr(ws),
                                     ws.numel() * ws.element_size(), _stream(stream)), "moe_backward_mxfp8")
+
+
+def moe_set_tile_scheduler(mode):
+    """0: static walk; 1: cluster launch control (one-CTA weight gradients)."""
+    _check(lib().moe_set_tile_scheduler(int(mode)), "moe_set_tile_scheduler")
+
+
+def moe_get_tile_scheduler():
+    return int(lib().moe_get_tile_scheduler())
 
 
 def moe_read_status(ws, stream=None):

@@ -9,6 +9,8 @@
 
 namespace moe {
 
+int g_tile_scheduler = MOE_GEMM_CLC ? 1 : 0;
+
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 bool config_valid(const moe_config* c) {
@@ -480,6 +482,14 @@ moe_status moe_trace_read(int32_t i, const char** name, float* ms) {
   *name = g_trace.names[i];
   return MOE_OK;
 }
+
+moe_status moe_set_tile_scheduler(int32_t mode) {
+  if (mode != 0 && mode != 1) return MOE_ERR_INVALID_ARG;
+  g_tile_scheduler = mode;
+  return MOE_OK;
+}
+
+int32_t moe_get_tile_scheduler(void) { return g_tile_scheduler; }
 
 const char* moe_status_string(moe_status s) {
   switch (s) {

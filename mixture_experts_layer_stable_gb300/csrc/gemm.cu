@@ -99,7 +99,7 @@ struct KCfg {
   static constexpr bool kLightSwiglu = UM == UNITS_LIGHT && EPI == EPI_SWIGLU;
   static constexpr size_t kStaging = kLightSwiglu ? 2 * 4096 + (size_t)kEpiWarps * kTrTile
                                                   : (size_t)kEpiWarps * kOutBufs * kOutTile;
-  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kSfRegion + kStaging + 256;
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kSfRegion + kStaging + 512;
   // the thin tiles' transpose tile lives in the warp's staging tiles
   static_assert(EPI != EPI_SWIGLU || FP8 || kOutBufs * kOutTile >= kTrTile, "transpose tile");
   static_assert(kSmem <= 232448, "shared memory budget");
@@ -327,7 +327,16 @@ __device__ __forceinline__ void for_each_box(const Params& p, const Tile& t, int
   }
 }
 
-template <bool WGRAD, bool A_MN, bool B_MN, int EPI, bool FP8, bool PAIR, int UM = UNITS_ALL>
+// CLC: a grid of one CTA per work unit (an upper bound; units past the
+// schedule's total are skipped).  Each CTA takes its own unit first, and
+// while working on one asks the hardware (cluster launch control) to cancel
+// the launch of a CTA that has not started yet and takes that CTA's unit
+// next; the producer hands the units to the MMA and epilogue warps through
+// a small queue in shared memory.  One-CTA (not pair) kernels only.
+constexpr int kQ = 4;  // depth of the queue of units
+
+template <bool WGRAD, bool A_MN, bool B_MN, int EPI, bool FP8, bool PAIR, int UM = UNITS_ALL,
+          bool CLC = false>
 __global__ void __launch_bounds__(kThreads, UM == UNITS_ALL ? 1 : 2)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmA2,
@@ -335,6 +344,7 @@ __global__ void __launch_bounds__(kThreads, UM == UNITS_ALL ? 1 : 2)
                         const __grid_constant__ CUtensorMap tmO,
                         const __grid_constant__ CUtensorMap tmO2, const Params p) {
   using Cfg = KCfg<EPI, FP8, WGRAD, PAIR, UM>;
+  static_assert(!(CLC && PAIR), "the cluster-launch-control schedule is for one-CTA kernels");
   constexpr uint32_t kTmemAlloc = Cfg::kTmemAlloc;
   constexpr uint32_t kAccStride = Cfg::kAccStride;
   // split units: once every heavy CTA is resident, the light kernel queued
@@ -357,6 +367,12 @@ __global__ void __launch_bounds__(kThreads, UM == UNITS_ALL ? 1 : 2)
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // CLC: the queue of units and the cancel request's barrier and response
+  uint64_t* qfull = reinterpret_cast<uint64_t*>(ctrl + 256);
+  uint64_t* qempty = qfull + kQ;
+  uint64_t* cbar = qempty + kQ;
+  int* qunit = reinterpret_cast<int*>(cbar + 1);
+  const uint32_t cresp = smem_u32(ctrl + 256 + 96);  // 16-byte aligned
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Pair mode: the two CTAs of a cluster walk the same work units; the even
@@ -375,6 +391,13 @@ __global__ void __launch_bounds__(kThreads, UM == UNITS_ALL ? 1 : 2)
       mbar_init(&tempty[a], PAIR ? 2 * kEpiWarps : kEpiWarps * 32);
     }
     mbar_init(drain, 1);
+    if constexpr (CLC) {
+      for (int i = 0; i < kQ; ++i) {
+        mbar_init(&qfull[i], 1);
+        mbar_init(&qempty[i], 1 + kEpiWarps);
+      }
+      mbar_init(cbar, 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -398,6 +421,23 @@ __global__ void __launch_bounds__(kThreads, UM == UNITS_ALL ? 1 : 2)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total = total_units<WGRAD, PAIR, UM>(p);
+  // unit j of this CTA for the MMA and epilogue roles: the static walk, or
+  // the queue the producer fills (CLC); -1 ends the walk, units past the
+  // total are skipped
+  auto unit_of = [&](int j, bool& ok) -> int {
+    ok = true;
+    if constexpr (CLC) {
+      ok = mbar_wait(&qfull[j % kQ], (j / kQ) & 1, abort_flag, p.status, 170);
+      if (!ok) return -1;
+      const int U = qunit[j % kQ];
+      __syncwarp(__activemask());  // every lane of the role has read the slot
+      if ((threadIdx.x & 31) == 0) mbar_arrive(&qempty[j % kQ]);
+      return U;
+    } else {
+      const int L = unit0 + j * ustride;
+      return L < total ? unit_at(L, total, ustride) : -1;
+    }
+  };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -408,8 +448,29 @@ __global__ void __launch_bounds__(kThreads, UM == UNITS_ALL ? 1 : 2)
                                        : (uint32_t)(PAIR ? kBHalfBytes : kBBytes));
       int s = 0;
       uint32_t ph = 0, used = 0, last_par = 0;
-      for (int L = unit0; L < total; L += ustride) {
-        const int U = unit_at(L, total, ustride);
+      const uint64_t pol_stream = l2_policy_evict_first();  // weights streamed once (thin units)
+      int cur = (int)blockIdx.x;  // CLC: this CTA's own unit first
+      uint32_t cph = 0;
+      bool pending = false;       // CLC: a cancel request in flight
+      for (int j = 0;; ++j) {
+        int U;
+        if constexpr (CLC) {
+          if (!mbar_wait(&qempty[j % kQ], ((j / kQ) & 1) ^ 1, abort_flag, p.status, 150)) goto producer_done;
+          qunit[j % kQ] = cur;
+          mbar_arrive(&qfull[j % kQ]);
+          if (cur < 0) break;
+          // ask for the next unit while this one's operands go out
+          mbar_arrive_expect_tx(cbar, 16);
+          clc_try_cancel(cresp, smem_u32(cbar));
+          pending = true;
+          U = cur;
+        } else {
+          const int L = unit0 + j * ustride;
+          if (L >= total) break;
+          U = unit_at(L, total, ustride);
+        }
+        if (CLC && U >= total) goto next_unit;
+        {
         const Tile t = decode<WGRAD, PAIR, UM>(p, U, rank);
         // bytes landing on this stage's "full" barrier (pair: both CTAs' copies)
         uint32_t tx = (t.valid ? (uint32_t)kABytes : 0u) + b_bytes + (FP8 ? (uint32_t)kSfBytes : 0u);
@@ -461,17 +522,24 @@ __global__ void __launch_bounds__(kThreads, UM == UNITS_ALL ? 1 : 2)
               // thin pair unit: this CTA's weight columns as the MMA's A --
               // SwiGLU: 64 gate and the matching 64 up columns; otherwise 128
               // output columns (MN-major, or K-major rows for dgrad) -- then its
-              // half of the rows in 16-row boxes (the MMA's B, K-major)
+              // half of the rows in 16-row boxes (the MMA's B, K-major).  The
+              // weight slice is read by this unit alone: it goes into L2 with
+              // evict-first priority, so the stream does not push out the
+              // row tiles and weight slices other units read again
+              auto loadw = [&](uint32_t off, int c0, int c1) {
+                if constexpr (PAIR) tma_load_3d_pair_hint(sa + off, &tmB, fb, c0, c1, t.e, pol_stream);
+                else tma_load_3d_hint(sa + off, &tmB, fb, c0, c1, t.e, pol_stream);
+              };
               if (EPI == EPI_SWIGLU) {
                 const int c0 = t.n * p.hn + rank * 64;
-                load3(0u, &tmB, c0, kb * BK, t.e);
-                load3(8192u, &tmB, p.f + c0, kb * BK, t.e);
+                loadw(0u, c0, kb * BK);
+                loadw(8192u, p.f + c0, kb * BK);
               } else if (B_MN) {
                 const int c0 = t.n * 256 + rank * 128;
-                load3(0u, &tmB, c0, kb * BK, t.e);
-                load3(8192u, &tmB, c0 + 64, kb * BK, t.e);
+                loadw(0u, c0, kb * BK);
+                loadw(8192u, c0 + 64, kb * BK);
               } else {
-                load3(0u, &tmB, kb * BK, t.n * 256 + rank * 128, t.e);
+                loadw(0u, kb * BK, t.n * 256 + rank * 128);
               }
               const int nt2 = t.nt / 2;
               for (int i = 0; i < nt2; i += 16)
@@ -487,8 +555,19 @@ __global__ void __launch_bounds__(kThreads, UM == UNITS_ALL ? 1 : 2)
             ph ^= 1u;
           }
         }
+        }
+      next_unit:
+        if constexpr (CLC) {
+          if (!mbar_wait(cbar, cph, abort_flag, p.status, 180)) goto producer_done;
+          pending = false;
+          cph ^= 1u;
+          cur = clc_canceled_x(cresp);
+          fence_proxy_async_smem();  // the response is read before the next request overwrites it
+        }
       }
     producer_done:
+      // no cancel request may still be writing into shared memory at exit
+      if (CLC && pending) mbar_wait_drain(cbar, cph);
       // every issued copy has landed before the CTA can exit (in pair mode the
       // even CTA's "full" barriers also count the odd CTA's copies)
       if (!PAIR || rank == 0)
@@ -508,8 +587,13 @@ __global__ void __launch_bounds__(kThreads, UM == UNITS_ALL ? 1 : 2)
       const uint32_t idesc = idesc_bf16(PAIR ? 2 * kBM : kBM, p.umma_n, A_MN, B_MN);
       int s = 0, acc = 0;
       uint32_t ph = 0, aph = 0;
-      for (int L = unit0; L < total; L += ustride) {
-        const Tile t = decode<WGRAD, PAIR, UM>(p, unit_at(L, total, ustride), 0);
+      for (int j = 0;; ++j) {
+        bool ok;
+        const int U = unit_of(j, ok);
+        if (!ok) goto mma_done;
+        if (U < 0) break;
+        if (CLC && U >= total) continue;
+        const Tile t = decode<WGRAD, PAIR, UM>(p, U, 0);
         if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, p.status, 200 + acc)) goto mma_done;
         tc_fence_after();
         const uint32_t dt = tmem_base + (uint32_t)acc * kAccStride;
@@ -650,8 +734,12 @@ __global__ void __launch_bounds__(kThreads, UM == UNITS_ALL ? 1 : 2)
       }
       if (++buf32 == 2 * Cfg::kOutBufs) buf32 = 0;
     };
-    for (int L = unit0; L < total; L += ustride) {
-      const Tile t = decode<WGRAD, PAIR, UM>(p, unit_at(L, total, ustride), rank);
+    for (int j = 0;; ++j) {
+      bool ok;
+      const int U = unit_of(j, ok);
+      if (!ok || U < 0) break;
+      if (CLC && U >= total) continue;
+      const Tile t = decode<WGRAD, PAIR, UM>(p, U, rank);
       if (!mbar_wait(&tfull[acc], aph, abort_flag, p.status, 400 + acc)) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + (uint32_t)acc * kAccStride + ((uint32_t)(q * 32) << 16);
@@ -1019,15 +1107,22 @@ __global__ void __launch_bounds__(kThreads, UM == UNITS_ALL ? 1 : 2)
 }
 
 // ------------------------------------------------------------------ host side
-template <bool WGRAD, bool A_MN, bool B_MN, int EPI, bool FP8 = false, bool PAIR = false, int UM = UNITS_ALL>
+template <bool WGRAD, bool A_MN, bool B_MN, int EPI, bool FP8 = false, bool PAIR = false, int UM = UNITS_ALL,
+          bool CLC = false>
 cudaError_t launch(const char* name, const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b,
                    const CUtensorMap& o, const CUtensorMap& o2, const Params& p, long long max_units,
                    cudaStream_t st) {
-  auto kern = grouped_gemm_kernel<WGRAD, A_MN, B_MN, EPI, FP8, PAIR, UM>;
+  auto kern = grouped_gemm_kernel<WGRAD, A_MN, B_MN, EPI, FP8, PAIR, UM, CLC>;
   const size_t smem = KCfg<EPI, FP8, WGRAD, PAIR, UM>::kSmem;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  if constexpr (!PAIR) {
+  if constexpr (CLC) {
+    // one CTA per unit; the running CTAs cancel the launches of the others
+    if (max_units < 1 || max_units > 0x7fffffffLL) return cudaErrorInvalidValue;
+    TraceScope ts(name, st);
+    kern<<<(unsigned)max_units, kThreads, smem, st>>>(a, a2, b, o, o2, p);
+    return cudaGetLastError();
+  } else if constexpr (!PAIR) {
     long long grid = num_sms();
     if (max_units < grid) grid = max_units;
     if (grid < 1) grid = 1;
@@ -1244,6 +1339,9 @@ cudaError_t gemm_wgrad(const moe_config& c, const Ws& ws, const moe_sched& s,
   if (gemm_pair_enabled(c, kGemmWgrad))
     return launch<true, true, true, EPI_STORE, false, true>(
         name, ta, ta, tb, to, to, p, (long long)c.E * ((p.m_tiles_w + 1) / 2) * p.n_tiles, st);
+  if (gemm_clc_enabled(c))
+    return launch<true, true, true, EPI_STORE, false, false, UNITS_ALL, true>(
+        name, ta, ta, tb, to, to, p, (long long)c.E * p.m_tiles_w * p.n_tiles, st);
   return launch<true, true, true, EPI_STORE>(name, ta, ta, tb, to, to, p,
                                              (long long)c.E * p.m_tiles_w * p.n_tiles, st);
 }
@@ -1446,6 +1544,9 @@ cudaError_t gemm_wgrad_mx(const moe_config& c, const Ws& ws, const moe_sched& s,
   if (!map2d(&ta, AqT, ldt, (uint64_t)M, 128, kBM, true) || !map3d(&tb, BqT, ldt, (uint64_t)N, 1, 128, 256, true) ||
       !map3d(&to, dW, N, M, c.E, 64, 32))
     return cudaErrorInvalidValue;
+  if (gemm_clc_enabled(c))
+    return launch<true, false, false, EPI_STORE, true, false, UNITS_ALL, true>(
+        name, ta, ta, tb, to, to, p, (long long)c.E * p.m_tiles_w * p.n_tiles, st);
   return launch<true, false, false, EPI_STORE, true>(name, ta, ta, tb, to, to, p,
                                                      (long long)c.E * p.m_tiles_w * p.n_tiles, st);
 }

@@ -53,6 +53,17 @@ inline bool gemm_pair_enabled(const moe_config&, GemmKind k) {
 #endif
 inline bool gemm_split_units(const moe_config&) { return MOE_SPLIT_UNITS != 0; }
 
+// The one-CTA weight-gradient GEMMs can take their work units from the
+// hardware's cluster launch control instead of a static walk: a grid of one
+// CTA per unit, the running CTAs cancelling the launches of the pending ones
+// and taking over their units.  Chosen process-wide with
+// moe_set_tile_scheduler (default MOE_GEMM_CLC at build time).
+#ifndef MOE_GEMM_CLC
+#define MOE_GEMM_CLC 0
+#endif
+extern int g_tile_scheduler;  // 0 static walk, 1 cluster launch control
+inline bool gemm_clc_enabled(const moe_config&) { return g_tile_scheduler == 1; }
+
 // A light unit: an expert's lone last 128-row tile with at most this many
 // rows (the thin pair unit of an expert with a few rows), which streams its
 // weight slice with little to compute.

@@ -350,7 +350,7 @@ def backward_tokens(x, W1, W2, ids, g, dOut, tokens):
 
 
 # --------------------------------------------------------------------------
-# MXFP8 ([LP] 02, MXFP8 paragraph; [MT] "BF16 and MXFP8 precision modes").
+# MXFP8 ([LP] 02, MXFP8 paragraph; [MT] three design decisions, on its BF16 and MXFP8 modes).
 # The pages do not give the block format; the reading is the OCP MX format:
 # blocks of 32 consecutive elements along the contraction dimension share a
 # UE8M0 power-of-two scale 2^s; elements are FP8 E4M3 (bias 7, max 448,
@@ -516,9 +516,10 @@ def _expert_backward_mxfp8(Xe, W1e, W2e, ge, dOe, q):
 def backward_mxfp8(x, W1, W2, ids, g, dOut, qdq=None, quantise=None):
     """Full backward with MXFP8 operands.
 
-    Reading (the pages name an MXFP8 mode for the layer, [MT] "BF16 and MXFP8
-    precision modes", and put the quantisation on the GEMMs' data path, [LP]
-    02, but do not say how the backward quantises): every GEMM quantises both
+    Reading (the pages name an MXFP8 mode for the layer, [MT] three design
+    decisions, on its BF16 and MXFP8 modes, and put the quantisation on the
+    GEMMs' data path, [LP] 02, but do not say how the backward quantises):
+    every GEMM quantises both
     of its operands along its own contraction dimension, in blocks of 32 with
     the scale rule above; for the weight-gradient GEMMs that dimension is the
     expert's rows in the stable expert order, blocked from the start of the

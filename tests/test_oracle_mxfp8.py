@@ -1,5 +1,5 @@
 """Pins for the oracle's MXFP8 quantiser (activation quantisation on the
-dispatch / SwiGLU data path, leiphone "MoK..." 02; "BF16 and MXFP8 modes",
+dispatch / SwiGLU data path, leiphone "MoK..." 02; the BF16 and MXFP8 modes of
 Marktechpost "Cursor开源MoK..." three design decisions).  Block format read
 as OCP MX: 32 elements share a UE8M0 scale, elements are FP8 E4M3."""
 import numpy as np

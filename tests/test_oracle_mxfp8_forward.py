@@ -1,5 +1,5 @@
 """Pins of the oracle's MXFP8 forward (activation quantisation on the dispatch
-and SwiGLU data path, leiphone "MoK..." 02; "BF16 and MXFP8 precision modes",
+and SwiGLU data path, leiphone "MoK..." 02; the BF16 and MXFP8 modes of
 Marktechpost "Cursor开源MoK..." three design decisions).  Reading: each GEMM
 quantises both operands along its own contraction dimension -- x and W1 along
 d, the SwiGLU output A and W2 along f -- in OCP MX blocks of 32.
