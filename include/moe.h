@@ -63,15 +63,16 @@ typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_precision;
  *   Limits: 1 <= k <= min(E, 32); 1 <= E <= 1024; T >= 1; d and f multiples
  *   of 64 (d also of 128 in MXFP8 mode).
  *   minibatch_rows: 0 runs the layer as a chain of kernels over the whole
- *     expert-ordered buffer.  > 0 runs the BF16 forward as one persistent
- *     cooperative kernel that hands windows of this many expert-ordered rows
+ *     expert-ordered buffer.  > 0 runs the forward (BF16 or MXFP8) as one
+ *     persistent cooperative kernel that hands windows of this many expert-ordered rows
  *     (rounded up to a multiple of 128) from gather warps or CTAs to GEMM
  *     warps through a ring of ring_slots slots, with GPU-side counters and
  *     the weighted merge at the end ([LP] 02: SM partition, local counters,
  *     minibatch, ring token buffer).  Results are bitwise identical to the chain path
- *     for every window size.  MXFP8 with minibatch_rows > 0 returns
- *     MOE_ERR_UNSUPPORTED.  The backward runs as a chain of kernels; it
- *     reuses the rows the ring still holds (see moe_backward).
+ *     of the same precision for every window size (in MXFP8 mode the gather
+ *     side quantises each window's rows into the ring slot).  The backward
+ *     runs as a chain of kernels; after a BF16 ring forward it reuses the
+ *     rows the ring still holds (see moe_backward).
  *   ring_slots: ring depth, 2..64, when minibatch_rows > 0.
  *   gather_ctas: how the work is split when minibatch_rows > 0.  0 (the
  *     default): every CTA runs the GEMM warps and one gather warp, so all
