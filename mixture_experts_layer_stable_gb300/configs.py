@@ -42,6 +42,11 @@ CONFIGS = {
                               logit_std=0.1, prec="mxfp8"),
     "kimi_bwd": LayerConfig("kimi_bwd", T=2048, d=7168, f=2048, E=256, k=8,
                             logit_std=1.0, zipf=1.2, passes="fwd+bwd"),
+    # one GPU's share of the pages' expert-parallel run (64-way: 4 experts of
+    # the Kimi-like shape and about 4,096 rows each per GPU), reproduced on one
+    # GPU as k = 1 over 4 experts: the compute-bound end of the layer
+    "local_slice": LayerConfig("local_slice", T=16384, d=7168, f=2048, E=4, k=1,
+                               logit_std=0.1),
     # the Kimi-like expert shape at a size whose profiler captures stay within
     # a few GB of device memory (2.8 GB of weights, 22 of 32 experts with
     # fewer than 128 rows, as most experts of the Zipf-routed layer)

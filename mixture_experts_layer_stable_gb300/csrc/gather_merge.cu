@@ -1,11 +1,16 @@
 // gather_merge.cu -- the memory-bound steps of the layer.
 //
-//  * gather (dispatch by pull, leiphone "MoK..." section 02): the expert side
-//    reads each routed token row from its source position and lays rows out
-//    in expert order.  On one GPU this is an HBM row gather into the padded
-//    expert-ordered buffer.  The forward's gather leaves padding rows alone
-//    (GEMM1 zeroes what it computes from them); the backward's writes them as
-//    zeros, which the weight gradients' K loop over padded rows relies on.
+//  * gather (dispatch, leiphone "MoK..." section 02): every routed token row
+//    lands in its expert's segment of the padded expert-ordered buffer.  On
+//    one GPU this is an HBM row copy.  Without a ring it walks the tokens:
+//    each token row is read from HBM once and written from shared memory to
+//    its k positions (the buffer a pull by the expert side would build, with
+//    each source row read once instead of k times).  After a ring forward the
+//    backward's gather walks the padded rows instead (the pull order), so
+//    that it can take the rows the ring still holds.  The forward's gather
+//    leaves padding rows alone (GEMM1 zeroes what it computes from them); the
+//    backward's writes them as zeros, which the weight gradients' K loop over
+//    padded rows relies on.
 //  * merge (combine + final weighted merge, leiphone section 03): each token
 //    sums its k expert outputs in slot order in fp32 and rounds once to bf16.
 //    The same kernel without weights is the backward's reverse dispatch.
@@ -13,7 +18,8 @@
 //    of the fused SwiGLU backward (Marktechpost "Cursor开源MoK..." three design
 //    decisions, last paragraph), and its softmax backward to the logits.
 //  * MXFP8 quantisation (leiphone section 02, MXFP8 paragraph): fused into the
-//    gather for activations; a separate pass for weights.
+//    gather for activations (each token row quantised once, its codes and
+//    scales written to its k positions); a separate pass for weights.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -21,6 +27,17 @@
 
 #ifndef MOE_BULK_GATHER
 #define MOE_BULK_GATHER 1  // 0: the plain-load gather everywhere
+#endif
+
+// L2 priorities of the gathers' copies.  A token's k rows lie in k different
+// experts' segments, so its source row is read again only after a large part
+// of the (larger than L2) gathered buffer has been written; the gathered rows
+// themselves are read again only by the next kernel, which starts from the
+// first rows.  1: the gathered rows are written evict-first, so that the
+// source rows stay in L2 between their k reads; 2: the source rows are in
+// addition read evict-last; 0: no policy.
+#ifndef MOE_GATHER_L2
+#define MOE_GATHER_L2 1
 #endif
 
 #include "bulk_rows.cuh"
@@ -121,6 +138,9 @@ __global__ void __launch_bounds__(256, 1) gather_bulk_kernel(
   rp.nbw = nbw;
   rp.depth = nbw / 2;
   rp.ph = rp.pend = 0;
+  rp.hints = MOE_GATHER_L2 >= 2 ? 3u : MOE_GATHER_L2 == 1 ? 2u : 0u;
+  rp.ld_pol = MOE_GATHER_L2 >= 2 ? l2_policy_evict_last() : 0;
+  rp.st_pol = MOE_GATHER_L2 >= 1 ? l2_policy_evict_first() : 0;
   if (zero_pad) {
     for (uint32_t i = threadIdx.x; i < rb / 16; i += blockDim.x)
       reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
@@ -184,6 +204,174 @@ __device__ __forceinline__ void quant32(const uint4 (&in)[4], uint4 (&out)[2], u
   scale = mx_quant32(v, out[0], out[1]);
 }
 
+// Shared-memory layout of the bulk-copy gathers: a zero row, gw warps x nbw
+// row buffers of rb bytes, then one mbarrier per buffer (and, for the MXFP8
+// gather, gw scale rows of sb bytes after the barriers).
+struct GatherSmem {
+  uint8_t* base;
+  RowPipe rp;
+};
+
+__device__ __forceinline__ GatherSmem gather_smem_init(uint8_t* smem_raw, uint32_t rb, int gw, int nbw,
+                                                       int warp, int lane) {
+  GatherSmem g;
+  g.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                      ~static_cast<uintptr_t>(127));
+  RowPipe& rp = g.rp;
+  rp.zrow = smem_u32(g.base);
+  rp.rb = rb;
+  rp.wbuf = rp.zrow + rb + (uint32_t)(warp * nbw) * rb;
+  rp.bars = reinterpret_cast<uint64_t*>(g.base + (size_t)(1 + gw * nbw) * rb) + warp * nbw;
+  rp.nbw = nbw;
+  rp.depth = nbw / 2;
+  rp.ph = rp.pend = 0;
+  rp.hints = MOE_GATHER_L2 >= 2 ? 3u : MOE_GATHER_L2 == 1 ? 2u : 0u;
+  rp.ld_pol = MOE_GATHER_L2 >= 2 ? l2_policy_evict_last() : 0;
+  rp.st_pol = MOE_GATHER_L2 >= 1 ? l2_policy_evict_first() : 0;
+  for (uint32_t i = threadIdx.x; i < rb / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(g.base)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();  // the zero row is read by bulk stores
+  if (warp < gw && lane == 0) {
+    for (int b = 0; b < nbw; ++b) mbar_init(&rp.bars[b], 1);
+    fence_mbar_init();
+  }
+  return g;
+}
+
+// Gather in token order (no ring): each source row is read from HBM once and
+// written from shared memory to each of its k padded positions (pos_pad).
+// Items of the warps' walk: tokens (with two sources, item 2t + pass), then,
+// with zero_pad, every padded position, written as a zero row in both
+// destinations where it holds no routed row.
+__global__ void __launch_bounds__(256, 1) gather_tokens_kernel(
+    const __nv_bfloat16* __restrict__ src, __nv_bfloat16* __restrict__ dst,
+    const __nv_bfloat16* __restrict__ src2, __nv_bfloat16* __restrict__ dst2,
+    const int* __restrict__ pos_pad, const int* __restrict__ row_of_pad, const int* __restrict__ hdr,
+    int T, int k, int d, int zero_pad, int gw, int nbw, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int s_abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  GatherSmem gs = gather_smem_init(smem_raw, (uint32_t)d * 2u, gw, nbw, warp, lane);
+  RowPipe& rp = gs.rp;
+  if (threadIdx.x == 0) s_abort = 0;
+  __syncthreads();
+  if (warp >= gw) return;
+  const int rows = hdr[kHdrRpTotal];
+  const int npass = dst2 != nullptr ? 2 : 1;
+  const int ntok = T * npass;
+  const int N = ntok + (zero_pad ? rows : 0);
+  const int gid = blockIdx.x * gw + warp, ni = gridDim.x * gw;
+  const int n = gid < N ? (N - gid + ni - 1) / ni : 0;
+  if (n == 0) return;
+  const bool done = bulk_rows_fan(
+      rp, n, max(k, npass), rp.rb,
+      [&](int i) {
+        const int g = gid + i * ni;
+        if (g < ntok) return g;
+        return __ldg(row_of_pad + (g - ntok)) < 0 ? kRowZero : kRowSkip;
+      },
+      [&](int code) { return ((code % npass) ? src2 : src) + (size_t)(code / npass) * d; },
+      [&](int i, int j) -> __nv_bfloat16* {
+        const int g = gid + i * ni;
+        if (g < ntok) {
+          if (j >= k) return nullptr;
+          const int pp = __ldg(pos_pad + (size_t)(g / npass) * k + j);
+          return ((g % npass) ? dst2 : dst) + (size_t)pp * d;
+        }
+        if (j >= npass) return nullptr;
+        return (j ? dst2 : dst) + (size_t)(g - ntok) * d;
+      },
+      RowAsIs(), &s_abort, status, 920);
+  if (lane == 0) {
+    bulk_wait<0>();
+    if (!done)
+      for (int b = 0; b < nbw; ++b)  // no copy may still target shared memory at exit
+        if ((rp.pend >> b) & 1u) mbar_wait_drain(&rp.bars[b], (rp.ph >> b) & 1u);
+  }
+}
+
+// The MXFP8 gather in token order: each token row is read once, quantised
+// once in its shared-memory buffer (codes over the first d bytes, block
+// scales into the warp's scale row), and its codes and scales are written to
+// each of its k padded positions; every padded position without a routed
+// row gets zero codes and zero scale bytes.
+__global__ void __launch_bounds__(256, 1) gather_tokens_mxfp8_kernel(
+    const __nv_bfloat16* __restrict__ src, uint8_t* __restrict__ q, uint8_t* __restrict__ sc,
+    const int* __restrict__ pos_pad, const int* __restrict__ row_of_pad, const int* __restrict__ hdr,
+    int T, int k, int d, int gw, int nbw, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int s_abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rb = (uint32_t)d * 2u;
+  GatherSmem gs = gather_smem_init(smem_raw, rb, gw, nbw, warp, lane);
+  RowPipe& rp = gs.rp;
+  const int nblk = d >> 5, kgroups = d >> 7;
+  uint8_t* srow = gs.base + (size_t)(1 + gw * nbw) * rb + (size_t)gw * nbw * 8 + (size_t)warp * nblk;
+  if (threadIdx.x == 0) s_abort = 0;
+  __syncthreads();
+  if (warp >= gw) return;
+  const int rows = hdr[kHdrRpTotal];
+  const int N = T + rows;
+  const int gid = blockIdx.x * gw + warp, ni = gridDim.x * gw;
+  const int n = gid < N ? (N - gid + ni - 1) / ni : 0;
+  if (n == 0) return;
+  auto xform = [&](int i, int code, uint32_t buf) {
+    const int g = gid + i * ni;
+    if (code >= 0) {
+      // quantise in place: iteration m reads blocks 32m..32m+31 (bf16 bytes
+      // [2048m, 2048m + 2048)) before any lane writes their codes at
+      // [1024m, 1024m + 1024), which only overlap bytes read before
+      uint8_t* row = gs.base + (buf - rp.zrow);
+      for (int b0 = 0; b0 < nblk; b0 += 32) {
+        const int blk = b0 + lane;
+        uint4 in[4], out[2];
+        uint8_t s8 = 0;
+        if (blk < nblk)
+#pragma unroll
+          for (int u = 0; u < 4; ++u) in[u] = reinterpret_cast<const uint4*>(row)[blk * 4 + u];
+        __syncwarp();
+        if (blk < nblk) {
+          quant32(in, out, s8);
+          reinterpret_cast<uint4*>(row)[blk * 2] = out[0];
+          reinterpret_cast<uint4*>(row)[blk * 2 + 1] = out[1];
+          srow[blk] = s8;
+        }
+      }
+      __syncwarp();
+      for (int j = 0; j < k; ++j) {
+        const size_t pp = (size_t)__ldg(pos_pad + (size_t)g * k + j);
+        for (int blk = lane; blk < nblk; blk += 32) sc[mx_sf_offset(pp, blk, kgroups)] = srow[blk];
+      }
+      fence_proxy_async_smem();  // the codes are read by bulk stores, the buffer refilled by bulk loads
+      __syncwarp();
+    } else {
+      const size_t pp = (size_t)(g - T);
+      for (int blk = lane; blk < nblk; blk += 32) sc[mx_sf_offset(pp, blk, kgroups)] = 0;
+    }
+  };
+  const bool done = bulk_rows_fan(
+      rp, n, k, (uint32_t)d,
+      [&](int i) {
+        const int g = gid + i * ni;
+        if (g < T) return g;
+        return __ldg(row_of_pad + (g - T)) < 0 ? kRowZero : kRowSkip;
+      },
+      [&](int code) { return src + (size_t)code * d; },
+      [&](int i, int j) -> uint8_t* {
+        const int g = gid + i * ni;
+        if (g < T) return q + (size_t)__ldg(pos_pad + (size_t)g * k + j) * d;
+        return j == 0 ? q + (size_t)(g - T) * d : nullptr;
+      },
+      xform, &s_abort, status, 930);
+  if (lane == 0) {
+    bulk_wait<0>();
+    if (!done)
+      for (int b = 0; b < nbw; ++b)  // no copy may still target shared memory at exit
+        if ((rp.pend >> b) & 1u) mbar_wait_drain(&rp.bars[b], (rp.ph >> b) & 1u);
+  }
+}
+
+
 // Gather + quantise: one warp per padded row, each lane one block of 32.
 __global__ void __launch_bounds__(256) gather_mxfp8_kernel(const __nv_bfloat16* __restrict__ src,
                                                            uint8_t* __restrict__ q,
@@ -212,89 +400,6 @@ __global__ void __launch_bounds__(256) gather_mxfp8_kernel(const __nv_bfloat16* 
       sc[mx_sf_offset((size_t)pp, b, d >> 7)] = s;
     }
   }
-}
-
-// Gather + quantise staged through shared memory: warps [0, gw) each keep up
-// to nbw rows in flight as bulk copies into their own buffers; the 32 lanes
-// quantise a landed row's 32-element blocks from shared memory (lane = block
-// mod 32) and store codes and scales, then the buffer takes the row nbw
-// items later.  Padding rows give zero codes and the all-zero scale, as in
-// gather_mxfp8_kernel.
-__global__ void __launch_bounds__(256, 1) gather_mxfp8_bulk_kernel(
-    const __nv_bfloat16* __restrict__ src, uint8_t* __restrict__ q, uint8_t* __restrict__ sc,
-    const int* __restrict__ row_of_pad, const int* __restrict__ hdr, int k, int d, int gw, int nbw,
-    int* status) {
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ int s_abort;
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
-                                             ~static_cast<uintptr_t>(127));
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rb = (uint32_t)d * 2u;
-  uint8_t* wbuf = smem + (size_t)warp * nbw * rb;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)gw * nbw * rb) + warp * nbw;
-  if (warp < gw && lane == 0) {
-    for (int b = 0; b < nbw; ++b) mbar_init(&bars[b], 1);
-    fence_mbar_init();
-  }
-  if (threadIdx.x == 0) s_abort = 0;
-  __syncthreads();
-  if (warp >= gw) return;
-  const int rows = hdr[kHdrRpTotal];
-  const int gid = blockIdx.x * gw + warp, ni = gridDim.x * gw;
-  const int n = gid < rows ? (rows - gid + ni - 1) / ni : 0;
-  const int nblk = d >> 5;
-  // source rows 32 items at a time in two registers, shuffled to every lane
-  int c0 = 0;
-  int ia = lane < n ? __ldg(row_of_pad + gid + (size_t)lane * ni) : -1;
-  int ib = 32 + lane < n ? __ldg(row_of_pad + gid + (size_t)(32 + lane) * ni) : -1;
-  auto row_at = [&](int i) { return __shfl_sync(0xffffffffu, (i - c0) < 32 ? ia : ib, (i - c0) & 31); };
-  uint32_t ph = 0, pend = 0;
-  auto issue = [&](int i) {
-    const int r = row_at(i);
-    if (lane == 0 && r >= 0) {
-      const int b = i % nbw;
-      mbar_arrive_expect_tx(&bars[b], rb);
-      bulk_load(smem_u32(wbuf + (size_t)b * rb), src + (size_t)(r / k) * d, rb, smem_u32(&bars[b]));
-      pend |= 1u << b;
-    }
-  };
-  for (int i = 0; i < min(nbw, n); ++i) issue(i);
-  bool ok = true;
-  for (int i = 0; i < n; ++i) {
-    if (i - c0 == 32) {
-      c0 += 32;
-      ia = ib;
-      ib = c0 + 32 + lane < n ? __ldg(row_of_pad + gid + (size_t)(c0 + 32 + lane) * ni) : -1;
-    }
-    const int r = row_at(i);
-    const int b = i % nbw;
-    if (r >= 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars[b], (ph >> b) & 1u, &s_abort, status, 910));
-      if (!ok) break;
-      ph ^= 1u << b;
-      pend &= ~(1u << b);
-    }
-    const size_t pp = (size_t)gid + (size_t)i * ni;
-    const uint4* row = reinterpret_cast<const uint4*>(wbuf + (size_t)b * rb);
-    for (int blk = lane; blk < nblk; blk += 32) {
-      uint4 in[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) in[u] = (r >= 0) ? row[blk * 4 + u] : make_uint4(0, 0, 0, 0);
-      uint4 out[2];
-      uint8_t s8;
-      quant32(in, out, s8);
-      uint4* qv = reinterpret_cast<uint4*>(q + pp * d + blk * 32);
-      stg_v4(qv, out[0]);
-      stg_v4(qv + 1, out[1]);
-      sc[mx_sf_offset(pp, blk, d >> 7)] = s8;
-    }
-    fence_proxy_async_smem();  // this lane's reads of the buffer come before the next copy into it
-    __syncwarp();
-    if (i + nbw < n) issue(i + nbw);
-  }
-  if (lane == 0 && !ok)
-    for (int b = 0; b < nbw; ++b)  // no copy may still target shared memory at exit
-      if ((pend >> b) & 1u) mbar_wait_drain(&bars[b], (ph >> b) & 1u);
 }
 
 // Weights [batch, K, N] bf16 -> codes [batch, N, K] and scale tiles over [batch*N, K].
@@ -460,6 +565,17 @@ cudaError_t launch_gather(const moe_config& c, const Ws& ws, const __nv_bfloat16
       gw = (int)((kBudget - rb) / (2 * rb));
     }
     const size_t smem = 128 + (1 + (size_t)gw * nbw) * rb + (size_t)gw * nbw * 8;
+    if (ring == nullptr) {
+      // token order: every source row read once, written to its k positions
+      cudaError_t err = cudaFuncSetAttribute(gather_tokens_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (err != cudaSuccess) return err;
+      gather_tokens_kernel<<<num_sms(), 256, smem, st>>>(src, dst, src2, dst2, ws.pos_pad(), ws.row_of_pad(),
+                                                         ws.hdr(), c.T, c.k, c.d, zero_pad, gw, nbw,
+                                                         ws.hdr() + kHdrStatus);
+      return cudaGetLastError();
+    }
+    // after a ring forward: padded order, the rows the ring still holds read from it
     cudaError_t err = cudaFuncSetAttribute(gather_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)smem);
     if (err != cudaSuccess) return err;
@@ -477,23 +593,25 @@ cudaError_t launch_gather(const moe_config& c, const Ws& ws, const __nv_bfloat16
 cudaError_t launch_gather_mxfp8(const moe_config& c, const Ws& ws, const __nv_bfloat16* src,
                                 uint8_t* q, uint8_t* sc, cudaStream_t st) {
   TraceScope ts("gather_mxfp8", st);
-  // bf16 rows staged through shared memory: up to 16 buffers in each of 8
-  // warps (fewer warps for wide rows, at least two buffers each)
+  // token order, bf16 rows staged through shared memory: a zero row, up to
+  // 16 buffers in each of 8 warps (fewer warps for wide rows, at least two
+  // buffers each) and a scale row per warp
+  const size_t rb = (size_t)c.d * 2, sb = (size_t)c.d / 32;
   constexpr size_t kBudget = 227 * 1024 - 128 - 8 * 16 * 8;
-  const size_t rb = (size_t)c.d * 2;
-  if (kBudget >= 2 * rb && MOE_BULK_GATHER) {
+  if (kBudget >= 3 * rb + 8 * sb && MOE_BULK_GATHER) {
     int gw = 8;
-    int nbw = (int)std::min<size_t>(16, kBudget / (gw * rb));
+    int nbw = (int)std::min<size_t>(16, (kBudget - rb - gw * sb) / (gw * rb));
     if (nbw < 2) {
       nbw = 2;
-      gw = (int)(kBudget / (2 * rb));
+      gw = (int)((kBudget - rb) / (2 * rb + sb));
     }
-    const size_t smem = 128 + (size_t)gw * nbw * rb + (size_t)gw * nbw * 8;
-    cudaError_t err = cudaFuncSetAttribute(gather_mxfp8_bulk_kernel,
+    const size_t smem = 128 + (1 + (size_t)gw * nbw) * rb + (size_t)gw * nbw * 8 + (size_t)gw * sb;
+    cudaError_t err = cudaFuncSetAttribute(gather_tokens_mxfp8_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    gather_mxfp8_bulk_kernel<<<num_sms(), 256, smem, st>>>(src, q, sc, ws.row_of_pad(), ws.hdr(), c.k,
-                                                           c.d, gw, nbw, ws.hdr() + kHdrStatus);
+    gather_tokens_mxfp8_kernel<<<num_sms(), 256, smem, st>>>(src, q, sc, ws.pos_pad(), ws.row_of_pad(),
+                                                             ws.hdr(), c.T, c.k, c.d, gw, nbw,
+                                                             ws.hdr() + kHdrStatus);
     return cudaGetLastError();
   }
   gather_mxfp8_kernel<<<num_sms() * 8, 256, 0, st>>>(src, q, sc, ws.row_of_pad(), ws.hdr(), c.k, c.d);

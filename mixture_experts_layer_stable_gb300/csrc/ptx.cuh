@@ -147,6 +147,11 @@ MOE_DEV uint64_t l2_policy_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+MOE_DEV uint64_t l2_policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 MOE_DEV uint64_t l2_policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
@@ -354,12 +359,29 @@ MOE_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t b
       : "memory");
 }
 
+// The same copy with an L2 cache policy (createpolicy) for the source lines.
+MOE_DEV void bulk_load_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, "
+      "[%3], %4;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(pol)
+      : "memory");
+}
+
 // Plain bulk copy shared -> global (same alignment rules), in the thread's
 // current bulk async-group.
 MOE_DEV void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
                    reinterpret_cast<uint64_t>(dst)),
                "r"(src), "r"(bytes)
+               : "memory");
+}
+
+// The same store with an L2 cache policy for the written lines.
+MOE_DEV void bulk_store_hint(void* dst, uint32_t src, uint32_t bytes, uint64_t pol) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(
+                   reinterpret_cast<uint64_t>(dst)),
+               "r"(src), "r"(bytes), "l"(pol)
                : "memory");
 }
 

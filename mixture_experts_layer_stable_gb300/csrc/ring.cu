@@ -272,6 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     rp.nbw = p.nbw;
     rp.depth = p.nbw / 2;
     rp.ph = rp.pend = 0;
+    rp.hints = 0;  // the ring's rows are read by the GEMM warps right away: normal priority
+    rp.ld_pol = rp.st_pol = 0;
     if constexpr (!FP8) {
       for (uint32_t i = threadIdx.x; i < rb / 16; i += kThreads)
         reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);

@@ -36,6 +36,13 @@ __device__ __forceinline__ void stg_v4(void* p, uint4 v) {
                : "memory");
 }
 
+// The same store with an L2 cache policy (createpolicy) for the line.
+__device__ __forceinline__ void stg_v4_hint(void* p, uint4 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w), "l"(pol)
+               : "memory");
+}
+
 // Merge token t with threads [tid0, tid0 + nthr) of the block, each owning
 // 8-column vectors.  sp / sw hold the token's k padded row positions and
 // weights.  COHERENT selects L2 loads for rows written in the same kernel.

@@ -45,7 +45,8 @@ def _check_schedule(L, logits_cpu, k):
     return ids, g
 
 
-@pytest.mark.parametrize("name", ["tiny", "balanced", "kimi_zipf", "kimi_mxfp8", "kimi_bwd"])
+@pytest.mark.parametrize("name", ["tiny", "balanced", "kimi_zipf", "kimi_mxfp8", "kimi_bwd",
+                                  "local_slice"])
 def test_schedule_bit_exact(name):
     cfg = CONFIGS[name]
     inp = make_inputs(cfg, parts=("logits",))
@@ -211,6 +212,27 @@ def test_kimi_zipf_forward_sampled():
     logits = dev["logits"].cpu()
     ids, g = _check_schedule(L, logits, cfg.k)
     toks = _sample_tokens(cfg.T, 48)
+    want = O.forward_tokens(to_np(dev["x"]), ExpertView(dev["W1"]), ExpertView(dev["W2"]), ids, g,
+                            toks)
+    got = out.float().cpu().numpy()[toks]
+    assert rel_err(got, want) <= TOL_BF16
+    for i in range(len(toks)):
+        assert rel_err(got[i], want[i]) <= 3 * TOL_BF16
+
+
+@pytest.mark.slow
+def test_local_slice_forward_sampled():
+    # k = 1 over 4 experts of about 4,096 rows each: every unit a full pair
+    cfg = CONFIGS["local_slice"]
+    dev = make_inputs(cfg, device="cuda", with_grad=False)
+    L = Layer(cfg)
+    L.schedule(dev["logits"])
+    out = L.forward(dev["x"], dev["W1"], dev["W2"], save=False)
+    torch.cuda.synchronize()
+    assert L.status() == 0
+    ids, g = _check_schedule(L, dev["logits"].cpu(), cfg.k)
+    assert np.all(g == 1.0)  # one expert per token: the renormalised weight is 1
+    toks = _sample_tokens(cfg.T, 48, seed=2)
     want = O.forward_tokens(to_np(dev["x"]), ExpertView(dev["W1"]), ExpertView(dev["W2"]), ids, g,
                             toks)
     got = out.float().cpu().numpy()[toks]
