@@ -272,7 +272,7 @@ moe_status moe_forward(const moe_config* cfg, const moe_bf16* x, const void* w1,
     auto* Yp = static_cast<__nv_bfloat16*>(W.at(W.L.Yp));
     cudaError_t e = launch_gather_mxfp8(c, W, reinterpret_cast<const __nv_bfloat16*>(x), Xq, Xs, st);
     if (e == cudaSuccess)
-      e = gemm_fwd1_mx(c, W, Xq, Xs, static_cast<const uint8_t*>(w1), w1_scales, Aq, As,
+      e = gemm_fwd1_mx(c, W, sched.counts, Xq, Xs, static_cast<const uint8_t*>(w1), w1_scales, Aq, As,
                        saved ? reinterpret_cast<__nv_bfloat16*>(saved->A) : nullptr,
                        saved ? reinterpret_cast<__nv_bfloat16*>(saved->H) : nullptr, st);
     if (e == cudaSuccess)

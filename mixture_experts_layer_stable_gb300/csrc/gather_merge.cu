@@ -293,12 +293,11 @@ __global__ void __launch_bounds__(256, 1) gather_tokens_kernel(
 // The MXFP8 gather in token order: each token row is read once, quantised
 // once in its shared-memory buffer (codes over the first d bytes, block
 // scales into the warp's scale row), and its codes and scales are written to
-// each of its k padded positions; every padded position without a routed
-// row gets zero codes and zero scale bytes.
+// each of its k padded positions.  Padding rows are left alone: the MXFP8
+// GEMM1 writes zeros for them whatever they hold.
 __global__ void __launch_bounds__(256, 1) gather_tokens_mxfp8_kernel(
     const __nv_bfloat16* __restrict__ src, uint8_t* __restrict__ q, uint8_t* __restrict__ sc,
-    const int* __restrict__ pos_pad, const int* __restrict__ row_of_pad, const int* __restrict__ hdr,
-    int T, int k, int d, int gw, int nbw, int* status) {
+    const int* __restrict__ pos_pad, int T, int k, int d, int gw, int nbw, int* status) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -310,14 +309,12 @@ __global__ void __launch_bounds__(256, 1) gather_tokens_mxfp8_kernel(
   if (threadIdx.x == 0) s_abort = 0;
   __syncthreads();
   if (warp >= gw) return;
-  const int rows = hdr[kHdrRpTotal];
-  const int N = T + rows;
   const int gid = blockIdx.x * gw + warp, ni = gridDim.x * gw;
-  const int n = gid < N ? (N - gid + ni - 1) / ni : 0;
+  const int n = gid < T ? (T - gid + ni - 1) / ni : 0;
   if (n == 0) return;
-  auto xform = [&](int i, int code, uint32_t buf) {
+  auto xform = [&](int i, int, uint32_t buf) {
     const int g = gid + i * ni;
-    if (code >= 0) {
+    {
       // quantise in place: iteration m reads blocks 32m..32m+31 (bf16 bytes
       // [2048m, 2048m + 2048)) before any lane writes their codes at
       // [1024m, 1024m + 1024), which only overlap bytes read before
@@ -338,30 +335,23 @@ __global__ void __launch_bounds__(256, 1) gather_tokens_mxfp8_kernel(
         }
       }
       __syncwarp();
+      // the scales of blocks 4w..4w+3 of a row are one 32-bit word of its
+      // 128-row scale tile: lane l writes words l, l + 32, ... of every copy
+      const int my_pp = lane < k ? __ldg(pos_pad + (size_t)g * k + lane) : 0;
       for (int j = 0; j < k; ++j) {
-        const size_t pp = (size_t)__ldg(pos_pad + (size_t)g * k + j);
-        for (int blk = lane; blk < nblk; blk += 32) sc[mx_sf_offset(pp, blk, kgroups)] = srow[blk];
+        const int pp = __shfl_sync(0xffffffffu, my_pp, j);
+        uint8_t* tile = sc + (size_t)(pp >> 7) * kgroups * 512u + mx_sf_byte(pp & 127, 0);
+        for (int w = lane; w < kgroups; w += 32)
+          *reinterpret_cast<uint32_t*>(tile + (size_t)w * 512u) = reinterpret_cast<const uint32_t*>(srow)[w];
       }
       fence_proxy_async_smem();  // the codes are read by bulk stores, the buffer refilled by bulk loads
       __syncwarp();
-    } else {
-      const size_t pp = (size_t)(g - T);
-      for (int blk = lane; blk < nblk; blk += 32) sc[mx_sf_offset(pp, blk, kgroups)] = 0;
     }
   };
   const bool done = bulk_rows_fan(
-      rp, n, k, (uint32_t)d,
-      [&](int i) {
-        const int g = gid + i * ni;
-        if (g < T) return g;
-        return __ldg(row_of_pad + (g - T)) < 0 ? kRowZero : kRowSkip;
-      },
+      rp, n, k, (uint32_t)d, [&](int i) { return gid + i * ni; },
       [&](int code) { return src + (size_t)code * d; },
-      [&](int i, int j) -> uint8_t* {
-        const int g = gid + i * ni;
-        if (g < T) return q + (size_t)__ldg(pos_pad + (size_t)g * k + j) * d;
-        return j == 0 ? q + (size_t)(g - T) * d : nullptr;
-      },
+      [&](int i, int j) { return q + (size_t)__ldg(pos_pad + (size_t)(gid + i * ni) * k + j) * d; },
       xform, &s_abort, status, 930);
   if (lane == 0) {
     bulk_wait<0>();
@@ -609,9 +599,8 @@ cudaError_t launch_gather_mxfp8(const moe_config& c, const Ws& ws, const __nv_bf
     cudaError_t err = cudaFuncSetAttribute(gather_tokens_mxfp8_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    gather_tokens_mxfp8_kernel<<<num_sms(), 256, smem, st>>>(src, q, sc, ws.pos_pad(), ws.row_of_pad(),
-                                                             ws.hdr(), c.T, c.k, c.d, gw, nbw,
-                                                             ws.hdr() + kHdrStatus);
+    gather_tokens_mxfp8_kernel<<<num_sms(), 256, smem, st>>>(src, q, sc, ws.pos_pad(), c.T, c.k, c.d, gw,
+                                                             nbw, ws.hdr() + kHdrStatus);
     return cudaGetLastError();
   }
   gather_mxfp8_kernel<<<num_sms() * 8, 256, 0, st>>>(src, q, sc, ws.row_of_pad(), ws.hdr(), c.k, c.d);

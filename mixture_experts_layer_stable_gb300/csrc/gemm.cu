@@ -64,6 +64,15 @@ enum Epi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2, EPI_LOGITS = 3 };
 // heavy kernel leaves room (shared memory, TMEM) for one light CTA per SM.
 // Their pipeline depths (stages) share one SM's shared memory.
 enum UnitSet { UNITS_ALL = 0, UNITS_HEAVY = 1, UNITS_LIGHT = 2 };
+// Thin pair units of at most 32 rows take two K blocks per pipeline stage
+// (36 KB stages, five of them): such a unit mostly streams its weight slice
+// from HBM, and with one 16 KB K block of weights per 32 KB stage it kept
+// too few bytes in flight per SM to stream at the SM's L2 ingress rate.
+#ifndef MOE_THIN_DOUBLE
+#define MOE_THIN_DOUBLE 0
+#endif
+constexpr int kThinDblRows = 32;  // MMA N of a double-stage thin unit (16 rows per CTA)
+
 #ifndef MOE_SPLIT_HEAVY_STAGES
 #define MOE_SPLIT_HEAVY_STAGES 3
 #endif
@@ -77,11 +86,14 @@ struct KCfg {
   static_assert(UM == UNITS_ALL || (PAIR && !WGRAD), "unit sets split the row pair GEMMs");
   // a light unit's stage: its weight slice (MMA A) and at most 16 of its rows
   // per CTA (MMA B, nt <= kLightRows)
+  // double-stage thin units: two K blocks of weights (2 x 16 KB) and of
+  // their 16 rows (2 x 2 KB) per stage
+  static constexpr bool kThinDbl = MOE_THIN_DOUBLE && PAIR && !WGRAD && UM == UNITS_ALL;
   static constexpr int kStageBytes = UM == UNITS_LIGHT ? kABytes + 16 * 128
-                                                       : kABytes + (PAIR ? kBHalfBytes : kBBytes);
+                                     : kABytes + (PAIR ? kBHalfBytes : kBBytes) + (kThinDbl ? 4096 : 0);
   static constexpr int kStages = UM == UNITS_HEAVY ? MOE_SPLIT_HEAVY_STAGES
                                  : UM == UNITS_LIGHT ? MOE_SPLIT_LIGHT_STAGES
-                                 : PAIR ? 6 : (FP8 && EPI == EPI_STORE) ? 3 : 4;
+                                 : PAIR ? (kThinDbl ? 5 : 6) : (FP8 && EPI == EPI_STORE) ? 3 : 4;
   // swizzled staging tiles per epilogue warp for the TMA-store epilogues
   // (light units only need their transpose tiles)
   static constexpr int kOutBufs = (UM == UNITS_LIGHT && EPI == EPI_STORE) ? 1
@@ -156,6 +168,7 @@ struct Tile {
   int nt;      // thin pair unit: MMA N (rows rounded up to 32), half in each CTA
   bool thin;   // tile computed as (weights)^T x (rows)^T, tokens on N
   bool valid;  // pair mode: the odd CTA's tile past the expert's last tile is not
+  bool dbl;    // thin pair unit with two K blocks per stage (kb_count counts stages)
 };
 
 // Work units: tiles, or in pair mode pairs of M-adjacent tiles of one expert
@@ -191,6 +204,7 @@ template <bool WGRAD, bool PAIR, int UM = UNITS_ALL>
 __device__ __forceinline__ Tile decode(const Params& p, int L, int rank) {
   Tile t;
   t.valid = true;
+  t.dbl = false;
   if (!WGRAD && p.mt_off == nullptr) {
     // dense: tile m of one [T, K] matrix
     t.e = 0;
@@ -239,6 +253,11 @@ __device__ __forceinline__ Tile decode(const Params& p, int L, int rank) {
       const int cnt = __ldg(p.counts + e);
       t.rows = min(kBM, cnt - mrel * kBM);
       if (!PAIR && p.thin && thin_tile(t.rows, cnt)) t.thin = true;
+    }
+    if (MOE_THIN_DOUBLE && PAIR && UM == UNITS_ALL && t.thin && t.nt == kThinDblRows &&
+        (p.num_kb & 1) == 0) {
+      t.dbl = true;
+      t.kb_count = p.num_kb >> 1;
     }
   } else {
     t.nt = 0;
@@ -474,7 +493,8 @@ __global__ void __launch_bounds__(kThreads, UM == UNITS_ALL ? 1 : 2)
         const Tile t = decode<WGRAD, PAIR, UM>(p, U, rank);
         // bytes landing on this stage's "full" barrier (pair: both CTAs' copies)
         uint32_t tx = (t.valid ? (uint32_t)kABytes : 0u) + b_bytes + (FP8 ? (uint32_t)kSfBytes : 0u);
-        if (PAIR && t.thin) tx = 16384u + (uint32_t)(t.nt / 2) * 128u;  // weights + half the rows
+        if (PAIR && t.thin)  // weights + half the rows, of one or two K blocks
+          tx = (16384u + (uint32_t)(t.nt / 2) * 128u) * (t.dbl ? 2u : 1u);
         if (PAIR && rank == 0)
           tx += t.thin ? tx : (decode<WGRAD, PAIR, UM>(p, U, 1).valid ? (uint32_t)kABytes : 0u) + b_bytes;
         for (int kb = 0; kb < t.kb_count; ++kb) {
@@ -530,20 +550,28 @@ __global__ void __launch_bounds__(kThreads, UM == UNITS_ALL ? 1 : 2)
                 if constexpr (PAIR) tma_load_3d_pair_hint(sa + off, &tmB, fb, c0, c1, t.e, pol_stream);
                 else tma_load_3d_hint(sa + off, &tmB, fb, c0, c1, t.e, pol_stream);
               };
-              if (EPI == EPI_SWIGLU) {
-                const int c0 = t.n * p.hn + rank * 64;
-                loadw(0u, c0, kb * BK);
-                loadw(8192u, p.f + c0, kb * BK);
-              } else if (B_MN) {
-                const int c0 = t.n * 256 + rank * 128;
-                loadw(0u, c0, kb * BK);
-                loadw(8192u, c0 + 64, kb * BK);
-              } else {
-                loadw(0u, kb * BK, t.n * 256 + rank * 128);
+              // a double stage holds K blocks 2kb and 2kb + 1: weights at 0 and
+              // 16 KB, their 16 rows at 32 KB and 34 KB
+              const int nsub = t.dbl ? 2 : 1;
+              for (int u = 0; u < nsub; ++u) {
+                const int kk = t.dbl ? 2 * kb + u : kb;
+                const uint32_t wo = (uint32_t)u * 16384u;
+                if (EPI == EPI_SWIGLU) {
+                  const int c0 = t.n * p.hn + rank * 64;
+                  loadw(wo, c0, kk * BK);
+                  loadw(wo + 8192u, p.f + c0, kk * BK);
+                } else if (B_MN) {
+                  const int c0 = t.n * 256 + rank * 128;
+                  loadw(wo, c0, kk * BK);
+                  loadw(wo + 8192u, c0 + 64, kk * BK);
+                } else {
+                  loadw(wo, kk * BK, t.n * 256 + rank * 128);
+                }
+                const int nt2 = t.nt / 2;
+                const uint32_t ro = t.dbl ? 32768u + (uint32_t)u * 2048u : (uint32_t)kABytes;
+                for (int i = 0; i < nt2; i += 16)
+                  load2(ro + (uint32_t)(i * 128), &tmA2, kk * BK, t.row0 + rank * nt2 + i);
               }
-              const int nt2 = t.nt / 2;
-              for (int i = 0; i < nt2; i += 16)
-                load2((uint32_t)(kABytes + i * 128), &tmA2, kb * BK, t.row0 + rank * nt2 + i);
             } else {
               for_each_box<WGRAD, A_MN, B_MN, EPI, PAIR>(p, t, kb, rank, &tmA, &tmB, load2, load3);
             }
@@ -642,12 +670,17 @@ __global__ void __launch_bounds__(kThreads, UM == UNITS_ALL ? 1 : 2)
                 // = W^T x rows^T
                 constexpr bool kWmn = (EPI == EPI_SWIGLU) || B_MN;  // weights MN-major in smem
                 const uint32_t idt = idesc_bf16(2 * kBM, t.nt, kWmn, false);
+                const int nsub = t.dbl ? 2 : 1;
+                for (int u = 0; u < nsub; ++u) {
+                  const uint32_t wa = sa + (uint32_t)u * 16384u;
+                  const uint32_t ra = t.dbl ? sa + 32768u + (uint32_t)u * 2048u : sb;
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk)
-                  tc_mma_f16_pair(dt, kWmn ? sdesc_sw128(sa + kk * 2048, 8192, 1024)
-                                           : sdesc_sw128(sa + kk * 32, 16, 1024),
-                                  sdesc_sw128(sb + kk * 32, 16, 1024), idt,
-                                  (kb > 0 || kk > 0) ? 1u : 0u);
+                  for (int kk = 0; kk < BK / 16; ++kk)
+                    tc_mma_f16_pair(dt, kWmn ? sdesc_sw128(wa + kk * 2048, 8192, 1024)
+                                             : sdesc_sw128(wa + kk * 32, 16, 1024),
+                                    sdesc_sw128(ra + kk * 32, 16, 1024), idt,
+                                    (kb > 0 || u > 0 || kk > 0) ? 1u : 0u);
+                }
                 issued = true;
               }
             }
@@ -900,10 +933,17 @@ __global__ void __launch_bounds__(kThreads, UM == UNITS_ALL ? 1 : 2)
         }
       } else if constexpr (EPI == EPI_SWIGLU) {
         const size_t row = (size_t)t.row0 + q * 32 + lane;
+        // a padding row of the expert's last tile (its input row is not
+        // written by the gather): saved and passed on as zeros
+        const bool pad_row = q * 32 + lane >= t.rows;
         for (int c = 0; c < p.hn; c += 32) {
           float g[32], u[32], a[32];
           tmem_ld32(tb + c, g);
           tmem_ld32(tb + p.hn + c, u);
+          if (pad_row) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) g[i] = u[i] = 0.f;
+          }
           const int col = t.n * p.hn + c;
 #pragma unroll
           for (int i = 0; i < 32; ++i) a[i] = silu_f(g[i]) * u[i];
@@ -1411,12 +1451,13 @@ cudaError_t router_bwd(const moe_config& c, const Ws& ws, const __nv_bfloat16* d
 
 // MXFP8 GEMM1: Xq [rows, d] E4M3 (+ scale tiles) x W1q [E, 2f, d] E4M3 (+ scale
 // tiles) -> SwiGLU -> Aq [rows, f] E4M3 + scale tiles; optionally A and H in bf16.
-cudaError_t gemm_fwd1_mx(const moe_config& c, const Ws& ws, const uint8_t* Xq, const uint8_t* Xs,
-                         const uint8_t* W1q, const uint8_t* W1s, uint8_t* Aq, uint8_t* As,
-                         __nv_bfloat16* A, __nv_bfloat16* H, cudaStream_t st) {
+cudaError_t gemm_fwd1_mx(const moe_config& c, const Ws& ws, const int* counts, const uint8_t* Xq,
+                         const uint8_t* Xs, const uint8_t* W1q, const uint8_t* W1s, uint8_t* Aq,
+                         uint8_t* As, __nv_bfloat16* A, __nv_bfloat16* H, cudaStream_t st) {
   CUtensorMap ta, tb, to;
   const uint64_t rows = (uint64_t)ws.L.Rp_max;
   Params p = base_params(c, ws);
+  p.counts = counts;  // the rows of each tile: padding rows leave as zeros
   p.hn = 128;
   p.umma_n = 256;
   p.n_tiles = c.f / 128;

@@ -225,9 +225,9 @@ cudaError_t router_gemm(const moe_config& c, const Ws& ws, const __nv_bfloat16* 
 cudaError_t router_bwd(const moe_config& c, const Ws& ws, const __nv_bfloat16* dl16, int Epad,
                        const __nv_bfloat16* x, const __nv_bfloat16* Wr, __nv_bfloat16* dx_r,
                        __nv_bfloat16* dWr, cudaStream_t st);
-cudaError_t gemm_fwd1_mx(const moe_config& c, const Ws& ws, const uint8_t* Xq, const uint8_t* Xs,
-                         const uint8_t* W1q, const uint8_t* W1s, uint8_t* Aq, uint8_t* As,
-                         __nv_bfloat16* A, __nv_bfloat16* H, cudaStream_t st);
+cudaError_t gemm_fwd1_mx(const moe_config& c, const Ws& ws, const int* counts, const uint8_t* Xq,
+                         const uint8_t* Xs, const uint8_t* W1q, const uint8_t* W1s, uint8_t* Aq,
+                         uint8_t* As, __nv_bfloat16* A, __nv_bfloat16* H, cudaStream_t st);
 cudaError_t gemm_fwd2_mx(const moe_config& c, const Ws& ws, const uint8_t* Aq, const uint8_t* As,
                          const uint8_t* W2q, const uint8_t* W2s, __nv_bfloat16* Yp,
                          cudaStream_t st);

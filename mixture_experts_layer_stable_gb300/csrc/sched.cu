@@ -89,63 +89,138 @@ __device__ __forceinline__ void topk_token(const float* __restrict__ logits, int
   *w = ex / s;
 }
 
+// Per-expert exclusive prefix, in place, over chunks [c0, c1) of the chunk
+// histograms, starting from `run`; returns the running sum.  Loads go out 32
+// at a time so that their latencies overlap.
+__device__ __forceinline__ int prefix_chunks(int* __restrict__ hist, int E, int e, int c0, int c1,
+                                             int run) {
+  for (int b0 = c0; b0 < c1; b0 += 32) {
+    int c[32];
+#pragma unroll
+    for (int u = 0; u < 32; ++u) c[u] = (b0 + u < c1) ? __ldcg(hist + (size_t)(b0 + u) * E + e) : 0;
+#pragma unroll
+    for (int u = 0; u < 32; ++u) {
+      if (b0 + u < c1) hist[(size_t)(b0 + u) * E + e] = run;
+      run += c[u];
+    }
+  }
+  return run;
+}
+
+__device__ __forceinline__ int sum_chunks(const int* __restrict__ hist, int E, int e, int c0, int c1) {
+  int run = 0;
+  for (int b0 = c0; b0 < c1; b0 += 32) {
+    int c[32];
+#pragma unroll
+    for (int u = 0; u < 32; ++u) c[u] = (b0 + u < c1) ? __ldcg(hist + (size_t)(b0 + u) * E + e) : 0;
+#pragma unroll
+    for (int u = 0; u < 32; ++u) run += c[u];
+  }
+  return run;
+}
+
 // The last block of a chunked histogram pass: per-expert exclusive prefixes
 // over the chunks (in place), counts, offsets and the padded layout.
+// sh: kMaxE ints, aux: blockDim.x ints of shared memory (G * E <= blockDim.x).
 __device__ void finish_histograms(int* __restrict__ hist, int nb, int E, int* __restrict__ hdr,
                                   int* __restrict__ counts, int* __restrict__ offsets,
                                   int* __restrict__ poff, int* __restrict__ mt_off,
-                                  int* __restrict__ pt_off, int* sh) {
+                                  int* __restrict__ pt_off, int* sh, int* aux) {
   const int tid = threadIdx.x;
-  // per-expert exclusive prefix over chunks (loads issued in batches so they overlap)
-  for (int e = tid; e < E; e += blockDim.x) {
-    int run = 0;
-    for (int b0 = 0; b0 < nb; b0 += 8) {
-      int c[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) c[u] = (b0 + u < nb) ? __ldcg(hist + (size_t)(b0 + u) * E + e) : 0;
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (b0 + u < nb) {
-          hist[(size_t)(b0 + u) * E + e] = run;
-          run += c[u];
-        }
+  // G thread groups split the chunks of every expert: group q sums chunks
+  // [q*len, (q+1)*len), then writes their prefixes from its start
+  const int G = E >= (int)blockDim.x ? 1 : min(8, (int)blockDim.x / E);
+  const int len = (nb + G - 1) / G;
+  const int q = tid / E;
+  if (G > 1) {
+    if (q < G) {
+      const int e = tid - q * E;
+      aux[q * E + e] = sum_chunks(hist, E, e, min(nb, q * len), min(nb, (q + 1) * len));
+    }
+    __syncthreads();
+    if (q < G) {
+      const int e = tid - q * E;
+      int start = 0;
+      for (int j = 0; j < q; ++j) start += aux[j * E + e];
+      prefix_chunks(hist, E, e, min(nb, q * len), min(nb, (q + 1) * len), start);
+      if (q == 0) {
+        int tot = 0;
+        for (int j = 0; j < G; ++j) tot += aux[j * E + e];
+        sh[e] = tot;
+        counts[e] = tot;
       }
     }
-    sh[e] = run;
-    counts[e] = run;
+  } else {
+    for (int e = tid; e < E; e += blockDim.x) {
+      const int tot = prefix_chunks(hist, E, e, 0, nb, 0);
+      sh[e] = tot;
+      counts[e] = tot;
+    }
   }
   __syncthreads();
-  if (tid == 0) {
-    // pt_off: work units of the CTA-pair GEMMs per expert (pairs of 128-row
-    // tiles, an odd last tile alone); hv_off / lt_off split them into heavy
-    // units and light ones (an odd last tile of at most kLightRows rows)
+  if (tid < 32) {
+    // prefixes over experts, one warp: lane l takes experts [l*per, (l+1)*per).
+    // Per expert: its rows; its padded rows (128-row tiles); pt_off: work
+    // units of the CTA-pair GEMMs (pairs of 128-row tiles, an odd last tile
+    // alone); hv_off / lt_off split them into heavy units and light ones (an
+    // odd last tile of at most kLightRows rows)
     int* hv_off = pt_off + (E + 1);
     int* lt_off = hv_off + (E + 1);
-    int o = 0, po = 0, pt = 0, hv = 0, lt = 0;
-    for (int e = 0; e < E; ++e) {
-      offsets[e] = o;
-      poff[e] = po;
-      mt_off[e] = po / kBM;
-      pt_off[e] = pt;
-      hv_off[e] = hv;
-      lt_off[e] = lt;
-      const int mt = (sh[e] + kBM - 1) / kBM;
-      const int light = ((mt & 1) && sh[e] - (mt - 1) * kBM <= kLightRows) ? 1 : 0;
-      o += sh[e];
-      po += mt * kBM;
-      pt += (mt + 1) >> 1;
-      hv += ((mt + 1) >> 1) - light;
-      lt += light;
+    const int lane = tid;
+    const int per = (E + 31) / 32;
+    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+    auto sizes = [&](int e, int& o, int& po, int& pt, int& hv, int& lt) {
+      const int c = sh[e];
+      const int mt = (c + kBM - 1) / kBM;
+      const int light = ((mt & 1) && c - (mt - 1) * kBM <= kLightRows) ? 1 : 0;
+      o = c;
+      po = mt * kBM;
+      pt = (mt + 1) >> 1;
+      hv = pt - light;
+      lt = light;
+    };
+    int v[5] = {0, 0, 0, 0, 0};
+    for (int e = e0; e < e1; ++e) {
+      int d[5];
+      sizes(e, d[0], d[1], d[2], d[3], d[4]);
+#pragma unroll
+      for (int i = 0; i < 5; ++i) v[i] += d[i];
     }
-    offsets[E] = o;
-    poff[E] = po;
-    mt_off[E] = po / kBM;
-    pt_off[E] = pt;
-    hv_off[E] = hv;
-    lt_off[E] = lt;
-    hdr[kHdrRpTotal] = po;
-    hdr[kHdrMtTotal] = po / kBM;
-    hdr[kHdrDone] = 0;
+    // exclusive scan of the lanes' sums
+    int x[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) {
+      int inc = v[i];
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += y;
+      }
+      x[i] = inc - v[i];
+    }
+    for (int e = e0; e < e1; ++e) {
+      offsets[e] = x[0];
+      poff[e] = x[1];
+      mt_off[e] = x[1] / kBM;
+      pt_off[e] = x[2];
+      hv_off[e] = x[3];
+      lt_off[e] = x[4];
+      int d[5];
+      sizes(e, d[0], d[1], d[2], d[3], d[4]);
+#pragma unroll
+      for (int i = 0; i < 5; ++i) x[i] += d[i];
+    }
+    if (lane == 31) {
+      offsets[E] = x[0];
+      poff[E] = x[1];
+      mt_off[E] = x[1] / kBM;
+      pt_off[E] = x[2];
+      hv_off[E] = x[3];
+      lt_off[E] = x[4];
+      hdr[kHdrRpTotal] = x[1];
+      hdr[kHdrMtTotal] = x[1] / kBM;
+      hdr[kHdrDone] = 0;
+    }
   }
 }
 
@@ -158,6 +233,7 @@ __global__ void __launch_bounds__(kSchedThreads) sched_topk_hist_kernel(
     int* __restrict__ offsets, int* __restrict__ poff, int* __restrict__ mt_off,
     int* __restrict__ pt_off) {
   __shared__ int sh[kMaxE];
+  __shared__ int aux[kSchedThreads];
   __shared__ int sh_last;
   const int tid = threadIdx.x, lane = tid & 31;
   for (int e = tid; e < E; e += blockDim.x) sh[e] = 0;
@@ -181,7 +257,7 @@ __global__ void __launch_bounds__(kSchedThreads) sched_topk_hist_kernel(
   __syncthreads();
   if (!sh_last) return;
   __threadfence();
-  finish_histograms(hist, gridDim.x, E, hdr, counts, offsets, poff, mt_off, pt_off, sh);
+  finish_histograms(hist, gridDim.x, E, hdr, counts, offsets, poff, mt_off, pt_off, sh, aux);
 }
 
 __global__ void __launch_bounds__(kSchedThreads) sched_hist_kernel(
@@ -189,6 +265,7 @@ __global__ void __launch_bounds__(kSchedThreads) sched_hist_kernel(
     int* __restrict__ counts, int* __restrict__ offsets, int* __restrict__ poff,
     int* __restrict__ mt_off, int* __restrict__ pt_off) {
   __shared__ int sh[kMaxE];
+  __shared__ int aux[kSchedThreads];
   __shared__ int sh_last;
   const int tid = threadIdx.x;
   for (int e = tid; e < E; e += blockDim.x) sh[e] = 0;
@@ -203,7 +280,7 @@ __global__ void __launch_bounds__(kSchedThreads) sched_hist_kernel(
   __syncthreads();
   if (!sh_last) return;
   __threadfence();
-  finish_histograms(hist, gridDim.x, E, hdr, counts, offsets, poff, mt_off, pt_off, sh);
+  finish_histograms(hist, gridDim.x, E, hdr, counts, offsets, poff, mt_off, pt_off, sh, aux);
 }
 
 __global__ void __launch_bounds__(kSchedThreads) sched_scatter_kernel(
