@@ -33,7 +33,8 @@ WsLayout ws_layout(const moe_config* c) {
   const int64_t nonempty = c->E < L.R ? c->E : L.R;
   L.Rp_max = (int64_t)align_up((size_t)(L.R + nonempty * (kBM - 1)), kBM);
   L.MT_max = L.Rp_max / kBM;
-  L.nblk = (c->T + sched_chunk_tokens(c->k) - 1) / sched_chunk_tokens(c->k);
+  const int tb = sched_chunk_tokens(c->T, c->k);
+  L.nblk = (c->T + tb - 1) / tb;
   L.nt_dg = (c->f + 255) / 256;
   const size_t A = 1024;
   size_t off = 0;

@@ -64,15 +64,6 @@ enum Epi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2, EPI_LOGITS = 3 };
 // heavy kernel leaves room (shared memory, TMEM) for one light CTA per SM.
 // Their pipeline depths (stages) share one SM's shared memory.
 enum UnitSet { UNITS_ALL = 0, UNITS_HEAVY = 1, UNITS_LIGHT = 2 };
-// Thin pair units of at most 32 rows take two K blocks per pipeline stage
-// (36 KB stages, five of them): such a unit mostly streams its weight slice
-// from HBM, and with one 16 KB K block of weights per 32 KB stage it kept
-// too few bytes in flight per SM to stream at the SM's L2 ingress rate.
-#ifndef MOE_THIN_DOUBLE
-#define MOE_THIN_DOUBLE 0
-#endif
-constexpr int kThinDblRows = 32;  // MMA N of a double-stage thin unit (16 rows per CTA)
-
 #ifndef MOE_SPLIT_HEAVY_STAGES
 #define MOE_SPLIT_HEAVY_STAGES 3
 #endif
@@ -86,14 +77,11 @@ struct KCfg {
   static_assert(UM == UNITS_ALL || (PAIR && !WGRAD), "unit sets split the row pair GEMMs");
   // a light unit's stage: its weight slice (MMA A) and at most 16 of its rows
   // per CTA (MMA B, nt <= kLightRows)
-  // double-stage thin units: two K blocks of weights (2 x 16 KB) and of
-  // their 16 rows (2 x 2 KB) per stage
-  static constexpr bool kThinDbl = MOE_THIN_DOUBLE && PAIR && !WGRAD && UM == UNITS_ALL;
   static constexpr int kStageBytes = UM == UNITS_LIGHT ? kABytes + 16 * 128
-                                     : kABytes + (PAIR ? kBHalfBytes : kBBytes) + (kThinDbl ? 4096 : 0);
+                                                       : kABytes + (PAIR ? kBHalfBytes : kBBytes);
   static constexpr int kStages = UM == UNITS_HEAVY ? MOE_SPLIT_HEAVY_STAGES
                                  : UM == UNITS_LIGHT ? MOE_SPLIT_LIGHT_STAGES
-                                 : PAIR ? (kThinDbl ? 5 : 6) : (FP8 && EPI == EPI_STORE) ? 3 : 4;
+                                 : PAIR ? 6 : (FP8 && EPI == EPI_STORE) ? 3 : 4;
   // swizzled staging tiles per epilogue warp for the TMA-store epilogues
   // (light units only need their transpose tiles)
   static constexpr int kOutBufs = (UM == UNITS_LIGHT && EPI == EPI_STORE) ? 1
@@ -168,7 +156,6 @@ struct Tile {
   int nt;      // thin pair unit: MMA N (rows rounded up to 32), half in each CTA
   bool thin;   // tile computed as (weights)^T x (rows)^T, tokens on N
   bool valid;  // pair mode: the odd CTA's tile past the expert's last tile is not
-  bool dbl;    // thin pair unit with two K blocks per stage (kb_count counts stages)
 };
 
 // Work units: tiles, or in pair mode pairs of M-adjacent tiles of one expert
@@ -204,7 +191,6 @@ template <bool WGRAD, bool PAIR, int UM = UNITS_ALL>
 __device__ __forceinline__ Tile decode(const Params& p, int L, int rank) {
   Tile t;
   t.valid = true;
-  t.dbl = false;
   if (!WGRAD && p.mt_off == nullptr) {
     // dense: tile m of one [T, K] matrix
     t.e = 0;
@@ -253,11 +239,6 @@ __device__ __forceinline__ Tile decode(const Params& p, int L, int rank) {
       const int cnt = __ldg(p.counts + e);
       t.rows = min(kBM, cnt - mrel * kBM);
       if (!PAIR && p.thin && thin_tile(t.rows, cnt)) t.thin = true;
-    }
-    if (MOE_THIN_DOUBLE && PAIR && UM == UNITS_ALL && t.thin && t.nt == kThinDblRows &&
-        (p.num_kb & 1) == 0) {
-      t.dbl = true;
-      t.kb_count = p.num_kb >> 1;
     }
   } else {
     t.nt = 0;
@@ -493,8 +474,7 @@ __global__ void __launch_bounds__(kThreads, UM == UNITS_ALL ? 1 : 2)
         const Tile t = decode<WGRAD, PAIR, UM>(p, U, rank);
         // bytes landing on this stage's "full" barrier (pair: both CTAs' copies)
         uint32_t tx = (t.valid ? (uint32_t)kABytes : 0u) + b_bytes + (FP8 ? (uint32_t)kSfBytes : 0u);
-        if (PAIR && t.thin)  // weights + half the rows, of one or two K blocks
-          tx = (16384u + (uint32_t)(t.nt / 2) * 128u) * (t.dbl ? 2u : 1u);
+        if (PAIR && t.thin) tx = 16384u + (uint32_t)(t.nt / 2) * 128u;  // weights + half the rows
         if (PAIR && rank == 0)
           tx += t.thin ? tx : (decode<WGRAD, PAIR, UM>(p, U, 1).valid ? (uint32_t)kABytes : 0u) + b_bytes;
         for (int kb = 0; kb < t.kb_count; ++kb) {
@@ -550,28 +530,20 @@ __global__ void __launch_bounds__(kThreads, UM == UNITS_ALL ? 1 : 2)
                 if constexpr (PAIR) tma_load_3d_pair_hint(sa + off, &tmB, fb, c0, c1, t.e, pol_stream);
                 else tma_load_3d_hint(sa + off, &tmB, fb, c0, c1, t.e, pol_stream);
               };
-              // a double stage holds K blocks 2kb and 2kb + 1: weights at 0 and
-              // 16 KB, their 16 rows at 32 KB and 34 KB
-              const int nsub = t.dbl ? 2 : 1;
-              for (int u = 0; u < nsub; ++u) {
-                const int kk = t.dbl ? 2 * kb + u : kb;
-                const uint32_t wo = (uint32_t)u * 16384u;
-                if (EPI == EPI_SWIGLU) {
-                  const int c0 = t.n * p.hn + rank * 64;
-                  loadw(wo, c0, kk * BK);
-                  loadw(wo + 8192u, p.f + c0, kk * BK);
-                } else if (B_MN) {
-                  const int c0 = t.n * 256 + rank * 128;
-                  loadw(wo, c0, kk * BK);
-                  loadw(wo + 8192u, c0 + 64, kk * BK);
-                } else {
-                  loadw(wo, kk * BK, t.n * 256 + rank * 128);
-                }
-                const int nt2 = t.nt / 2;
-                const uint32_t ro = t.dbl ? 32768u + (uint32_t)u * 2048u : (uint32_t)kABytes;
-                for (int i = 0; i < nt2; i += 16)
-                  load2(ro + (uint32_t)(i * 128), &tmA2, kk * BK, t.row0 + rank * nt2 + i);
+              if (EPI == EPI_SWIGLU) {
+                const int c0 = t.n * p.hn + rank * 64;
+                loadw(0u, c0, kb * BK);
+                loadw(8192u, p.f + c0, kb * BK);
+              } else if (B_MN) {
+                const int c0 = t.n * 256 + rank * 128;
+                loadw(0u, c0, kb * BK);
+                loadw(8192u, c0 + 64, kb * BK);
+              } else {
+                loadw(0u, kb * BK, t.n * 256 + rank * 128);
               }
+              const int nt2 = t.nt / 2;
+              for (int i = 0; i < nt2; i += 16)
+                load2((uint32_t)(kABytes + i * 128), &tmA2, kb * BK, t.row0 + rank * nt2 + i);
             } else {
               for_each_box<WGRAD, A_MN, B_MN, EPI, PAIR>(p, t, kb, rank, &tmA, &tmB, load2, load3);
             }
@@ -670,17 +642,12 @@ __global__ void __launch_bounds__(kThreads, UM == UNITS_ALL ? 1 : 2)
                 // = W^T x rows^T
                 constexpr bool kWmn = (EPI == EPI_SWIGLU) || B_MN;  // weights MN-major in smem
                 const uint32_t idt = idesc_bf16(2 * kBM, t.nt, kWmn, false);
-                const int nsub = t.dbl ? 2 : 1;
-                for (int u = 0; u < nsub; ++u) {
-                  const uint32_t wa = sa + (uint32_t)u * 16384u;
-                  const uint32_t ra = t.dbl ? sa + 32768u + (uint32_t)u * 2048u : sb;
 #pragma unroll
-                  for (int kk = 0; kk < BK / 16; ++kk)
-                    tc_mma_f16_pair(dt, kWmn ? sdesc_sw128(wa + kk * 2048, 8192, 1024)
-                                             : sdesc_sw128(wa + kk * 32, 16, 1024),
-                                    sdesc_sw128(ra + kk * 32, 16, 1024), idt,
-                                    (kb > 0 || u > 0 || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < BK / 16; ++kk)
+                  tc_mma_f16_pair(dt, kWmn ? sdesc_sw128(sa + kk * 2048, 8192, 1024)
+                                           : sdesc_sw128(sa + kk * 32, 16, 1024),
+                                  sdesc_sw128(sb + kk * 32, 16, 1024), idt,
+                                  (kb > 0 || kk > 0) ? 1u : 0u);
                 issued = true;
               }
             }

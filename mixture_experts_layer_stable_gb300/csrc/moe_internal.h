@@ -68,10 +68,16 @@ inline bool gemm_clc_enabled(const moe_config&) { return g_tile_scheduler == 1; 
 // rows (the thin pair unit of an expert with a few rows), which streams its
 // weight slice with little to compute.
 constexpr int kLightRows = 32;
-constexpr int kSchedChunk = 256;  // at most this many routed rows per histogram / scatter block
+constexpr int kSchedChunk = 256;   // at most this many routed rows per histogram / scatter block
+constexpr int kSchedBlocks = 152;  // chunks shrink until the schedule has this many blocks
 // Tokens per schedule chunk: whole tokens (their k rows each), at most
-// kSchedChunk rows.
-__host__ __device__ inline int sched_chunk_tokens(int k) { return kSchedChunk / k > 0 ? kSchedChunk / k : 1; }
+// kSchedChunk rows, fewer for small T so that the schedule kernels still
+// spread over about kSchedBlocks blocks.
+__host__ __device__ inline int sched_chunk_tokens(int T, int k) {
+  const int cap = kSchedChunk / k > 0 ? kSchedChunk / k : 1;
+  const int want = (T + kSchedBlocks - 1) / kSchedBlocks;
+  return want < 1 ? 1 : (want < cap ? want : cap);
+}
 constexpr int kSchedThreads = 256;
 constexpr int kMaxE = 1024;
 constexpr int kMaxK = 32;

@@ -7,8 +7,8 @@
 // one table serves all four transfer modes, at < 3 % of the MoE runtime).
 //
 // Two kernels after a clear of the header words, no host synchronisation.
-// Rows are handled in chunks of sched_chunk_tokens(k) tokens (their k rows
-// each, at most kSchedChunk rows):
+// Rows are handled in chunks of sched_chunk_tokens(T, k) tokens (their k rows
+// each, at most kSchedChunk rows, about kSchedBlocks chunks for small T):
 //  1. sched_topk_hist: per chunk, one warp per token runs k rounds of a warp
 //     arg-max over the E fp32 logits (value descending, id ascending);
 //     weights = softmax over the k selected logits in fp32, summed in slot
@@ -38,21 +38,28 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
   return (v > bv) || (v == bv && i < bi);
 }
 
-// Top-k of token t by one warp, NCH chunks of 32 logits per lane (E <= 32 NCH):
-// lane j < k returns the j-th pick in *id and its weight in *w.
+// Logits of token t for one warp: NCH chunks of 32 per lane (E <= 32 NCH);
+// zeros past E (excluded from the top-k by topk_token).
 template <int NCH>
-__device__ __forceinline__ void topk_token(const float* __restrict__ logits, int t, int E, int k,
-                                           int lane, int* id, float* w) {
-  float v[NCH];
-  uint32_t taken = 0;
+__device__ __forceinline__ void load_logits(const float* __restrict__ logits, int t, int E, int lane,
+                                            float (&v)[NCH]) {
   const float* zrow = logits + (size_t)t * E;
 #pragma unroll
   for (int c = 0; c < NCH; ++c) {
     const int e = c * 32 + lane;
-    const bool in = e < E;
-    v[c] = in ? __ldg(zrow + e) : 0.f;
-    if (!in) taken |= 1u << c;
+    v[c] = e < E ? __ldg(zrow + e) : 0.f;
   }
+}
+
+// Top-k of one token's logits v (load_logits) by one warp: lane j < k
+// returns the j-th pick in *id and its weight in *w.
+template <int NCH>
+__device__ __forceinline__ void topk_token(const float (&v)[NCH], int E, int k, int lane, int* id,
+                                           float* w) {
+  uint32_t taken = 0;
+#pragma unroll
+  for (int c = 0; c < NCH; ++c)
+    if (c * 32 + lane >= E) taken |= 1u << c;
   int my_id = 0;
   float my_v = 0.f;
   for (int r = 0; r < k; ++r) {
@@ -239,10 +246,17 @@ __global__ void __launch_bounds__(kSchedThreads) sched_topk_hist_kernel(
   for (int e = tid; e < E; e += blockDim.x) sh[e] = 0;
   __syncthreads();
   const int t0 = blockIdx.x * tb, t1 = min(T, t0 + tb);
-  for (int t = t0 + (tid >> 5); t < t1; t += kWarps) {
+  // the next token's logits are loaded while this one's top-k runs
+  float v[NCH] = {}, vn[NCH] = {};
+  int t = t0 + (tid >> 5);
+  if (t < t1) load_logits<NCH>(logits, t, E, lane, v);
+  for (; t < t1; t += kWarps) {
+    if (t + kWarps < t1) load_logits<NCH>(logits, t + kWarps, E, lane, vn);
     int id;
     float w;
-    topk_token<NCH>(logits, t, E, k, lane, &id, &w);
+    topk_token<NCH>(v, E, k, lane, &id, &w);
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) v[c] = vn[c];
     if (lane < k) {
       ids[(size_t)t * k + lane] = id;
       wts[(size_t)t * k + lane] = w;
@@ -356,7 +370,7 @@ cudaError_t launch_scatter(const moe_config& c, const moe_sched& s, const Ws& ws
   TraceScope ts("sched_scatter", st);
   sched_scatter_kernel<<<(int)ws.L.nblk, kSchedThreads, 0, st>>>(
       s.topk_ids, s.topk_w, R, c.E, ws.hist(), s.counts, s.offsets, ws.poff(), s.perm, s.inv,
-      ws.pos_pad(), ws.row_of_pad(), ws.g_pad(), sched_chunk_tokens(c.k) * c.k);
+      ws.pos_pad(), ws.row_of_pad(), ws.g_pad(), sched_chunk_tokens(c.T, c.k) * c.k);
   return cudaGetLastError();
 }
 }  // namespace
@@ -368,7 +382,7 @@ cudaError_t launch_schedule_tail(const moe_config& c, const moe_sched& s, const 
   {
     TraceScope ts("sched_hist", st);
     sched_hist_kernel<<<(int)ws.L.nblk, kSchedThreads, 0, st>>>(
-        s.topk_ids, R, c.E, sched_chunk_tokens(c.k) * c.k, ws.hist(), ws.hdr(), s.counts, s.offsets,
+        s.topk_ids, R, c.E, sched_chunk_tokens(c.T, c.k) * c.k, ws.hist(), ws.hdr(), s.counts, s.offsets,
         ws.poff(), ws.mt_off(), ws.pt_off());
     err = cudaGetLastError();
   }
@@ -378,7 +392,7 @@ cudaError_t launch_schedule_tail(const moe_config& c, const moe_sched& s, const 
 
 cudaError_t launch_schedule_from_logits(const moe_config& c, const float* logits, const moe_sched& s,
                                         const Ws& ws, cudaStream_t st) {
-  const int nb = (int)ws.L.nblk, tb = sched_chunk_tokens(c.k);
+  const int nb = (int)ws.L.nblk, tb = sched_chunk_tokens(c.T, c.k);
   cudaError_t err;
   {
     TraceScope ts("sched_topk_hist", st);
