@@ -423,30 +423,52 @@ __global__ void __launch_bounds__(256) quant_weights_kernel(const __nv_bfloat16*
 }
 
 // Rows [rows, K] bf16 (K contiguous) -> E4M3 codes [rows, K] and scale tiles,
-// blocks of 32 along K: one thread per (row, block), consecutive threads on
-// consecutive blocks of a row.  rows_dev (optional) caps the rows at a
-// device-side count (the padded row total of the schedule).
+// blocks of 32 along K.  Each lane takes 8 consecutive elements (one 16-byte
+// load, a warp 512 contiguous bytes); the 4 lanes of a 32-element block share
+// its maximum through two shuffles, and each stores its 8 codes.  The same
+// scale rule and rounding steps as mx_quant32.  rows_dev (optional) caps the
+// rows at a device-side count (the padded row total of the schedule).
 __global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16* __restrict__ w,
                                                          int64_t rows, int K, const int* rows_dev,
                                                          uint8_t* __restrict__ q, uint8_t* __restrict__ sc) {
-  const int nkb = K >> 5;
+  const int lane = threadIdx.x & 31;
   const int64_t nr = rows_dev ? (int64_t)*rows_dev : rows;
-  const int64_t total = nr * nkb;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = i / nkb;
-    const int kb = (int)(i - r * nkb);
-    const uint4* src = reinterpret_cast<const uint4*>(w + r * K + (int64_t)kb * 32);
-    uint4 in[4];
+  const int64_t nv = nr * (K >> 3);  // 8-element vectors; K % 32 == 0, so a block never straddles warps
+  const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t base = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * 32; base < nv;
+       base += nw * 32) {
+    const int64_t i = base + lane;
+    const bool in = i < nv;
+    float f[8];
+    {
+      const uint4 v = in ? ldg_nc_v4(reinterpret_cast<const uint4*>(w) + i) : make_uint4(0, 0, 0, 0);
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) in[u] = ldg_nc_v4(src + u);
-    uint4 out[2];
-    uint8_t s8;
-    quant32(in, out, s8);
-    uint4* qv = reinterpret_cast<uint4*>(q + r * K + (int64_t)kb * 32);
-    stg_v4(qv, out[0]);
-    stg_v4(qv + 1, out[1]);
-    sc[mx_sf_offset((size_t)r, kb, K >> 7)] = s8;
+      for (int j = 0; j < 4; ++j) {
+        const float2 p2 = __bfloat1622float2(h[j]);
+        f[2 * j] = p2.x;
+        f[2 * j + 1] = p2.y;
+      }
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const int sx = mx_scale_exp(amax);
+    const int s1 = -sx / 2, s2 = -sx - s1;
+    const float f1 = mx_exp2i(s1), f2 = mx_exp2i(s2);
+    if (in) {
+      uint2 cw;
+      cw.x = mx_pack4(f[0] * f1 * f2, f[1] * f1 * f2, f[2] * f1 * f2, f[3] * f1 * f2);
+      cw.y = mx_pack4(f[4] * f1 * f2, f[5] * f1 * f2, f[6] * f1 * f2, f[7] * f1 * f2);
+      *reinterpret_cast<uint2*>(q + i * 8) = cw;
+      if ((lane & 3) == 0) {
+        const int64_t r = (i * 8) / K;
+        const int kb = (int)((i * 8 - r * K) >> 5);
+        sc[mx_sf_offset((size_t)r, kb, K >> 7)] = (uint8_t)(sx + 127);
+      }
+    }
   }
 }
 
@@ -454,38 +476,44 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16* __
 // K contiguous) -> codes qt [K, ld] (row k holds column k of src, rows
 // contiguous) and scale tiles over [K, ld], blocks of 32 rows: the K-major
 // operand of a weight-gradient GEMM that contracts over the rows.  A CTA
-// stages 32 rows x 256 columns through shared memory; thread c then holds
-// column c's 32 values, one block.  Rows past the device-side count
+// stages 64 rows x 256 columns through shared memory; thread c then holds
+// column c's values, two blocks of 32.  Rows past the device-side count
 // (*rows_dev) are left alone.
 __global__ void __launch_bounds__(256) quant_cols_kernel(const __nv_bfloat16* __restrict__ src, int K,
                                                          const int* __restrict__ rows_dev, int ld,
                                                          uint8_t* __restrict__ qt, uint8_t* __restrict__ sct) {
-  __shared__ __nv_bfloat16 tile[32][256 + 8];
+  constexpr int kR = 64;  // rows per block: two 32-row blocks per column
+  __shared__ __align__(16) __nv_bfloat16 tile[kR][256 + 8];
   const int rows = *rows_dev;
-  const int r0 = blockIdx.x * 32, c0 = blockIdx.y * 256;
+  const int r0 = blockIdx.x * kR, c0 = blockIdx.y * 256;
   if (r0 >= rows) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // each warp loads 4 rows of 256 columns: 32 lanes x 8 columns (16 bytes)
-  for (int rr = warp; rr < 32; rr += 8) {
-    const int c = c0 + lane * 8;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (c < K) v = ldg_nc_v4(src + (size_t)(r0 + rr) * K + c);
-    const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&v);
+  // each warp loads 8 rows of 256 columns: 32 lanes x 8 columns (16 bytes),
+  // all eight loads in flight before the first store to shared memory
+  uint4 v8[kR / 8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) tile[rr][lane * 8 + j] = h[j];
+  for (int j = 0; j < kR / 8; ++j) {
+    const int rr = warp + 8 * j, c = c0 + lane * 8;
+    v8[j] = (c < K && r0 + rr < rows) ? ldg_nc_v4(src + (size_t)(r0 + rr) * K + c) : make_uint4(0, 0, 0, 0);
   }
+#pragma unroll
+  for (int j = 0; j < kR / 8; ++j) *reinterpret_cast<uint4*>(&tile[warp + 8 * j][lane * 8]) = v8[j];
   __syncthreads();
   const int c = c0 + tid;
   if (c >= K) return;
-  float v[32];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __bfloat162float(tile[i][tid]);
-  uint4 lo, hi;
-  const uint8_t s8 = mx_quant32(v, lo, hi);
-  uint4* qv = reinterpret_cast<uint4*>(qt + (size_t)c * ld + r0);
-  stg_v4(qv, lo);
-  stg_v4(qv + 1, hi);
-  sct[mx_sf_offset((size_t)c, r0 >> 5, ld >> 7)] = s8;
+  for (int h = 0; h < kR / 32; ++h) {
+    if (r0 + 32 * h >= rows) break;
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __bfloat162float(tile[32 * h + i][tid]);
+    uint4 lo, hi;
+    const uint8_t s8 = mx_quant32(v, lo, hi);
+    uint4* qv = reinterpret_cast<uint4*>(qt + (size_t)c * ld + r0 + 32 * h);
+    stg_v4(qv, lo);
+    stg_v4(qv + 1, hi);
+    sct[mx_sf_offset((size_t)c, (r0 >> 5) + h, ld >> 7)] = s8;
+  }
 }
 
 // One CTA per token (grid-stride); each thread owns 8-column vectors.
@@ -638,9 +666,9 @@ cudaError_t launch_quantize_mxfp8(const __nv_bfloat16* w, int64_t batch, int K, 
 
 cudaError_t launch_quant_rows(const __nv_bfloat16* w, int64_t rows, int K, const int* rows_dev,
                               uint8_t* q, uint8_t* sc, cudaStream_t st, const char* name) {
-  const int64_t total = rows * (K / 32);
+  const int64_t total = rows * (K / 8);  // 8-element vectors, one per thread
   int64_t blocks = (total + 255) / 256;
-  const int64_t cap = (int64_t)num_sms() * 16;
+  const int64_t cap = (int64_t)num_sms() * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   TraceScope ts(name, st);
@@ -650,7 +678,7 @@ cudaError_t launch_quant_rows(const __nv_bfloat16* w, int64_t rows, int K, const
 
 cudaError_t launch_quant_cols(const __nv_bfloat16* src, int64_t max_rows, int K, const int* rows_dev,
                               uint8_t* qt, uint8_t* sct, int ld, cudaStream_t st, const char* name) {
-  dim3 grid((unsigned)((max_rows + 31) / 32), (unsigned)((K + 255) / 256));
+  dim3 grid((unsigned)((max_rows + 63) / 64), (unsigned)((K + 255) / 256));
   TraceScope ts(name, st);
   quant_cols_kernel<<<grid, 256, 0, st>>>(src, K, rows_dev, ld, qt, sct);
   return cudaGetLastError();

@@ -64,6 +64,12 @@ enum Epi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2, EPI_LOGITS = 3 };
 // heavy kernel leaves room (shared memory, TMEM) for one light CTA per SM.
 // Their pipeline depths (stages) share one SM's shared memory.
 enum UnitSet { UNITS_ALL = 0, UNITS_HEAVY = 1, UNITS_LIGHT = 2 };
+// Order of an expert's units: N tile by N tile with its M units fastest (1),
+// or in blocks of MOE_UNIT_NBLOCK N tiles with the M units fastest inside.
+#ifndef MOE_UNIT_NBLOCK
+#define MOE_UNIT_NBLOCK 1
+#endif
+
 #ifndef MOE_SPLIT_HEAVY_STAGES
 #define MOE_SPLIT_HEAVY_STAGES 3
 #endif
@@ -209,7 +215,14 @@ __device__ __forceinline__ Tile decode(const Params& p, int L, int rank) {
     const int ue = __ldg(uoff + e + 1) - u0;
     const int m0 = PAIR ? __ldg(p.mt_off + e) : u0;
     const int loc = L - u0 * p.n_tiles;
+#if MOE_UNIT_NBLOCK > 1
+    // units in blocks of NB N tiles, the expert's M units fastest inside
+    const int nbk = (p.n_tiles % MOE_UNIT_NBLOCK == 0) ? MOE_UNIT_NBLOCK : 1;
+    const int blk = loc / (ue * nbk), rr = loc - blk * ue * nbk;
+    int mrel = rr / nbk;
+#else
     int mrel = loc % ue;
+#endif
     t.rows = kBM;
     t.nt = 0;
     t.thin = false;
@@ -229,7 +242,11 @@ __device__ __forceinline__ Tile decode(const Params& p, int L, int rank) {
       }
     }
     t.e = e;
+#if MOE_UNIT_NBLOCK > 1
+    t.n = blk * nbk + (rr - (rr / nbk) * nbk);
+#else
     t.n = loc / ue;
+#endif
     t.m = m0 + mrel;
     t.row0 = t.m * kBM;
     t.kb_count = p.num_kb;
@@ -990,13 +1007,32 @@ __global__ void __launch_bounds__(kThreads, UM == UNITS_ALL ? 1 : 2)
         const int kq = (2 * p.f) >> 7, kt = p.ldt >> 7;
         const float gw = p.g_pad[row];
         float dg = 0.f;
+        // fragments of A, H_gate, H_up for the next 32 columns are loaded while
+        // the current ones are processed
+        uint4 nxt[12];
+        auto fetch = [&](int col) {
+          const uint4* a = reinterpret_cast<const uint4*>(p.As + row * p.f + col);
+          const uint4* g = reinterpret_cast<const uint4*>(p.Hs + row * (2 * p.f) + col);
+          const uint4* u = reinterpret_cast<const uint4*>(p.Hs + row * (2 * p.f) + p.f + col);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            nxt[i] = __ldg(a + i);
+            nxt[4 + i] = __ldg(g + i);
+            nxt[8 + i] = __ldg(u + i);
+          }
+        };
+        if (t.n * 256 < p.f) fetch(t.n * 256);
         for (int c = 0; c < 256; c += 32) {
           const int col = t.n * 256 + c;
           if (col >= p.f) break;
           float da[32], av[32], hg[32], hu[32], o1[32], o2[32], o3[32];
-          load32_bf16(p.As + row * p.f + col, av);
-          load32_bf16(p.Hs + row * (2 * p.f) + col, hg);
-          load32_bf16(p.Hs + row * (2 * p.f) + p.f + col, hu);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            unpack8(nxt[i], av + 8 * i);
+            unpack8(nxt[4 + i], hg + 8 * i);
+            unpack8(nxt[8 + i], hu + 8 * i);
+          }
+          if (c + 32 < 256 && col + 32 < p.f) fetch(col + 32);
           tmem_ld32(tb + c, da);
 #pragma unroll
           for (int i = 0; i < 32; ++i) {

@@ -73,9 +73,9 @@ __device__ __forceinline__ uint8_t mx_quant32(const float* v, uint4& lo, uint4& 
 // lane's E4M3 code (same rounding and scale steps as mx_quant32).  Returns
 // the code; *scale gets the scale byte (s + 127) in every lane.
 __device__ __forceinline__ uint8_t mx_quant_lane(float v, uint8_t* scale) {
-  float amax = fabsf(v);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  // the bit patterns of non-negative floats order as their values: one
+  // warp-wide integer max gives the block maximum of |v|
+  const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v))));
   const int s = mx_scale_exp(amax);
   const int s1 = -s / 2, s2 = -s - s1;
   const float y = v * mx_exp2i(s1) * mx_exp2i(s2);
