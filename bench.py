@@ -105,7 +105,9 @@ def load_peaks():
 KERNEL_SOURCE = {"ring_forward": "ring.cu", "gather": "gather_merge.cu", "gather_x_dy": "gather_merge.cu",
                  "gather_mxfp8": "gather_merge.cu", "merge": "gather_merge.cu",
                  "reverse_dispatch": "gather_merge.cu", "dg_reduce": "gather_merge.cu",
-                 "sched_topk_hist": "sched.cu", "sched_hist": "sched.cu", "sched_scatter": "sched.cu"}
+                 "sched_topk_hist": "sched.cu", "sched_hist": "sched.cu", "sched_scatter": "sched.cu",
+                 "quant_dy_rows": "gather_merge.cu", "quant_x_cols": "gather_merge.cu",
+                 "quant_dy_cols": "gather_merge.cu", "quantize_weights": "gather_merge.cu"}
 
 
 def strip_comments(text):

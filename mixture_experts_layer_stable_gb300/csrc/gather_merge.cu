@@ -423,50 +423,57 @@ __global__ void __launch_bounds__(256) quant_weights_kernel(const __nv_bfloat16*
 }
 
 // Rows [rows, K] bf16 (K contiguous) -> E4M3 codes [rows, K] and scale tiles,
-// blocks of 32 along K.  Each lane takes 8 consecutive elements (one 16-byte
-// load, a warp 512 contiguous bytes); the 4 lanes of a 32-element block share
-// its maximum through two shuffles, and each stores its 8 codes.  The same
-// scale rule and rounding steps as mx_quant32.  rows_dev (optional) caps the
-// rows at a device-side count (the padded row total of the schedule).
+// blocks of 32 along K.  A warp takes 4 x 512 contiguous bytes at a time, all
+// four 16-byte loads of a lane in flight together; a lane holds 8 consecutive
+// elements of each, the 4 lanes of a 32-element block share its maximum
+// through two shuffles, and each lane stores its 8 codes.  The same scale rule
+// and rounding steps as mx_quant32.  rows_dev (optional) caps the rows at a
+// device-side count (the padded row total of the schedule).
 __global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16* __restrict__ w,
                                                          int64_t rows, int K, const int* rows_dev,
                                                          uint8_t* __restrict__ q, uint8_t* __restrict__ sc) {
+  constexpr int kU = 4;  // 512-byte segments per warp iteration
   const int lane = threadIdx.x & 31;
   const int64_t nr = rows_dev ? (int64_t)*rows_dev : rows;
-  const int64_t nv = nr * (K >> 3);  // 8-element vectors; K % 32 == 0, so a block never straddles warps
+  const int64_t nv = nr * (K >> 3);  // 8-element vectors; K % 32 == 0, so a block never straddles segments
   const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
-  for (int64_t base = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * 32; base < nv;
-       base += nw * 32) {
-    const int64_t i = base + lane;
-    const bool in = i < nv;
-    float f[8];
-    {
-      const uint4 v = in ? ldg_nc_v4(reinterpret_cast<const uint4*>(w) + i) : make_uint4(0, 0, 0, 0);
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+  for (int64_t base = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * (32 * kU); base < nv;
+       base += nw * 32 * kU) {
+    uint4 raw[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t i = base + u * 32 + lane;
+      raw[u] = i < nv ? ldg_nc_v4(reinterpret_cast<const uint4*>(w) + i) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t i = base + u * 32 + lane;
+      float f[8];
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[u]);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const float2 p2 = __bfloat1622float2(h[j]);
         f[2 * j] = p2.x;
         f[2 * j + 1] = p2.y;
       }
-    }
-    float amax = 0.f;
+      float amax = 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    const int sx = mx_scale_exp(amax);
-    const int s1 = -sx / 2, s2 = -sx - s1;
-    const float f1 = mx_exp2i(s1), f2 = mx_exp2i(s2);
-    if (in) {
-      uint2 cw;
-      cw.x = mx_pack4(f[0] * f1 * f2, f[1] * f1 * f2, f[2] * f1 * f2, f[3] * f1 * f2);
-      cw.y = mx_pack4(f[4] * f1 * f2, f[5] * f1 * f2, f[6] * f1 * f2, f[7] * f1 * f2);
-      *reinterpret_cast<uint2*>(q + i * 8) = cw;
-      if ((lane & 3) == 0) {
-        const int64_t r = (i * 8) / K;
-        const int kb = (int)((i * 8 - r * K) >> 5);
-        sc[mx_sf_offset((size_t)r, kb, K >> 7)] = (uint8_t)(sx + 127);
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      const int sx = mx_scale_exp(amax);
+      const int s1 = -sx / 2, s2 = -sx - s1;
+      const float f1 = mx_exp2i(s1), f2 = mx_exp2i(s2);
+      if (i < nv) {
+        uint2 cw;
+        cw.x = mx_pack4(f[0] * f1 * f2, f[1] * f1 * f2, f[2] * f1 * f2, f[3] * f1 * f2);
+        cw.y = mx_pack4(f[4] * f1 * f2, f[5] * f1 * f2, f[6] * f1 * f2, f[7] * f1 * f2);
+        *reinterpret_cast<uint2*>(q + i * 8) = cw;
+        if ((lane & 3) == 0) {
+          const int64_t r = (i * 8) / K;
+          const int kb = (int)((i * 8 - r * K) >> 5);
+          sc[mx_sf_offset((size_t)r, kb, K >> 7)] = (uint8_t)(sx + 127);
+        }
       }
     }
   }
@@ -666,7 +673,7 @@ cudaError_t launch_quantize_mxfp8(const __nv_bfloat16* w, int64_t batch, int K, 
 
 cudaError_t launch_quant_rows(const __nv_bfloat16* w, int64_t rows, int K, const int* rows_dev,
                               uint8_t* q, uint8_t* sc, cudaStream_t st, const char* name) {
-  const int64_t total = rows * (K / 8);  // 8-element vectors, one per thread
+  const int64_t total = rows * (K / 8) / 4;  // four 8-element vectors per thread and iteration
   int64_t blocks = (total + 255) / 256;
   const int64_t cap = (int64_t)num_sms() * 8;
   if (blocks > cap) blocks = cap;

@@ -64,12 +64,6 @@ enum Epi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2, EPI_LOGITS = 3 };
 // heavy kernel leaves room (shared memory, TMEM) for one light CTA per SM.
 // Their pipeline depths (stages) share one SM's shared memory.
 enum UnitSet { UNITS_ALL = 0, UNITS_HEAVY = 1, UNITS_LIGHT = 2 };
-// Order of an expert's units: N tile by N tile with its M units fastest (1),
-// or in blocks of MOE_UNIT_NBLOCK N tiles with the M units fastest inside.
-#ifndef MOE_UNIT_NBLOCK
-#define MOE_UNIT_NBLOCK 1
-#endif
-
 #ifndef MOE_SPLIT_HEAVY_STAGES
 #define MOE_SPLIT_HEAVY_STAGES 3
 #endif
@@ -215,14 +209,7 @@ __device__ __forceinline__ Tile decode(const Params& p, int L, int rank) {
     const int ue = __ldg(uoff + e + 1) - u0;
     const int m0 = PAIR ? __ldg(p.mt_off + e) : u0;
     const int loc = L - u0 * p.n_tiles;
-#if MOE_UNIT_NBLOCK > 1
-    // units in blocks of NB N tiles, the expert's M units fastest inside
-    const int nbk = (p.n_tiles % MOE_UNIT_NBLOCK == 0) ? MOE_UNIT_NBLOCK : 1;
-    const int blk = loc / (ue * nbk), rr = loc - blk * ue * nbk;
-    int mrel = rr / nbk;
-#else
     int mrel = loc % ue;
-#endif
     t.rows = kBM;
     t.nt = 0;
     t.thin = false;
@@ -242,11 +229,7 @@ __device__ __forceinline__ Tile decode(const Params& p, int L, int rank) {
       }
     }
     t.e = e;
-#if MOE_UNIT_NBLOCK > 1
-    t.n = blk * nbk + (rr - (rr / nbk) * nbk);
-#else
     t.n = loc / ue;
-#endif
     t.m = m0 + mrel;
     t.row0 = t.m * kBM;
     t.kb_count = p.num_kb;
