@@ -89,6 +89,8 @@ def _run_forward(cfg, inp):
 @pytest.mark.parametrize("name,kw,x_std", [
     ("tiny", {}, None), ("tiny", {}, 1.0), ("tiny", dict(f=192, d=256), 1.0),
     ("tiny", dict(d=64, f=128, E=3, k=3, T=200), 1.0), ("tiny", dict(T=1, k=8), 1.0),
+    # the token-order gather at its widest and narrowest fan-out
+    ("tiny", dict(T=97, E=40, k=32), 1.0), ("tiny", dict(T=133, E=5, k=1), 1.0),
     ("balanced", {}, None)])
 def test_forward_full(name, kw, x_std):
     cfg = with_config(name, **kw)
@@ -136,6 +138,7 @@ def _backward_case(cfg, x_std=None, logits_fn=None):
 
 
 @pytest.mark.parametrize("kw,x_std", [({}, None), ({}, 1.0), (dict(f=192, d=256, T=300), 1.0),
+                                      (dict(T=97, E=40, k=32), 1.0), (dict(T=133, E=5, k=1), 1.0),
                                       (dict(T=1, k=8), 1.0), (dict(d=64, E=3, k=3), 1.0)])
 def test_backward_tiny(kw, x_std):
     cfg = with_config("tiny", **kw)

@@ -172,6 +172,8 @@ def _mx_run(cfg, dev):
 
 
 @pytest.mark.parametrize("name,kw", [("tiny", dict(f=128, d=256, T=300, E=6, k=3)),
+                                     ("tiny", dict(f=128, d=256, T=99, E=40, k=32)),
+                                     ("tiny", dict(f=128, d=256, T=77, E=3, k=1)),
                                      ("balanced", {})])
 def test_gather_codes_and_scales_bit_exact(name, kw):
     cfg = with_config(name, prec="mxfp8", **kw)
