@@ -260,8 +260,9 @@ moe_status moe_backward(const moe_config* cfg, const moe_bf16* dout, const moe_b
  * region, a null pointer, or a region the configuration does not have.
  *   MOE_WS_XQ_CODES   MXFP8: E4M3 codes of the gathered token rows,
  *                     [moe_saved_rows(cfg), d] in the padded expert order
- *                     (written by moe_forward for rows below the padded
- *                     total; padding rows hold zero codes)
+ *                     (moe_forward writes the routed rows; padding rows
+ *                     are not written, and GEMM1 zeroes what it computes
+ *                     from them)
  *   MOE_WS_XQ_SCALES  their UE8M0 scales in 512-byte tiles (the layout
  *                     moe_quantize_mxfp8 documents, K = d)
  *   MOE_WS_AQ_CODES   MXFP8: E4M3 codes of the SwiGLU output A that GEMM1's
