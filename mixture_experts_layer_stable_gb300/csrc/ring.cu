@@ -19,14 +19,20 @@
 //                  rows in and releases ready[slot].
 //   compute        the warp-specialised tcgen05 pipeline of gemm.cu (TMA
 //                  producer, MMA issuer, four epilogue warps) in every CTA that
-//                  is not a gather CTA, over the tile stream G1(0) ... G1(lag-1),
+//                  is not a gather CTA, over the unit stream G1(0) ... G1(lag-1),
 //                  [G1(lag), G2(0)], ..., G2(last); each CTA claims the next
-//                  tile from a global counter when its producer is ready for
-//                  one, so tiles of mixed cost balance themselves.  GEMM1 +
-//                  SwiGLU tiles of window w read the ring slot after acquiring
-//                  ready[slot] and release freed[slot] once their loads have
-//                  landed; GEMM2 tiles of a 128-row tile wait for that tile's
-//                  GEMM1 epilogues (a_ready) and store Y in expert order.
+//                  unit from a global counter when its producer is ready for
+//                  one, so units of mixed cost balance themselves.  A unit is
+//                  one N tile of two M-adjacent 128-row tiles of a window (BF16;
+//                  one tile in MXFP8): when both belong to one expert and
+//                  neither is thin, each stage holds both A tiles and the
+//                  shared B tile and the MMAs feed two accumulators, so B
+//                  crosses the SM's L2 ingress once for 256 rows; otherwise
+//                  the tiles run one after the other.  GEMM1 + SwiGLU tiles of
+//                  window w read the ring slot after acquiring ready[slot] and
+//                  release freed[slot] once their loads have landed; GEMM2
+//                  tiles of a 128-row tile wait for that tile's GEMM1
+//                  epilogues (a_ready) and store Y in expert order.
 //   all CTAs       after the last GEMM2 store (done2), the fixed-order
 //                  weighted merge of every token.
 // MXFP8 mode: the gather quantises each row into E4M3 codes and UE8M0 scale
@@ -57,10 +63,8 @@ namespace {
 
 constexpr int BK = 64;
 constexpr int BK8 = 128;                       // MXFP8: K elements (bytes) per stage
-constexpr int kStages = 4;
 constexpr int kABytes = kBM * BK * 2;          // 16 KB (MXFP8: 128 rows x 128 bytes, the same)
 constexpr int kBBox = 64 * BK * 2;             // 8 KB: 64 columns x 64 K rows, MN-major
-constexpr int kStageBytes = kABytes + 4 * kBBox;  // MXFP8: 16 KB of A + 256 rows x 128 bytes of B
 constexpr int kSfBytes = 1536;                 // MXFP8: A scale tile + two B scale tiles a stage
 constexpr int kEpiWarps = 4;
 constexpr int kGatherWarps = 2;  // gather warps of a CTA in the warp split
@@ -69,10 +73,16 @@ constexpr int kOutTile = 32 * 128;
 constexpr int kTmemCols = 512;
 constexpr int kTmemSf = 256;                   // MXFP8: scale columns of stage s at 256 + 16 s
 constexpr int kQ = 4;  // depth of the per-CTA queue of claimed tile indices
-// bf16: staging tiles for the Y stores (and the thin tiles' transposes);
-// MXFP8: per-stage scale tiles instead (Y leaves with direct stores)
+// bf16: units of up to two 128-row tiles of one expert that share their B
+// operand (a stage holds both A tiles and B: 64 KB, three stages); staging
+// tiles for the Y stores (and the thin tiles' transposes).  MXFP8: units of
+// one tile (a stage: 16 KB of A + 256 rows x 128 bytes of B, four stages)
+// and per-stage scale tiles instead of staging (Y leaves with direct stores).
 template <bool FP8>
 struct RingCfg {
+  static constexpr int kTiles = FP8 ? 1 : 2;  // 128-row tiles per unit
+  static constexpr int kStageBytes = kTiles * kABytes + 4 * kBBox;
+  static constexpr int kStages = FP8 ? 4 : 3;
   static constexpr size_t kExtra = FP8 ? (size_t)kStages * kSfBytes : (size_t)kEpiWarps * 2 * kOutTile;
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + (kExtra + 1023) / 1024 * 1024 + 256;
   static_assert(kSmem <= 232448, "shared memory budget");
@@ -115,19 +125,29 @@ struct RingParams {
 };
 
 // Window geometry of this call (from the padded row total the schedule wrote).
+// The stream is counted in units of up to tpu 128-row tiles (the tiles of a
+// window are grouped along M: tiles 2u and 2u + 1 form unit u when tpu = 2).
 struct Geo {
-  int rp, nW, mt_last, F1, F2, total, total2;
+  int rp, nW, mt_last;
+  int F1;          // GEMM1 tiles of a full window (the ring slot's readers)
+  int um, uml;     // units along M of a full window / of the last window
+  int U1, U2;      // GEMM1 / GEMM2 units of a full window
+  int total;       // units in the stream
+  int total2;      // GEMM2 tiles in the stream
 };
 
-__device__ __forceinline__ Geo make_geo(const RingParams& p) {
+__device__ __forceinline__ Geo make_geo(const RingParams& p, int tpu) {
   Geo g;
   g.rp = p.hdr[kHdrRpTotal];
   g.nW = (g.rp + p.mb - 1) / p.mb;
   g.mt_last = (g.rp - (g.nW - 1) * p.mb) / kBM;
   g.F1 = p.mtw * p.nt1;
-  g.F2 = p.mtw * p.nt2;
-  g.total = (g.nW - 1) * (g.F1 + g.F2) + g.mt_last * (p.nt1 + p.nt2);
-  g.total2 = (g.nW - 1) * g.F2 + g.mt_last * p.nt2;
+  g.um = (p.mtw + tpu - 1) / tpu;
+  g.uml = (g.mt_last + tpu - 1) / tpu;
+  g.U1 = g.um * p.nt1;
+  g.U2 = g.um * p.nt2;
+  g.total = (g.nW - 1) * (g.U1 + g.U2) + g.uml * (p.nt1 + p.nt2);
+  g.total2 = (g.nW - 1) * p.mtw * p.nt2 + g.mt_last * p.nt2;
   return g;
 }
 
@@ -135,6 +155,16 @@ struct RTile {
   int phase, w, mloc, mt, n, e;
   int rows;   // valid rows of the 128-row tile
   bool thin;  // computed as (weights)^T x (rows)^T with the tokens on N
+};
+
+// A unit of the stream: one or two tiles of one window, phase and N tile.
+// pair: two tiles of the same expert, neither thin -- their MMAs share each
+// stage's B operand, one accumulator each; otherwise the tiles run one after
+// the other.
+struct RUnit {
+  RTile t[2];
+  int nt;     // tiles in the unit (1 or 2)
+  bool pair;
 };
 
 // A 32-token x 32-column block held one column per lane is written to rows
@@ -156,65 +186,75 @@ __device__ __forceinline__ void ring_store_cols_t(uint8_t* tr, const float* v, _
   }
 }
 
-// Tile L of the stream G1(0), ..., G1(lag - 1), [G1(lag) G2(0)], [G1(lag + 1)
+// Unit L of the stream G1(0), ..., G1(lag - 1), [G1(lag) G2(0)], [G1(lag + 1)
 // G2(1)], ..., [G1(nW - 1) G2(nW - 1 - lag)], G2(nW - lag), ..., G2(nW - 1):
 // GEMM2 of a window is claimed `lag` windows after its GEMM1, by when its
-// GEMM1 tiles are mostly done.  Inside a phase block, tiles run
-// N-tile-major so that the tiles sharing an expert's weight slice are
+// GEMM1 tiles are mostly done.  Inside a phase block, units run
+// N-tile-major so that the units sharing an expert's weight slice are
 // adjacent.  Only the last window can be short (mt_last tiles).
-__device__ __forceinline__ RTile ring_decode(const RingParams& p, const Geo& g, int L) {
+__device__ __forceinline__ RUnit ring_decode(const RingParams& p, const Geo& g, int L, int tpu) {
   int phase, w, loc;
-  const int t1l = g.mt_last * p.nt1;
+  const int u1l = g.uml * p.nt1;
   const int lag = min(p.lag, g.nW);
   if (lag == g.nW) {
-    // every GEMM1 tile, then every GEMM2 tile
-    const int n1 = (g.nW - 1) * g.F1 + t1l;
+    // every GEMM1 unit, then every GEMM2 unit
+    const int n1 = (g.nW - 1) * g.U1 + u1l;
     phase = L < n1 ? 1 : 2;
     const int l = L < n1 ? L : L - n1;
-    const int F = phase == 1 ? g.F1 : g.F2;
+    const int F = phase == 1 ? g.U1 : g.U2;
     w = min(l / F, g.nW - 1);
     loc = l - w * F;
-  } else if (L < lag * g.F1) {
-    phase = 1; w = L / g.F1; loc = L % g.F1;
+  } else if (L < lag * g.U1) {
+    phase = 1; w = L / g.U1; loc = L % g.U1;
   } else {
-    int l = L - lag * g.F1;
-    const int blk = g.F1 + g.F2;
+    int l = L - lag * g.U1;
+    const int blk = g.U1 + g.U2;
     const int nfull = g.nW - 1 - lag;  // blocks [G1(b) G2(b - lag)] of full windows
     if (l < nfull * blk) {
       const int b = lag + l / blk, r = l % blk;
-      if (r < g.F1) { phase = 1; w = b; loc = r; }
-      else { phase = 2; w = b - lag; loc = r - g.F1; }
+      if (r < g.U1) { phase = 1; w = b; loc = r; }
+      else { phase = 2; w = b - lag; loc = r - g.U1; }
     } else {
       l -= nfull * blk;
-      if (l < t1l) { phase = 1; w = g.nW - 1; loc = l; }
-      else if ((l -= t1l) < g.F2) { phase = 2; w = g.nW - 1 - lag; loc = l; }
+      if (l < u1l) { phase = 1; w = g.nW - 1; loc = l; }
+      else if ((l -= u1l) < g.U2) { phase = 2; w = g.nW - 1 - lag; loc = l; }
       else {
-        l -= g.F2;
+        l -= g.U2;
         phase = 2;
-        w = min(g.nW - lag + l / g.F2, g.nW - 1);
-        loc = l - (w - (g.nW - lag)) * g.F2;
+        w = min(g.nW - lag + l / g.U2, g.nW - 1);
+        loc = l - (w - (g.nW - lag)) * g.U2;
       }
     }
   }
-  const int mtw = (w == g.nW - 1) ? g.mt_last : p.mtw;
-  RTile t;
-  t.phase = phase;
-  t.w = w;
-  t.mloc = loc % mtw;
-  t.n = loc / mtw;
-  t.mt = w * p.mtw + t.mloc;
-  t.e = find_expert(p.mt_off, p.E, t.mt);
-  t.rows = kBM;
-  t.thin = false;
-  if (p.thin && t.phase == 1) {
-    const int cnt = __ldg(p.counts + t.e);
-    const int rows = cnt - (t.mt - __ldg(p.mt_off + t.e)) * kBM;
-    if (thin_tile(rows, cnt)) {
-      t.rows = rows;
-      t.thin = true;
+  const bool last = (w == g.nW - 1);
+  const int umw = last ? g.uml : g.um;
+  const int mtw = last ? g.mt_last : p.mtw;
+  const int mu = loc % umw, n = loc / umw;
+  RUnit u;
+  u.nt = 0;
+  for (int i = 0; i < tpu; ++i) {
+    const int mloc = mu * tpu + i;
+    if (mloc >= mtw) break;
+    RTile& t = u.t[u.nt++];
+    t.phase = phase;
+    t.w = w;
+    t.mloc = mloc;
+    t.n = n;
+    t.mt = w * p.mtw + mloc;
+    t.e = find_expert(p.mt_off, p.E, t.mt);
+    t.rows = kBM;
+    t.thin = false;
+    if (p.thin && phase == 1) {
+      const int cnt = __ldg(p.counts + t.e);
+      const int rows = cnt - (t.mt - __ldg(p.mt_off + t.e)) * kBM;
+      if (thin_tile(rows, cnt)) {
+        t.rows = rows;
+        t.thin = true;
+      }
     }
   }
-  return t;
+  u.pair = u.nt == 2 && u.t[0].e == u.t[1].e && !u.t[0].thin && !u.t[1].thin;
+  return u;
 }
 
 // MXFP8: one warp quantises the source row of routed row r (zeros for a
@@ -251,7 +291,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int kAcc = FP8 ? 1 : 2;  // MXFP8: one accumulator, the scales in TMEM columns 256..
-  const Geo geo = make_geo(p);
+  constexpr int kStages = RingCfg<FP8>::kStages;
+  constexpr int kStageBytes = RingCfg<FP8>::kStageBytes;
+  constexpr int kTpu = RingCfg<FP8>::kTiles;
+  const Geo geo = make_geo(p, kTpu);
   const int inject = p.hdr[kHdrInject];        // test hook: window + 1 whose arrival is withheld
   const int lim_ms = p.hdr[kHdrInject + 1];    // test hook: wait limit in ms (0: default)
   const uint64_t limit = lim_ms > 0 ? (uint64_t)lim_ms * 1000000ull : kWaitLimitNs;
@@ -398,14 +441,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           qtile[j % kQ] = L;
           mbar_arrive(&qfull[j % kQ]);
           if (L >= geo.total) break;
-          const RTile t = ring_decode(p, geo, L);
-          const bool g1 = (t.phase == 1);
-          const int slot = t.w % p.S;
+          const RUnit u = ring_decode(p, geo, L, kTpu);
+          const bool g1 = (u.t[0].phase == 1);
+          const int slot = u.t[0].w % p.S;
           bool ok;
           if (g1)
-            ok = wait_counter(&p.ready[slot], p.nrel * (t.w / p.S + 1), p.gabort, p.status, 600 + slot, limit);
+            ok = wait_counter(&p.ready[slot], p.nrel * (u.t[0].w / p.S + 1), p.gabort, p.status, 600 + slot, limit);
           else
-            ok = wait_counter(&p.a_ready[t.mt], kEpiWarps * p.nt1, p.gabort, p.status, 700, limit);
+            ok = wait_counter(&p.a_ready[u.t[0].mt], kEpiWarps * p.nt1, p.gabort, p.status, 700, limit) &&
+                 (u.nt < 2 || wait_counter(&p.a_ready[u.t[1].mt], kEpiWarps * p.nt1, p.gabort, p.status, 700, limit));
           if (!ok) {
             *abort_flag = 1;
             goto producer_done;
@@ -413,10 +457,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_global();  // rows written by other CTAs, read by TMA below
           const int nbox = g1 ? (2 * p.hn) / 64 : 4;
           const int nkb = g1 ? p.kb1 : p.kb2;
+          // a pair unit: both A tiles and the shared B in one stage; otherwise
+          // the unit's tiles one after the other, A then B in each stage
+          const int passes = u.pair ? 1 : u.nt;
+          for (int ti = 0; ti < passes; ++ti) {
+          const RTile t = ti == 0 ? u.t[0] : u.t[1];
+          const int na = u.pair ? 2 : 1;
           for (int kb = 0; kb < nkb; ++kb) {
             if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status, 100 + s)) goto producer_done;
             const uint32_t sa = smem_u32(stages + (size_t)s * kStageBytes);
-            const uint32_t sb = sa + kABytes;
+            const uint32_t sb = sa + (uint32_t)na * kABytes;
             const uint32_t fb = smem_u32(&full[s]);
             if constexpr (FP8) {
               // K-major E4M3 tiles (128 bytes of K per row) and their scale
@@ -442,16 +492,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bulk_load(sf + 1024, p.W2s + (((size_t)t.e * nbt + nb1) * kg + kb) * 512u, 512u, fb);
               }
             } else {
-            mbar_arrive_expect_tx(&full[s], (uint32_t)kABytes + (uint32_t)nbox * kBBox);
+            mbar_arrive_expect_tx(&full[s], (uint32_t)(na * kABytes) + (uint32_t)nbox * kBBox);
+            for (int i = 0; i < na; ++i) {
+              const RTile ta = (ti + i) == 0 ? u.t[0] : u.t[1];
+              if (g1) tma_load_2d(sa + i * kABytes, &tmX, fb, kb * BK, slot * p.mb + ta.mloc * kBM);
+              else tma_load_2d(sa + i * kABytes, &tmA, fb, kb * BK, ta.mt * kBM);
+            }
             if (g1) {
-              tma_load_2d(sa, &tmX, fb, kb * BK, slot * p.mb + t.mloc * kBM);
               const int half = nbox / 2;
               for (int i = 0; i < nbox; ++i) {
                 const int col = (i < half) ? t.n * p.hn + 64 * i : p.f + t.n * p.hn + 64 * (i - half);
                 tma_load_3d(sb + i * kBBox, &tmW1, fb, col, kb * BK, t.e);
               }
             } else {
-              tma_load_2d(sa, &tmA, fb, kb * BK, t.mt * kBM);
               for (int i = 0; i < 4; ++i) tma_load_3d(sb + i * kBBox, &tmW2, fb, t.n * 256 + 64 * i, kb * BK, t.e);
             }
             }
@@ -461,6 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               s = 0;
               ph ^= 1u;
             }
+          }
           }
         }
       producer_done:
@@ -479,18 +533,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int L = qtile[j % kQ];
           mbar_arrive(&qempty[j % kQ]);
           if (L >= geo.total) break;
-          const RTile t = ring_decode(p, geo, L);
-          const bool g1 = (t.phase == 1);
+          const RUnit u = ring_decode(p, geo, L, kTpu);
+          const bool g1 = (u.t[0].phase == 1);
           const int nkb = g1 ? p.kb1 : p.kb2;
+          // a pair unit takes two accumulators at once (the next two in the
+          // order the epilogue drains them); other units one per tile, in turn
+          const int passes = u.pair ? 1 : u.nt;
+          for (int ti = 0; ti < passes; ++ti) {
+          const RTile t = ti == 0 ? u.t[0] : u.t[1];
+          const int acc0 = acc;
           if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, p.status, 200 + acc)) goto mma_done;
+          if (++acc == kAcc) {
+            acc = 0;
+            aph ^= 1u;
+          }
+          int acc1 = acc0;
+          if (u.pair) {
+            acc1 = acc;
+            if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, p.status, 200 + acc)) goto mma_done;
+            if (++acc == kAcc) {
+              acc = 0;
+              aph ^= 1u;
+            }
+          }
           tc_fence_after();
-          const uint32_t dt = tmem_base + (uint32_t)acc * 256u;
+          const uint32_t dt = tmem_base + (uint32_t)acc0 * 256u;
+          const uint32_t dt1 = tmem_base + (uint32_t)acc1 * 256u;
           for (int kb = 0; kb < nkb; ++kb) {
             if (!mbar_wait(&full[s], ph, abort_flag, p.status, 300 + s)) goto mma_done;
             tc_fence_after();
-            if (g1 && kb == nkb - 1) red_release_add(&p.freed[t.w % p.S], 1);  // ring rows landed
+            if (g1 && kb == nkb - 1) red_release_add(&p.freed[t.w % p.S], u.pair ? 2 : 1);  // ring rows landed
             const uint32_t sa = smem_u32(stages + (size_t)s * kStageBytes);
-            const uint32_t sb = sa + kABytes;
+            const uint32_t sb = sa + (u.pair ? 2u : 1u) * kABytes;
             if constexpr (FP8) {
               // stage the scale tiles into this stage's TMEM columns, then 4
               // block-scaled MMAs of K = 32, each reading its block's scale byte
@@ -515,10 +589,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_mma_f16(dt + 128u, sdesc_sw128(sb + 16384 + kk * 2048, 8192, 1024), bd, idt, accf);
               }
             } else {
+              // each tile's accumulator sees the same MMAs in the same order
+              // as a tile of its own
 #pragma unroll
               for (int kk = 0; kk < BK / 16; ++kk)
                 tc_mma_f16(dt, sdesc_sw128(sa + kk * 32, 16, 1024), sdesc_sw128(sb + kk * 2048, 8192, 1024),
                            g1 ? idesc1 : idesc2, (kb > 0 || kk > 0) ? 1u : 0u);
+              if (u.pair) {
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)
+                  tc_mma_f16(dt1, sdesc_sw128(sa + kABytes + kk * 32, 16, 1024),
+                             sdesc_sw128(sb + kk * 2048, 8192, 1024), g1 ? idesc1 : idesc2,
+                             (kb > 0 || kk > 0) ? 1u : 0u);
+              }
             }
             tc_commit(smem_u32(&empty[s]));
             if (++s == kStages) {
@@ -526,10 +609,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               ph ^= 1u;
             }
           }
-          tc_commit(smem_u32(&tfull[acc]));
-          if (++acc == kAcc) {
-            acc = 0;
-            aph ^= 1u;
+          tc_commit(smem_u32(&tfull[acc0]));
+          if (u.pair) tc_commit(smem_u32(&tfull[acc1]));
           }
         }
       mma_done:
@@ -548,8 +629,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&qempty[j % kQ]);
         if (L >= geo.total) break;
-        const RTile t = ring_decode(p, geo, L);
-        if (!mbar_wait(&tfull[acc], aph, abort_flag, p.status, 400 + acc)) break;
+        const RUnit un = ring_decode(p, geo, L, kTpu);
+        bool eok = true;
+        for (int ti = 0; ti < un.nt; ++ti) {  // the unit's tiles, in accumulator order
+        const RTile t = ti == 0 ? un.t[0] : un.t[1];
+        if (!mbar_wait(&tfull[acc], aph, abort_flag, p.status, 400 + acc)) {
+          eok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t tb = tmem_base + (uint32_t)acc * 256u + ((uint32_t)(q * 32) << 16);
         if (FP8 && t.phase == 1) {
@@ -692,6 +779,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc = 0;
           aph ^= 1u;
         }
+        }
+        if (!eok) break;
       }
       if (lane == 0) bulk_wait<0>();
     } else if (p.G == 0) {
