@@ -73,18 +73,18 @@ constexpr int kOutTile = 32 * 128;
 constexpr int kTmemCols = 512;
 constexpr int kTmemSf = 256;                   // MXFP8: scale columns of stage s at 256 + 16 s
 constexpr int kQ = 4;  // depth of the per-CTA queue of claimed tile indices
-// bf16: units of up to two 128-row tiles of one expert that share their B
-// operand (a stage holds both A tiles and B: 64 KB, three stages); staging
-// tiles for the Y stores (and the thin tiles' transposes).  MXFP8: units of
-// one tile (a stage: 16 KB of A + 256 rows x 128 bytes of B, four stages)
-// and per-stage scale tiles instead of staging (Y leaves with direct stores).
+// The stage region holds four stages of one A tile and B (48 KB each) or,
+// for units of two tiles (bf16, see the unit stream), three stages of two A
+// tiles and B (64 KB each).  bf16: staging tiles for the Y stores (and the
+// thin tiles' transposes) after it; MXFP8 (units of one tile): per-stage
+// scale tiles instead (Y leaves with direct stores).
+constexpr int kMaxStages = 4;
+constexpr int kStageRegion = 4 * (kABytes + 4 * kBBox);
+static_assert(kStageRegion == 3 * (2 * kABytes + 4 * kBBox), "both stage layouts fill the region");
 template <bool FP8>
 struct RingCfg {
-  static constexpr int kTiles = FP8 ? 1 : 2;  // 128-row tiles per unit
-  static constexpr int kStageBytes = kTiles * kABytes + 4 * kBBox;
-  static constexpr int kStages = FP8 ? 4 : 3;
-  static constexpr size_t kExtra = FP8 ? (size_t)kStages * kSfBytes : (size_t)kEpiWarps * 2 * kOutTile;
-  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + (kExtra + 1023) / 1024 * 1024 + 256;
+  static constexpr size_t kExtra = FP8 ? (size_t)kMaxStages * kSfBytes : (size_t)kEpiWarps * 2 * kOutTile;
+  static constexpr size_t kSmem = 1024 + (size_t)kStageRegion + (kExtra + 1023) / 1024 * 1024 + 256;
   static_assert(kSmem <= 232448, "shared memory budget");
 };
 
@@ -95,6 +95,7 @@ struct RingParams {
   int nrel;                   // arrivals that complete one window (gather CTAs or gather warps)
   int gw, nbw;                // gather warps per CTA issuing bulk copies, row buffers per such warp
   int lag;                    // windows between a window's GEMM1 and GEMM2 tiles in the stream
+  int tpu;                    // 128-row tiles per unit (bf16: 1 or 2)
   int hn, nt1, nt2, kb1, kb2;  // GEMM1 half width, N tiles of GEMM1 / GEMM2, K blocks
   const int* mt_off;
   const int* counts;   // rows per expert: a partial last tile runs thin (swapped)
@@ -230,12 +231,8 @@ __device__ __forceinline__ RUnit ring_decode(const RingParams& p, const Geo& g, 
   const int umw = last ? g.uml : g.um;
   const int mtw = last ? g.mt_last : p.mtw;
   const int mu = loc % umw, n = loc / umw;
-  RUnit u;
-  u.nt = 0;
-  for (int i = 0; i < tpu; ++i) {
-    const int mloc = mu * tpu + i;
-    if (mloc >= mtw) break;
-    RTile& t = u.t[u.nt++];
+  auto tile = [&](int mloc) {
+    RTile t;
     t.phase = phase;
     t.w = w;
     t.mloc = mloc;
@@ -252,7 +249,13 @@ __device__ __forceinline__ RUnit ring_decode(const RingParams& p, const Geo& g, 
         t.thin = true;
       }
     }
-  }
+    return t;
+  };
+  RUnit u;
+  u.t[0] = tile(mu * tpu);
+  u.nt = (tpu == 2 && mu * 2 + 1 < mtw) ? 2 : 1;
+  if (u.nt == 2) u.t[1] = tile(mu * 2 + 1);
+  else u.t[1] = u.t[0];
   u.pair = u.nt == 2 && u.t[0].e == u.t[1].e && !u.t[0].thin && !u.t[1].thin;
   return u;
 }
@@ -281,7 +284,8 @@ template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     ring_forward_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW1,
                         const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW2,
-                        const __grid_constant__ CUtensorMap tmY, const RingParams p) {
+                        const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmX16,
+                        const RingParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_ok;
   __shared__ int s_gab;
@@ -291,9 +295,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int kAcc = FP8 ? 1 : 2;  // MXFP8: one accumulator, the scales in TMEM columns 256..
-  constexpr int kStages = RingCfg<FP8>::kStages;
-  constexpr int kStageBytes = RingCfg<FP8>::kStageBytes;
-  constexpr int kTpu = RingCfg<FP8>::kTiles;
+  // tiles per unit (host's choice, 1 in MXFP8) and the stage layout it implies
+  const int kTpu = FP8 ? 1 : p.tpu;
+  const int kStages = kTpu == 2 ? 3 : 4;
+  const int kStageBytes = kTpu * kABytes + 4 * kBBox;
   const Geo geo = make_geo(p, kTpu);
   const int inject = p.hdr[kHdrInject];        // test hook: window + 1 whose arrival is withheld
   const int lim_ms = p.hdr[kHdrInject + 1];    // test hook: wait limit in ms (0: default)
@@ -384,12 +389,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ====================================================== compute side
     uint8_t* stages = smem;
-    uint8_t* staging = smem + (size_t)kStages * kStageBytes;  // MXFP8: the stages' scale tiles
+    uint8_t* staging = smem + (size_t)kStageRegion;  // MXFP8: the stages' scale tiles
     uint8_t* sfbuf = staging;
     uint8_t* ctrl = staging + (RingCfg<FP8>::kExtra + 1023) / 1024 * 1024;
     uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
-    uint64_t* empty = full + kStages;
-    uint64_t* tfull = empty + kStages;
+    uint64_t* empty = full + kMaxStages;
+    uint64_t* tfull = empty + kMaxStages;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
     uint64_t* qfull = drain + 1;     // tile queue: claimed tile index published
@@ -419,6 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmW2);
       tma_prefetch_desc(&tmY);
+      tma_prefetch_desc(&tmX16);
     }
     if (warp == 1) {
       tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -492,11 +498,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bulk_load(sf + 1024, p.W2s + (((size_t)t.e * nbt + nb1) * kg + kb) * 512u, 512u, fb);
               }
             } else {
-            mbar_arrive_expect_tx(&full[s], (uint32_t)(na * kABytes) + (uint32_t)nbox * kBBox);
-            for (int i = 0; i < na; ++i) {
-              const RTile ta = (ti + i) == 0 ? u.t[0] : u.t[1];
-              if (g1) tma_load_2d(sa + i * kABytes, &tmX, fb, kb * BK, slot * p.mb + ta.mloc * kBM);
-              else tma_load_2d(sa + i * kABytes, &tmA, fb, kb * BK, ta.mt * kBM);
+            if (t.thin) {
+              // a thin tile reads only the 16-row boxes that hold its rows
+              const int nr16 = (t.rows + 15) >> 4;
+              mbar_arrive_expect_tx(&full[s], (uint32_t)nr16 * 2048u + (uint32_t)nbox * kBBox);
+              for (int i = 0; i < nr16; ++i)
+                tma_load_2d(sa + i * 2048, &tmX16, fb, kb * BK, slot * p.mb + t.mloc * kBM + 16 * i);
+            } else {
+              mbar_arrive_expect_tx(&full[s], (uint32_t)(na * kABytes) + (uint32_t)nbox * kBBox);
+              for (int i = 0; i < na; ++i) {
+                const RTile ta = (ti + i) == 0 ? u.t[0] : u.t[1];
+                if (g1) tma_load_2d(sa + i * kABytes, &tmX, fb, kb * BK, slot * p.mb + ta.mloc * kBM);
+                else tma_load_2d(sa + i * kABytes, &tmA, fb, kb * BK, ta.mt * kBM);
+              }
             }
             if (g1) {
               const int half = nbox / 2;
@@ -917,6 +931,11 @@ cudaError_t ring_launch(const moe_config& c, const Ws& ws, const int* counts, co
   p.nt2 = (c.d + 255) / 256;
   p.kb1 = FP8 ? c.d / BK8 : c.d / BK;
   p.kb2 = FP8 ? c.f / BK8 : c.f / BK;
+  // units of two tiles halve B's L2 ingress per row but halve the units a
+  // window offers; they pay where a tile's K loop is long (hidden 7168: ring
+  // forward 3.75 -> 3.63 ms) and cost where it is short and the windows'
+  // handover dominates (hidden 2048: 0.235 -> 0.330 ms)
+  p.tpu = (!FP8 && p.kb1 >= 64) ? 2 : 1;
   {
     // lag: one window more than it takes for the tiles claimed between a
     // window's GEMM1 and its GEMM2 to keep every compute CTA busy for one
@@ -957,7 +976,7 @@ cudaError_t ring_launch(const moe_config& c, const Ws& ws, const int* counts, co
   p.ring_valid = ws.hdr() + kHdrRingValid;
 
   const uint64_t rows = (uint64_t)ws.L.Rp_max;
-  CUtensorMap tmX, tmW1, tmA, tmW2, tmY;
+  CUtensorMap tmX, tmW1, tmA, tmW2, tmY, tmX16;
   if (FP8) {
     // K-major E4M3: 128-byte K boxes of 128 rows (W2: 256 rows)
     if (!map2d(&tmX, p.ring, c.d, (uint64_t)p.S * p.mb, 128, kBM, true) ||
@@ -965,7 +984,9 @@ cudaError_t ring_launch(const moe_config& c, const Ws& ws, const int* counts, co
         !map2d(&tmA, p.Aq, c.f, rows, 128, kBM, true) || !map3d(&tmW2, W2, c.f, c.d, c.E, 128, 256, true))
       return cudaErrorInvalidValue;
     tmY = tmX;  // Y leaves with direct stores
+    tmX16 = tmX;
   } else if (!map2d(&tmX, p.ring, c.d, (uint64_t)p.S * p.mb, 64, kBM) ||
+             !map2d(&tmX16, p.ring, c.d, (uint64_t)p.S * p.mb, 64, 16) ||
              !map3d(&tmW1, W1, 2ull * c.f, c.d, c.E, 64, 64) || !map2d(&tmA, A, c.f, rows, 64, kBM) ||
              !map3d(&tmW2, W2, c.d, c.f, c.E, 64, 64) || !map2d(&tmY, p.Y, c.d, rows, 64, 32)) {
     return cudaErrorInvalidValue;
@@ -980,7 +1001,7 @@ cudaError_t ring_launch(const moe_config& c, const Ws& ws, const int* counts, co
   err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, kSmem);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
-  void* args[] = {&tmX, &tmW1, &tmA, &tmW2, &tmY, &p};
+  void* args[] = {&tmX, &tmW1, &tmA, &tmW2, &tmY, &tmX16, &p};
   TraceScope ts(FP8 ? "ring_forward_mxfp8" : "ring_forward", st);
   return cudaLaunchCooperativeKernel((const void*)kern, dim3(sms), dim3(kThreads), args, kSmem, st);
 }
