@@ -100,6 +100,7 @@ struct RingParams {
   const int* mt_off;
   const int* counts;   // rows per expert: a partial last tile runs thin (swapped)
   int thin;
+  int thin_rows;        // largest partial tile that runs thin
   const int* hdr;
   const int* row_of_pad;
   const int* pos_pad;
@@ -244,7 +245,7 @@ __device__ __forceinline__ RUnit ring_decode(const RingParams& p, const Geo& g, 
     if (p.thin && phase == 1) {
       const int cnt = __ldg(p.counts + t.e);
       const int rows = cnt - (t.mt - __ldg(p.mt_off + t.e)) * kBM;
-      if (thin_tile(rows, cnt)) {
+      if (thin_tile(rows, cnt) && rows <= p.thin_rows) {
         t.rows = rows;
         t.thin = true;
       }
@@ -498,8 +499,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bulk_load(sf + 1024, p.W2s + (((size_t)t.e * nbt + nb1) * kg + kb) * 512u, 512u, fb);
               }
             } else {
-            if (t.thin) {
-              // a thin tile reads only the 16-row boxes that hold its rows
+            if (t.thin && t.rows <= 32) {
+              // a thin tile of a few rows reads only the 16-row boxes that hold them
               const int nr16 = (t.rows + 15) >> 4;
               mbar_arrive_expect_tx(&full[s], (uint32_t)nr16 * 2048u + (uint32_t)nbox * kBBox);
               for (int i = 0; i < nr16; ++i)
@@ -947,7 +948,11 @@ cudaError_t ring_launch(const moe_config& c, const Ws& ws, const int* counts, co
   }
   p.mt_off = ws.mt_off();
   p.counts = counts;
-  p.thin = (!FP8 && gemm1_thin_enabled(c)) ? 1 : 0;
+  // thin GEMM1 tiles (weights on the MMA's M, the tile's rows on N): every
+  // partial tile at hidden <= 4096; at larger hidden only tiles of at most 32
+  // rows, which then also load just their rows
+  p.thin = (!FP8 && c.f % 128 == 0) ? 1 : 0;
+  p.thin_rows = gemm1_thin_enabled(c) ? kBM - 1 : 32;
   p.hdr = ws.hdr();
   p.row_of_pad = ws.row_of_pad();
   p.pos_pad = ws.pos_pad();
