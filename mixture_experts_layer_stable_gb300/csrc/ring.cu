@@ -95,7 +95,7 @@ struct RingParams {
   int nrel;                   // arrivals that complete one window (gather CTAs or gather warps)
   int gw, nbw;                // gather warps per CTA issuing bulk copies, row buffers per such warp
   int lag;                    // windows between a window's GEMM1 and GEMM2 tiles in the stream
-  int tpu;                    // 128-row tiles per unit (bf16: 1 or 2)
+  int tpu;                    // 128-row tiles per unit (bf16: 1 or 2; selects the kernel)
   int hn, nt1, nt2, kb1, kb2;  // GEMM1 half width, N tiles of GEMM1 / GEMM2, K blocks
   const int* mt_off;
   const int* counts;   // rows per expert: a partial last tile runs thin (swapped)
@@ -281,7 +281,7 @@ __device__ __forceinline__ void ring_quant_row(const RingParams& p, int r, size_
   }
 }
 
-template <bool FP8>
+template <bool FP8, int TPU>
 __global__ void __launch_bounds__(kThreads, 1)
     ring_forward_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW1,
                         const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW2,
@@ -296,10 +296,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int kAcc = FP8 ? 1 : 2;  // MXFP8: one accumulator, the scales in TMEM columns 256..
-  // tiles per unit (host's choice, 1 in MXFP8) and the stage layout it implies
-  const int kTpu = FP8 ? 1 : p.tpu;
-  const int kStages = kTpu == 2 ? 3 : 4;
-  const int kStageBytes = kTpu * kABytes + 4 * kBBox;
+  // tiles per unit (the host's choice, 1 in MXFP8) and the stage layout it implies
+  static_assert(TPU == 1 || (TPU == 2 && !FP8), "two-tile units are bf16 only");
+  constexpr int kTpu = TPU;
+  constexpr int kStages = kTpu == 2 ? 3 : 4;
+  constexpr int kStageBytes = kTpu * kABytes + 4 * kBBox;
   const Geo geo = make_geo(p, kTpu);
   const int inject = p.hdr[kHdrInject];        // test hook: window + 1 whose arrival is withheld
   const int lim_ms = p.hdr[kHdrInject + 1];    // test hook: wait limit in ms (0: default)
@@ -499,8 +500,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bulk_load(sf + 1024, p.W2s + (((size_t)t.e * nbt + nb1) * kg + kb) * 512u, 512u, fb);
               }
             } else {
-            if (t.thin && t.rows <= 32) {
-              // a thin tile of a few rows reads only the 16-row boxes that hold them
+            if (t.thin && p.thin_rows <= 32) {
+              // at large hidden sizes a thin tile (at most 32 rows) reads only
+              // the 16-row boxes that hold its rows
               const int nr16 = (t.rows + 15) >> 4;
               mbar_arrive_expect_tx(&full[s], (uint32_t)nr16 * 2048u + (uint32_t)nbox * kBBox);
               for (int i = 0; i < nr16; ++i)
@@ -999,7 +1001,7 @@ cudaError_t ring_launch(const moe_config& c, const Ws& ws, const int* counts, co
 
   cudaError_t err = cudaMemsetAsync(ctr, 0, ws.L.ctr_bytes, st);
   if (err != cudaSuccess) return err;
-  auto kern = ring_forward_kernel<FP8>;
+  auto kern = p.tpu == 2 ? ring_forward_kernel<FP8, FP8 ? 1 : 2> : ring_forward_kernel<FP8, 1>;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
   if (err != cudaSuccess) return err;
   int per_sm = 0;
