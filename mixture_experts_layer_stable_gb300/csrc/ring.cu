@@ -101,6 +101,7 @@ struct RingParams {
   const int* counts;   // rows per expert: a partial last tile runs thin (swapped)
   int thin;
   int thin_rows;        // largest partial tile that runs thin
+  int thin2;            // GEMM2 tiles of at most 32 rows run thin (bf16)
   const int* hdr;
   const int* row_of_pad;
   const int* pos_pad;
@@ -242,10 +243,10 @@ __device__ __forceinline__ RUnit ring_decode(const RingParams& p, const Geo& g, 
     t.e = find_expert(p.mt_off, p.E, t.mt);
     t.rows = kBM;
     t.thin = false;
-    if (p.thin && phase == 1) {
+    if ((p.thin && phase == 1) || (p.thin2 && phase == 2)) {
       const int cnt = __ldg(p.counts + t.e);
       const int rows = cnt - (t.mt - __ldg(p.mt_off + t.e)) * kBM;
-      if (thin_tile(rows, cnt) && rows <= p.thin_rows) {
+      if (thin_tile(rows, cnt) && rows <= (phase == 1 ? p.thin_rows : 32)) {
         t.rows = rows;
         t.thin = true;
       }
@@ -286,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ring_forward_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW1,
                         const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW2,
                         const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmX16,
-                        const RingParams p) {
+                        const __grid_constant__ CUtensorMap tmA16, const RingParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_ok;
   __shared__ int s_gab;
@@ -427,6 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmW2);
       tma_prefetch_desc(&tmY);
       tma_prefetch_desc(&tmX16);
+      tma_prefetch_desc(&tmA16);
     }
     if (warp == 1) {
       tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -500,13 +502,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bulk_load(sf + 1024, p.W2s + (((size_t)t.e * nbt + nb1) * kg + kb) * 512u, 512u, fb);
               }
             } else {
-            if (t.thin && p.thin_rows <= 32) {
-              // at large hidden sizes a thin tile (at most 32 rows) reads only
-              // the 16-row boxes that hold its rows
+            if (t.thin && (!g1 || p.thin_rows <= 32)) {
+              // a thin tile of at most 32 rows (GEMM2; GEMM1 at large hidden
+              // sizes) reads only the 16-row boxes that hold its rows
               const int nr16 = (t.rows + 15) >> 4;
               mbar_arrive_expect_tx(&full[s], (uint32_t)nr16 * 2048u + (uint32_t)nbox * kBBox);
-              for (int i = 0; i < nr16; ++i)
-                tma_load_2d(sa + i * 2048, &tmX16, fb, kb * BK, slot * p.mb + t.mloc * kBM + 16 * i);
+              for (int i = 0; i < nr16; ++i) {
+                if (g1) tma_load_2d(sa + i * 2048, &tmX16, fb, kb * BK, slot * p.mb + t.mloc * kBM + 16 * i);
+                else tma_load_2d(sa + i * 2048, &tmA16, fb, kb * BK, t.mt * kBM + 16 * i);
+              }
             } else {
               mbar_arrive_expect_tx(&full[s], (uint32_t)(na * kABytes) + (uint32_t)nbox * kBBox);
               for (int i = 0; i < na; ++i) {
@@ -693,6 +697,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             float v[32];
             tmem_ld32(tb + c, v);
             store32_bf16(p.Y + row * p.d + col, v);
+          }
+          tc_fence_before();
+          mbar_arrive(&tempty[acc]);
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) red_release_add(p.done2, 1);
+        } else if (t.thin && t.phase == 2) {
+          // thin GEMM2 tile: lanes hold output columns (two halves of 128),
+          // TMEM columns the tile's rows; the rows of Y go out through the
+          // warp's drained staging area used as a transpose tile
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+          uint8_t* tr = staging + (size_t)(warp - 2) * 2 * kOutTile;
+          const int nthin = (t.rows + 15) & ~15;
+          for (int h = 0; h < 2; ++h) {
+            const int c0 = t.n * 256 + h * 128 + q * 32;
+            if (c0 >= p.d) continue;
+            for (int t0 = 0; t0 < nthin; t0 += 32) {
+              float v[32];
+              tmem_ld32(tb + h * 128 + t0, v);
+              const size_t r0 = (size_t)t.mt * kBM + t0;
+              ring_store_cols_t(tr, v, p.Y + r0 * p.d + c0, p.d, min(32, t.rows - t0), lane);
+            }
           }
           tc_fence_before();
           mbar_arrive(&tempty[acc]);
@@ -955,6 +982,7 @@ cudaError_t ring_launch(const moe_config& c, const Ws& ws, const int* counts, co
   // rows, which then also load just their rows
   p.thin = (!FP8 && c.f % 128 == 0) ? 1 : 0;
   p.thin_rows = gemm1_thin_enabled(c) ? kBM - 1 : 32;
+  p.thin2 = FP8 ? 0 : 1;
   p.hdr = ws.hdr();
   p.row_of_pad = ws.row_of_pad();
   p.pos_pad = ws.pos_pad();
@@ -983,7 +1011,7 @@ cudaError_t ring_launch(const moe_config& c, const Ws& ws, const int* counts, co
   p.ring_valid = ws.hdr() + kHdrRingValid;
 
   const uint64_t rows = (uint64_t)ws.L.Rp_max;
-  CUtensorMap tmX, tmW1, tmA, tmW2, tmY, tmX16;
+  CUtensorMap tmX, tmW1, tmA, tmW2, tmY, tmX16, tmA16;
   if (FP8) {
     // K-major E4M3: 128-byte K boxes of 128 rows (W2: 256 rows)
     if (!map2d(&tmX, p.ring, c.d, (uint64_t)p.S * p.mb, 128, kBM, true) ||
@@ -992,8 +1020,10 @@ cudaError_t ring_launch(const moe_config& c, const Ws& ws, const int* counts, co
       return cudaErrorInvalidValue;
     tmY = tmX;  // Y leaves with direct stores
     tmX16 = tmX;
+    tmA16 = tmA;
   } else if (!map2d(&tmX, p.ring, c.d, (uint64_t)p.S * p.mb, 64, kBM) ||
              !map2d(&tmX16, p.ring, c.d, (uint64_t)p.S * p.mb, 64, 16) ||
+             !map2d(&tmA16, A, c.f, rows, 64, 16) ||
              !map3d(&tmW1, W1, 2ull * c.f, c.d, c.E, 64, 64) || !map2d(&tmA, A, c.f, rows, 64, kBM) ||
              !map3d(&tmW2, W2, c.d, c.f, c.E, 64, 64) || !map2d(&tmY, p.Y, c.d, rows, 64, 32)) {
     return cudaErrorInvalidValue;
@@ -1008,7 +1038,7 @@ cudaError_t ring_launch(const moe_config& c, const Ws& ws, const int* counts, co
   err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, kSmem);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
-  void* args[] = {&tmX, &tmW1, &tmA, &tmW2, &tmY, &tmX16, &p};
+  void* args[] = {&tmX, &tmW1, &tmA, &tmW2, &tmY, &tmX16, &tmA16, &p};
   TraceScope ts(FP8 ? "ring_forward_mxfp8" : "ring_forward", st);
   return cudaLaunchCooperativeKernel((const void*)kern, dim3(sms), dim3(kThreads), args, kSmem, st);
 }
