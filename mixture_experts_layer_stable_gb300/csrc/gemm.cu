@@ -1037,6 +1037,9 @@ __global__ void __launch_bounds__(kThreads, UM == UNITS_ALL ? 1 : 2)
           qd[0] = lo;
           qd[1] = hi;
           p.q_sf[mx_sf_offset(row, (p.f + col) >> 5, kq)] = sc;
+          // column i's scale bytes (the same in every lane) are kept by lane
+          // i, which stores them after the loop
+          uint8_t m1 = 0, m2 = 0, m3 = 0;
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             uint8_t s1, s2, s3;
@@ -1046,12 +1049,15 @@ __global__ void __launch_bounds__(kThreads, UM == UNITS_ALL ? 1 : 2)
             p.qt0[(size_t)(col + i) * p.ldt + row] = c1;
             p.qt0[(size_t)(p.f + col + i) * p.ldt + row] = c2;
             p.qt1[(size_t)(col + i) * p.ldt + row] = c3;
-            if (lane == 0) {
-              p.qt0_sf[mx_sf_offset((size_t)(col + i), rblk, kt)] = s1;
-              p.qt0_sf[mx_sf_offset((size_t)(p.f + col + i), rblk, kt)] = s2;
-              p.qt1_sf[mx_sf_offset((size_t)(col + i), rblk, kt)] = s3;
+            if (lane == i) {
+              m1 = s1;
+              m2 = s2;
+              m3 = s3;
             }
           }
+          p.qt0_sf[mx_sf_offset((size_t)(col + lane), rblk, kt)] = m1;
+          p.qt0_sf[mx_sf_offset((size_t)(p.f + col + lane), rblk, kt)] = m2;
+          p.qt1_sf[mx_sf_offset((size_t)(col + lane), rblk, kt)] = m3;
         }
         p.dgp[row * p.n_tiles + t.n] = dg;
       } else {
