@@ -64,14 +64,6 @@ enum Epi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2, EPI_LOGITS = 3 };
 // heavy kernel leaves room (shared memory, TMEM) for one light CTA per SM.
 // Their pipeline depths (stages) share one SM's shared memory.
 enum UnitSet { UNITS_ALL = 0, UNITS_HEAVY = 1, UNITS_LIGHT = 2 };
-// An experiment on the forward pair GEMMs (off): instead of every cluster
-// alternating between heavy units and light units (the interleaved walk),
-// a share of the clusters proportional to the light units' estimated cost
-// walks only light units and the others only heavy units.
-#ifndef MOE_GEMM_PARTITION
-#define MOE_GEMM_PARTITION 0
-#endif
-
 #ifndef MOE_SPLIT_HEAVY_STAGES
 #define MOE_SPLIT_HEAVY_STAGES 3
 #endif
@@ -389,28 +381,6 @@ __global__ void __launch_bounds__(kThreads, UM == UNITS_ALL ? 1 : 2)
   const int rank = PAIR ? (int)cluster_ctarank() : 0;
   const int unit0 = PAIR ? (int)cluster_idx() : (int)blockIdx.x;
   const int ustride = PAIR ? (int)cluster_count() : (int)gridDim.x;
-  // partitioned walk: clusters [0, np) take the light units, the others the
-  // heavy ones (a light unit's stage carries 16 KB of weights and at most 2 KB
-  // of rows per CTA, a heavy unit's 32 KB: costs 9 : 16)
-  constexpr bool kPart = MOE_GEMM_PARTITION && PAIR && !WGRAD && UM == UNITS_ALL;
-  int part_light = 0, part_n = 0, part_u0 = 0, part_st = 1;
-  if constexpr (kPart) {
-    const long long nl = (long long)__ldg(p.lt_off + p.E) * p.n_tiles;
-    const long long nh = (long long)__ldg(p.hv_off + p.E) * p.n_tiles;
-    int np = nl == 0 ? 0 : nh == 0 ? ustride
-                                   : (int)((ustride * 9 * nl + (9 * nl + 16 * nh) / 2) / (9 * nl + 16 * nh));
-    if (nl > 0 && nh > 0) np = max(1, min(ustride - 1, np));
-    part_light = unit0 < np ? 1 : 0;
-    part_n = (int)(part_light ? nl : nh);
-    part_u0 = part_light ? unit0 : unit0 - np;
-    part_st = part_light ? np : ustride - np;
-  }
-  auto dec = [&](int U, int r) -> Tile {
-    if constexpr (kPart)
-      return part_light ? decode<WGRAD, PAIR, UNITS_LIGHT>(p, U, r) : decode<WGRAD, PAIR, UNITS_HEAVY>(p, U, r);
-    else
-      return decode<WGRAD, PAIR, UM>(p, U, r);
-  };
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -464,10 +434,6 @@ __global__ void __launch_bounds__(kThreads, UM == UNITS_ALL ? 1 : 2)
       if ((threadIdx.x & 31) == 0) mbar_arrive(&qempty[j % kQ]);
       return U;
     } else {
-      if constexpr (kPart) {
-        const int u = part_u0 + j * part_st;
-        return u < part_n ? u : -1;
-      }
       const int L = unit0 + j * ustride;
       return L < total ? unit_at(L, total, ustride) : -1;
     }
@@ -499,23 +465,18 @@ __global__ void __launch_bounds__(kThreads, UM == UNITS_ALL ? 1 : 2)
           pending = true;
           U = cur;
         } else {
-          if constexpr (kPart) {
-            U = part_u0 + j * part_st;
-            if (U >= part_n) break;
-          } else {
-            const int L = unit0 + j * ustride;
-            if (L >= total) break;
-            U = unit_at(L, total, ustride);
-          }
+          const int L = unit0 + j * ustride;
+          if (L >= total) break;
+          U = unit_at(L, total, ustride);
         }
         if (CLC && U >= total) goto next_unit;
         {
-        const Tile t = dec(U, rank);
+        const Tile t = decode<WGRAD, PAIR, UM>(p, U, rank);
         // bytes landing on this stage's "full" barrier (pair: both CTAs' copies)
         uint32_t tx = (t.valid ? (uint32_t)kABytes : 0u) + b_bytes + (FP8 ? (uint32_t)kSfBytes : 0u);
         if (PAIR && t.thin) tx = 16384u + (uint32_t)(t.nt / 2) * 128u;  // weights + half the rows
         if (PAIR && rank == 0)
-          tx += t.thin ? tx : (dec(U, 1).valid ? (uint32_t)kABytes : 0u) + b_bytes;
+          tx += t.thin ? tx : (decode<WGRAD, PAIR, UM>(p, U, 1).valid ? (uint32_t)kABytes : 0u) + b_bytes;
         for (int kb = 0; kb < t.kb_count; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status, 100 + s)) goto producer_done;
           const uint32_t sa = smem_u32(stages + (size_t)s * kStageB);
@@ -632,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, UM == UNITS_ALL ? 1 : 2)
         if (!ok) goto mma_done;
         if (U < 0) break;
         if (CLC && U >= total) continue;
-        const Tile t = dec(U, 0);
+        const Tile t = decode<WGRAD, PAIR, UM>(p, U, 0);
         if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, p.status, 200 + acc)) goto mma_done;
         tc_fence_after();
         const uint32_t dt = tmem_base + (uint32_t)acc * kAccStride;
@@ -778,7 +739,7 @@ __global__ void __launch_bounds__(kThreads, UM == UNITS_ALL ? 1 : 2)
       const int U = unit_of(j, ok);
       if (!ok || U < 0) break;
       if (CLC && U >= total) continue;
-      const Tile t = dec(U, rank);
+      const Tile t = decode<WGRAD, PAIR, UM>(p, U, rank);
       if (!mbar_wait(&tfull[acc], aph, abort_flag, p.status, 400 + acc)) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + (uint32_t)acc * kAccStride + ((uint32_t)(q * 32) << 16);
