@@ -106,6 +106,7 @@ KERNEL_SOURCE = {"ring_forward": "ring.cu", "gather": "gather_merge.cu", "gather
                  "gather_mxfp8": "gather_merge.cu", "merge": "gather_merge.cu",
                  "reverse_dispatch": "gather_merge.cu", "dg_reduce": "gather_merge.cu",
                  "sched_topk_hist": "sched.cu", "sched_hist": "sched.cu", "sched_scatter": "sched.cu",
+                 "sched_fused": "sched.cu",
                  "quant_dy_rows": "gather_merge.cu", "quant_x_cols": "gather_merge.cu",
                  "quant_dy_cols": "gather_merge.cu", "quantize_weights": "gather_merge.cu"}
 
@@ -692,7 +693,7 @@ def main():
                            "after the timed region" % n_tr})
     fwd_names = ("gather", "gather_mxfp8", "gemm1_swiglu", "gemm2", "gemm1_swiglu_mxfp8",
                  "gemm2_mxfp8", "merge", "ring_forward", "ring_forward_mxfp8")
-    sched_names = ("sched_topk_hist", "sched_hist", "sched_scatter", "router_logits")
+    sched_names = ("sched_fused", "sched_topk_hist", "sched_hist", "sched_scatter", "router_logits")
     fwd_ms = sum(per[n][1] for n in per if n in fwd_names) / n_tr
     sch_ms = sum(per[n][1] for n in per if n in sched_names) / n_tr
     bwd_ms = sum(per[n][1] for n in per if n not in fwd_names + sched_names) / n_tr

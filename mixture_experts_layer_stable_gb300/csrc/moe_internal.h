@@ -87,6 +87,7 @@ enum HdrWord {
   kHdrStatus = 0,     // device status (moe_status code), first error wins
   kHdrWhere = 1,      // which wait / check reported it
   kHdrDone = 2,       // schedule: blocks finished (last-block ticket)
+  kHdrSchedGo = 3,    // one-launch schedule: the table is ready (set by the last block)
   kHdrRpTotal = 4,    // padded rows of all experts (multiple of kBM)
   kHdrMtTotal = 5,    // kRpTotal / kBM
   kHdrInject = 8,     // fault-injection words for tests of the bounded waits (8 and 9)

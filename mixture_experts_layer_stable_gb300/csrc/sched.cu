@@ -27,6 +27,7 @@
 #include <math.h>
 
 #include "moe_internal.h"
+#include "ptx.cuh"
 
 namespace moe {
 
@@ -231,21 +232,18 @@ __device__ void finish_histograms(int* __restrict__ hist, int nb, int E, int* __
   }
 }
 
-// Top-k of the chunk's tokens (one warp per token) with the chunk's
-// histogram, then the table in the last block (see the file comment).
+// Top-k of chunk b's tokens (one warp per token) with the chunk's
+// histogram written to hist row b; true in the block that finishes last
+// (atomic ticket), which then owns the table.  sh: kMaxE ints of shared memory.
 template <int NCH>
-__global__ void __launch_bounds__(kSchedThreads) sched_topk_hist_kernel(
-    const float* __restrict__ logits, int T, int E, int k, int tb, int* __restrict__ ids,
-    float* __restrict__ wts, int* __restrict__ hist, int* __restrict__ hdr, int* __restrict__ counts,
-    int* __restrict__ offsets, int* __restrict__ poff, int* __restrict__ mt_off,
-    int* __restrict__ pt_off) {
-  __shared__ int sh[kMaxE];
-  __shared__ int aux[kSchedThreads];
-  __shared__ int sh_last;
+__device__ __forceinline__ bool topk_hist_chunk(const float* __restrict__ logits, int T, int E, int k,
+                                                int tb, int b, int nb, int* __restrict__ ids,
+                                                float* __restrict__ wts, int* __restrict__ hist,
+                                                int* __restrict__ hdr, int* sh, int* s_last) {
   const int tid = threadIdx.x, lane = tid & 31;
   for (int e = tid; e < E; e += blockDim.x) sh[e] = 0;
   __syncthreads();
-  const int t0 = blockIdx.x * tb, t1 = min(T, t0 + tb);
+  const int t0 = b * tb, t1 = min(T, t0 + tb);
   // the next token's logits are loaded while this one's top-k runs
   float v[NCH] = {}, vn[NCH] = {};
   int t = t0 + (tid >> 5);
@@ -264,14 +262,29 @@ __global__ void __launch_bounds__(kSchedThreads) sched_topk_hist_kernel(
     }
   }
   __syncthreads();
-  for (int e = tid; e < E; e += blockDim.x) hist[(size_t)blockIdx.x * E + e] = sh[e];
+  for (int e = tid; e < E; e += blockDim.x) hist[(size_t)b * E + e] = sh[e];
   __threadfence();
   __syncthreads();
-  if (tid == 0) sh_last = (atomicAdd(hdr + kHdrDone, 1) == (int)gridDim.x - 1);
+  if (tid == 0) *s_last = (atomicAdd(hdr + kHdrDone, 1) == nb - 1);
   __syncthreads();
-  if (!sh_last) return;
-  __threadfence();
-  finish_histograms(hist, gridDim.x, E, hdr, counts, offsets, poff, mt_off, pt_off, sh, aux);
+  const bool last = *s_last != 0;
+  if (last) __threadfence();
+  return last;
+}
+
+// Top-k with the per-chunk histogram, then the table in the last block (see
+// the file comment).
+template <int NCH>
+__global__ void __launch_bounds__(kSchedThreads) sched_topk_hist_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int tb, int* __restrict__ ids,
+    float* __restrict__ wts, int* __restrict__ hist, int* __restrict__ hdr, int* __restrict__ counts,
+    int* __restrict__ offsets, int* __restrict__ poff, int* __restrict__ mt_off,
+    int* __restrict__ pt_off) {
+  __shared__ int sh[kMaxE];
+  __shared__ int aux[kSchedThreads];
+  __shared__ int sh_last;
+  if (topk_hist_chunk<NCH>(logits, T, E, k, tb, blockIdx.x, gridDim.x, ids, wts, hist, hdr, sh, &sh_last))
+    finish_histograms(hist, gridDim.x, E, hdr, counts, offsets, poff, mt_off, pt_off, sh, aux);
 }
 
 __global__ void __launch_bounds__(kSchedThreads) sched_hist_kernel(
@@ -297,15 +310,18 @@ __global__ void __launch_bounds__(kSchedThreads) sched_hist_kernel(
   finish_histograms(hist, gridDim.x, E, hdr, counts, offsets, poff, mt_off, pt_off, sh, aux);
 }
 
-__global__ void __launch_bounds__(kSchedThreads) sched_scatter_kernel(
+// Stable positions of chunk b's rows (rows [b cr, (b+1) cr)): ranks within
+// the chunk by warp match and per-warp prefixes, offset by the chunk's
+// exclusive prefix; the padding rows of the experts this block owns (every
+// nb-th from b).  wcnt: kWarps x kMaxE ints of shared memory.
+__device__ __forceinline__ void scatter_chunk(
     const int* __restrict__ ids, const float* __restrict__ wts, int R, int E,
     const int* __restrict__ hist_prefix, const int* __restrict__ counts,
     const int* __restrict__ offsets, const int* __restrict__ poff, int* __restrict__ perm,
     int* __restrict__ inv, int* __restrict__ pos_pad, int* __restrict__ row_of_pad,
-    float* __restrict__ g_pad, int cr) {
-  __shared__ int wcnt[kWarps][kMaxE];
+    float* __restrict__ g_pad, int cr, int b, int nb, int (*wcnt)[kMaxE]) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int r_begin = blockIdx.x * cr;
+  const int r_begin = b * cr;
   const int r_end = min(R, r_begin + cr);
   const int per_warp = (r_end - r_begin + kWarps - 1) / kWarps;
   const int w_begin = r_begin + warp * per_warp;
@@ -341,7 +357,7 @@ __global__ void __launch_bounds__(kSchedThreads) sched_scatter_kernel(
     if (e >= 0 && lane == __ffs(peers) - 1) wcnt[warp][e] += __popc(peers);
     __syncwarp();
     if (e >= 0) {
-      const int within = hist_prefix[(size_t)blockIdx.x * E + e] + local;
+      const int within = hist_prefix[(size_t)b * E + e] + local;
       const int p = offsets[e] + within;
       const int pp = poff[e] + within;
       perm[p] = r;
@@ -352,7 +368,7 @@ __global__ void __launch_bounds__(kSchedThreads) sched_scatter_kernel(
     }
   }
   // padding rows of the experts this block owns
-  for (int e = blockIdx.x; e < E; e += gridDim.x) {
+  for (int e = b; e < E; e += nb) {
     const int c = counts[e];
     const int pc = (c + kBM - 1) / kBM * kBM;
     for (int i = c + tid; i < pc; i += blockDim.x) {
@@ -360,6 +376,63 @@ __global__ void __launch_bounds__(kSchedThreads) sched_scatter_kernel(
       g_pad[poff[e] + i] = 0.f;
     }
   }
+}
+
+__global__ void __launch_bounds__(kSchedThreads) sched_scatter_kernel(
+    const int* __restrict__ ids, const float* __restrict__ wts, int R, int E,
+    const int* __restrict__ hist_prefix, const int* __restrict__ counts,
+    const int* __restrict__ offsets, const int* __restrict__ poff, int* __restrict__ perm,
+    int* __restrict__ inv, int* __restrict__ pos_pad, int* __restrict__ row_of_pad,
+    float* __restrict__ g_pad, int cr) {
+  __shared__ int wcnt[kWarps][kMaxE];
+  scatter_chunk(ids, wts, R, E, hist_prefix, counts, offsets, poff, perm, inv, pos_pad, row_of_pad, g_pad,
+                cr, blockIdx.x, gridDim.x, wcnt);
+}
+
+// The whole schedule in one cooperative launch (every block co-resident):
+// each block's top-k and histogram, the table in the last block to finish,
+// which then releases the others (a header flag, waited on with a bound),
+// and every block's scatter of its own chunk.  Saves the second launch.
+template <int NCH>
+__global__ void __launch_bounds__(kSchedThreads) sched_fused_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int tb, int* __restrict__ ids,
+    float* __restrict__ wts, int* __restrict__ hist, int* __restrict__ hdr, int* __restrict__ counts,
+    int* __restrict__ offsets, int* __restrict__ poff, int* __restrict__ mt_off,
+    int* __restrict__ pt_off, int* __restrict__ perm, int* __restrict__ inv, int* __restrict__ pos_pad,
+    int* __restrict__ row_of_pad, float* __restrict__ g_pad) {
+  __shared__ int sh[kMaxE];
+  __shared__ int aux[kSchedThreads];
+  __shared__ int wcnt[kWarps][kMaxE];
+  __shared__ int sh_last, s_ok;
+  const int nb = gridDim.x;
+  const bool last = topk_hist_chunk<NCH>(logits, T, E, k, tb, blockIdx.x, nb, ids, wts, hist, hdr, sh, &sh_last);
+  if (last) {
+    finish_histograms(hist, nb, E, hdr, counts, offsets, poff, mt_off, pt_off, sh, aux);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      red_release_add(hdr + kHdrSchedGo, 1);
+    }
+  }
+  if (threadIdx.x == 0) {
+    bool ok = true;
+    if (!last && ld_acquire(hdr + kHdrSchedGo) == 0) {
+      const uint64_t t0 = global_timer_ns();
+      while (ld_acquire(hdr + kHdrSchedGo) == 0) {
+        __nanosleep(64);
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+          report_status(hdr + kHdrStatus, kStatusTimeout, 950);
+          ok = false;
+          break;
+        }
+      }
+    }
+    s_ok = ok ? 1 : 0;
+  }
+  __syncthreads();
+  if (!s_ok) return;
+  scatter_chunk(ids, wts, T * k, E, hist, counts, offsets, poff, perm, inv, pos_pad, row_of_pad, g_pad,
+                tb * k, blockIdx.x, nb, wcnt);
 }
 
 }  // namespace
@@ -390,26 +463,72 @@ cudaError_t launch_schedule_tail(const moe_config& c, const moe_sched& s, const 
   return launch_scatter(c, s, ws, st);
 }
 
-cudaError_t launch_schedule_from_logits(const moe_config& c, const float* logits, const moe_sched& s,
-                                        const Ws& ws, cudaStream_t st) {
+namespace {
+// Blocks of sched_fused_kernel<NCH> that fit on the GPU at once (0 if unknown).
+template <int NCH>
+int fused_capacity() {
+  static int cap = -1;
+  if (cap < 0) {
+    int per_sm = 0;
+    cap = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sched_fused_kernel<NCH>, kSchedThreads, 0) ==
+                  cudaSuccess
+              ? per_sm * num_sms()
+              : 0;
+  }
+  return cap;
+}
+
+template <int NCH>
+cudaError_t schedule_chunks(const moe_config& c, const float* logits, const moe_sched& s, const Ws& ws,
+                            cudaStream_t st) {
   const int nb = (int)ws.L.nblk, tb = sched_chunk_tokens(c.T, c.k);
+  if (nb <= fused_capacity<NCH>()) {
+    // one cooperative launch: every block is resident while the others wait
+    TraceScope ts("sched_fused", st);
+    const float* lg = logits;
+    int T = c.T, E = c.E, k = c.k, tbv = tb;
+    int* ids = s.topk_ids;
+    float* wts = s.topk_w;
+    int* hist = ws.hist();
+    int* hdr = ws.hdr();
+    int* counts = s.counts;
+    int* offsets = s.offsets;
+    int* poff = ws.poff();
+    int* mt_off = ws.mt_off();
+    int* pt_off = ws.pt_off();
+    int* perm = s.perm;
+    int* inv = s.inv;
+    int* pos_pad = ws.pos_pad();
+    int* row_of_pad = ws.row_of_pad();
+    float* g_pad = ws.g_pad();
+    void* args[] = {&lg, &T, &E, &k, &tbv, &ids, &wts, &hist, &hdr, &counts, &offsets, &poff,
+                    &mt_off, &pt_off, &perm, &inv, &pos_pad, &row_of_pad, &g_pad};
+    const cudaError_t e = cudaLaunchCooperativeKernel((const void*)sched_fused_kernel<NCH>, dim3(nb),
+                                                      dim3(kSchedThreads), args, 0, st);
+    if (e != cudaErrorCooperativeLaunchTooLarge) return e;
+    (void)cudaGetLastError();  // not resident after all: the two-launch form below
+  }
   cudaError_t err;
   {
     TraceScope ts("sched_topk_hist", st);
-    auto args = [&](auto kern) {
-      kern<<<nb, kSchedThreads, 0, st>>>(logits, c.T, c.E, c.k, tb, s.topk_ids, s.topk_w, ws.hist(),
-                                         ws.hdr(), s.counts, s.offsets, ws.poff(), ws.mt_off(),
-                                         ws.pt_off());
-    };
-    if (c.E <= 32) args(sched_topk_hist_kernel<1>);
-    else if (c.E <= 64) args(sched_topk_hist_kernel<2>);
-    else if (c.E <= 128) args(sched_topk_hist_kernel<4>);
-    else if (c.E <= 256) args(sched_topk_hist_kernel<8>);
-    else args(sched_topk_hist_kernel<kMaxE / 32>);
+    sched_topk_hist_kernel<NCH><<<nb, kSchedThreads, 0, st>>>(logits, c.T, c.E, c.k, tb, s.topk_ids, s.topk_w,
+                                                              ws.hist(), ws.hdr(), s.counts, s.offsets,
+                                                              ws.poff(), ws.mt_off(), ws.pt_off());
     err = cudaGetLastError();
   }
   if (err != cudaSuccess) return err;
   return launch_scatter(c, s, ws, st);
+}
+}  // namespace
+
+// The header must have been cleared (launch_schedule and moe_route do).
+cudaError_t launch_schedule_from_logits(const moe_config& c, const float* logits, const moe_sched& s,
+                                        const Ws& ws, cudaStream_t st) {
+  if (c.E <= 32) return schedule_chunks<1>(c, logits, s, ws, st);
+  if (c.E <= 64) return schedule_chunks<2>(c, logits, s, ws, st);
+  if (c.E <= 128) return schedule_chunks<4>(c, logits, s, ws, st);
+  if (c.E <= 256) return schedule_chunks<8>(c, logits, s, ws, st);
+  return schedule_chunks<kMaxE / 32>(c, logits, s, ws, st);
 }
 
 cudaError_t launch_schedule(const moe_config& c, const float* logits, const moe_sched& s,
