@@ -961,11 +961,13 @@ cudaError_t ring_launch(const moe_config& c, const Ws& ws, const int* counts, co
   p.nt2 = (c.d + 255) / 256;
   p.kb1 = FP8 ? c.d / BK8 : c.d / BK;
   p.kb2 = FP8 ? c.f / BK8 : c.f / BK;
-  // units of two tiles halve B's L2 ingress per row but halve the units a
-  // window offers; they pay where a tile's K loop is long (hidden 7168: ring
-  // forward 3.75 -> 3.63 ms) and cost where it is short and the windows'
-  // handover dominates (hidden 2048: 0.235 -> 0.330 ms)
-  p.tpu = (!FP8 && p.kb1 >= 64) ? 2 : 1;
+  // units of two tiles halve B's L2 ingress per row but halve the number of
+  // units; they pay where a tile's K loop is long and the layer offers at
+  // least 8 GEMM1 units of 256 rows per SM (hidden 7168, 32768 rows: ring
+  // forward 3.75 -> 3.63 ms) and cost where the K loop is short (hidden 2048:
+  // 0.235 -> 0.330 ms) or the units are few (512 tokens: 0.59 -> 0.68 ms)
+  const long long units2 = (long long)c.T * c.k / 256 * p.nt1;
+  p.tpu = (!FP8 && p.kb1 >= 64 && units2 >= 8LL * sms) ? 2 : 1;
   {
     // lag: one window more than it takes for the tiles claimed between a
     // window's GEMM1 and its GEMM2 to keep every compute CTA busy for one
