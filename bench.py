@@ -495,7 +495,7 @@ def main():
             with torch.cuda.graph(graph):
                 step()
             graph_note = "one CUDA graph per step (captured library calls)"
-        except Exception as ex:  # pragma: no cover - depends on the driver
+        except Exception as ex:  # pragma: no cover - depends on the CUDA version
             graph = None
             graph_note = f"eager launches (graph capture failed: {type(ex).__name__})"
             torch.cuda.synchronize()
