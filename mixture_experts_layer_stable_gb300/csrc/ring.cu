@@ -287,7 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     ring_forward_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW1,
                         const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW2,
                         const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmX16,
-                        const __grid_constant__ CUtensorMap tmA16, const RingParams p) {
+                        const __grid_constant__ CUtensorMap tmA16, const __grid_constant__ CUtensorMap tmAo,
+                        const __grid_constant__ CUtensorMap tmHo, const RingParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_ok;
   __shared__ int s_gab;
@@ -644,6 +645,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       int acc = 0, buf = 0;
       uint32_t aph = 0;
       const uint32_t stg = smem_u32(staging) + (uint32_t)(warp - 2) * 2u * kOutTile;
+      // this warp's 32 rows x 64 columns (v = this lane's row) as bf16 through
+      // the next swizzled staging tile to a TMA store at (col, row) of m
+      auto put64 = [&](const CUtensorMap* m, const float* v, int col, int row) {
+        if (lane == 0) bulk_wait_read<1>();
+        __syncwarp();
+        const uint32_t sbuf = stg + (uint32_t)buf * kOutTile;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          st_shared_v4(sbuf + lane * 128 + ((j ^ (lane & 7)) << 4),
+                       pack_bf16x2(v[8 * j + 0], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                       pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(m, sbuf, col, row);
+          bulk_commit();
+        }
+        buf ^= 1;
+      };
       for (int j = 0;; ++j) {
         if (!mbar_wait(&qfull[j % kQ], (j / kQ) & 1, abort_flag, p.status, 170)) break;
         const int L = qtile[j % kQ];
@@ -763,26 +784,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) red_release_add(&p.a_ready[t.mt], 1);
         } else if (t.phase == 1) {
-          // SwiGLU: A (and H when saving) with direct row stores
-          const size_t row = (size_t)t.mt * kBM + q * 32 + lane;
-          for (int c = 0; c < p.hn; c += 32) {
-            float g[32], u[32], a[32];
+          // SwiGLU: A (and H when saving) through swizzled staging and TMA
+          // stores of 32 x 64 tiles
+          const int row = t.mt * kBM + q * 32;
+          for (int c = 0; c < p.hn; c += 64) {
+            float g[64], u[64];
             tmem_ld32(tb + c, g);
+            tmem_ld32(tb + c + 32, g + 32);
             tmem_ld32(tb + p.hn + c, u);
+            tmem_ld32(tb + p.hn + c + 32, u + 32);
             const int col = t.n * p.hn + c;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) a[i] = silu_f(g[i]) * u[i];
-            store32_bf16(p.A + row * p.f + col, a);
             if (p.H != nullptr) {
-              store32_bf16(p.H + row * (2 * p.f) + col, g);
-              store32_bf16(p.H + row * (2 * p.f) + p.f + col, u);
+              put64(&tmHo, g, col, row);
+              put64(&tmHo, u, p.f + col, row);
             }
+#pragma unroll
+            for (int i = 0; i < 64; ++i) g[i] = silu_f(g[i]) * u[i];
+            put64(&tmAo, g, col, row);
           }
           tc_fence_before();
           mbar_arrive(&tempty[acc]);
-          __threadfence();
+          if (lane == 0) {
+            bulk_wait<0>();  // this warp's A rows are in global memory before GEMM2 reads them
+            fence_proxy_async_global();
+            __threadfence();
+            red_release_add(&p.a_ready[t.mt], 1);
+          }
           __syncwarp();
-          if (lane == 0) red_release_add(&p.a_ready[t.mt], 1);
         } else {
           // Y tile to expert order through swizzled staging + TMA stores
           const int row = t.mt * kBM + q * 32;
@@ -1013,7 +1041,7 @@ cudaError_t ring_launch(const moe_config& c, const Ws& ws, const int* counts, co
   p.ring_valid = ws.hdr() + kHdrRingValid;
 
   const uint64_t rows = (uint64_t)ws.L.Rp_max;
-  CUtensorMap tmX, tmW1, tmA, tmW2, tmY, tmX16, tmA16;
+  CUtensorMap tmX, tmW1, tmA, tmW2, tmY, tmX16, tmA16, tmAo, tmHo;
   if (FP8) {
     // K-major E4M3: 128-byte K boxes of 128 rows (W2: 256 rows)
     if (!map2d(&tmX, p.ring, c.d, (uint64_t)p.S * p.mb, 128, kBM, true) ||
@@ -1023,9 +1051,11 @@ cudaError_t ring_launch(const moe_config& c, const Ws& ws, const int* counts, co
     tmY = tmX;  // Y leaves with direct stores
     tmX16 = tmX;
     tmA16 = tmA;
+    tmAo = tmHo = tmX;
   } else if (!map2d(&tmX, p.ring, c.d, (uint64_t)p.S * p.mb, 64, kBM) ||
              !map2d(&tmX16, p.ring, c.d, (uint64_t)p.S * p.mb, 64, 16) ||
-             !map2d(&tmA16, A, c.f, rows, 64, 16) ||
+             !map2d(&tmA16, A, c.f, rows, 64, 16) || !map2d(&tmAo, A, c.f, rows, 64, 32) ||
+             (H != nullptr ? !map2d(&tmHo, H, 2ull * c.f, rows, 64, 32) : !map2d(&tmHo, A, c.f, rows, 64, 32)) ||
              !map3d(&tmW1, W1, 2ull * c.f, c.d, c.E, 64, 64) || !map2d(&tmA, A, c.f, rows, 64, kBM) ||
              !map3d(&tmW2, W2, c.d, c.f, c.E, 64, 64) || !map2d(&tmY, p.Y, c.d, rows, 64, 32)) {
     return cudaErrorInvalidValue;
@@ -1040,7 +1070,7 @@ cudaError_t ring_launch(const moe_config& c, const Ws& ws, const int* counts, co
   err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, kSmem);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
-  void* args[] = {&tmX, &tmW1, &tmA, &tmW2, &tmY, &tmX16, &tmA16, &p};
+  void* args[] = {&tmX, &tmW1, &tmA, &tmW2, &tmY, &tmX16, &tmA16, &tmAo, &tmHo, &p};
   TraceScope ts(FP8 ? "ring_forward_mxfp8" : "ring_forward", st);
   return cudaLaunchCooperativeKernel((const void*)kern, dim3(sms), dim3(kThreads), args, kSmem, st);
 }
