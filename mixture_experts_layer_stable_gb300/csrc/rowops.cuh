@@ -51,61 +51,6 @@ __device__ __forceinline__ void merge_token(const __nv_bfloat16* __restrict__ ro
                                             const float* sw, bool weighted, int t, int k, int d,
                                             __nv_bfloat16* __restrict__ out, int tid0, int nthr) {
   const int nvec = d >> 3;
-  if (k <= 2) {
-    // one or two slots: four of the thread's vectors in flight together
-    for (int v0 = tid0; v0 < nvec; v0 += 4 * nthr) {
-      uint4 y[4][2];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int v = v0 + q * nthr;
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          if (v < nvec && j < k) {
-            const void* src = rows + (size_t)sp[j] * d + (size_t)v * 8;
-            y[q][j] = COHERENT ? ldcg_v4(src) : ldg_nc_v4(src);
-          }
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int v = v0 + q * nthr;
-        if (v < nvec) {
-          float acc[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            if (j < k) {
-              const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&y[q][j]);
-              const float g = sw[j];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const float2 f = __bfloat1622float2(h[i]);
-                if (weighted) {
-                  acc[2 * i] = fmaf(g, f.x, acc[2 * i]);
-                  acc[2 * i + 1] = fmaf(g, f.y, acc[2 * i + 1]);
-                } else {
-                  acc[2 * i] += f.x;
-                  acc[2 * i + 1] += f.y;
-                }
-              }
-            }
-          }
-          uint4 o;
-          __nv_bfloat162 p0 = __floats2bfloat162_rn(acc[0], acc[1]);
-          __nv_bfloat162 p1 = __floats2bfloat162_rn(acc[2], acc[3]);
-          __nv_bfloat162 p2 = __floats2bfloat162_rn(acc[4], acc[5]);
-          __nv_bfloat162 p3 = __floats2bfloat162_rn(acc[6], acc[7]);
-          o.x = *reinterpret_cast<uint32_t*>(&p0);
-          o.y = *reinterpret_cast<uint32_t*>(&p1);
-          o.z = *reinterpret_cast<uint32_t*>(&p2);
-          o.w = *reinterpret_cast<uint32_t*>(&p3);
-          stg_v4(out + (size_t)t * d + (size_t)v * 8, o);
-        }
-      }
-    }
-    return;
-  }
   for (int v = tid0; v < nvec; v += nthr) {
     float acc[8];
 #pragma unroll
